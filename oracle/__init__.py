@@ -1,0 +1,200 @@
+"""fp64 CPU oracle for masked time-RoPE attention (test infrastructure only).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports it and has no CPU fallback.
+
+The arithmetic lives in ``rec_attn_oracle.c`` (plain C, fp64, one row at a
+time); this module compiles it with gcc into ``oracle/_build`` and wraps it with
+ctypes.  Citations for each function are in the C source.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rec_attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "librec_attn_oracle.so")
+
+SKIP, PARTIAL, FULL = 0, 1, 2
+TILE = 128
+GLOBAL, HIST, RT, CAND = 0, 1, 2, 3
+
+
+class OrcParams(ctypes.Structure):
+    _fields_ = [
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("use_delay", ctypes.c_int32),
+        ("delay_s", ctypes.c_int64),
+        ("window", ctypes.c_int32),
+        ("hist_bidirectional", ctypes.c_int32),
+        ("use_rope", ctypes.c_int32),
+        ("phi_min", ctypes.c_double),
+        ("dt_max_s", ctypes.c_double),
+        ("rope_base", ctypes.c_double),
+        ("softmax_scale", ctypes.c_double),
+    ]
+
+
+@dataclass
+class Params:
+    """Mask and RoPE parameters (CADET defaults: delta = 1 h, phi_min = 1e-4,
+    dt_max = 365 days, base = 6e5)."""
+
+    num_heads: int
+    head_dim: int
+    use_delay: bool = False
+    delay_s: int = 3600
+    window: int = 0
+    hist_bidirectional: bool = False
+    use_rope: bool = True
+    phi_min: float = 1e-4
+    dt_max_s: float = 365.0 * 86400.0
+    rope_base: float = 6e5
+    softmax_scale: float = 0.0
+
+    def c(self) -> OrcParams:
+        return OrcParams(self.num_heads, self.head_dim, int(self.use_delay), int(self.delay_s),
+                         int(self.window), int(self.hist_bidirectional), int(self.use_rope),
+                         float(self.phi_min), float(self.dt_max_s), float(self.rope_base),
+                         float(self.softmax_scale))
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no CUDA); returns the library path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "rec_attn_oracle.h"))):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # -ffp-contract=off: no fused multiply-add, so x86 and Arm hosts agree.
+    subprocess.run(["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-pthread", "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        P = ctypes.POINTER(OrcParams)
+        vp = ctypes.c_void_p
+        L.orc_visible.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
+        L.orc_visible.restype = ctypes.c_int
+        L.orc_mask.argtypes = [P, ctypes.c_int64, vp, vp, vp]
+        L.orc_mask.restype = None
+        L.orc_visible_pairs.argtypes = [P, ctypes.c_int32, vp, vp, vp]
+        L.orc_visible_pairs.restype = ctypes.c_uint64
+        L.orc_rope.argtypes = [P, ctypes.c_int64, vp, vp]
+        L.orc_rope.restype = None
+        L.orc_attention.argtypes = [P, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, vp,
+                                    ctypes.c_int64, vp, vp, vp, ctypes.c_int32]
+        L.orc_attention.restype = ctypes.c_int
+        L.orc_tile_classes.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp]
+        L.orc_tile_classes.restype = ctypes.c_int64
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _c64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def _c8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int8)
+
+
+def visible(p: Params, pi, ti, ty_i, pj, tj, ty_j) -> bool:
+    cp = p.c()
+    return bool(lib().orc_visible(ctypes.byref(cp), int(pi), int(ti), int(ty_i),
+                                  int(pj), int(tj), int(ty_j)))
+
+
+def mask(p: Params, t, ty) -> np.ndarray:
+    """L x L visibility mask (uint8, 1 = visible) of a single request."""
+    t, ty = _c64(t), _c8(ty)
+    L = t.shape[0]
+    out = np.zeros((L, L), dtype=np.uint8)
+    cp = p.c()
+    lib().orc_mask(ctypes.byref(cp), L, _ptr(t), _ptr(ty), _ptr(out))
+    return out
+
+
+def visible_pairs(p: Params, offsets, t, ty) -> int:
+    offsets, t, ty = _c64(offsets), _c64(t), _c8(ty)
+    cp = p.c()
+    return int(lib().orc_visible_pairs(ctypes.byref(cp), len(offsets) - 1, _ptr(offsets),
+                                       _ptr(t), _ptr(ty)))
+
+
+def rope(p: Params, t: int, x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.zeros_like(x)
+    cp = p.c()
+    lib().orc_rope(ctypes.byref(cp), int(t), _ptr(x), _ptr(y))
+    return y
+
+
+def tile_classes(p: Params, offsets, t, ty) -> np.ndarray:
+    offsets, t, ty = _c64(offsets), _c64(t), _c8(ty)
+    cp = p.c()
+    B = len(offsets) - 1
+    n = lib().orc_tile_classes(ctypes.byref(cp), B, _ptr(offsets), _ptr(t), _ptr(ty), None)
+    out = np.zeros(max(n, 1), dtype=np.uint8)
+    lib().orc_tile_classes(ctypes.byref(cp), B, _ptr(offsets), _ptr(t), _ptr(ty), _ptr(out))
+    return out[:n]
+
+
+def attention(p: Params, offsets, t, ty, q, k, v, rows=None, threads: int | None = None,
+              with_lse: bool = False):
+    """fp64 attention outputs for `rows` (sorted global token indices; None = all).
+
+    q, k, v: [T, H, d] arrays, either float32 or uint16 holding bf16 bit patterns
+    (widened exactly to fp64 inside the oracle).  Returns out [n_rows, H, d]
+    (float64) and, if requested, lse [n_rows, H].
+    """
+    offsets, t, ty = _c64(offsets), _c64(t), _c8(ty)
+    q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
+    if q.dtype == np.uint16:
+        dtype = 0
+    elif q.dtype == np.float32:
+        dtype = 1
+    else:
+        raise TypeError("q/k/v must be float32 or uint16 (bf16 bits)")
+    assert k.dtype == q.dtype and v.dtype == q.dtype
+    H, d = p.num_heads, p.head_dim
+    if rows is None:
+        n_rows = int(offsets[-1] - offsets[0])
+        rows_arr = None
+    else:
+        rows_arr = _c64(rows)
+        n_rows = rows_arr.shape[0]
+    out = np.zeros((max(n_rows, 1), H, d), dtype=np.float64)
+    lse = np.zeros((max(n_rows, 1), H), dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    cp = p.c()
+    rc = lib().orc_attention(ctypes.byref(cp), len(offsets) - 1, _ptr(offsets), _ptr(t), _ptr(ty),
+                             dtype, _ptr(q), _ptr(k), _ptr(v), n_rows,
+                             None if rows_arr is None else _ptr(rows_arr), _ptr(out), _ptr(lse),
+                             int(threads))
+    if rc != 0:
+        raise ValueError(f"orc_attention rejected its arguments (rc={rc})")
+    out, lse = out[:n_rows], lse[:n_rows]
+    return (out, lse) if with_lse else out

@@ -1,0 +1,378 @@
+/*
+ * rec_attn_oracle.c -- plain fp64 CPU oracle for masked time-RoPE softmax attention
+ * over a packed, jagged, request-centric token sequence.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the package smoke
+ * check and the benchmark's CPU-baseline leg may load this library.  It shares no
+ * code, header, table or constant with the CUDA path and must never serve as a
+ * fallback for it.
+ *
+ * Everything here is the definition written out, in fp64, one row at a time:
+ *
+ *   - Softmax attention with an additive -inf mask, Softmax(QK^T/sqrt(d) + M) V:
+ *     TM20K review page, section 2.1 (full-attention equation); LazFormer review
+ *     page, section 2.3, Eq. 19-21 (SparseAttn).
+ *   - Time-RoPE angle alpha_i(t) = t * phi_min / dt_max * base^(2i/d), applied to
+ *     adjacent component pairs of Q and K: CADET review page, section on time
+ *     encoding and self-gating.  The angle is formed from the absolute timestamp
+ *     exactly as printed; fp64 keeps it accurate to ~1e-12 rad at Unix scale.
+ *   - Mask predicate vis(i, j) (see orc_visible): CADET delay rule
+ *     M_ij = -inf if t_j > t_i - delta (section "why mask the last hour");
+ *     candidate isolation (section "scoring hundreds of candidates in 50 ms");
+ *     SORT U2U / C2U / C2C regions (section 3.1) and local attention (3.2.1);
+ *     LazFormer Eq. 19-21 (causal window + global history, target -> history,
+ *     target self only); MTGR hybrid dynamic mask (static part fully visible,
+ *     real-time block causal, targets see real-time events before them).
+ *   - The tile classification (orc_tile_classes) is NOT a definition from the
+ *     pages: it is the bounding-box interval rule this project uses to skip fully
+ *     masked 128x128 tiles (the pages' "mask preload check" of SORT section 4.1 and
+ *     the block skipping of the CADET serving kernel).  It is written here
+ *     independently so the GPU planner can be checked bit-exactly against it; the
+ *     tests check its soundness against the brute-force mask.
+ *
+ * Token types: 0 GLOBAL (special / profile / global summary), 1 HIST (history),
+ * 2 RT (real-time block), 3 CAND (candidate / target).  Positions are local to a
+ * request.  Tokens of different requests never see each other.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "rec_attn_oracle.h"
+
+enum { TY_GLOBAL = 0, TY_HIST = 1, TY_RT = 2, TY_CAND = 3 };
+
+/* ------------------------------------------------------------------------- */
+/* Mask predicate                                                             */
+/* ------------------------------------------------------------------------- */
+
+/* Delay clause t_j <= t_i - delta, evaluated exactly in 128-bit integers. */
+static int delay_clause(int64_t ti, int64_t tj, int64_t delta) {
+  return (__int128)tj <= (__int128)ti - (__int128)delta;
+}
+
+static int is_user(int ty) { return ty == TY_GLOBAL || ty == TY_HIST; }
+
+int orc_visible(const orc_params* p, int64_t pi, int64_t ti, int ty_i,
+                int64_t pj, int64_t tj, int ty_j) {
+  int vis;
+  if (ty_i < 0 || ty_i > 3 || ty_j < 0 || ty_j > 3) return 0;
+  if (is_user(ty_i) && is_user(ty_j)) {
+    if (p->hist_bidirectional) {
+      vis = 1; /* MTGR: profile + history fully mutually visible */
+    } else {
+      vis = (pj <= pi); /* causal user sequence (SORT U2U, LazFormer row 1) */
+      if (vis && p->window > 0 && ty_i != TY_GLOBAL && ty_j != TY_GLOBAL)
+        vis = (pi - pj) < p->window; /* local window; GLOBAL tokens exempt */
+    }
+  } else if (is_user(ty_i)) {
+    vis = 0; /* the user side reads neither real-time events nor candidates */
+  } else if (ty_i == TY_RT) {
+    if (is_user(ty_j)) vis = 1;            /* real-time block reads the static part */
+    else if (ty_j == TY_RT) vis = pj <= pi; /* and is causal inside itself */
+    else vis = 0;                           /* and never reads candidates */
+  } else { /* candidate query */
+    if (is_user(ty_j)) vis = 1;            /* C2U full */
+    else if (ty_j == TY_RT) vis = tj < ti;  /* real-time events strictly before it */
+    else vis = (pi == pj);                  /* C2C: itself only */
+  }
+  if (p->use_delay) {
+    int cand_self = (ty_i == TY_CAND && ty_j == TY_CAND && pi == pj);
+    if (!cand_self) vis = vis && delay_clause(ti, tj, p->delay_s);
+  }
+  return vis;
+}
+
+void orc_mask(const orc_params* p, int64_t L, const int64_t* t, const int8_t* ty,
+              uint8_t* out) {
+  for (int64_t i = 0; i < L; ++i)
+    for (int64_t j = 0; j < L; ++j)
+      out[i * L + j] = (uint8_t)orc_visible(p, i, t[i], ty[i], j, t[j], ty[j]);
+}
+
+uint64_t orc_visible_pairs(const orc_params* p, int32_t B, const int64_t* offsets,
+                           const int64_t* t, const int8_t* ty) {
+  uint64_t n = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    int64_t s = offsets[b], L = offsets[b + 1] - offsets[b];
+    for (int64_t i = 0; i < L; ++i)
+      for (int64_t j = 0; j < L; ++j)
+        n += (uint64_t)orc_visible(p, i, t[s + i], ty[s + i], j, t[s + j], ty[s + j]);
+  }
+  return n;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Time-RoPE                                                                  */
+/* ------------------------------------------------------------------------- */
+
+void orc_rope(const orc_params* p, int64_t t, const double* x, double* y) {
+  const int d = p->head_dim;
+  for (int i = 0; i < d / 2; ++i) {
+    double omega = p->phi_min / p->dt_max_s * pow(p->rope_base, 2.0 * i / d);
+    double a = (double)t * omega;
+    double c = cos(a), s = sin(a);
+    y[2 * i] = x[2 * i] * c - x[2 * i + 1] * s;
+    y[2 * i + 1] = x[2 * i] * s + x[2 * i + 1] * c;
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Attention                                                                  */
+/* ------------------------------------------------------------------------- */
+
+static double load_elem(int dtype, const void* base, int64_t idx) {
+  if (dtype == ORC_BF16) {
+    uint16_t h = ((const uint16_t*)base)[idx];
+    uint32_t bits = (uint32_t)h << 16; /* bf16 is the top half of an fp32 */
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+  }
+  return (double)((const float*)base)[idx];
+}
+
+typedef struct {
+  const orc_params* p;
+  int32_t B;
+  const int64_t* offsets;
+  const int64_t* t;
+  const int8_t* ty;
+  int dtype;
+  const void *q, *k, *v;
+  /* selected rows: sorted global token indices; row_lo[b]..row_hi[b] index rows[] */
+  const int64_t* rows;
+  const int64_t* row_lo;
+  const int64_t* row_hi;
+  double* out; /* [n_rows][H][d] */
+  double* lse; /* [n_rows][H] or NULL */
+  int64_t n_units;
+  int64_t next_unit; /* atomic work counter over (request, head) */
+} attn_job;
+
+static void attn_unit(attn_job* J, int32_t b, int32_t h, double* krot, double* vrow,
+                      double* qin, double* qrot, double* s, uint8_t* vis) {
+  const orc_params* p = J->p;
+  const int H = p->num_heads, d = p->head_dim;
+  const int64_t base = J->offsets[b], L = J->offsets[b + 1] - base;
+  const double scale = p->softmax_scale > 0 ? p->softmax_scale : 1.0 / sqrt((double)d);
+  (void)vrow;
+  /* rotated keys of this request and head */
+  for (int64_t j = 0; j < L; ++j) {
+    for (int e = 0; e < d; ++e)
+      qin[e] = load_elem(J->dtype, J->k, ((base + j) * H + h) * (int64_t)d + e);
+    if (p->use_rope) orc_rope(p, J->t[base + j], qin, krot + j * d);
+    else memcpy(krot + j * d, qin, sizeof(double) * d);
+  }
+  for (int64_t r = J->row_lo[b]; r < J->row_hi[b]; ++r) {
+    const int64_t gi = J->rows[r], i = gi - base;
+    for (int e = 0; e < d; ++e) qin[e] = load_elem(J->dtype, J->q, (gi * H + h) * (int64_t)d + e);
+    if (p->use_rope) orc_rope(p, J->t[gi], qin, qrot);
+    else memcpy(qrot, qin, sizeof(double) * d);
+    /* one row of the mask and of the scores */
+    double m = -INFINITY;
+    int any = 0;
+    for (int64_t j = 0; j < L; ++j) {
+      vis[j] = (uint8_t)orc_visible(p, i, J->t[gi], J->ty[gi], j, J->t[base + j], J->ty[base + j]);
+      if (!vis[j]) continue;
+      double acc = 0.0;
+      for (int e = 0; e < d; ++e) acc += qrot[e] * krot[j * d + e];
+      s[j] = scale * acc;
+      if (s[j] > m) m = s[j];
+      any = 1;
+    }
+    double* o = J->out + (r * H + h) * (int64_t)d;
+    for (int e = 0; e < d; ++e) o[e] = 0.0;
+    if (!any) { /* no visible key: defined zero output, lse = -inf */
+      if (J->lse) J->lse[r * H + h] = -INFINITY;
+      continue;
+    }
+    double den = 0.0;
+    for (int64_t j = 0; j < L; ++j)
+      if (vis[j]) den += exp(s[j] - m);
+    for (int64_t j = 0; j < L; ++j) {
+      if (!vis[j]) continue;
+      double w = exp(s[j] - m) / den;
+      for (int e = 0; e < d; ++e)
+        o[e] += w * load_elem(J->dtype, J->v, ((base + j) * H + h) * (int64_t)d + e);
+    }
+    if (J->lse) J->lse[r * H + h] = m + log(den);
+  }
+}
+
+static void* attn_worker(void* arg) {
+  attn_job* J = (attn_job*)arg;
+  const int d = J->p->head_dim;
+  int64_t Lmax = 0;
+  for (int32_t b = 0; b < J->B; ++b) {
+    int64_t L = J->offsets[b + 1] - J->offsets[b];
+    if (L > Lmax) Lmax = L;
+  }
+  double* krot = (double*)malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1) * d);
+  double* s = (double*)malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1));
+  uint8_t* vis = (uint8_t*)malloc((size_t)(Lmax > 0 ? Lmax : 1));
+  double* qin = (double*)malloc(sizeof(double) * d);
+  double* qrot = (double*)malloc(sizeof(double) * d);
+  for (;;) {
+    int64_t u = __atomic_fetch_add(&J->next_unit, 1, __ATOMIC_RELAXED);
+    if (u >= J->n_units) break;
+    int32_t b = (int32_t)(u / J->p->num_heads), h = (int32_t)(u % J->p->num_heads);
+    if (J->row_hi[b] > J->row_lo[b]) attn_unit(J, b, h, krot, NULL, qin, qrot, s, vis);
+  }
+  free(krot); free(s); free(vis); free(qin); free(qrot);
+  return NULL;
+}
+
+int orc_attention(const orc_params* p, int32_t B, const int64_t* offsets,
+                  const int64_t* t, const int8_t* ty, int32_t dtype,
+                  const void* q, const void* k, const void* v,
+                  int64_t n_rows, const int64_t* rows, double* out, double* lse,
+                  int32_t n_threads) {
+  if (!p || B < 0 || !offsets || p->num_heads <= 0 || p->head_dim <= 0 || (p->head_dim & 1))
+    return -1;
+  if (dtype != ORC_BF16 && dtype != ORC_FP32) return -1;
+  for (int32_t b = 0; b < B; ++b)
+    if (offsets[b + 1] < offsets[b]) return -1;
+  const int64_t T = offsets[B] - offsets[0];
+  int64_t* all_rows = NULL;
+  if (!rows) { /* every token of the batch */
+    n_rows = T;
+    all_rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1));
+    for (int64_t r = 0; r < T; ++r) all_rows[r] = offsets[0] + r;
+    rows = all_rows;
+  }
+  for (int64_t r = 0; r < n_rows; ++r) {
+    if (rows[r] < offsets[0] || rows[r] >= offsets[B]) { free(all_rows); return -2; }
+    if (r > 0 && rows[r] <= rows[r - 1]) { free(all_rows); return -2; } /* must be sorted */
+  }
+  int64_t* lo = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  int64_t* hi = (int64_t*)calloc((size_t)B + 1, sizeof(int64_t));
+  int64_t r = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    while (r < n_rows && rows[r] < offsets[b]) ++r;
+    lo[b] = r;
+    while (r < n_rows && rows[r] < offsets[b + 1]) ++r;
+    hi[b] = r;
+  }
+  attn_job J = {p, B, offsets, t, ty, dtype, q, k, v, rows, lo, hi, out, lse,
+                (int64_t)B * p->num_heads, 0};
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads == 1) {
+    attn_worker(&J);
+  } else {
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    for (int i = 0; i < n_threads; ++i) pthread_create(&th[i], NULL, attn_worker, &J);
+    for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+    free(th);
+  }
+  free(lo); free(hi); free(all_rows);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Tile classification (bounding-box interval rule)                           */
+/* ------------------------------------------------------------------------- */
+
+/* Three-valued clause outcome; with NONE < SOME < ALL a conjunction is the
+ * minimum and a disjunction the maximum. */
+enum { TV_NONE = 0, TV_SOME = 1, TV_ALL = 2 };
+
+typedef struct { int64_t cnt, pmin, pmax, tmin, tmax; } orc_box;
+
+static int tv_min(int a, int b) { return a < b ? a : b; }
+
+static int tv_causal(const orc_box* q, const orc_box* k) { /* p_j <= p_i */
+  if (k->pmax <= q->pmin) return TV_ALL;
+  if (k->pmin > q->pmax) return TV_NONE;
+  return TV_SOME;
+}
+static int tv_window(const orc_box* q, const orc_box* k, int64_t W) { /* p_i - p_j < W */
+  if (q->pmax - k->pmin < W) return TV_ALL;
+  if (q->pmin - k->pmax >= W) return TV_NONE;
+  return TV_SOME;
+}
+static int tv_delay(const orc_box* q, const orc_box* k, int64_t delta) { /* t_j <= t_i - delta */
+  if ((__int128)k->tmax <= (__int128)q->tmin - delta) return TV_ALL;
+  if ((__int128)k->tmin > (__int128)q->tmax - delta) return TV_NONE;
+  return TV_SOME;
+}
+static int tv_before(const orc_box* q, const orc_box* k) { /* t_j < t_i */
+  if (k->tmax < q->tmin) return TV_ALL;
+  if (k->tmin >= q->tmax) return TV_NONE;
+  return TV_SOME;
+}
+static int tv_diag(const orc_box* q, const orc_box* k) { /* i == j; never ALL */
+  if (k->pmax < q->pmin || k->pmin > q->pmax) return TV_NONE;
+  return TV_SOME;
+}
+
+static int tv_pair(const orc_params* p, int tq, int tk, const orc_box* q, const orc_box* k) {
+  int v;
+  if (is_user(tq) && is_user(tk)) {
+    if (p->hist_bidirectional) v = TV_ALL;
+    else {
+      v = tv_causal(q, k);
+      if (p->window > 0 && tq != TY_GLOBAL && tk != TY_GLOBAL) v = tv_min(v, tv_window(q, k, p->window));
+    }
+  } else if (is_user(tq)) v = TV_NONE;
+  else if (tq == TY_RT) v = is_user(tk) ? TV_ALL : (tk == TY_RT ? tv_causal(q, k) : TV_NONE);
+  else v = is_user(tk) ? TV_ALL : (tk == TY_RT ? tv_before(q, k) : tv_diag(q, k));
+  /* candidate -> candidate is its own diagonal, exempt from the delay */
+  if (p->use_delay && !(tq == TY_CAND && tk == TY_CAND)) v = tv_min(v, tv_delay(q, k, p->delay_s));
+  return v;
+}
+
+static void tile_boxes(int64_t base, int64_t L, int64_t tile, const int64_t* t,
+                       const int8_t* ty, orc_box box[4]) {
+  for (int c = 0; c < 4; ++c) {
+    box[c].cnt = 0; box[c].pmin = INT64_MAX; box[c].pmax = INT64_MIN;
+    box[c].tmin = INT64_MAX; box[c].tmax = INT64_MIN;
+  }
+  for (int64_t i = tile * ORC_TILE; i < L && i < (tile + 1) * ORC_TILE; ++i) {
+    int c = ty[base + i];
+    if (c < 0 || c > 3) continue;
+    int64_t tt = t[base + i];
+    box[c].cnt++;
+    if (i < box[c].pmin) box[c].pmin = i;
+    if (i > box[c].pmax) box[c].pmax = i;
+    if (tt < box[c].tmin) box[c].tmin = tt;
+    if (tt > box[c].tmax) box[c].tmax = tt;
+  }
+}
+
+int64_t orc_tile_classes(const orc_params* p, int32_t B, const int64_t* offsets,
+                         const int64_t* t, const int8_t* ty, uint8_t* cls) {
+  int64_t n = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t base = offsets[b], L = offsets[b + 1] - base;
+    const int64_t nt = (L + ORC_TILE - 1) / ORC_TILE;
+    for (int64_t qt = 0; qt < nt; ++qt) {
+      orc_box qb[4];
+      tile_boxes(base, L, qt, t, ty, qb);
+      for (int64_t kt = 0; kt < nt; ++kt) {
+        orc_box kb[4];
+        tile_boxes(base, L, kt, t, ty, kb);
+        int lo = TV_ALL, hi = TV_NONE;
+        for (int a = 0; a < 4; ++a) {
+          if (!qb[a].cnt) continue;
+          for (int c = 0; c < 4; ++c) {
+            if (!kb[c].cnt) continue;
+            int v = tv_pair(p, a, c, &qb[a], &kb[c]);
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+          }
+        }
+        const int k_full = (kt + 1) * ORC_TILE <= L;
+        uint8_t c;
+        if (hi == TV_NONE) c = ORC_SKIP;            /* every present type pair sees nothing */
+        else if (lo == TV_ALL && k_full) c = ORC_FULL; /* every pair visible, no ragged keys */
+        else c = ORC_PARTIAL;
+        if (cls) cls[n] = c;
+        ++n;
+      }
+    }
+  }
+  return n;
+}

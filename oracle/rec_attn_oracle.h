@@ -1,0 +1,59 @@
+/*
+ * rec_attn_oracle.h -- interface of the fp64 CPU oracle (test infrastructure only).
+ * Private to oracle/: the CUDA library has its own, unrelated header.
+ */
+#ifndef REC_ATTN_ORACLE_H
+#define REC_ATTN_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_BF16 = 0, ORC_FP32 = 1 };
+enum { ORC_SKIP = 0, ORC_PARTIAL = 1, ORC_FULL = 2 };
+#define ORC_TILE 128
+
+typedef struct {
+  int32_t num_heads;
+  int32_t head_dim;
+  int32_t use_delay;
+  int64_t delay_s;            /* delta_delay >= 0, seconds */
+  int32_t window;             /* 0 = no window */
+  int32_t hist_bidirectional; /* 1 = GLOBAL/HIST fully mutually visible */
+  int32_t use_rope;
+  double phi_min;             /* rad turned by the slowest pair over dt_max */
+  double dt_max_s;            /* seconds */
+  double rope_base;
+  double softmax_scale;       /* <= 0 means 1/sqrt(head_dim) */
+} orc_params;
+
+/* vis(i, j) for two tokens of one request (positions are request-local). */
+int orc_visible(const orc_params* p, int64_t pi, int64_t ti, int ty_i,
+                int64_t pj, int64_t tj, int ty_j);
+/* L x L mask of one request, row-major, 1 = visible. */
+void orc_mask(const orc_params* p, int64_t L, const int64_t* t, const int8_t* ty, uint8_t* out);
+/* Exact number of visible (query, key) pairs over the batch (per head). */
+uint64_t orc_visible_pairs(const orc_params* p, int32_t B, const int64_t* offsets,
+                           const int64_t* t, const int8_t* ty);
+/* Rotate one head vector x[0..head_dim) at absolute time t into y. */
+void orc_rope(const orc_params* p, int64_t t, const double* x, double* y);
+/* Attention outputs for the sorted global rows `rows` (NULL = all tokens):
+ * out[n_rows][H][d], lse[n_rows][H] (natural log; -inf for a row with no
+ * visible key).  q, k, v are [T][H][d] in dtype (bf16 bits or fp32).
+ * Returns 0, or a negative value on invalid arguments. */
+int orc_attention(const orc_params* p, int32_t B, const int64_t* offsets,
+                  const int64_t* t, const int8_t* ty, int32_t dtype,
+                  const void* q, const void* k, const void* v,
+                  int64_t n_rows, const int64_t* rows, double* out, double* lse,
+                  int32_t n_threads);
+/* Tile classes (SKIP/PARTIAL/FULL) of every (q-tile, k-tile) pair of every
+ * request, request-major then q-tile then k-tile; returns the count written.
+ * cls may be NULL to query the count. */
+int64_t orc_tile_classes(const orc_params* p, int32_t B, const int64_t* offsets,
+                         const int64_t* t, const int8_t* ty, uint8_t* cls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
