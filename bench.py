@@ -1,0 +1,376 @@
+"""Benchmark of the masked time-RoPE attention forward on GB300.
+
+One step = the whole hot path over one batch: plan (tile statistics, tile
+classes, key-tile lists, schedule), time-RoPE prologue, fused masked attention,
+plan release.  Default workload: CADET-style impression/action sequences, B=256
+requests x 512 tokens, H=4, d=64, bf16, causal + 1 h delay mask, time-RoPE.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line.  `value` is TFLOP/s counted over visible (query, key) pairs
+(4 * d * H per pair) for the whole step, inputs resident in HBM; L2 is flushed
+between timed steps.  `--impl reference` times the fp64 CPU oracle on the host
+cores instead (a bounded sample of the same workload per step).
+Under torchrun each rank runs its own batch of the same shape (weak scaling); the
+reported value is the total work of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from generative_recommender_ranking_gb300 import workloads as W  # noqa: E402
+
+METRIC = "masked-attn fwd TFLOP/s over visible pairs, % of GB300 bf16 peak; tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def _workload(name, rank):
+    seed_kw = {}
+    if rank:
+        base = {"tiny_fp32": 1001, "cadet": 1002, "sort": 1003, "mtgr": 1004}.get(name, 1005)
+        seed_kw["seed"] = base + 7919 * rank
+    return W.make(name, **seed_kw)
+
+
+def _config(w: W.Workload, name: str, parallelism: str):
+    lens = np.diff(w.offsets)
+    return {"workload": name, "batch": w.batch, "tokens": w.total_tokens,
+            "seq_len_mean": float(lens.mean()) if len(lens) else 0.0, "seq_len_max": int(lens.max()),
+            "heads": w.num_heads, "head_dim": w.head_dim, "mask": w.mask,
+            "time_rope": {k: v for k, v in w.rope.items()}, "parallelism": parallelism,
+            "l2": "flushed between timed steps (256 MiB write)"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}",
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[4:8]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _oracle_sample(w: W.Workload, budget_s: float):
+    """Time the fp64 oracle on the first requests of the workload (all heads)
+    until about `budget_s` seconds of work; returns (seconds, visible pairs, requests)."""
+    import oracle
+    oracle.build()
+    p = oracle.Params(w.num_heads, w.head_dim, **w.mask, **w.rope)
+    threads = os.cpu_count() or 1
+    done, secs, pairs = 0, 0.0, 0
+    chunk = 1
+    while done < w.batch and secs < budget_s:
+        n = min(chunk, w.batch - done)
+        s, e = int(w.offsets[done]), int(w.offsets[done + n])
+        off = w.offsets[done:done + n + 1] - s
+        sl = slice(s, e)
+        t0 = time.perf_counter()
+        oracle.attention(p, off, w.t[sl], w.types[sl], w.q[sl], w.k[sl], w.v[sl], threads=threads)
+        secs += time.perf_counter() - t0
+        pairs += oracle.visible_pairs(p, off, w.t[sl], w.types[sl])
+        done += n
+        chunk *= 2
+    return secs, pairs, done, threads
+
+
+def run_reference(args):
+    """--impl reference: the fp64 CPU oracle on the host cores, same metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    w = _workload(args.workload, 0)
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_sample(w, per_step / 4)
+    tot_s, tot_pairs, reqs = 0.0, 0, []
+    threads = 1
+    for _ in range(args.steps):
+        s, pairs, n, threads = _oracle_sample(w, per_step)
+        tot_s += s
+        tot_pairs += pairs
+        reqs.append(n)
+    flops = 4.0 * w.head_dim * w.num_heads * tot_pairs
+    value = flops / tot_s / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_s / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, args.workload, "host cores"),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"first {min(reqs)}-{max(reqs)} of {w.batch} requests per step, all heads"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from generative_recommender_ranking_gb300 import binding as bd
+    from generative_recommender_ranking_gb300 import build as bld
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    if rank == 0 or world == 1:
+        bld.build()
+    if world > 1:
+        dist.barrier()
+
+    w = _workload(args.workload, rank)
+    bf16 = w.dtype == "bf16"
+    elem = 2 if bf16 else 4
+
+    def host(a):
+        t = torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a))
+        return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
+
+    hq, hk, hv = (host(a).pin_memory() for a in (w.q, w.k, w.v))
+    ht = torch.from_numpy(np.ascontiguousarray(w.t)).pin_memory()
+    hty = torch.from_numpy(np.ascontiguousarray(w.types)).pin_memory()
+    hoff = torch.from_numpy(np.ascontiguousarray(w.offsets)).pin_memory()
+    q, k, v = (x.to(dev) for x in (hq, hk, hv))
+    t, ty, off_d = ht.to(dev), hty.to(dev), hoff.to(dev)
+    out = torch.empty_like(q)
+    off_h = np.ascontiguousarray(w.offsets)
+    params = bd.make_params(w.num_heads, w.head_dim, dtype=w.dtype, **w.mask, **w.rope)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    # exact visible pairs (FLOP accounting) from the library's own counter
+    plan = bd.rec_attn_plan(params, off_h, off_d, t, ty)
+    pairs = bd.rec_attn_visible_pairs(plan)
+    cls = bd.rec_attn_tile_classes(plan)
+    bd.rec_attn_free(plan)
+    flops = 4.0 * w.head_dim * w.num_heads * pairs
+    tokens = w.total_tokens
+
+    def step(timed=False):
+        p = bd.rec_attn_plan(params, off_h, off_d, t, ty, stream)
+        if timed:
+            bd.rec_attn_enable_timing(p)
+        bd.rec_attn_fwd(p, q, k, v, out, None, stream)
+        return p
+
+    # grow the library's workspace pool to K live plans first, so no timed step
+    # waits on a driver allocation
+    pre = [bd.rec_attn_plan(params, off_h, off_d, t, ty, stream) for _ in range(args.steps)]
+    for p_ in pre:
+        bd.rec_attn_free(p_)
+    for _ in range(max(args.warmup, 3)):
+        bd.rec_attn_free(step())
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, each bracketed by CUDA events on the launch stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    plans = []
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        p = step(timed=True)
+        ev[i][1].record(stream)
+        plans.append(p)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kt = [bd.rec_attn_read_timings(p) for p in plans]
+    status = max(bd.rec_attn_device_status(p) for p in plans)
+    for p in plans:
+        bd.rec_attn_free(p)
+    if status != bd.OK:
+        raise RuntimeError(f"device status {status}: {bd.rec_attn_status_string(status)}")
+    total_ms = float(sum(step_ms))
+    attn_ms = statistics.mean(x[1] for x in kt)
+    rope_ms = statistics.mean(x[0] for x in kt)
+
+    # ---- end to end through the C-ABI with host buffers (H2D inputs, D2H output)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dt, dty, doff = torch.empty_like(t), torch.empty_like(ty), torch.empty_like(off_d)
+    for i in range(args.steps + 1):
+        flush.zero_()
+        if i > 0:
+            e2e_ev[i - 1][0].record(stream)
+        for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (dt, ht), (dty, hty), (doff, hoff)):
+            d_.copy_(h_, non_blocking=True)
+        p = bd.rec_attn_plan(params, off_h, doff, dt, dty, stream)
+        bd.rec_attn_fwd(p, dq, dk, dv, out, None, stream)
+        hout.copy_(out, non_blocking=True)
+        if i > 0:
+            e2e_ev[i - 1][1].record(stream)
+        bd.rec_attn_free(p)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, ht, hty, hoff))
+    d2h = hout.numel() * hout.element_size()
+
+    # max over ranks
+    tot = torch.tensor([total_ms, e2e_ms, attn_ms], dtype=torch.float64, device=dev)
+    work = torch.tensor([flops, float(tokens)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
+        dist.all_reduce(work, op=dist.ReduceOp.SUM)
+    total_ms, e2e_ms, attn_max = tot.tolist()
+    all_flops, all_tokens = work.tolist()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    pk = _peaks()
+    ms_step = total_ms / args.steps
+    value = all_flops * args.steps / (total_ms * 1e-3) / 1e12
+    bytes_attn = 4.0 * tokens * w.num_heads * w.head_dim * elem + 9.0 * tokens
+    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    attn_gbs = bytes_attn / (attn_ms * 1e-3) / 1e9
+    hbm_bound = (flops / bytes_attn) < (pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9))
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": attn_gbs / pk["hbm_gbs"], "traffic": None,
+                "kernel": "k_attn_tc (masked softmax attention)", "peak_source": pk["source"],
+                "algorithmic_bytes_per_launch": bytes_attn, "ms_per_launch": attn_ms}
+    else:
+        roof = {"bound": "tensor", "achieved": attn_tflops, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": attn_tflops / pk["bf16_tflops"], "traffic": None,
+                "kernel": "k_attn_tc (masked softmax attention)", "peak_source": pk["source"],
+                "algorithmic_flops_per_launch": flops, "ms_per_launch": attn_ms}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "fp32",
+        "data": "synthetic (seeded generators standing in for the pages' private logs)",
+        "config": _config(w, args.workload, f"dp{world} (requests sharded, no collective)"),
+        "tokens_per_s": all_tokens * args.steps / (total_ms * 1e-3),
+        "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
+        "visible_pairs_per_head": pairs,
+        "tile_classes": {"skip": int((cls == 0).sum()), "partial": int((cls == 1).sum()),
+                         "full": int((cls == 2).sum())},
+        "kernel_ms": {"attention": attn_ms, "rope": rope_ms, "plan_and_overhead": ms_step - attn_ms - rope_ms},
+        "fwd_only_tflops": flops / ((attn_ms + rope_ms) * 1e-3) / 1e12,
+        "roofline": roof,
+        "e2e": {"value": all_flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        secs, cpairs, nreq, threads = _oracle_sample(w, args.cpu_budget)
+        cval = 4.0 * w.head_dim * w.num_heads * cpairs / secs / 1e12
+        line["cpu_baseline"] = {"value": cval, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"first {nreq} of {w.batch} requests, all heads ({secs:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="cadet", choices=W.NAMES)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

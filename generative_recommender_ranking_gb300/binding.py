@@ -1,0 +1,204 @@
+"""ctypes binding of librec_attn.so with the C-ABI's names (include/rec_attn.h).
+
+Argument marshalling only: tensors are passed as raw device pointers, streams as
+raw cudaStream_t handles.  Every step of the computation runs in the library's
+CUDA kernels; there is no CPU fallback.  If the library has not been built,
+loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "librec_attn.so")
+
+ABI_VERSION = 1
+TILE = 128
+MAX_REQUEST_LEN = 262144
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_DEVICE_INPUT = range(7)
+BF16, FP32 = 0, 1
+GLOBAL, HIST, RT, CAND = 0, 1, 2, 3
+TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
+
+
+class RecAttnParams(ctypes.Structure):
+    _fields_ = [
+        ("abi_version", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("use_delay", ctypes.c_int32),
+        ("delay_s", ctypes.c_int64),
+        ("window", ctypes.c_int32),
+        ("hist_bidirectional", ctypes.c_int32),
+        ("use_rope", ctypes.c_int32),
+        ("phi_min", ctypes.c_double),
+        ("dt_max_s", ctypes.c_double),
+        ("rope_base", ctypes.c_double),
+        ("softmax_scale", ctypes.c_float),
+    ]
+
+
+class RecAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn}: {rec_attn_status_string(code)} (status {code})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load librec_attn.so (raises OSError if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise OSError(f"{_LIB_PATH} not found: build it with "
+                          "python -m generative_recommender_ranking_gb300.build")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.rec_attn_plan.argtypes = [ctypes.POINTER(RecAttnParams), i32, vp, vp, vp, vp, vp,
+                                    ctypes.POINTER(vp)]
+        L.rec_attn_plan.restype = ctypes.c_int
+        L.rec_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.rec_attn_fwd.restype = ctypes.c_int
+        L.rec_attn_free.argtypes = [vp]
+        L.rec_attn_free.restype = None
+        L.rec_attn_tile_classes.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
+        L.rec_attn_tile_classes.restype = ctypes.c_int
+        L.rec_attn_visible_pairs.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
+        L.rec_attn_visible_pairs.restype = ctypes.c_int
+        L.rec_attn_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+        L.rec_attn_device_status.restype = ctypes.c_int
+        L.rec_attn_status_string.argtypes = [ctypes.c_int]
+        L.rec_attn_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def make_params(num_heads: int, head_dim: int, dtype: str = "bf16", use_delay: bool = False,
+                delay_s: int = 0, window: int = 0, hist_bidirectional: bool = False,
+                use_rope: bool = True, phi_min: float = 1e-4, dt_max_s: float = 365.0 * 86400.0,
+                rope_base: float = 6e5, softmax_scale: float = 0.0) -> RecAttnParams:
+    return RecAttnParams(ABI_VERSION, int(num_heads), int(head_dim), BF16 if dtype == "bf16" else FP32,
+                         int(bool(use_delay)), int(delay_s), int(window), int(bool(hist_bidirectional)),
+                         int(bool(use_rope)), float(phi_min), float(dt_max_s), float(rope_base),
+                         float(softmax_scale))
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()  # torch.Tensor
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, code: int):
+    if code != OK:
+        raise RecAttnError(fn, code)
+
+
+@dataclass
+class Plan:
+    handle: int
+    batch: int
+    total_tokens: int
+    # keep the device arrays the plan reads alive for as long as the plan
+    _keep: tuple = ()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        rec_attn_free(self)
+
+
+def rec_attn_status_string(code: int) -> str:
+    return lib().rec_attn_status_string(int(code)).decode()
+
+
+def rec_attn_plan(params: RecAttnParams, offsets_host, offsets_dev, timestamps_dev, types_dev,
+                  stream=None) -> Plan:
+    """Plan a packed batch.  offsets_host: host int64 [B+1] (numpy or CPU tensor);
+    offsets_dev / timestamps_dev: device int64; types_dev: device int8."""
+    off_h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int64))
+    B = len(off_h) - 1
+    h = ctypes.c_void_p()
+    code = lib().rec_attn_plan(ctypes.byref(params), B, _ptr(off_h), _ptr(offsets_dev),
+                               _ptr(timestamps_dev), _ptr(types_dev), _stream(stream), ctypes.byref(h))
+    _check("rec_attn_plan", code)
+    return Plan(h.value, B, int(off_h[-1]) if B > 0 else 0, (offsets_dev, timestamps_dev, types_dev))
+
+
+def rec_attn_fwd(plan: Plan, q, k, v, out, lse=None, stream=None) -> None:
+    code = lib().rec_attn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                              _stream(stream))
+    _check("rec_attn_fwd", code)
+
+
+def rec_attn_free(plan: Plan) -> None:
+    if plan is not None and plan.handle:
+        lib().rec_attn_free(plan.handle)
+        plan.handle = 0
+
+
+def rec_attn_tile_classes(plan: Plan) -> np.ndarray:
+    n = ctypes.c_size_t()
+    _check("rec_attn_tile_classes", lib().rec_attn_tile_classes(plan.handle, None, 0, ctypes.byref(n)))
+    out = np.zeros(max(n.value, 1), dtype=np.uint8)
+    _check("rec_attn_tile_classes",
+           lib().rec_attn_tile_classes(plan.handle, out.ctypes.data, out.size, ctypes.byref(n)))
+    return out[:n.value]
+
+
+def rec_attn_visible_pairs(plan: Plan) -> int:
+    n = ctypes.c_uint64()
+    _check("rec_attn_visible_pairs", lib().rec_attn_visible_pairs(plan.handle, ctypes.byref(n)))
+    return int(n.value)
+
+
+def rec_attn_device_status(plan: Plan) -> int:
+    s = ctypes.c_int32()
+    _check("rec_attn_device_status", lib().rec_attn_device_status(plan.handle, ctypes.byref(s)))
+    return int(s.value)
+
+
+class RecAttnTimings(ctypes.Structure):
+    _fields_ = [("rope_ms", ctypes.c_float), ("attn_ms", ctypes.c_float)]
+
+
+def rec_attn_enable_timing(plan: Plan) -> None:
+    L = lib()
+    L.rec_attn_enable_timing.argtypes = [ctypes.c_void_p]
+    L.rec_attn_enable_timing.restype = ctypes.c_int
+    _check("rec_attn_enable_timing", L.rec_attn_enable_timing(plan.handle))
+
+
+def rec_attn_read_timings(plan: Plan) -> tuple[float, float]:
+    """(rope_ms, attn_ms) of the last timed rec_attn_fwd."""
+    L = lib()
+    L.rec_attn_read_timings.argtypes = [ctypes.c_void_p, ctypes.POINTER(RecAttnTimings)]
+    L.rec_attn_read_timings.restype = ctypes.c_int
+    t = RecAttnTimings()
+    _check("rec_attn_read_timings", L.rec_attn_read_timings(plan.handle, ctypes.byref(t)))
+    return float(t.rope_ms), float(t.attn_ms)

@@ -1,0 +1,402 @@
+// api.cu -- host side of the C-ABI declared in include/rec_attn.h: argument
+// validation (always before any CUDA call, so bad arguments never launch work),
+// plan ownership, stream-ordered workspace from a library-owned memory pool, TMA
+// descriptor encoding and kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "launchers.cuh"
+#include "rec_attn.h"
+
+#define REC_ATTN_API extern "C" __attribute__((visibility("default")))
+
+using namespace recattn;
+
+struct rec_attn_plan_s {
+  rec_attn_params p;
+  int device = 0;
+  int num_sms = 0;
+  int32_t batch = 0;
+  long long T = 0, NT = 0, NC = 0;
+  cudaStream_t stream = nullptr;  // stream of the last use
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  PlanDev pd{};
+  void* qrot = nullptr;
+  void* krot = nullptr;
+  const long long* t = nullptr;
+  const int8_t* ty = nullptr;
+  MaskP mask{};
+  float omega[kMaxPairs] = {};
+  // cached TMA descriptors for the last (q', k', v) pointers
+  const void* map_src[3] = {nullptr, nullptr, nullptr};
+  CUtensorMap maps[3];
+  // optional kernel timing: events around the RoPE prologue and the attention kernel
+  bool timing = false;
+  bool timed = false;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+};
+
+namespace {
+
+std::mutex g_pool_mu;
+std::map<int, cudaMemPool_t> g_pools;
+
+rec_attn_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return REC_ATTN_OK;
+  if (e == cudaErrorMemoryAllocation) return REC_ATTN_ERR_OOM;
+  return REC_ATTN_ERR_CUDA;
+}
+
+// Library-owned pool per device; it keeps freed blocks so repeated plan/free cycles
+// do not return to the driver.
+cudaError_t pool_for(int device, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  auto it = g_pools.find(device);
+  if (it != g_pools.end()) { *out = it->second; return cudaSuccess; }
+  cudaMemPoolProps props;
+  std::memset(&props, 0, sizeof props);
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = device;
+  cudaMemPool_t pool;
+  cudaError_t e = cudaMemPoolCreate(&pool, &props);
+  if (e != cudaSuccess) return e;
+  uint64_t keep = ~0ull;
+  e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  if (e != cudaSuccess) return e;
+  g_pools[device] = pool;
+  *out = pool;
+  return cudaSuccess;
+}
+
+rec_attn_status check_params(const rec_attn_params* p) {
+  if (!p) return REC_ATTN_ERR_INVALID_ARG;
+  if (p->abi_version != REC_ATTN_ABI_VERSION) return REC_ATTN_ERR_INVALID_ARG;
+  if (p->num_heads < 1 || p->head_dim < 2 || (p->head_dim & 1)) return REC_ATTN_ERR_INVALID_ARG;
+  if (p->dtype != REC_ATTN_BF16 && p->dtype != REC_ATTN_FP32) return REC_ATTN_ERR_INVALID_ARG;
+  if ((p->use_delay != 0 && p->use_delay != 1) || (p->use_rope != 0 && p->use_rope != 1) ||
+      (p->hist_bidirectional != 0 && p->hist_bidirectional != 1))
+    return REC_ATTN_ERR_INVALID_ARG;
+  if (p->delay_s < 0 || p->delay_s > (1LL << 62) || p->window < 0) return REC_ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(p->softmax_scale) && p->softmax_scale >= 0.f)) return REC_ATTN_ERR_INVALID_ARG;
+  if (p->use_rope) {
+    if (!(std::isfinite(p->phi_min) && std::isfinite(p->dt_max_s) && std::isfinite(p->rope_base)))
+      return REC_ATTN_ERR_INVALID_ARG;
+    if (p->dt_max_s <= 0.0 || p->rope_base <= 0.0) return REC_ATTN_ERR_INVALID_ARG;
+  }
+  if (p->dtype == REC_ATTN_BF16 && p->head_dim != 64 && p->head_dim != 128) return REC_ATTN_ERR_UNSUPPORTED;
+  if (p->dtype == REC_ATTN_FP32 && p->head_dim != 32 && p->head_dim != 64) return REC_ATTN_ERR_UNSUPPORTED;
+  // TMA rows of the [T][H*d] bf16 view must stay below 2^32 elements per dimension
+  if ((long long)p->num_heads * p->head_dim > (1LL << 20)) return REC_ATTN_ERR_UNSUPPORTED;
+  return REC_ATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a [T][H*d] bf16 tensor; box = 64 columns x 128 rows, 128-byte swizzle.
+bool encode_map(CUtensorMap* m, const void* base, long long T, long long cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)T};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Closes the attention kernel's timing window: events 0..1 bracket the RoPE
+// prologue, events 2..3 the attention kernel.
+rec_attn_status finish_timing(rec_attn_plan_s* plan, cudaStream_t st, cudaError_t launch_err) {
+  if (launch_err != cudaSuccess) return from_cuda(launch_err);
+  if (!plan->timing) return REC_ATTN_OK;
+  cudaError_t e = cudaEventRecord(plan->ev[3], st);
+  if (e != cudaSuccess) return from_cuda(e);
+  plan->timed = true;
+  return REC_ATTN_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const char* x = static_cast<const char*>(a);
+  const char* y = static_cast<const char*>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+REC_ATTN_API const char* rec_attn_status_string(rec_attn_status s) {
+  switch (s) {
+    case REC_ATTN_OK: return "ok";
+    case REC_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case REC_ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case REC_ATTN_ERR_CUDA: return "CUDA runtime error";
+    case REC_ATTN_ERR_OOM: return "out of device memory";
+    case REC_ATTN_ERR_TIMEOUT: return "device wait timed out";
+    case REC_ATTN_ERR_DEVICE_INPUT: return "device input out of range (token type, timestamp or offsets)";
+  }
+  return "unknown status";
+}
+
+REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_t batch,
+                                           const int64_t* offsets_host, const int64_t* offsets_dev,
+                                           const int64_t* timestamps_dev, const int8_t* types_dev, void* stream,
+                                           rec_attn_plan_t** plan_out) {
+  if (!plan_out) return REC_ATTN_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  rec_attn_status st = check_params(params);
+  if (st != REC_ATTN_OK) return st;
+  if (batch < 0 || (batch > 0 && !offsets_host)) return REC_ATTN_ERR_INVALID_ARG;
+  std::vector<ReqMeta> meta((size_t)batch);
+  long long NT = 0, NC = 0, T = 0;
+  if (batch > 0) {
+    if (offsets_host[0] != 0) return REC_ATTN_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < batch; ++b) {
+      const long long len = offsets_host[b + 1] - offsets_host[b];
+      if (len < 0) return REC_ATTN_ERR_INVALID_ARG;
+      if (len > REC_ATTN_MAX_REQUEST_LEN) return REC_ATTN_ERR_UNSUPPORTED;
+      ReqMeta& m = meta[b];
+      m.tok_start = offsets_host[b];
+      m.len = (int)len;
+      m.ntiles = (int)((len + kTile - 1) / kTile);
+      m.tile_start = NT;
+      m.cls_start = NC;
+      NT += m.ntiles;
+      NC += (long long)m.ntiles * m.ntiles;
+    }
+    T = offsets_host[batch];
+    if (T >= (1LL << 31)) return REC_ATTN_ERR_UNSUPPORTED;
+    if (!offsets_dev || (T > 0 && (!timestamps_dev || !types_dev))) return REC_ATTN_ERR_INVALID_ARG;
+  }
+
+  rec_attn_plan_s* plan = new (std::nothrow) rec_attn_plan_s();
+  if (!plan) return REC_ATTN_ERR_OOM;
+  plan->p = *params;
+  if (plan->p.softmax_scale == 0.f) plan->p.softmax_scale = 1.f / std::sqrt((float)params->head_dim);
+  plan->batch = batch;
+  plan->T = T; plan->NT = NT; plan->NC = NC;
+  plan->stream = static_cast<cudaStream_t>(stream);
+  plan->t = reinterpret_cast<const long long*>(timestamps_dev);
+  plan->ty = types_dev;
+  plan->mask.use_delay = params->use_delay;
+  plan->mask.delay = params->use_delay ? params->delay_s : 0;
+  plan->mask.window = params->window;
+  plan->mask.bidir = params->hist_bidirectional;
+  if (params->use_rope)
+    for (int i = 0; i < params->head_dim / 2 && i < kMaxPairs; ++i)
+      plan->omega[i] = (float)(params->phi_min / params->dt_max_s *
+                               std::pow(params->rope_base, 2.0 * i / (double)params->head_dim));
+
+  cudaError_t e = cudaGetDevice(&plan->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, plan->device);
+  if (e != cudaSuccess) { delete plan; return from_cuda(e); }
+
+  // workspace layout
+  const size_t elem = params->dtype == REC_ATTN_BF16 ? 2 : 4;
+  const size_t qk_bytes = (size_t)T * params->num_heads * params->head_dim * elem;
+  size_t off = 0;
+  const size_t o_hdr = off; off = align256(off + 256);
+  const size_t o_meta = off; off = align256(off + sizeof(ReqMeta) * (size_t)batch);
+  const size_t o_box = off; off = align256(off + sizeof(TileBox) * kTypes * (size_t)NT);
+  const size_t o_cls = off; off = align256(off + (size_t)NC);
+  const size_t o_kl = off; off = align256(off + 4 * (size_t)NC);
+  const size_t o_kc = off; off = align256(off + 4 * (size_t)NT);
+  const size_t o_qc = off; off = align256(off + 4 * (size_t)NT);
+  const size_t o_qr = off; off = align256(off + 4 * (size_t)NT);
+  const size_t o_qo = off; off = align256(off + 4 * (size_t)NT);
+  const size_t o_rq = off; off = align256(off + (params->use_rope ? qk_bytes : 0));
+  const size_t o_rk = off; off = align256(off + (params->use_rope ? qk_bytes : 0));
+  plan->ws_bytes = off;
+
+  cudaMemPool_t pool;
+  e = pool_for(plan->device, &pool);
+  if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&plan->ws, plan->ws_bytes, pool, plan->stream);
+  if (e != cudaSuccess) { delete plan; return from_cuda(e); }
+  char* w = static_cast<char*>(plan->ws);
+  PlanDev& pd = plan->pd;
+  pd.counters = reinterpret_cast<int*>(w + o_hdr);
+  pd.status = pd.counters + 8;
+  pd.pairs = reinterpret_cast<unsigned long long*>(w + o_hdr + 64);
+  pd.meta = reinterpret_cast<ReqMeta*>(w + o_meta);
+  pd.boxes = reinterpret_cast<TileBox*>(w + o_box);
+  pd.cls = reinterpret_cast<uint8_t*>(w + o_cls);
+  pd.klist = reinterpret_cast<uint32_t*>(w + o_kl);
+  pd.kcount = reinterpret_cast<int*>(w + o_kc);
+  pd.qcost = reinterpret_cast<int*>(w + o_qc);
+  pd.qreq = reinterpret_cast<int*>(w + o_qr);
+  pd.qorder = reinterpret_cast<int*>(w + o_qo);
+  plan->qrot = params->use_rope ? w + o_rq : nullptr;
+  plan->krot = params->use_rope ? w + o_rk : nullptr;
+
+  e = cudaMemsetAsync(w + o_hdr, 0, 256, plan->stream);
+  if (e == cudaSuccess && batch > 0)
+    e = cudaMemcpyAsync(pd.meta, meta.data(), sizeof(ReqMeta) * (size_t)batch, cudaMemcpyHostToDevice, plan->stream);
+  if (e == cudaSuccess)
+    e = launch_plan(plan->mask, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t, plan->ty, batch, NT,
+                    plan->stream);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(plan->ws, plan->stream);
+    delete plan;
+    return from_cuda(e);
+  }
+  *plan_out = plan;
+  return REC_ATTN_OK;
+}
+
+REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                                          void* out, float* lse, void* stream) {
+  if (!plan) return REC_ATTN_ERR_INVALID_ARG;
+  const rec_attn_params& p = plan->p;
+  const long long T = plan->T;
+  if (T > 0) {
+    if (!q || !k || !v || !out) return REC_ATTN_ERR_INVALID_ARG;
+    const void* ptrs[4] = {q, k, v, out};
+    for (const void* x : ptrs)
+      if (reinterpret_cast<uintptr_t>(x) & 15u) return REC_ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return REC_ATTN_ERR_INVALID_ARG;
+    const size_t elem = p.dtype == REC_ATTN_BF16 ? 2 : 4;
+    const size_t bytes = (size_t)T * p.num_heads * p.head_dim * elem;
+    if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) || overlaps(out, bytes, v, bytes))
+      return REC_ATTN_ERR_INVALID_ARG;
+    if (lse && (overlaps(lse, (size_t)T * p.num_heads * 4, out, bytes)))
+      return REC_ATTN_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (dev != plan->device) return REC_ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  plan->stream = st;
+  if (T == 0) return REC_ATTN_OK;
+
+  const void* qs = q;
+  const void* ks = k;
+  if (plan->timing) {
+    plan->timed = false;
+    e = cudaEventRecord(plan->ev[0], st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  if (p.use_rope) {
+    RopeArgs ra;
+    ra.meta = plan->pd.meta; ra.qreq = plan->pd.qreq; ra.t = plan->t;
+    ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
+    ra.heads = p.num_heads; ra.head_dim = p.head_dim;
+    std::memcpy(ra.omega, plan->omega, sizeof ra.omega);
+    e = launch_rope(ra, p.dtype, plan->NT, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    qs = plan->qrot; ks = plan->krot;
+  }
+  if (plan->timing) {
+    e = cudaEventRecord(plan->ev[1], st);
+    if (e == cudaSuccess) e = cudaEventRecord(plan->ev[2], st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  AttnArgs a;
+  a.meta = plan->pd.meta; a.qreq = plan->pd.qreq; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
+  a.qorder = plan->pd.qorder; a.t = plan->t; a.ty = plan->ty;
+  a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = plan->pd.status;
+  a.n_items = plan->NT * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale; a.mask = plan->mask;
+  if (p.dtype == REC_ATTN_FP32) {
+    e = launch_attn_simt(a, p.head_dim, st);
+    return finish_timing(plan, st, e);
+  }
+  const void* srcs[3] = {qs, ks, v};
+  const long long cols = (long long)p.num_heads * p.head_dim;
+  for (int i = 0; i < 3; ++i) {
+    if (plan->map_src[i] != srcs[i]) {
+      if (!encode_map(&plan->maps[i], srcs[i], T, cols)) { plan->map_src[i] = nullptr; return REC_ATTN_ERR_CUDA; }
+      plan->map_src[i] = srcs[i];
+    }
+  }
+  const long long items = a.n_items;
+  const int grid = (int)(items < plan->num_sms ? items : plan->num_sms);
+  e = launch_attn_tc(a, plan->maps[0], plan->maps[1], plan->maps[2], p.head_dim, grid, st);
+  return finish_timing(plan, st, e);
+}
+
+REC_ATTN_API void rec_attn_free(rec_attn_plan_t* plan) {
+  if (!plan) return;
+  if (plan->ws) cudaFreeAsync(plan->ws, plan->stream);
+  for (cudaEvent_t ev : plan->ev)
+    if (ev) cudaEventDestroy(ev);
+  delete plan;
+}
+
+REC_ATTN_API rec_attn_status rec_attn_enable_timing(rec_attn_plan_t* plan) {
+  if (!plan) return REC_ATTN_ERR_INVALID_ARG;
+  if (plan->timing) return REC_ATTN_OK;
+  for (cudaEvent_t& ev : plan->ev) {
+    cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  plan->timing = true;
+  return REC_ATTN_OK;
+}
+
+REC_ATTN_API rec_attn_status rec_attn_read_timings(rec_attn_plan_t* plan, rec_attn_timings* out) {
+  if (!plan || !out || !plan->timing || !plan->timed) return REC_ATTN_ERR_INVALID_ARG;
+  cudaError_t e = cudaEventSynchronize(plan->ev[3]);
+  float a = 0.f, b = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&a, plan->ev[0], plan->ev[1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&b, plan->ev[2], plan->ev[3]);
+  if (e != cudaSuccess) return from_cuda(e);
+  out->rope_ms = a;
+  out->attn_ms = b;
+  return REC_ATTN_OK;
+}
+
+REC_ATTN_API rec_attn_status rec_attn_tile_classes(rec_attn_plan_t* plan, uint8_t* host_out, size_t capacity,
+                                                   size_t* n_needed) {
+  if (!plan || !n_needed) return REC_ATTN_ERR_INVALID_ARG;
+  *n_needed = (size_t)plan->NC;
+  if (!host_out) return REC_ATTN_OK;
+  if (capacity < (size_t)plan->NC) return REC_ATTN_ERR_INVALID_ARG;
+  if (plan->NC == 0) return REC_ATTN_OK;
+  cudaError_t e = cudaMemcpyAsync(host_out, plan->pd.cls, (size_t)plan->NC, cudaMemcpyDeviceToHost, plan->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(plan->stream);
+  return from_cuda(e);
+}
+
+REC_ATTN_API rec_attn_status rec_attn_visible_pairs(rec_attn_plan_t* plan, uint64_t* host_out) {
+  if (!plan || !host_out) return REC_ATTN_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(plan->pd.pairs, 0, sizeof(unsigned long long), plan->stream);
+  if (e == cudaSuccess) e = launch_count_pairs(plan->mask, plan->pd, plan->t, plan->ty, plan->NT, plan->stream);
+  unsigned long long n = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&n, plan->pd.pairs, sizeof n, cudaMemcpyDeviceToHost, plan->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(plan->stream);
+  if (e == cudaSuccess) *host_out = n;
+  return from_cuda(e);
+}
+
+REC_ATTN_API rec_attn_status rec_attn_device_status(rec_attn_plan_t* plan, int32_t* status_out) {
+  if (!plan || !status_out) return REC_ATTN_ERR_INVALID_ARG;
+  int s = 0;
+  cudaError_t e = cudaMemcpyAsync(&s, plan->pd.status, sizeof s, cudaMemcpyDeviceToHost, plan->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(plan->stream);
+  if (e == cudaSuccess) *status_out = s;
+  return from_cuda(e);
+}

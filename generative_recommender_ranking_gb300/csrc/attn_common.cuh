@@ -1,0 +1,61 @@
+// attn_common.cuh -- arguments shared by the attention kernels.
+#pragma once
+
+#include "rec_attn_internal.cuh"
+
+namespace recattn {
+
+struct AttnArgs {
+  const ReqMeta* meta;
+  const int* qreq;
+  const int* kcount;
+  const uint32_t* klist;
+  const int* qorder;
+  const long long* t;
+  const int8_t* ty;
+  const void* q;     // rotated (or raw when RoPE is off) queries [T][H][d]
+  const void* k;     // rotated keys
+  const void* v;
+  void* out;
+  float* lse;        // optional [T][H]
+  int* status;
+  long long n_items; // query tiles x heads
+  int heads;
+  float scale;       // softmax scale (natural-log domain)
+  MaskP mask;
+};
+
+// Arguments of the time-RoPE prologue.
+struct RopeArgs {
+  const ReqMeta* meta;
+  const int* qreq;         // request of each global tile
+  const long long* t;
+  const void* q;
+  const void* k;
+  void* qr;                // rotated outputs, same layout [T][H][d]
+  void* kr;
+  int heads, head_dim;
+  float omega[kMaxPairs];  // rad per second, pair i
+};
+
+// One work item: (query tile, head).
+struct WorkItem {
+  ReqMeta m;
+  int qt;            // query tile index inside the request
+  int h;
+  int n;             // non-SKIP key tiles
+  const uint32_t* list;
+};
+
+__device__ __forceinline__ WorkItem decode_item(const AttnArgs& a, long long w, bool ordered) {
+  WorkItem it;
+  const long long qg = ordered ? (long long)a.qorder[w / a.heads] : w / a.heads;
+  it.h = (int)(w % a.heads);
+  it.m = a.meta[a.qreq[qg]];
+  it.qt = (int)(qg - it.m.tile_start);
+  it.n = a.kcount[qg];
+  it.list = a.klist + it.m.cls_start + (long long)it.qt * it.m.ntiles;
+  return it;
+}
+
+}  // namespace recattn

@@ -1,0 +1,292 @@
+// plan.cu -- planning kernels: per-tile type bounding boxes, (query tile, key tile)
+// classification SKIP / PARTIAL / FULL, per-query-tile key-tile lists and a
+// longest-first order of query tiles for the attention scheduler.
+//
+// The tile skipping follows the block-skipping idea of the CADET serving kernel
+// (CADET review page, section on scoring hundreds of candidates in 50 ms) and SORT's
+// "mask preload check" (SORT page, section 4.1): a key tile whose every pair is
+// masked is never loaded, and a tile whose every pair is visible runs without
+// per-element mask evaluation.
+#include "rec_attn_internal.cuh"
+
+namespace recattn {
+
+namespace {
+
+// Three-valued outcome of a mask clause over two bounding boxes.  With
+// NONE < SOME < ALL a conjunction is the minimum.
+enum : int { kNone = 0, kSome = 1, kAll = 2 };
+
+__device__ __forceinline__ int tv_and(int a, int b) { return a < b ? a : b; }
+
+// p_j <= p_i
+__device__ __forceinline__ int tv_causal(const TileBox& q, const TileBox& k) {
+  return k.pmax <= q.pmin ? kAll : (k.pmin > q.pmax ? kNone : kSome);
+}
+// p_i - p_j < W
+__device__ __forceinline__ int tv_window(const TileBox& q, const TileBox& k, int W) {
+  return (q.pmax - k.pmin < W) ? kAll : ((q.pmin - k.pmax >= W) ? kNone : kSome);
+}
+// t_j <= t_i - delta, exact: x <= y - delta  <=>  (y >= MIN + delta) && x <= y - delta
+__device__ __forceinline__ bool le_minus(long long x, long long y, long long delta) {
+  return y >= (long long)(-0x7fffffffffffffffLL - 1) + delta && x <= y - delta;
+}
+__device__ __forceinline__ int tv_delay(const TileBox& q, const TileBox& k, long long delta) {
+  if (le_minus(k.tmax, q.tmin, delta)) return kAll;
+  if (!le_minus(k.tmin, q.tmax, delta)) return kNone;  // even the oldest key is too recent
+  return kSome;
+}
+// t_j < t_i
+__device__ __forceinline__ int tv_before(const TileBox& q, const TileBox& k) {
+  return k.tmax < q.tmin ? kAll : (k.tmin >= q.tmax ? kNone : kSome);
+}
+// i == j (never ALL)
+__device__ __forceinline__ int tv_diag(const TileBox& q, const TileBox& k) {
+  return (k.pmax < q.pmin || k.pmin > q.pmax) ? kNone : kSome;
+}
+
+__device__ int tv_type_pair(const MaskP& m, int tq, int tk, const TileBox& q, const TileBox& k) {
+  int v;
+  const bool uq = is_user(tq), uk = is_user(tk);
+  if (uq) {
+    if (!uk) {
+      v = kNone;
+    } else if (m.bidir) {
+      v = kAll;
+    } else {
+      v = tv_causal(q, k);
+      if (m.window > 0 && tq != REC_ATTN_GLOBAL && tk != REC_ATTN_GLOBAL)
+        v = tv_and(v, tv_window(q, k, m.window));
+    }
+  } else if (tq == REC_ATTN_RT) {
+    v = uk ? kAll : (tk == REC_ATTN_RT ? tv_causal(q, k) : kNone);
+  } else {
+    v = uk ? kAll : (tk == REC_ATTN_RT ? tv_before(q, k) : tv_diag(q, k));
+  }
+  if (m.use_delay && !(tq == REC_ATTN_CAND && tk == REC_ATTN_CAND)) v = tv_and(v, tv_delay(q, k, m.delay));
+  return v;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_min(T v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    T w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w < v ? w : v;
+  }
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ T warp_max(T v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    T w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+constexpr int kPlanThreads = 512;
+constexpr int kCostBins = 4096;
+
+__global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, PlanDev pd, const long long* offsets,
+                                                       const long long* t, const int8_t* ty,
+                                                       long long n_tiles) {
+  const int b = blockIdx.x;
+  const ReqMeta m = pd.meta[b];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  // the device offsets must describe the same requests as the host copy
+  if (threadIdx.x == 0 && (offsets[b] != m.tok_start || offsets[b + 1] != m.tok_start + m.len))
+    set_status(pd.status, REC_ATTN_ERR_DEVICE_INPUT);
+
+  // Phase 1: bounding boxes of each type in each tile (one warp per tile).
+  for (int tl = warp; tl < m.ntiles; tl += nwarps) {
+    int cnt[kTypes], pmin[kTypes], pmax[kTypes];
+    long long tmin[kTypes], tmax[kTypes];
+#pragma unroll
+    for (int c = 0; c < kTypes; ++c) {
+      cnt[c] = 0; pmin[c] = 0x7fffffff; pmax[c] = -1;
+      tmin[c] = 0x7fffffffffffffffLL; tmax[c] = -0x7fffffffffffffffLL - 1;
+    }
+    for (int r = lane; r < kTile; r += 32) {
+      const int pos = tl * kTile + r;
+      if (pos >= m.len) break;
+      const long long tt = t[m.tok_start + pos];
+      const int c = ty[m.tok_start + pos];
+      if ((unsigned)c > 3u || tt >= kTimeLimit || tt <= -kTimeLimit) {
+        set_status(pd.status, REC_ATTN_ERR_DEVICE_INPUT);
+        if ((unsigned)c > 3u) continue;
+      }
+#pragma unroll
+      for (int e = 0; e < kTypes; ++e) {
+        if (e != c) continue;
+        cnt[e] += 1;
+        pmin[e] = min(pmin[e], pos); pmax[e] = max(pmax[e], pos);
+        tmin[e] = min(tmin[e], tt); tmax[e] = max(tmax[e], tt);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kTypes; ++c) {
+      int n = cnt[c];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+      const int a0 = warp_min(pmin[c]), a1 = warp_max(pmax[c]);
+      const long long a2 = warp_min(tmin[c]), a3 = warp_max(tmax[c]);
+      if (lane == 0) {
+        TileBox bx;
+        bx.cnt = n; bx.pmin = a0; bx.pmax = a1; bx.pad = 0; bx.tmin = a2; bx.tmax = a3;
+        pd.boxes[(m.tile_start + tl) * kTypes + c] = bx;
+      }
+    }
+  }
+  __syncthreads();
+
+  // Phase 2: class of every (query tile, key tile) pair of the request.
+  const long long npairs = (long long)m.ntiles * m.ntiles;
+  for (long long idx = threadIdx.x; idx < npairs; idx += blockDim.x) {
+    const int qt = (int)(idx / m.ntiles), kt = (int)(idx % m.ntiles);
+    const TileBox* qb = pd.boxes + (m.tile_start + qt) * kTypes;
+    const TileBox* kb = pd.boxes + (m.tile_start + kt) * kTypes;
+    int lo = kAll, hi = kNone;
+    for (int a = 0; a < kTypes; ++a) {
+      const TileBox q = qb[a];
+      if (!q.cnt) continue;
+      for (int c = 0; c < kTypes; ++c) {
+        const TileBox k = kb[c];
+        if (!k.cnt) continue;
+        const int v = tv_type_pair(mp, a, c, q, k);
+        lo = min(lo, v); hi = max(hi, v);
+      }
+    }
+    const bool k_full = (kt + 1) * kTile <= m.len;
+    uint8_t cl;
+    if (hi == kNone) cl = REC_ATTN_TILE_SKIP;
+    else if (lo == kAll && k_full) cl = REC_ATTN_TILE_FULL;
+    else cl = REC_ATTN_TILE_PARTIAL;
+    pd.cls[m.cls_start + idx] = cl;
+  }
+  __syncthreads();
+
+  // Phase 3: compact each query tile's non-SKIP key tiles (one warp per query tile).
+  for (int qt = warp; qt < m.ntiles; qt += nwarps) {
+    const uint8_t* row = pd.cls + m.cls_start + (long long)qt * m.ntiles;
+    uint32_t* out = pd.klist + m.cls_start + (long long)qt * m.ntiles;
+    int n = 0, nfull = 0;
+    for (int k0 = 0; k0 < m.ntiles; k0 += 32) {
+      const int kt = k0 + lane;
+      const uint32_t c = kt < m.ntiles ? row[kt] : 0u;
+      const unsigned bal = __ballot_sync(0xffffffffu, c != 0);
+      if (c) out[n + __popc(bal & ((1u << lane) - 1u))] = (uint32_t)kt | (c << 24);
+      n += __popc(bal);
+      nfull += __popc(__ballot_sync(0xffffffffu, c == REC_ATTN_TILE_FULL));
+    }
+    if (lane == 0) {
+      const long long g = m.tile_start + qt;
+      pd.kcount[g] = n;
+      pd.qcost[g] = 2 * nfull + 3 * (n - nfull) + 1;  // a PARTIAL tile costs ~1.5 FULL ones
+      pd.qreq[g] = b;
+    }
+  }
+
+  // Phase 4: the last block to finish orders all query tiles by cost, descending
+  // (counting sort; the order only affects load balance, never results).
+  __shared__ int s_ticket;
+  __shared__ int s_hist[kCostBins];
+  __shared__ int s_part[kPlanThreads];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(&pd.counters[0], 1);
+  __syncthreads();
+  if (s_ticket != (int)gridDim.x - 1) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) s_hist[i] = 0;
+  __syncthreads();
+  for (long long q = threadIdx.x; q < n_tiles; q += blockDim.x) {
+    const int c = min(__ldcg(pd.qcost + q), kCostBins - 1);
+    atomicAdd(&s_hist[kCostBins - 1 - c], 1);
+  }
+  __syncthreads();
+  // exclusive scan of s_hist (kCostBins / kPlanThreads = 8 bins per thread)
+  constexpr int per = kCostBins / kPlanThreads;
+  int local = 0;
+  for (int i = 0; i < per; ++i) local += s_hist[threadIdx.x * per + i];
+  s_part[threadIdx.x] = local;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int v = threadIdx.x >= off ? s_part[threadIdx.x - off] : 0;
+    __syncthreads();
+    s_part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int run = s_part[threadIdx.x] - local;
+  for (int i = 0; i < per; ++i) {
+    const int h = s_hist[threadIdx.x * per + i];
+    s_hist[threadIdx.x * per + i] = run;
+    run += h;
+  }
+  __syncthreads();
+  for (long long q = threadIdx.x; q < n_tiles; q += blockDim.x) {
+    const int c = min(__ldcg(pd.qcost + q), kCostBins - 1);
+    const int pos = atomicAdd(&s_hist[kCostBins - 1 - c], 1);
+    pd.qorder[pos] = (int)q;
+  }
+}
+
+// Visible-pair counter: one block per query tile, one thread per query row.
+__global__ void __launch_bounds__(kTile) k_count_pairs(MaskP mp, PlanDev pd, const long long* t,
+                                                       const int8_t* ty) {
+  const long long g = blockIdx.x;
+  const int b = pd.qreq[g];
+  const ReqMeta m = pd.meta[b];
+  const int qt = (int)(g - m.tile_start);
+  const int r = threadIdx.x, pi = qt * kTile + r;
+  __shared__ long long s_t[kTile];
+  __shared__ int s_ty[kTile];
+  __shared__ unsigned long long s_sum;
+  if (r == 0) s_sum = 0;
+  __syncthreads();
+  const bool row_ok = pi < m.len;
+  long long ti = 0;
+  int tyi = -1;
+  if (row_ok) { ti = t[m.tok_start + pi]; tyi = ty[m.tok_start + pi]; }
+  bool thr_ok; long long thr;
+  delay_bound(ti, mp.delay, thr_ok, thr);
+  unsigned long long cnt = 0;
+  const int n = pd.kcount[g];
+  const uint32_t* list = pd.klist + m.cls_start + (long long)qt * m.ntiles;
+  for (int j = 0; j < n; ++j) {
+    const uint32_t e = list[j];
+    const int kt = (int)(e & 0xffffffu), cl = (int)(e >> 24);
+    __syncthreads();
+    const int pj = kt * kTile + r;
+    s_t[r] = pj < m.len ? t[m.tok_start + pj] : 0;
+    s_ty[r] = pj < m.len ? (int)ty[m.tok_start + pj] : -1;
+    __syncthreads();
+    if (!row_ok) continue;
+    if (cl == REC_ATTN_TILE_FULL) { cnt += kTile; continue; }
+    for (int c = 0; c < kTile; ++c)
+      cnt += vis_pred(mp, pi, ti, tyi, thr_ok, thr, kt * kTile + c, s_t[c], s_ty[c]) ? 1u : 0u;
+  }
+  atomicAdd(&s_sum, cnt);
+  __syncthreads();
+  if (r == 0) atomicAdd(pd.pairs, s_sum);
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const MaskP& mp, const PlanDev& pd, const long long* offsets_dev,
+                        const long long* t, const int8_t* ty, int batch, long long n_tiles,
+                        cudaStream_t st) {
+  if (batch <= 0) return cudaSuccess;
+  k_plan<<<batch, kPlanThreads, 0, st>>>(mp, pd, offsets_dev, t, ty, n_tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_count_pairs(const MaskP& mp, const PlanDev& pd, const long long* t,
+                               const int8_t* ty, long long n_tiles, cudaStream_t st) {
+  if (n_tiles <= 0) return cudaSuccess;
+  k_count_pairs<<<(unsigned)n_tiles, kTile, 0, st>>>(mp, pd, t, ty);
+  return cudaGetLastError();
+}
+
+}  // namespace recattn

@@ -1,0 +1,97 @@
+// rec_attn_internal.cuh -- structures and device helpers shared by the CUDA sources
+// of the GB300 masked time-RoPE attention library (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "rec_attn.h"
+
+namespace recattn {
+
+constexpr int kTile = REC_ATTN_TILE;  // tokens per query / key tile
+constexpr int kTypes = 4;             // GLOBAL, HIST, RT, CAND
+constexpr int kMaxPairs = 64;         // head_dim <= 128
+constexpr long long kTimeLimit = (1LL << 62);
+
+// One request of the packed batch.
+struct ReqMeta {
+  long long tok_start;   // first token (global index)
+  int len;               // tokens in the request
+  int ntiles;            // ceil(len / kTile)
+  long long tile_start;  // first tile (global tile index)
+  long long cls_start;   // first entry of the request's ntiles x ntiles class matrix
+};
+
+// Bounding box of one token type inside one tile (positions are request-local).
+struct TileBox {
+  int cnt, pmin, pmax, pad;
+  long long tmin, tmax;
+};
+
+// Mask parameters as the kernels see them.
+struct MaskP {
+  int use_delay;
+  int window;
+  int bidir;
+  int pad;
+  long long delay;
+};
+
+// Device workspace owned by a plan.
+struct PlanDev {
+  ReqMeta* meta;        // [B]
+  TileBox* boxes;       // [NT][4]
+  uint8_t* cls;         // [NC]
+  uint32_t* klist;      // [NC]: per query tile, the non-SKIP key tiles (kt | class << 24)
+  int* kcount;          // [NT]: entries in each query tile's list
+  int* qcost;           // [NT]: scheduling cost of each query tile
+  int* qreq;            // [NT]: request of each query tile
+  int* qorder;          // [NT]: query tiles, most expensive first
+  int* counters;        // [4]: plan ticket, scheduler, spare
+  int* status;          // [1]: first device error (rec_attn_status)
+  unsigned long long* pairs;  // [1]: visible-pair counter
+};
+
+// Record a device-side error; the first error wins.
+__device__ __forceinline__ void set_status(int* st, int code) { atomicCAS(st, 0, code); }
+
+__device__ __forceinline__ bool is_user(int ty) { return ty == REC_ATTN_GLOBAL || ty == REC_ATTN_HIST; }
+
+// vis(i, j) for two tokens of one request.  `thr_ok`/`thr` encode the exact delay
+// bound of the query (t_i - delta): thr_ok is false when t_i - delta lies below the
+// int64 range, in which case no key is old enough.  Types outside 0..3 see nothing.
+__device__ __forceinline__ bool vis_pred(const MaskP& m, int pi, long long ti, int tyi,
+                                         bool thr_ok, long long thr, int pj, long long tj,
+                                         int tyj) {
+  if ((unsigned)tyi > 3u || (unsigned)tyj > 3u) return false;
+  bool v;
+  const bool ui = is_user(tyi), uj = is_user(tyj);
+  if (ui) {
+    if (!uj) {
+      v = false;
+    } else if (m.bidir) {
+      v = true;
+    } else {
+      v = pj <= pi;
+      if (m.window > 0 && tyi != REC_ATTN_GLOBAL && tyj != REC_ATTN_GLOBAL)
+        v = v && (pi - pj < m.window);
+    }
+  } else if (tyi == REC_ATTN_RT) {
+    v = uj || (tyj == REC_ATTN_RT && pj <= pi);
+  } else {  // candidate
+    v = uj || (tyj == REC_ATTN_RT ? (tj < ti) : (pi == pj));
+  }
+  if (m.use_delay && !(tyi == REC_ATTN_CAND && tyj == REC_ATTN_CAND && pi == pj))
+    v = v && thr_ok && (tj <= thr);
+  return v;
+}
+
+// Query-side delay bound t_i - delta, exact (see vis_pred).
+__device__ __forceinline__ void delay_bound(long long ti, long long delta, bool& ok,
+                                            long long& thr) {
+  ok = ti >= (long long)(-0x7fffffffffffffffLL - 1) + delta;
+  thr = ok ? ti - delta : 0;
+}
+
+}  // namespace recattn

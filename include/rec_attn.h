@@ -1,0 +1,205 @@
+/*
+ * rec_attn.h -- C-ABI of the GB300 (sm_103a) masked time-RoPE attention library.
+ *
+ * The library computes the forward pass of multi-head softmax attention over a
+ * packed, jagged batch of request-centric token sequences
+ *
+ *     O_i = sum_j P_ij V_j,  P_ij = vis(i,j) exp(s_ij) / sum_j' vis(i,j') exp(s_ij'),
+ *     s_ij = scale * < RoPE_t(Q_i, t_i), RoPE_t(K_j, t_j) >,
+ *
+ * with O_i = 0 when no key is visible.  Citations (page, section / equation):
+ *   - softmax attention with an additive -inf mask: TM20K review page, section 2.1
+ *     (full-attention equation); LazFormer review page, section 2.3, Eq. 19-21;
+ *   - time-RoPE alpha_i(t) = t * phi_min / dt_max * base^(2i/d) on adjacent pairs of
+ *     Q and K: CADET review page, section on time encoding and self-gating;
+ *   - mask vis(i,j) from per-token timestamps and types: CADET delay rule
+ *     M_ij = -inf if t_j > t_i - delta (section on masking the last hour), CADET
+ *     candidate isolation (section on scoring hundreds of candidates in 50 ms),
+ *     SORT U2U/C2U/C2C regions (section 3.1) and local attention (3.2.1), LazFormer
+ *     Eq. 19-21, MTGR hybrid dynamic mask (MTGR notes on the blog index page);
+ *   - packed jagged batch (one contiguous token buffer plus per-sequence start and
+ *     end): CADET review page, training data engineering paragraph;
+ *   - skipping fully masked blocks: CADET serving kernel and SORT section 4.1
+ *     ("mask preload check").
+ *
+ * Mask predicate vis(i, j), for tokens i (query) and j (key) of the same request
+ * (tokens of different requests never see each other; p = request-local position,
+ * t = timestamp, U = {GLOBAL, HIST}):
+ *   U    -> U   : hist_bidirectional ? 1 : p_j <= p_i and (window == 0 or either
+ *                 token is GLOBAL or p_i - p_j < window)
+ *   U    -> RT, CAND : 0
+ *   RT   -> U   : 1;   RT -> RT : p_j <= p_i;   RT -> CAND : 0
+ *   CAND -> U   : 1;   CAND -> RT : t_j < t_i;  CAND -> CAND : i == j
+ *   use_delay   : every pair additionally needs t_j <= t_i - delay_s, except the
+ *                 candidate self pair.
+ * Time-RoPE: pair i (components 2i, 2i+1, i < d/2) turns by alpha_i(t) =
+ * t * phi_min / dt_max_s * rope_base^(2i/d); Q_i and K_j are rotated at their own
+ * timestamps (x' = x cos a - y sin a, y' = x sin a + y cos a).  The library
+ * subtracts the first timestamp of each request in int64 before forming fp32
+ * angles; scores depend only on time differences, so results are the same.
+ *
+ * Threading: functions are thread-safe for distinct plans.  All device work is
+ * asynchronous on the stream passed in (a cudaStream_t given as void*; NULL =
+ * legacy default stream) unless a function says it synchronizes.
+ */
+#ifndef REC_ATTN_H
+#define REC_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define REC_ATTN_ABI_VERSION 1
+#define REC_ATTN_TILE 128            /* tokens per tile (query and key side) */
+#define REC_ATTN_MAX_REQUEST_LEN 262144 /* longest request a plan accepts */
+
+typedef enum {
+  REC_ATTN_OK = 0,
+  REC_ATTN_ERR_INVALID_ARG = 1,   /* bad argument, detected on the host before any launch */
+  REC_ATTN_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim, dtype, size) */
+  REC_ATTN_ERR_CUDA = 3,          /* a CUDA runtime call failed (no GPU, launch error, ...) */
+  REC_ATTN_ERR_OOM = 4,           /* device allocation failed */
+  REC_ATTN_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (device status) */
+  REC_ATTN_ERR_DEVICE_INPUT = 6   /* device data out of range: type not in 0..3 or |t| >= 2^62 */
+} rec_attn_status;
+
+typedef enum { REC_ATTN_BF16 = 0, REC_ATTN_FP32 = 1 } rec_attn_dtype;
+
+/* token types (int8 per token) */
+enum { REC_ATTN_GLOBAL = 0, REC_ATTN_HIST = 1, REC_ATTN_RT = 2, REC_ATTN_CAND = 3 };
+
+/* tile classes reported by rec_attn_tile_classes */
+enum { REC_ATTN_TILE_SKIP = 0, REC_ATTN_TILE_PARTIAL = 1, REC_ATTN_TILE_FULL = 2 };
+
+typedef struct {
+  int32_t abi_version;        /* must be REC_ATTN_ABI_VERSION */
+  int32_t num_heads;          /* H >= 1 */
+  int32_t head_dim;           /* d: bf16 -> 64 or 128; fp32 -> 32 or 64 */
+  int32_t dtype;              /* rec_attn_dtype; Q, K, V and O share it */
+  int32_t use_delay;          /* 0/1: CADET delay rule */
+  int64_t delay_s;            /* delta >= 0 seconds (CADET uses 3600) */
+  int32_t window;             /* 0 = none; else user->user needs p_i - p_j < window */
+  int32_t hist_bidirectional; /* 0/1: GLOBAL and HIST tokens fully mutually visible */
+  int32_t use_rope;           /* 0/1: apply the time-RoPE to Q and K */
+  double phi_min;             /* rad turned by the slowest pair over dt_max_s (1e-4) */
+  double dt_max_s;            /* > 0, seconds (one year = 31536000) */
+  double rope_base;           /* > 0 (6e5) */
+  float softmax_scale;        /* > 0, or 0 for 1/sqrt(head_dim) */
+} rec_attn_params;
+
+typedef struct rec_attn_plan_s rec_attn_plan_t; /* opaque */
+
+/*
+ * rec_attn_plan -- validate a batch and build its attention plan.
+ *
+ * Arguments:
+ *   params          mask / RoPE / shape parameters (copied).
+ *   batch           number of requests B >= 0.
+ *   offsets_host    host int64[B+1]: offsets[0] = 0, non-decreasing; request b owns
+ *                   tokens [offsets[b], offsets[b+1]).  Read during the call only.
+ *                   Must hold the same values as offsets_dev.
+ *   offsets_dev     device int64[B+1], same values.
+ *   timestamps_dev  device int64[T] seconds, T = offsets[B]; |t| < 2^62.
+ *   types_dev       device int8[T], each in 0..3.
+ *   stream          cudaStream_t for the planning kernels.
+ *   plan_out        receives the plan.
+ * The device arrays must stay valid and unchanged while the plan is used.  The
+ * plan owns a device workspace (per-tile statistics, tile classes, per-query-tile
+ * key-tile lists, the schedule and the rotated Q/K buffers), allocated in stream
+ * order from a library-owned memory pool.  A plan depends only on the offsets,
+ * timestamps, types and params, so one plan serves any number of rec_attn_fwd
+ * calls (e.g. every layer of a model).
+ * Errors: INVALID_ARG (bad params, offsets or NULL pointers; nothing launched),
+ * UNSUPPORTED (head_dim/dtype combination, a request longer than
+ * REC_ATTN_MAX_REQUEST_LEN, T >= 2^31), OOM, CUDA.  Invalid device values (types,
+ * timestamps) are reported by rec_attn_device_status; the kernels never fault on
+ * them.  On error *plan_out is NULL.
+ */
+rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_t batch,
+                              const int64_t* offsets_host, const int64_t* offsets_dev,
+                              const int64_t* timestamps_dev, const int8_t* types_dev,
+                              void* stream, rec_attn_plan_t** plan_out);
+
+/*
+ * rec_attn_fwd -- attention forward for a planned batch.
+ *
+ *   q, k, v   device [T][H][d] row-major, contiguous, in params->dtype (bf16 bit
+ *             patterns or fp32), 16-byte aligned, finite.
+ *   out       device [T][H][d] in params->dtype; every row is written (rows that see
+ *             no key get zeros).  May not alias q, k or v.
+ *   lse       optional device float[T][H]: natural-log sum of exp(scaled scores) over
+ *             visible keys, -inf for rows that see no key; NULL to skip.
+ *   stream    cudaStream_t for the launches.
+ * Errors: INVALID_ARG (NULL plan or pointers, misalignment, aliasing), CUDA.
+ * Asynchronous: returns after enqueueing.  Launch-time anomalies inside kernels
+ * (a timed-out wait) are reported by rec_attn_device_status.
+ */
+rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, const void* k,
+                             const void* v, void* out, float* lse, void* stream);
+
+/*
+ * rec_attn_free -- release a plan (NULL-safe).  The workspace returns to the
+ * library pool in stream order on the stream of the plan's last use, so work
+ * already enqueued there may still run; callers that used other streams must
+ * synchronize them first.
+ */
+void rec_attn_free(rec_attn_plan_t* plan);
+
+/*
+ * rec_attn_tile_classes -- copy the plan's tile classes to host memory.
+ * Order: request-major, then query tile, then key tile (n_tiles(b)^2 entries per
+ * request, n_tiles(b) = ceil(len_b / 128)); values REC_ATTN_TILE_*.  SKIP: no
+ * visible pair; FULL: every (query, key) pair of the tile visible and the key
+ * tile complete (128 keys); PARTIAL otherwise.  Classes come from per-type bounding
+ * boxes of positions and timestamps in each tile, so PARTIAL is conservative.
+ * *n_needed receives the count; host_out may be NULL to query it.  Synchronizes
+ * the plan's stream.  Errors: INVALID_ARG (NULL plan/n_needed, capacity too
+ * small), CUDA.
+ */
+rec_attn_status rec_attn_tile_classes(rec_attn_plan_t* plan, uint8_t* host_out,
+                                      size_t capacity, size_t* n_needed);
+
+/*
+ * rec_attn_visible_pairs -- exact number of visible (query, key) pairs of the batch
+ * (per head), counted on the device.  Used for FLOP accounting (4 * d * H * pairs).
+ * Synchronizes the plan's stream.  Errors: INVALID_ARG, CUDA.
+ */
+rec_attn_status rec_attn_visible_pairs(rec_attn_plan_t* plan, uint64_t* host_out);
+
+/*
+ * rec_attn_device_status -- status word the plan's kernels wrote (REC_ATTN_OK,
+ * REC_ATTN_ERR_DEVICE_INPUT or REC_ATTN_ERR_TIMEOUT; the first error wins).
+ * Synchronizes the plan's stream.  Errors: INVALID_ARG, CUDA.
+ */
+rec_attn_status rec_attn_device_status(rec_attn_plan_t* plan, int32_t* status_out);
+
+/* Kernel timings of the most recent rec_attn_fwd on a plan with timing enabled. */
+typedef struct {
+  float rope_ms;  /* time-RoPE prologue (0 when use_rope == 0) */
+  float attn_ms;  /* attention kernel */
+} rec_attn_timings;
+
+/*
+ * rec_attn_enable_timing -- from now on, rec_attn_fwd records CUDA events on its
+ * stream around each kernel it launches (the events are owned by the plan).
+ * Errors: INVALID_ARG (NULL plan), CUDA.
+ */
+rec_attn_status rec_attn_enable_timing(rec_attn_plan_t* plan);
+
+/*
+ * rec_attn_read_timings -- elapsed times of the last timed rec_attn_fwd; waits for
+ * its events.  Errors: INVALID_ARG (NULL arguments, timing not enabled or no timed
+ * call yet), CUDA.
+ */
+rec_attn_status rec_attn_read_timings(rec_attn_plan_t* plan, rec_attn_timings* out);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* rec_attn_status_string(rec_attn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* REC_ATTN_H */

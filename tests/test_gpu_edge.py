@@ -1,0 +1,149 @@
+"""Edge cases of the CUDA path: empty batches and requests, ragged lengths around
+the tile size, rows with no visible key, plan reuse and determinism, the
+time-shift invariance (bit-identical on the GPU, since the library works on
+int64 time differences), invalid device data (reported, never a fault) and the
+largest accepted request."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as gu
+import oracle
+from generative_recommender_ranking_gb300 import binding as bd
+from generative_recommender_ranking_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gu.ensure_built()
+
+
+def _custom(lengths, H=2, d=64, dtype="bf16", seed=7, types=None, t=None, mask=None):
+    rng = np.random.default_rng(seed)
+    off = np.zeros(len(lengths) + 1, dtype=np.int64)
+    off[1:] = np.cumsum(lengths)
+    T = int(off[-1])
+    if t is None:
+        t = W.EPOCH + np.sort(rng.integers(0, 10**7, size=T)).astype(np.int64)
+    if types is None:
+        types = np.full(T, W.HIST, dtype=np.int8)
+    x = [rng.standard_normal((T, H, d), dtype=np.float32) for _ in range(3)]
+    if dtype == "bf16":
+        x = [W.round_to_bf16_bits(a) for a in x]
+    return W.Workload("custom", H, d, dtype, off, np.asarray(t, np.int64), np.asarray(types, np.int8),
+                      *x, mask or dict(use_delay=False, delay_s=0, window=0, hist_bidirectional=False),
+                      dict(use_rope=True, phi_min=1e-4, dt_max_s=float(W.YEAR), rope_base=6e5))
+
+
+def _check_all(w):
+    out, lse, plan = gu.run_gpu(w, with_lse=True)
+    try:
+        ref = oracle.attention(gu.oracle_params(w), w.offsets, w.t, w.types, w.q, w.k, w.v)
+        gu.assert_close(w, gu.to_f64(out), ref, "custom")
+        op = gu.oracle_params(w)
+        np.testing.assert_array_equal(bd.rec_attn_tile_classes(plan),
+                                      oracle.tile_classes(op, w.offsets, w.t, w.types))
+        assert bd.rec_attn_visible_pairs(plan) == oracle.visible_pairs(op, w.offsets, w.t, w.types)
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
+    return out
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 128), ("fp32", 32)])
+def test_ragged_lengths_and_empty_requests(dtype, d):
+    _check_all(_custom([1, 0, 127, 128, 129, 0, 255, 256, 257, 3], d=d, dtype=dtype))
+
+
+def test_empty_batch_and_all_empty_requests():
+    for lengths in ([], [0, 0, 0]):
+        w = _custom(lengths)
+        tens = gu.device_inputs(w)
+        plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+        out = torch.empty((0, 2, 64), dtype=torch.bfloat16, device="cuda")
+        bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out)
+        assert bd.rec_attn_tile_classes(plan).size == 0
+        assert bd.rec_attn_visible_pairs(plan) == 0
+        bd.rec_attn_free(plan)
+
+
+def test_rows_without_visible_keys_are_zero():
+    # every timestamp equal and a one-hour delay: nothing is old enough, except the
+    # candidates' self pairs
+    L = 300
+    ty = np.full(L, W.HIST, dtype=np.int8)
+    ty[-20:] = W.CAND
+    w = _custom([L, 170], types=np.concatenate([ty, np.full(170, W.HIST, np.int8)]),
+                t=np.full(L + 170, W.EPOCH, dtype=np.int64),
+                mask=dict(use_delay=True, delay_s=3600, window=0, hist_bidirectional=False))
+    out = _check_all(w)
+    o = out.float().cpu().numpy()
+    assert np.all(o[:L - 20] == 0.0) and np.all(o[L:] == 0.0)
+    np.testing.assert_array_equal(o[L - 20:L], W.bf16_bits_to_float32(w.v[L - 20:L]))
+
+
+def test_time_shift_is_bit_identical_and_plan_reuse_is_deterministic():
+    w = W.sort(batch=3, n_hist=400, n_cand=30)
+    tens = gu.device_inputs(w)
+    out1, _, plan = gu.run_gpu(w, tens=tens)
+    out2 = torch.empty_like(out1)
+    bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out2)   # same plan, second call
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+    bd.rec_attn_free(plan)
+    tens["t"] = tens["t"] + 123_456_789
+    out3, _, plan = gu.run_gpu(w, tens=tens)
+    bd.rec_attn_free(plan)
+    assert torch.equal(out1, out3)
+
+
+def test_invalid_device_types_are_reported_not_faulted():
+    w = _custom([200, 100])
+    tens = gu.device_inputs(w)
+    tens["ty"][5] = 7
+    tens["ty"][250] = -3
+    plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    out = torch.empty_like(tens["q"])
+    bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out)
+    assert bd.rec_attn_device_status(plan) == bd.ERR_DEVICE_INPUT
+    bd.rec_attn_free(plan)
+    # offsets on the device that disagree with the host copy are reported too
+    w = _custom([200, 100])
+    tens = gu.device_inputs(w)
+    tens["off_d"][1] = 150
+    plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    assert bd.rec_attn_device_status(plan) == bd.ERR_DEVICE_INPUT
+    bd.rec_attn_free(plan)
+
+
+def test_host_argument_errors_on_gpu():
+    w = _custom([130])
+    tens = gu.device_inputs(w)
+    plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    with pytest.raises(bd.RecAttnError) as e:   # output aliasing an input
+        bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], tens["q"])
+    assert e.value.code == bd.ERR_INVALID_ARG
+    with pytest.raises(bd.RecAttnError):       # misaligned pointer
+        bd.rec_attn_fwd(plan, tens["q"].data_ptr() + 2, tens["k"], tens["v"], torch.empty_like(tens["q"]))
+    bd.rec_attn_free(plan)
+
+
+def test_longest_request_sampled():
+    L = bd.MAX_REQUEST_LEN
+    rng = np.random.default_rng(11)
+    t = W.EPOCH + np.cumsum(rng.integers(1, 100, size=L)).astype(np.int64)
+    ty = np.full(L, W.HIST, dtype=np.int8)
+    ty[:64] = W.GLOBAL
+    ty[-8:] = W.CAND
+    w = _custom([L], H=1, t=t, types=ty, mask=dict(use_delay=False, delay_s=0, window=1024,
+                                                    hist_bidirectional=False))
+    out, _, plan = gu.run_gpu(w)
+    try:
+        rows = np.array([0, 63, 64, 1000, 131071, 131072, L - 9, L - 8, L - 1], dtype=np.int64)
+        ref = oracle.attention(gu.oracle_params(w), w.offsets, w.t, w.types, w.q, w.k, w.v, rows=rows)
+        gu.assert_close(w, gu.to_f64(out[torch.from_numpy(rows).cuda()]), ref, "max length")
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
