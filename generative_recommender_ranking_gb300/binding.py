@@ -202,3 +202,22 @@ def rec_attn_read_timings(plan: Plan) -> tuple[float, float]:
     t = RecAttnTimings()
     _check("rec_attn_read_timings", L.rec_attn_read_timings(plan.handle, ctypes.byref(t)))
     return float(t.rope_ms), float(t.attn_ms)
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def rec_attn_fwd_noalloc(params: RecAttnParams, offsets_host, offsets_dev, timestamps_dev, types_dev,
+                         q, k, v, out, lse=None, stream=None) -> None:
+    """Plan + RoPE + attention without any device allocation (static workspace of
+    NOALLOC_SCRATCH_BYTES shared by all calls; calls must not overlap on the GPU)."""
+    L = lib()
+    vp = ctypes.c_void_p
+    L.rec_attn_fwd_noalloc.argtypes = [ctypes.POINTER(RecAttnParams), ctypes.c_int32, vp, vp, vp, vp,
+                                       vp, vp, vp, vp, vp, vp]
+    L.rec_attn_fwd_noalloc.restype = ctypes.c_int
+    off_h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int64))
+    code = L.rec_attn_fwd_noalloc(ctypes.byref(params), len(off_h) - 1, _ptr(off_h), _ptr(offsets_dev),
+                                  _ptr(timestamps_dev), _ptr(types_dev), _ptr(q), _ptr(k), _ptr(v),
+                                  _ptr(out), _ptr(lse), _stream(stream))
+    _check("rec_attn_fwd_noalloc", code)

@@ -196,6 +196,36 @@ rec_attn_status rec_attn_enable_timing(rec_attn_plan_t* plan);
  */
 rec_attn_status rec_attn_read_timings(rec_attn_plan_t* plan, rec_attn_timings* out);
 
+/*
+ * rec_attn_fwd_noalloc -- plan + time-RoPE + attention in one call that allocates
+ * no device memory.  The pages have no counterpart to this entry point: it exists
+ * for callers that cannot call cudaMalloc, such as a process whose inference
+ * runtime has reserved the GPU's memory for its own allocator and forbids other
+ * allocations, or a serving loop that cannot afford cudaMalloc's latency and
+ * implicit synchronisation on every request.
+ *
+ * Arguments mean what they mean for rec_attn_plan and rec_attn_fwd; the result is
+ * the one those two calls produce.  All per-call workspace lives in one static
+ * device array of REC_ATTN_NOALLOC_SCRATCH_BYTES that every GPU which loads the
+ * library holds until the process exits.  A batch whose workspace does not fit
+ * (request table, tile statistics and classes, key-tile lists, schedule and, with
+ * the RoPE on, two rotated copies of the [T][H][d] Q/K) is rejected with
+ * REC_ATTN_ERR_UNSUPPORTED before any work is enqueued; REC_ATTN_ERR_INVALID_ARG
+ * as for rec_attn_plan / rec_attn_fwd.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  Every call shares the one array and leaves its contents
+ * behind, so calls whose GPU work overlaps (other streams, other host threads)
+ * race and must be serialised by the caller.  Device-side input errors are not
+ * reported by this entry point (the plan-based API reports them).
+ */
+#define REC_ATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params, int32_t batch,
+                                     const int64_t* offsets_host, const int64_t* offsets_dev,
+                                     const int64_t* timestamps_dev, const int8_t* types_dev,
+                                     const void* q, const void* k, const void* v, void* out,
+                                     float* lse, void* stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* rec_attn_status_string(rec_attn_status status);
 
