@@ -185,6 +185,7 @@ def run_ours(args):
 
     from generative_recommender_ranking_gb300 import binding as bd
     from generative_recommender_ranking_gb300 import build as bld
+    from generative_recommender_ranking_gb300 import sharding
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -296,14 +297,9 @@ def run_ours(args):
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, ht, hty, hoff))
     d2h = hout.numel() * hout.element_size()
 
-    # max over ranks
-    tot = torch.tensor([total_ms, e2e_ms, attn_ms], dtype=torch.float64, device=dev)
-    work = torch.tensor([flops, float(tokens)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
-        dist.all_reduce(work, op=dist.ReduceOp.SUM)
-    total_ms, e2e_ms, attn_max = tot.tolist()
-    all_flops, all_tokens = work.tolist()
+    # slowest rank's times, total work of all ranks
+    (total_ms, e2e_ms, attn_max), (all_flops, all_tokens) = sharding.aggregate(
+        [total_ms, e2e_ms, attn_ms], [flops, float(tokens)], device=dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
