@@ -15,6 +15,7 @@
 
 #include "launchers.cuh"
 #include "rec_attn.h"
+#include "workspace.cuh"
 
 #define REC_ATTN_API extern "C" __attribute__((visibility("default")))
 
@@ -99,8 +100,6 @@ rec_attn_status check_params(const rec_attn_params* p) {
   if ((long long)p->num_heads * p->head_dim > (1LL << 20)) return REC_ATTN_ERR_UNSUPPORTED;
   return REC_ATTN_OK;
 }
-
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -189,7 +188,7 @@ REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_
       NC += (long long)m.ntiles * m.ntiles;
     }
     T = offsets_host[batch];
-    if (T >= (1LL << 31)) return REC_ATTN_ERR_UNSUPPORTED;
+    if (T >= (1LL << 31) || NT * params->num_heads >= (1LL << 31)) return REC_ATTN_ERR_UNSUPPORTED;
     if (!offsets_dev || (T > 0 && (!timestamps_dev || !types_dev))) return REC_ATTN_ERR_INVALID_ARG;
   }
 
@@ -218,41 +217,20 @@ REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_
   // workspace layout
   const size_t elem = params->dtype == REC_ATTN_BF16 ? 2 : 4;
   const size_t qk_bytes = (size_t)T * params->num_heads * params->head_dim * elem;
-  size_t off = 0;
-  const size_t o_hdr = off; off = align256(off + 256);
-  const size_t o_meta = off; off = align256(off + sizeof(ReqMeta) * (size_t)batch);
-  const size_t o_box = off; off = align256(off + sizeof(TileBox) * kTypes * (size_t)NT);
-  const size_t o_cls = off; off = align256(off + (size_t)NC);
-  const size_t o_kl = off; off = align256(off + 4 * (size_t)NC);
-  const size_t o_kc = off; off = align256(off + 4 * (size_t)NT);
-  const size_t o_qc = off; off = align256(off + 4 * (size_t)NT);
-  const size_t o_qr = off; off = align256(off + 4 * (size_t)NT);
-  const size_t o_qo = off; off = align256(off + 4 * (size_t)NT);
-  const size_t o_rq = off; off = align256(off + (params->use_rope ? qk_bytes : 0));
-  const size_t o_rk = off; off = align256(off + (params->use_rope ? qk_bytes : 0));
-  plan->ws_bytes = off;
+  const WsLayout lay = ws_layout(batch, NT, NC, params->use_rope ? qk_bytes : 0);
+  plan->ws_bytes = lay.total;
 
   cudaMemPool_t pool;
   e = pool_for(plan->device, &pool);
   if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&plan->ws, plan->ws_bytes, pool, plan->stream);
   if (e != cudaSuccess) { delete plan; return from_cuda(e); }
   char* w = static_cast<char*>(plan->ws);
+  plan->pd = ws_bind(w, lay);
   PlanDev& pd = plan->pd;
-  pd.counters = reinterpret_cast<int*>(w + o_hdr);
-  pd.status = pd.counters + 8;
-  pd.pairs = reinterpret_cast<unsigned long long*>(w + o_hdr + 64);
-  pd.meta = reinterpret_cast<ReqMeta*>(w + o_meta);
-  pd.boxes = reinterpret_cast<TileBox*>(w + o_box);
-  pd.cls = reinterpret_cast<uint8_t*>(w + o_cls);
-  pd.klist = reinterpret_cast<uint32_t*>(w + o_kl);
-  pd.kcount = reinterpret_cast<int*>(w + o_kc);
-  pd.qcost = reinterpret_cast<int*>(w + o_qc);
-  pd.qreq = reinterpret_cast<int*>(w + o_qr);
-  pd.qorder = reinterpret_cast<int*>(w + o_qo);
-  plan->qrot = params->use_rope ? w + o_rq : nullptr;
-  plan->krot = params->use_rope ? w + o_rk : nullptr;
+  plan->qrot = params->use_rope ? w + lay.rq : nullptr;
+  plan->krot = params->use_rope ? w + lay.rk : nullptr;
 
-  e = cudaMemsetAsync(w + o_hdr, 0, 256, plan->stream);
+  e = cudaMemsetAsync(w + lay.hdr, 0, 256, plan->stream);
   if (e == cudaSuccess && batch > 0)
     e = cudaMemcpyAsync(pd.meta, meta.data(), sizeof(ReqMeta) * (size_t)batch, cudaMemcpyHostToDevice, plan->stream);
   if (e == cudaSuccess)
@@ -318,6 +296,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, 
   AttnArgs a;
   a.meta = plan->pd.meta; a.qreq = plan->pd.qreq; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
   a.qorder = plan->pd.qorder; a.t = plan->t; a.ty = plan->ty;
+  a.counters = plan->pd.counters; a.krec = plan->pd.krec;
   a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = plan->pd.status;
   a.n_items = plan->NT * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale; a.mask = plan->mask;
   if (p.dtype == REC_ATTN_FP32) {

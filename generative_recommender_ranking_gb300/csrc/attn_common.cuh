@@ -19,6 +19,8 @@ struct AttnArgs {
   void* out;
   float* lse;        // optional [T][H]
   int* status;
+  int* counters;     // [1]: dynamic item counter, [2]: exit ticket (both reset at kernel end)
+  const KeyTileRec* krec;
   long long n_items; // query tiles x heads
   int heads;
   float scale;       // softmax scale (natural-log domain)

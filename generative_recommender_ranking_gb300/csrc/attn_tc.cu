@@ -5,18 +5,27 @@
 // key tiles the plan classified SKIP (block skipping of the CADET serving kernel;
 // SORT section 4.1).  Rows that see no key are written as zeros.
 //
-// One persistent CTA per SM, 6 warps with fixed roles:
-//   warp 0      TMA producer: Q' tile once per item, K'/V tiles into an NS-stage ring;
-//   warp 1      MMA issuer: S = Q'K'^T into one of two TMEM S buffers (tcgen05.mma,
-//               kind::f16, fp32 accumulate), then O += P V into the TMEM O buffer;
-//   warps 2..5  softmax: one query row per thread (TMEM lane quadrant = warp % 4).
-//               tcgen05.ld of the S row, per-element mask on PARTIAL tiles, online
-//               softmax in the exp2 domain, P rounded to bf16 into shared memory in the
-//               128-byte-swizzled K-major layout the PV MMA reads, O rescaled in TMEM
-//               when the running maximum grows, O / l in the epilogue.
-// The row sum l is accumulated from the bf16-rounded P values the PV MMA consumes, so
-// every output row is an exact convex combination of the value rows it saw.
+// One persistent CTA per SM runs two independent item streams, so the tensor core
+// works on one stream while the other stream's softmax runs.  12 warps:
+//   warp 0, 1     TMA producers (stream 0, 1): claim items from a global counter in
+//                 longest-first order, publish item descriptors and per-stage tile
+//                 info in shared memory, load Q', K', V (and, for PARTIAL tiles, the
+//                 key-tile record) with TMA / bulk copies into per-stream rings;
+//   warp 2, 3     MMA issuers (stream 0, 1): S = Q'K'^T into the stream's TMEM S
+//                 buffer, then O += P V with P read straight from TMEM (P overwrites
+//                 the first 64 columns of S);
+//   warps 4..7    softmax of stream 0, warps 8..11 softmax of stream 1: one query row
+//                 per thread (TMEM lane quadrant = warp % 4).  PARTIAL tiles build the
+//                 row's 128-bit visibility mask from position ranges, per-type key
+//                 bitmaps and, for time clauses, a binary search over time-sorted
+//                 runs; FULL tiles skip the mask.  Online softmax in the exp2 domain
+//                 with a lazily updated reference maximum; O rescaled in TMEM only when
+//                 the maximum grows by more than 2^8; P rounded to bf16 and the row sum
+//                 l accumulated from the rounded values, so every output row is an
+//                 exact convex combination of the value rows it saw.
 // Every wait on an mbarrier is bounded (REC_ATTN_ERR_TIMEOUT in the status word).
+#include <climits>
+
 #include <cuda_bf16.h>
 
 #include "attn_common.cuh"
@@ -26,54 +35,68 @@ namespace recattn {
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kSlab = kTile * 128;        // 128 rows x 128 B: one 64-column swizzle slab
+constexpr int kStreams = 2;
+constexpr int kThreads = 384;
+constexpr int kSlab = kTile * 128;           // 128 rows x 128 B: one 64-column swizzle slab
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256;
+constexpr float kRescaleLog2 = 8.f;          // keep the reference max until it is exceeded by 2^8
+constexpr int kRecBytes = (int)sizeof(KeyTileRec);
 
-template <int D, int NS>
+template <int D>
+struct Cfg;
+template <>
+struct Cfg<64> { static constexpr int QB = 2, NS = 2; };
+template <>
+struct Cfg<128> { static constexpr int QB = 1, NS = 1; };
+
+struct ItemDesc {
+  long long tok0;  // first token of the query tile (global index)
+  int pos0;        // request-local position of the tile's first row
+  int rows;        // valid rows in the tile
+  int h;
+  int n;           // non-SKIP key tiles
+  int end;         // 1: the stream is done
+  int pad;
+};
+static_assert(sizeof(ItemDesc) == 32, "");
+
+struct StageInfo {
+  int kt;
+  int cls;
+};
+
+template <int D>
 struct Layout {
+  static constexpr int QB = Cfg<D>::QB, NS = Cfg<D>::NS;
   static constexpr int kQBytes = kTile * D * 2;
   static constexpr int kKVBytes = kTile * D * 2;
-  static constexpr int kPBytes = kTile * kTile * 2;
-  static constexpr int kMetaWarp = kTile * 8 + kTile;  // int64 times + int8 types
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBytes;
-  static constexpr int kV = kK + NS * kKVBytes;
-  static constexpr int kP = kV + NS * kKVBytes;
-  static constexpr int kMeta = kP + kPBytes;
-  static constexpr int kBars = (kMeta + 4 * kMetaWarp + 7) & ~7;
-  static constexpr int kNumBars = 2 + 3 * NS + 2 + 1 + 1 + 1;
-  static constexpr int kTotal = kBars + kNumBars * 8 + 16;
+  static constexpr int kQ = 0;                                   // [stream][QB]
+  static constexpr int kK = kQ + kStreams * QB * kQBytes;        // [stream][NS]
+  static constexpr int kV = kK + kStreams * NS * kKVBytes;       // [stream][NS]
+  static constexpr int kRec = kV + kStreams * NS * kKVBytes;     // [stream][NS] KeyTileRec
+  static constexpr int kInfo = kRec + kStreams * NS * kRecBytes; // [stream][NS] StageInfo
+  static constexpr int kItems = (kInfo + kStreams * NS * 8 + 15) & ~15;  // [stream][2] ItemDesc
+  static constexpr int kBars = (kItems + kStreams * 2 * 32 + 7) & ~7;
+  static constexpr int kBarsPerStream = 2 + 2 + 2 * QB + 3 * NS + 4;
+  static constexpr int kTotal = kBars + kStreams * kBarsPerStream * 8 + 16;
   static constexpr int kDynamic = kTotal + 1024;  // slack to align the base to 1024 B
 };
 
-template <int NS>
-struct Bars {
-  uint64_t* q_full;
-  uint64_t* q_empty;
-  uint64_t* k_full;
-  uint64_t* v_full;
-  uint64_t* kv_empty;
-  uint64_t* s_full;  // [2]
-  uint64_t* p_full;
-  uint64_t* pv_done;
-  uint64_t* mma_done;
-  volatile int* abort_flag;
-  uint32_t* tmem_slot;
-  __device__ Bars(uint8_t* base) {
-    uint64_t* b = reinterpret_cast<uint64_t*>(base);
-    q_full = b; q_empty = b + 1; k_full = b + 2; v_full = k_full + NS; kv_empty = v_full + NS;
-    s_full = kv_empty + NS; p_full = s_full + 2; pv_done = p_full + 1; mma_done = pv_done + 1;
-    abort_flag = reinterpret_cast<volatile int*>(mma_done + 1);
-    tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1) + 1;
+// mbarriers of one stream
+struct SBars {
+  uint64_t *item_full, *item_empty, *q_full, *q_empty, *k_full, *v_full, *kv_empty;
+  uint64_t *s_full, *p_full, *o_ready, *mma_done;
+  template <int D>
+  __device__ void bind(uint64_t* b) {
+    constexpr int QB = Cfg<D>::QB, NS = Cfg<D>::NS;
+    item_full = b; item_empty = b + 2; q_full = b + 4; q_empty = q_full + QB;
+    k_full = q_empty + QB; v_full = k_full + NS; kv_empty = v_full + NS;
+    s_full = kv_empty + NS; p_full = s_full + 1; o_ready = p_full + 1; mma_done = o_ready + 1;
   }
 };
 
-// Bounded wait; on timeout raises the CTA abort flag and records the status.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         int* status) {
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (;;) {
@@ -88,13 +111,11 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     }
   }
 }
-// Bounded wait used only while shutting down after an abort.
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar, parity))
     if (ptx::globaltimer() - t0 > kWaitNs / 4) return;
 }
-// Warp-uniform wait: every lane waits, then the warp agrees on the outcome.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int* status) {
   const bool ok = wait_bar(bar, parity, abort_flag, status);
@@ -107,252 +128,369 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// ------------------------------------------------------------------ producer
-template <int D, int NS>
-__device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, const void* tv,
-                             uint8_t* sm, const Bars<NS>& B) {
-  using L = Layout<D, NS>;
-  uint32_t q_it = 0, kv_it = 0;
-  uint32_t stage_phase[NS];
-  bool stage_used[NS];
-  for (int s = 0; s < NS; ++s) { stage_phase[s] = 0; stage_used[s] = false; }
-  bool q_used = false;
-  uint32_t q_phase = 0;
-  ptx::prefetch_tensormap(tq);
-  ptx::prefetch_tensormap(tk);
-  ptx::prefetch_tensormap(tv);
-  for (long long w = blockIdx.x; w < a.n_items; w += gridDim.x) {
-    const WorkItem it = decode_item(a, w, true);
-    if (it.n == 0) continue;
-    if (!wait_bar(B.q_empty, (q_it & 1) ^ 1, B.abort_flag, a.status)) goto drain;
-    ptx::mbar_arrive_expect_tx(B.q_full, L::kQBytes);
-    {
-      const int y = (int)(it.m.tok_start + (long long)it.qt * kTile);
+// Bits lo..hi (inclusive, tile-local key indices) of a 128-bit mask.
+__device__ __forceinline__ void range_bits(int lo, int hi, uint32_t (&r)[4]) {
+  lo = max(lo, 0);
+  hi = min(hi, kTile - 1);
 #pragma unroll
-      for (int s = 0; s < D / 64; ++s) ptx::tma_load_2d(sm + L::kQ + s * kSlab, tq, it.h * D + s * 64, y, B.q_full);
+  for (int w = 0; w < 4; ++w) {
+    const int a = max(lo - 32 * w, 0), b = min(hi - 32 * w, 31);
+    r[w] = (a > b) ? 0u : ((0xffffffffu >> (31 - b)) & (0xffffffffu << a));
+  }
+}
+
+// A query row's visibility, per key type, as a position interval [plo, phi]
+// (request-local; empty when plo > phi) and an optional time bound t_j <= thr.
+struct RowMask {
+  int plo[kTypes], phi[kTypes];
+  long long thr[kTypes];
+  int timed[kTypes];
+};
+
+// The predicate of include/rec_attn.h, split per key type into the interval and time
+// clauses it reduces to for a fixed query row.
+__device__ __forceinline__ void row_mask_setup(const MaskP& m, bool row_ok, int pi, long long ti, int tyi,
+                                               RowMask& r) {
+  bool dok; long long dthr;
+  delay_bound(ti, m.delay, dok, dthr);
+  const bool valid = row_ok && (unsigned)tyi <= 3u;
+#pragma unroll
+  for (int c = 0; c < kTypes; ++c) {
+    int lo = INT_MIN / 2, hi = INT_MAX / 2;
+    bool vis = valid, timed = false;
+    long long thr = LLONG_MAX;
+    const bool uq = is_user(tyi), uk = is_user(c);
+    if (uq) {
+      if (!uk) {
+        vis = false;
+      } else if (!m.bidir) {
+        hi = pi;
+        if (m.window > 0 && tyi != REC_ATTN_GLOBAL && c != REC_ATTN_GLOBAL) lo = pi - m.window + 1;
+      }
+    } else if (tyi == REC_ATTN_RT) {
+      if (!uk) {
+        if (c == REC_ATTN_RT) hi = pi;
+        else vis = false;
+      }
+    } else {  // candidate query
+      if (!uk) {
+        if (c == REC_ATTN_RT) {  // real-time events strictly before the candidate
+          timed = true;
+          if (ti == LLONG_MIN) vis = false;
+          else thr = ti - 1;
+        } else {                 // itself only
+          lo = pi; hi = pi;
+        }
+      }
     }
-    q_used = true; q_phase = q_it & 1; ++q_it;
+    if (m.use_delay && !(tyi == REC_ATTN_CAND && c == REC_ATTN_CAND)) {
+      if (!dok) vis = false;
+      timed = true;
+      thr = min(thr, dthr);
+    }
+    r.plo[c] = vis ? lo : 1;
+    r.phi[c] = vis ? hi : 0;
+    r.thr[c] = thr;
+    r.timed[c] = timed ? 1 : 0;
+  }
+}
+
+// 128-bit visibility mask of one row against a PARTIAL key tile starting at
+// request-local position k0.
+__device__ __forceinline__ void build_mask(const RowMask& rm, const KeyTileRec* rec, int k0, uint32_t (&vm)[4]) {
+  vm[0] = vm[1] = vm[2] = vm[3] = 0u;
+#pragma unroll
+  for (int c = 0; c < kTypes; ++c) {
+    const int n = rec->run_n[c];
+    const int lo = rm.plo[c] - k0, hi = rm.phi[c] - k0;
+    if (n == 0 || lo > hi || hi < 0 || lo >= kTile) continue;
+    uint32_t r[4];
+    range_bits(lo, hi, r);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) r[w] &= rec->typebits[c][w];
+    if (rm.timed[c]) {
+      const long long thr = rm.thr[c];
+      if (rec->sorted[c]) {
+        // keys of this type form a run with non-decreasing times: count t_j <= thr
+        const int rl = rec->run_lo[c];
+        int first = 0, len = n;
+        while (len > 0) {
+          const int half = len >> 1;
+          if (rec->t[rl + first + half] <= thr) { first += half + 1; len -= half + 1; }
+          else len = half;
+        }
+        uint32_t tr[4];
+        range_bits(rl, rl + first - 1, tr);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) r[w] &= tr[w];
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t bits = 0;
+#pragma unroll 8
+          for (int b = 0; b < 32; ++b) bits |= (rec->t[w * 32 + b] <= thr ? 1u : 0u) << b;
+          r[w] &= bits;
+        }
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) vm[w] |= r[w];
+  }
+}
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, const void* tv, uint8_t* sm,
+                             int s, const SBars& B, volatile int* abort_flag) {
+  using L = Layout<D>;
+  constexpr int QB = L::QB, NS = L::NS;
+  ItemDesc* items = reinterpret_cast<ItemDesc*>(sm + L::kItems) + s * 2;
+  StageInfo* info = reinterpret_cast<StageInfo*>(sm + L::kInfo) + s * NS;
+  uint8_t* qbuf = sm + L::kQ + s * QB * L::kQBytes;
+  uint8_t* kbuf = sm + L::kK + s * NS * L::kKVBytes;
+  uint8_t* vbuf = sm + L::kV + s * NS * L::kKVBytes;
+  uint8_t* rbuf = sm + L::kRec + s * NS * kRecBytes;
+  uint32_t it_cnt = 0, q_it = 0, kv_it = 0;
+  bool q_used[QB], st_used[NS];
+  uint32_t q_ph[QB], st_ph[NS];
+  for (int i = 0; i < QB; ++i) { q_used[i] = false; q_ph[i] = 0; }
+  for (int i = 0; i < NS; ++i) { st_used[i] = false; st_ph[i] = 0; }
+  for (;;) {
+    const long long w = atomicAdd(a.counters + 1, 1);
+    const int slot = (int)(it_cnt & 1);
+    if (!wait_bar(B.item_empty + slot, ((it_cnt >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+    ++it_cnt;
+    ItemDesc* d = items + slot;
+    if (w >= a.n_items) {
+      d->end = 1;
+      ptx::mbar_arrive(B.item_full + slot);
+      break;
+    }
+    const WorkItem it = decode_item(a, w, true);
+    d->tok0 = it.m.tok_start + (long long)it.qt * kTile;
+    d->pos0 = it.qt * kTile;
+    d->rows = min(kTile, it.m.len - it.qt * kTile);
+    d->h = it.h;
+    d->n = it.n;
+    d->end = 0;
+    ptx::mbar_arrive(B.item_full + slot);
+    if (it.n == 0) continue;
+    const int qb = (int)(q_it % QB);
+    if (!wait_bar(B.q_empty + qb, ((q_it / QB) & 1) ^ 1, abort_flag, a.status)) break;
+    ptx::mbar_arrive_expect_tx(B.q_full + qb, L::kQBytes);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c)
+      ptx::tma_load_2d(qbuf + qb * L::kQBytes + c * kSlab, tq, it.h * D + c * 64, (int)d->tok0, B.q_full + qb);
+    q_used[qb] = true; q_ph[qb] = (q_it / QB) & 1;
+    ++q_it;
     for (int j = 0; j < it.n; ++j) {
-      const int kt = (int)(it.list[j] & 0xffffffu);
+      const uint32_t e = it.list[j];
+      const int kt = (int)(e & 0xffffffu), cl = (int)(e >> 24);
       const int st = (int)(kv_it % NS);
       const uint32_t ph = (kv_it / NS) & 1;
-      if (!wait_bar(B.kv_empty + st, ph ^ 1, B.abort_flag, a.status)) goto drain;
+      if (!wait_bar(B.kv_empty + st, ph ^ 1, abort_flag, a.status)) goto drain;
+      info[st].kt = kt;
+      info[st].cls = cl;
+      const bool partial = cl != REC_ATTN_TILE_FULL;
       const int y = (int)(it.m.tok_start + (long long)kt * kTile);
-      ptx::mbar_arrive_expect_tx(B.k_full + st, L::kKVBytes);
+      ptx::mbar_arrive_expect_tx(B.k_full + st, L::kKVBytes + (partial ? kRecBytes : 0));
 #pragma unroll
-      for (int s = 0; s < D / 64; ++s)
-        ptx::tma_load_2d(sm + L::kK + st * L::kKVBytes + s * kSlab, tk, it.h * D + s * 64, y, B.k_full + st);
+      for (int c = 0; c < D / 64; ++c)
+        ptx::tma_load_2d(kbuf + st * L::kKVBytes + c * kSlab, tk, it.h * D + c * 64, y, B.k_full + st);
+      if (partial) ptx::bulk_load(rbuf + st * kRecBytes, a.krec + it.m.tile_start + kt, kRecBytes, B.k_full + st);
       ptx::mbar_arrive_expect_tx(B.v_full + st, L::kKVBytes);
 #pragma unroll
-      for (int s = 0; s < D / 64; ++s)
-        ptx::tma_load_2d(sm + L::kV + st * L::kKVBytes + s * kSlab, tv, it.h * D + s * 64, y, B.v_full + st);
-      stage_used[st] = true; stage_phase[st] = ph;
+      for (int c = 0; c < D / 64; ++c)
+        ptx::tma_load_2d(vbuf + st * L::kKVBytes + c * kSlab, tv, it.h * D + c * 64, y, B.v_full + st);
+      st_used[st] = true; st_ph[st] = ph;
       ++kv_it;
     }
   }
 drain:
-  // Every load issued must land before the CTA exits (only waits after an abort).
-  if (q_used) drain_bar(B.q_full, q_phase);
-  for (int s = 0; s < NS; ++s)
-    if (stage_used[s]) { drain_bar(B.k_full + s, stage_phase[s]); drain_bar(B.v_full + s, stage_phase[s]); }
+  // every load issued must land before the CTA exits (only waits after an abort)
+  for (int i = 0; i < QB; ++i)
+    if (q_used[i]) drain_bar(B.q_full + i, q_ph[i]);
+  for (int i = 0; i < NS; ++i)
+    if (st_used[i]) { drain_bar(B.k_full + i, st_ph[i]); drain_bar(B.v_full + i, st_ph[i]); }
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D, int NS>
-__device__ void run_mma(const AttnArgs& a, uint8_t* sm, const Bars<NS>& B, uint32_t tmem) {
-  using L = Layout<D, NS>;
+template <int D>
+__device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, uint32_t tmem,
+                        volatile int* abort_flag) {
+  using L = Layout<D>;
+  constexpr int QB = L::QB, NS = L::NS;
   constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kTile, kTile, false, false);
   constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kTile, D, false, true);
-  const uint32_t q_addr = ptx::smem_u32(sm + L::kQ);
-  const uint32_t k_addr = ptx::smem_u32(sm + L::kK);
-  const uint32_t v_addr = ptx::smem_u32(sm + L::kV);
-  const uint32_t p_addr = ptx::smem_u32(sm + L::kP);
-  uint32_t q_it = 0, kv_it = 0, s_it = 0, p_it = 0;
-  for (long long w = blockIdx.x; w < a.n_items; w += gridDim.x) {
-    const WorkItem it = decode_item(a, w, true);
-    if (it.n == 0) continue;
-    if (!wait_bar(B.q_full, q_it & 1, B.abort_flag, a.status)) goto out;
+  const ItemDesc* items = reinterpret_cast<const ItemDesc*>(sm + L::kItems) + s * 2;
+  const uint32_t q_addr = ptx::smem_u32(sm + L::kQ + s * QB * L::kQBytes);
+  const uint32_t k_addr = ptx::smem_u32(sm + L::kK + s * NS * L::kKVBytes);
+  const uint32_t v_addr = ptx::smem_u32(sm + L::kV + s * NS * L::kKVBytes);
+  const uint32_t tm_s = tmem + (uint32_t)(s * kTile);
+  const uint32_t tm_o = tmem + 2u * kTile + (uint32_t)(s * D);
+  uint32_t it_cnt = 0, q_it = 0, kv_it = 0, p_it = 0;
+  for (;;) {
+    const int slot = (int)(it_cnt & 1);
+    if (!wait_bar(B.item_full + slot, (it_cnt >> 1) & 1, abort_flag, a.status)) break;
+    ++it_cnt;
+    const int end = items[slot].end, n = items[slot].n;
+    ptx::mbar_arrive(B.item_empty + slot);
+    if (end) break;
+    if (n == 0) continue;
+    const int qb = (int)(q_it % QB);
+    if (!wait_bar(B.q_full + qb, (q_it / QB) & 1, abort_flag, a.status)) break;
     ++q_it;
     ptx::tc_fence_after();
-    for (int j = -1; j < it.n; ++j) {
-      // S(j + 1) = Q' K'(j + 1)^T into S buffer (s_it & 1)
-      if (j + 1 < it.n) {
-        const int st = (int)((kv_it + j + 1) % NS);
-        const uint32_t ph = ((kv_it + j + 1) / NS) & 1;
-        if (!wait_bar(B.k_full + st, ph, B.abort_flag, a.status)) goto out;
+    const uint32_t qa = q_addr + qb * L::kQBytes;
+    for (int j = -1; j < n; ++j) {
+      if (j >= 0) {
+        // O += P(j) V(j), P read from TMEM
+        if (!wait_bar(B.p_full, p_it & 1, abort_flag, a.status)) goto out;
+        ++p_it;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem + ((s_it & 1) ? kTmemS1 : kTmemS0);
+        const int st = (int)((kv_it + j) % NS);
+        if (!wait_bar(B.v_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) goto out;
+        ptx::tc_fence_after();
+        const uint32_t vb = v_addr + st * L::kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          ptx::umma_f16_ts(tm_o, tm_s + kk * 8, ptx::smem_desc_sw128(vb + kk * 16 * 128, kSlab, 1024), idesc_o,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::umma_commit(B.kv_empty + st);
+      }
+      if (j + 1 < n) {
+        // S(j+1) = Q' K'(j+1)^T (overwrites P(j) after the PV MMA above has read it)
+        const int st = (int)((kv_it + j + 1) % NS);
+        if (!wait_bar(B.k_full + st, ((kv_it + j + 1) / NS) & 1, abort_flag, a.status)) goto out;
+        ptx::tc_fence_after();
         const uint32_t kb = k_addr + st * L::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-          ptx::umma_f16(d_tmem, ptx::smem_desc_sw128(q_addr + off, 16, 1024),
-                        ptx::smem_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0);
+          ptx::umma_f16(tm_s, ptx::smem_desc_sw128(qa + off, 16, 1024), ptx::smem_desc_sw128(kb + off, 16, 1024),
+                        idesc_s, kk > 0 ? 1u : 0u);
         }
-        ptx::umma_commit(B.s_full + (s_it & 1));
-        ++s_it;
-        if (j + 2 == it.n) ptx::umma_commit(B.q_empty);  // last S of the item issued
+        ptx::umma_commit(B.s_full);
+        if (j + 2 == n) ptx::umma_commit(B.q_empty + qb);  // last S of the item issued
       }
-      if (j < 0) continue;
-      // O += P(j) V(j)
-      if (!wait_bar(B.p_full, p_it & 1, B.abort_flag, a.status)) goto out;
-      ++p_it;
-      ptx::tc_fence_after();
-      const int st = (int)((kv_it + j) % NS);
-      const uint32_t ph = ((kv_it + j) / NS) & 1;
-      if (!wait_bar(B.v_full + st, ph, B.abort_flag, a.status)) goto out;
-      ptx::tc_fence_after();
-      const uint32_t vb = v_addr + st * L::kKVBytes;
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint32_t pa = p_addr + (kk >> 2) * kSlab + (kk & 3) * 32;
-        const uint32_t va = vb + kk * 16 * 128;  // 16 keys per step, 128 B per key row
-        ptx::umma_f16(tmem + kTmemO, ptx::smem_desc_sw128(pa, 16, 1024), ptx::smem_desc_sw128(va, kSlab, 1024),
-                      idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      ptx::umma_commit(B.pv_done);
-      ptx::umma_commit(B.kv_empty + st);
     }
-    kv_it += it.n;
+    ptx::umma_commit(B.o_ready);
+    kv_it += n;
   }
 out:
-  // All issued MMAs must complete before TMEM is released.
+  // all issued MMAs must complete before TMEM is released
   ptx::umma_commit(B.mma_done);
   drain_bar(B.mma_done, 0);
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D, int NS>
-__device__ void run_softmax(const AttnArgs& a, uint8_t* sm, const Bars<NS>& B, uint32_t tmem, int sw) {
-  using L = Layout<D, NS>;
+template <int D>
+__device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, uint32_t tmem,
+                            volatile int* abort_flag) {
+  using L = Layout<D>;
+  constexpr int NS = L::NS;
+  const ItemDesc* items = reinterpret_cast<const ItemDesc*>(sm + L::kItems) + s * 2;
+  const StageInfo* info = reinterpret_cast<const StageInfo*>(sm + L::kInfo) + s * NS;
+  const KeyTileRec* recs = reinterpret_cast<const KeyTileRec*>(sm + L::kRec) + s * NS;
   const int lane = threadIdx.x & 31;
   const int quad = (threadIdx.x >> 5) & 3;  // TMEM lanes this warp may access
   const int row = quad * 32 + lane;
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  long long* kmt = reinterpret_cast<long long*>(sm + L::kMeta + sw * L::kMetaWarp);
-  int8_t* kmy = reinterpret_cast<int8_t*>(kmt + kTile);
-  uint8_t* prow = sm + L::kP + row * 128;
+  const uint32_t tm_s = tmem + lane_off + (uint32_t)(s * kTile);
+  const uint32_t tm_o = tmem + lane_off + 2u * kTile + (uint32_t)(s * D);
   const float sl2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
   const int H = a.heads;
-  uint32_t s_it = 0, pv_it = 0;
-  for (long long w = blockIdx.x; w < a.n_items; w += gridDim.x) {
-    const WorkItem it = decode_item(a, w, true);
-    const int pi = it.qt * kTile + row;
-    const bool row_ok = pi < it.m.len;
-    const long long tok = it.m.tok_start + pi;
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (tok * H + it.h) * D;
-    if (it.n == 0) {
+  uint32_t it_cnt = 0, kv_it = 0, s_it = 0, o_it = 0;
+  for (;;) {
+    const int slot = (int)(it_cnt & 1);
+    if (!wait_bar_warp(B.item_full + slot, (it_cnt >> 1) & 1, abort_flag, a.status)) return;
+    ++it_cnt;
+    const ItemDesc d = items[slot];
+    ptx::mbar_arrive(B.item_empty + slot);
+    if (d.end) return;
+    const bool row_ok = row < d.rows;
+    const int pi = d.pos0 + row;
+    const long long tok = d.tok0 + row;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (tok * H + d.h) * D;
+    if (d.n == 0) {
       if (row_ok) {
-        uint4 z = make_uint4(0, 0, 0, 0);
+        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
-        if (a.lse) a.lse[tok * H + it.h] = -INFINITY;
+        if (a.lse) a.lse[tok * H + d.h] = -INFINITY;
       }
       continue;
     }
     long long ti = 0;
     int tyi = -1;
     if (row_ok) { ti = a.t[tok]; tyi = a.ty[tok]; }
-    bool thr_ok; long long thr;
-    delay_bound(ti, a.mask.delay, thr_ok, thr);
-    float m_run = -INFINITY, l = 0.f;
-    for (int j = 0; j < it.n; ++j) {
-      const uint32_t ent = it.list[j];
-      const int kt = (int)(ent & 0xffffffu);
-      const bool partial = (ent >> 24) != REC_ATTN_TILE_FULL;
-      if (partial) {  // key metadata of this tile, staged per warp
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < kTile / 32; ++u) {
-          const int c = lane + 32 * u, pj = kt * kTile + c;
-          const bool ok = pj < it.m.len;
-          kmt[c] = ok ? a.t[it.m.tok_start + pj] : 0;
-          kmy[c] = ok ? a.ty[it.m.tok_start + pj] : (int8_t)-1;
-        }
-        __syncwarp();
-      }
-      if (!wait_bar_warp(B.s_full + (s_it & 1), (s_it >> 1) & 1, B.abort_flag, a.status)) return;
+    RowMask rm;
+    row_mask_setup(a.mask, row_ok, pi, ti, tyi, rm);
+    float m_ref = -INFINITY, l = 0.f;
+    for (int j = 0; j < d.n; ++j) {
+      const int st = (int)(kv_it % NS);
+      const uint32_t kph = (kv_it / NS) & 1;
+      ++kv_it;
+      // the stage's tile info and key record (written by the producer / bulk copy)
+      if (!wait_bar_warp(B.k_full + st, kph, abort_flag, a.status)) return;
+      const StageInfo inf = info[st];
+      if (!wait_bar_warp(B.s_full, s_it & 1, abort_flag, a.status)) return;
+      ++s_it;
       ptx::tc_fence_after();
       uint32_t sr[kTile];
-      ptx::tmem_ld128(tmem + lane_off + ((s_it & 1) ? kTmemS1 : kTmemS0), sr);
-      ++s_it;
-      float s[kTile];
+      ptx::tmem_ld128(tm_s, sr);
+      float x[kTile];
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) s[c] = __uint_as_float(sr[c]);
-      if (partial) {
-        uint32_t vm[kTile / 32];
-#pragma unroll
-        for (int w4 = 0; w4 < kTile / 32; ++w4) {
-          uint32_t bits = 0;
-#pragma unroll 4
-          for (int b = 0; b < 32; ++b) {
-            const int c = w4 * 32 + b;
-            const bool v = vis_pred(a.mask, pi, ti, tyi, thr_ok, thr, kt * kTile + c, kmt[c], kmy[c]);
-            bits |= (v ? 1u : 0u) << b;
-          }
-          vm[w4] = row_ok ? bits : 0u;
-        }
+      for (int c = 0; c < kTile; ++c) x[c] = __uint_as_float(sr[c]);
+      if (inf.cls != REC_ATTN_TILE_FULL) {
+        uint32_t vm[4];
+        build_mask(rm, recs + st, inf.kt * kTile, vm);
 #pragma unroll
         for (int c = 0; c < kTile; ++c)
-          if (!((vm[c >> 5] >> (c & 31)) & 1u)) s[c] = -INFINITY;
+          if (!((vm[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
       }
-      float mx = s[0];
+      float mx = x[0];
 #pragma unroll
-      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, s[c]);
+      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, x[c]);
       const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
-      const float m_new = fmaxf(m_run, m_tile);
+      const float m_new = (m_tile > m_ref + kRescaleLog2) ? m_tile : m_ref;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float corr = ex2(m_run - m_use);
+      const float corr = ex2(m_ref - m_use);  // 0 when m_ref = -inf, 1 when unchanged
       uint32_t pk[kTile / 2];
       float rs = 0.f;
 #pragma unroll
       for (int c = 0; c < kTile / 2; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], sl2, -m_use));
-        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, -m_use));
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+        const __nv_bfloat162 pb =
+            __floats2bfloat162_rn(ex2(fmaf(x[2 * c], sl2, -m_use)), ex2(fmaf(x[2 * c + 1], sl2, -m_use)));
         rs += __low2float(pb) + __high2float(pb);
         pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
       }
       l = l * corr + rs;
-      if (j > 0) {
-        // PV(j-1) must be done before P is overwritten and before O is rescaled.
-        if (!wait_bar_warp(B.pv_done, pv_it & 1, B.abort_flag, a.status)) return;
-        ++pv_it;
-        ptx::tc_fence_after();
-        if (__any_sync(0xffffffffu, corr != 1.f)) {
+      // O holds PV(0..j-1): S(j) was issued after PV(j-1), so its completion implies it
+      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
-          for (int half = 0; half < D / 64; ++half) {
-            uint32_t o[64];
-            const uint32_t ta = tmem + lane_off + kTmemO + half * 64;
-            ptx::tmem_ld64(ta, o);
+        for (int half = 0; half < D / 64; ++half) {
+          uint32_t o[64];
+          ptx::tmem_ld64(tm_o + half * 64, o);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-            ptx::tmem_st64(ta, o);
-          }
+          for (int e = 0; e < 64; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+          ptx::tmem_st64(tm_o + half * 64, o);
         }
       }
-      // P row -> shared memory, K-major with the 128-byte swizzle (16-byte chunk
-      // index XOR row % 8), two 64-key slabs.
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        const int slab = c16 >> 3, cc = c16 & 7;
-        uint4 v4 = make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-        *reinterpret_cast<uint4*>(prow + slab * kSlab + ((cc ^ (row & 7)) << 4)) = v4;
-      }
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_st64(tm_s, pk);  // P(j) over the first 64 columns of S(j)
       ptx::tc_fence_before();
       ptx::mbar_arrive(B.p_full);
-      m_run = m_new;
+      m_ref = m_new;
     }
     // epilogue: O / l
-    if (!wait_bar_warp(B.pv_done, pv_it & 1, B.abort_flag, a.status)) return;
-    ++pv_it;
+    if (!wait_bar_warp(B.o_ready, o_it & 1, abort_flag, a.status)) return;
+    ++o_it;
     ptx::tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int half = 0; half < D / 64; ++half) {
       uint32_t o[64];
-      ptx::tmem_ld64(tmem + lane_off + kTmemO + half * 64, o);
+      ptx::tmem_ld64(tm_o + half * 64, o);
       if (row_ok) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -368,70 +506,100 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, const Bars<NS>& B, u
       }
     }
     if (row_ok && a.lse) {
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      a.lse[tok * H + it.h] = l > 0.f ? (m_use + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      a.lse[tok * H + d.h] = l > 0.f ? (m_use + __log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
-    ptx::tc_fence_before();
+    ptx::tc_fence_before();  // O reads ordered before the next item's PV(0)
   }
 }
 
-template <int D, int NS>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  using L = Layout<D, NS>;
+  using L = Layout<D>;
+  constexpr int QB = L::QB, NS = L::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars<NS> B(sm + L::kBars);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kStreams * L::kBarsPerStream);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kStreams * L::kBarsPerStream) + 1;
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    ptx::mbar_init(B.q_full, 1);
-    ptx::mbar_init(B.q_empty, 1);
-    for (int s = 0; s < NS; ++s) {
-      ptx::mbar_init(B.k_full + s, 1);
-      ptx::mbar_init(B.v_full + s, 1);
-      ptx::mbar_init(B.kv_empty + s, 1);
+    for (int s = 0; s < kStreams; ++s) {
+      SBars B;
+      B.bind<D>(bars + s * L::kBarsPerStream);
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(B.item_full + i, 1);
+        ptx::mbar_init(B.item_empty + i, 1 + 128);
+      }
+      for (int i = 0; i < QB; ++i) {
+        ptx::mbar_init(B.q_full + i, 1);
+        ptx::mbar_init(B.q_empty + i, 1);
+      }
+      for (int i = 0; i < NS; ++i) {
+        ptx::mbar_init(B.k_full + i, 1);
+        ptx::mbar_init(B.v_full + i, 1);
+        ptx::mbar_init(B.kv_empty + i, 1);
+      }
+      ptx::mbar_init(B.s_full, 1);
+      ptx::mbar_init(B.p_full, 128);
+      ptx::mbar_init(B.o_ready, 1);
+      ptx::mbar_init(B.mma_done, 1);
     }
-    ptx::mbar_init(B.s_full, 1);
-    ptx::mbar_init(B.s_full + 1, 1);
-    ptx::mbar_init(B.p_full, 128);
-    ptx::mbar_init(B.pv_done, 1);
-    ptx::mbar_init(B.mma_done, 1);
-    *B.abort_flag = 0;
+    *abort_flag = 0;
     ptx::fence_barrier_init();
   }
-  if (warp == 1) {
-    ptx::tmem_alloc(B.tmem_slot, kTmemCols);
+  if (warp == 2) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = *B.tmem_slot;
+  const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) run_producer<D, NS>(a, &tm_q, &tm_k, &tm_v, sm, B);
-  } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0) run_mma<D, NS>(a, sm, B, tmem);
+  if (warp < 4) {
+    ptx::setmaxnreg_dec<56>();
+    const int s = warp & 1;
+    SBars B;
+    B.bind<D>(bars + s * L::kBarsPerStream);
+    if ((threadIdx.x & 31) == 0) {
+      if (warp < 2) run_producer<D>(a, &tm_q, &tm_k, &tm_v, sm, s, B, abort_flag);
+      else run_mma<D>(a, sm, s, B, tmem, abort_flag);
+    }
   } else {
-    run_softmax<D, NS>(a, sm, B, tmem, warp - 2);
+    ptx::setmaxnreg_inc<224>();
+    const int s = (warp - 4) >> 2;
+    SBars B;
+    B.bind<D>(bars + s * L::kBarsPerStream);
+    run_softmax<D>(a, sm, s, B, tmem, abort_flag);
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
+  // the last CTA to leave resets the item counter for the next launch
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.counters + 2, 1) == (int)gridDim.x - 1) {
+      atomicExch(a.counters + 1, 0);
+      atomicExch(a.counters + 2, 0);
+    }
+  }
 }
 
-template <int D, int NS>
-cudaError_t launch(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                   int grid, cudaStream_t st) {
-  using L = Layout<D, NS>;
-  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<D, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
+template <int D>
+cudaError_t launch(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, int grid,
+                   cudaStream_t st) {
+  using L = Layout<D>;
+  static_assert(L::kDynamic <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
   if (e != cudaSuccess) return e;
-  k_attn_tc<D, NS><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
+  k_attn_tc<D><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
   return cudaGetLastError();
 }
 
@@ -441,8 +609,8 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& q, const CUtens
                            int head_dim, int grid, cudaStream_t st) {
   if (a.n_items <= 0) return cudaSuccess;
   switch (head_dim) {
-    case 64: return launch<64, 3>(a, q, k, v, grid, st);
-    case 128: return launch<128, 2>(a, q, k, v, grid, st);
+    case 64: return launch<64>(a, q, k, v, grid, st);
+    case 128: return launch<128>(a, q, k, v, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -20,6 +20,7 @@
 
 #include "launchers.cuh"
 #include "rec_attn.h"
+#include "workspace.cuh"
 
 #define REC_ATTN_API extern "C" __attribute__((visibility("default")))
 
@@ -37,8 +38,6 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_scratch_dev[kMaxDevices] = {};
-
-size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 rec_attn_status status_of(cudaError_t e) {
   if (e == cudaSuccess) return REC_ATTN_OK;
@@ -122,24 +121,13 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
       NC += nt * nt;
     }
     T = offsets_host[batch];
-    if (T >= (1LL << 31)) return REC_ATTN_ERR_UNSUPPORTED;
+    if (T >= (1LL << 31) || NT * params->num_heads >= (1LL << 31)) return REC_ATTN_ERR_UNSUPPORTED;
   }
   const size_t elem = params->dtype == REC_ATTN_BF16 ? 2 : 4;
   const size_t tensor_bytes = (size_t)T * params->num_heads * params->head_dim * elem;
   // workspace layout inside the static array
-  size_t off = 0;
-  const size_t o_hdr = off; off = up256(off + 256);
-  const size_t o_meta = off; off = up256(off + sizeof(ReqMeta) * (size_t)batch);
-  const size_t o_box = off; off = up256(off + sizeof(TileBox) * kTypes * (size_t)NT);
-  const size_t o_cls = off; off = up256(off + (size_t)NC);
-  const size_t o_kl = off; off = up256(off + 4 * (size_t)NC);
-  const size_t o_kc = off; off = up256(off + 4 * (size_t)NT);
-  const size_t o_qc = off; off = up256(off + 4 * (size_t)NT);
-  const size_t o_qr = off; off = up256(off + 4 * (size_t)NT);
-  const size_t o_qo = off; off = up256(off + 4 * (size_t)NT);
-  const size_t o_rq = off; off = up256(off + (params->use_rope ? tensor_bytes : 0));
-  const size_t o_rk = off; off = up256(off + (params->use_rope ? tensor_bytes : 0));
-  if (off > kScratchBytes) return REC_ATTN_ERR_UNSUPPORTED;  // batch too large for the static workspace
+  const WsLayout lay = ws_layout(batch, NT, NC, params->use_rope ? tensor_bytes : 0);
+  if (lay.total > kScratchBytes) return REC_ATTN_ERR_UNSUPPORTED;  // batch too large for the static workspace
   if (T > 0) {
     if (!offsets_dev || !timestamps_dev || !types_dev || !q || !k || !v || !out) return REC_ATTN_ERR_INVALID_ARG;
     const void* ptrs[4] = {q, k, v, out};
@@ -164,21 +152,10 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   if (e != cudaSuccess) return status_of(e);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(base);
-  PlanDev pd{};
-  pd.counters = reinterpret_cast<int*>(w + o_hdr);
-  pd.status = pd.counters + 8;
-  pd.pairs = reinterpret_cast<unsigned long long*>(w + o_hdr + 64);
-  pd.meta = reinterpret_cast<ReqMeta*>(w + o_meta);
-  pd.boxes = reinterpret_cast<TileBox*>(w + o_box);
-  pd.cls = reinterpret_cast<uint8_t*>(w + o_cls);
-  pd.klist = reinterpret_cast<uint32_t*>(w + o_kl);
-  pd.kcount = reinterpret_cast<int*>(w + o_kc);
-  pd.qcost = reinterpret_cast<int*>(w + o_qc);
-  pd.qreq = reinterpret_cast<int*>(w + o_qr);
-  pd.qorder = reinterpret_cast<int*>(w + o_qo);
+  const PlanDev pd = ws_bind(w, lay);
 
   // the previous call's counters and status stay in the array: clear them
-  e = cudaMemsetAsync(w + o_hdr, 0, 256, s);
+  e = cudaMemsetAsync(w + lay.hdr, 0, 256, s);
   // request table, uploaded from a stack buffer in chunks (pageable copies are staged
   // before cudaMemcpyAsync returns, so the buffer can be refilled at once)
   ReqMeta chunk[128];
@@ -213,7 +190,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   if (params->use_rope) {
     RopeArgs ra;
     ra.meta = pd.meta; ra.qreq = pd.qreq; ra.t = t;
-    ra.q = q; ra.k = k; ra.qr = w + o_rq; ra.kr = w + o_rk;
+    ra.q = q; ra.k = k; ra.qr = w + lay.rq; ra.kr = w + lay.rk;
     ra.heads = params->num_heads; ra.head_dim = params->head_dim;
     for (int i = 0; i < kMaxPairs; ++i)
       ra.omega[i] = i < params->head_dim / 2
@@ -222,11 +199,12 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
                         : 0.f;
     e = launch_rope(ra, params->dtype, NT, s);
     if (e != cudaSuccess) return status_of(e);
-    qs = w + o_rq;
-    ks = w + o_rk;
+    qs = w + lay.rq;
+    ks = w + lay.rk;
   }
   AttnArgs a;
   a.meta = pd.meta; a.qreq = pd.qreq; a.kcount = pd.kcount; a.klist = pd.klist; a.qorder = pd.qorder;
+  a.counters = pd.counters; a.krec = pd.krec;
   a.t = t; a.ty = types_dev; a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = pd.status;
   a.n_items = NT * params->num_heads; a.heads = params->num_heads;
   a.scale = params->softmax_scale > 0.f ? params->softmax_scale : 1.f / std::sqrt((float)params->head_dim);

@@ -99,43 +99,69 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, PlanDev pd, con
   if (threadIdx.x == 0 && (offsets[b] != m.tok_start || offsets[b + 1] != m.tok_start + m.len))
     set_status(pd.status, REC_ATTN_ERR_DEVICE_INPUT);
 
-  // Phase 1: bounding boxes of each type in each tile (one warp per tile).
+  // Phase 1 (one warp per tile): per-type bounding boxes, and the key-tile record the
+  // attention kernel builds visibility bits from.
   for (int tl = warp; tl < m.ntiles; tl += nwarps) {
-    int cnt[kTypes], pmin[kTypes], pmax[kTypes];
-    long long tmin[kTypes], tmax[kTypes];
+    long long kt_t[4];
+    int kt_y[4];
 #pragma unroll
-    for (int c = 0; c < kTypes; ++c) {
-      cnt[c] = 0; pmin[c] = 0x7fffffff; pmax[c] = -1;
-      tmin[c] = 0x7fffffffffffffffLL; tmax[c] = -0x7fffffffffffffffLL - 1;
-    }
-    for (int r = lane; r < kTile; r += 32) {
-      const int pos = tl * kTile + r;
-      if (pos >= m.len) break;
-      const long long tt = t[m.tok_start + pos];
-      const int c = ty[m.tok_start + pos];
-      if ((unsigned)c > 3u || tt >= kTimeLimit || tt <= -kTimeLimit) {
-        set_status(pd.status, REC_ATTN_ERR_DEVICE_INPUT);
-        if ((unsigned)c > 3u) continue;
-      }
-#pragma unroll
-      for (int e = 0; e < kTypes; ++e) {
-        if (e != c) continue;
-        cnt[e] += 1;
-        pmin[e] = min(pmin[e], pos); pmax[e] = max(pmax[e], pos);
-        tmin[e] = min(tmin[e], tt); tmax[e] = max(tmax[e], tt);
+    for (int u = 0; u < 4; ++u) {
+      const int pos = tl * kTile + u * 32 + lane;
+      kt_t[u] = 0;
+      kt_y[u] = -1;
+      if (pos < m.len) {
+        const long long tt = t[m.tok_start + pos];
+        const int c = ty[m.tok_start + pos];
+        if ((unsigned)c > 3u || tt >= kTimeLimit || tt <= -kTimeLimit) set_status(pd.status, REC_ATTN_ERR_DEVICE_INPUT);
+        kt_t[u] = tt;
+        kt_y[u] = (unsigned)c > 3u ? -1 : c;
       }
     }
+    // next key's type and time, for the sortedness check of each type's run
+    long long nx_t[4];
+    int nx_y[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      nx_t[u] = __shfl_down_sync(0xffffffffu, kt_t[u], 1);
+      nx_y[u] = __shfl_down_sync(0xffffffffu, kt_y[u], 1);
+      const long long t0 = __shfl_sync(0xffffffffu, kt_t[u < 3 ? u + 1 : u], 0);
+      const int y0 = __shfl_sync(0xffffffffu, kt_y[u < 3 ? u + 1 : u], 0);
+      if (lane == 31) { nx_t[u] = t0; nx_y[u] = u < 3 ? y0 : -1; }
+    }
+    KeyTileRec* rec = pd.krec + (m.tile_start + tl);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) rec->t[u * 32 + lane] = kt_t[u];
 #pragma unroll
     for (int c = 0; c < kTypes; ++c) {
-      int n = cnt[c];
+      int n = 0, pmn = 0x7fffffff, pmx = -1;
+      long long tmn = 0x7fffffffffffffffLL, tmx = -0x7fffffffffffffffLL - 1;
+      bool bad = false;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool mine = kt_y[u] == c;
+        const unsigned bits = __ballot_sync(0xffffffffu, mine);
+        if (lane == 0) rec->typebits[c][u] = bits;
+        if (mine) {
+          const int pos = tl * kTile + u * 32 + lane;
+          n += 1;
+          pmn = min(pmn, pos); pmx = max(pmx, pos);
+          tmn = min(tmn, kt_t[u]); tmx = max(tmx, kt_t[u]);
+          bad |= (nx_y[u] == c && nx_t[u] < kt_t[u]);
+        }
+      }
 #pragma unroll
       for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-      const int a0 = warp_min(pmin[c]), a1 = warp_max(pmax[c]);
-      const long long a2 = warp_min(tmin[c]), a3 = warp_max(tmax[c]);
+      const int a0 = warp_min(pmn), a1 = warp_max(pmx);
+      const long long a2 = warp_min(tmn), a3 = warp_max(tmx);
+      const bool any_bad = __any_sync(0xffffffffu, bad);
       if (lane == 0) {
         TileBox bx;
         bx.cnt = n; bx.pmin = a0; bx.pmax = a1; bx.pad = 0; bx.tmin = a2; bx.tmax = a3;
         pd.boxes[(m.tile_start + tl) * kTypes + c] = bx;
+        rec->run_lo[c] = n ? a0 - tl * kTile : 0;
+        rec->run_n[c] = n;
+        rec->sorted[c] = (n > 0 && a1 - a0 + 1 == n && !any_bad) ? 1 : 0;
+        rec->pad[c] = 0;
       }
     }
   }

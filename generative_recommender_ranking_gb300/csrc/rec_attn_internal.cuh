@@ -29,6 +29,19 @@ struct TileBox {
   long long tmin, tmax;
 };
 
+// Per key tile, what the attention kernel needs to build a row's visibility bits
+// without per-element predicate calls (filled by the planner, copied into shared
+// memory next to the K tile for PARTIAL tiles).
+struct KeyTileRec {
+  uint32_t typebits[kTypes][4];  // bit c of word c/32: key c of the tile has this type
+  int run_lo[kTypes];            // first key (tile-local) of the type
+  int run_n[kTypes];             // keys of the type in the tile
+  int sorted[kTypes];            // 1: the type's keys are contiguous with non-decreasing times
+  int pad[kTypes];
+  long long t[kTile];            // key timestamps (0 past the request end)
+};
+static_assert(sizeof(KeyTileRec) == 1152, "record must stay a multiple of 16 bytes");
+
 // Mask parameters as the kernels see them.
 struct MaskP {
   int use_delay;
@@ -42,13 +55,14 @@ struct MaskP {
 struct PlanDev {
   ReqMeta* meta;        // [B]
   TileBox* boxes;       // [NT][4]
+  KeyTileRec* krec;     // [NT]
   uint8_t* cls;         // [NC]
   uint32_t* klist;      // [NC]: per query tile, the non-SKIP key tiles (kt | class << 24)
   int* kcount;          // [NT]: entries in each query tile's list
   int* qcost;           // [NT]: scheduling cost of each query tile
   int* qreq;            // [NT]: request of each query tile
   int* qorder;          // [NT]: query tiles, most expensive first
-  int* counters;        // [4]: plan ticket, scheduler, spare
+  int* counters;        // [8]: plan ticket, attention item counter, attention exit ticket
   int* status;          // [1]: first device error (rec_attn_status)
   unsigned long long* pairs;  // [1]: visible-pair counter
 };

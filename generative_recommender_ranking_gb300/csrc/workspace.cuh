@@ -1,0 +1,54 @@
+// workspace.cuh -- layout of a plan's device workspace (shared by the plan-based
+// entry points and the no-allocation entry point).
+#pragma once
+
+#include <cstddef>
+
+#include "rec_attn_internal.cuh"
+
+namespace recattn {
+
+struct WsLayout {
+  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, qo, rq, rk, total;
+};
+
+inline size_t ws_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+// rot_bytes: bytes of one rotated [T][H][d] copy (0 when the RoPE is off).
+inline WsLayout ws_layout(long long batch, long long NT, long long NC, size_t rot_bytes) {
+  WsLayout L;
+  size_t off = 0;
+  L.hdr = off; off = ws_up(off + 256);
+  L.meta = off; off = ws_up(off + sizeof(ReqMeta) * (size_t)batch);
+  L.box = off; off = ws_up(off + sizeof(TileBox) * kTypes * (size_t)NT);
+  L.rec = off; off = ws_up(off + sizeof(KeyTileRec) * (size_t)NT);
+  L.cls = off; off = ws_up(off + (size_t)NC);
+  L.kl = off; off = ws_up(off + 4 * (size_t)NC);
+  L.kc = off; off = ws_up(off + 4 * (size_t)NT);
+  L.qc = off; off = ws_up(off + 4 * (size_t)NT);
+  L.qr = off; off = ws_up(off + 4 * (size_t)NT);
+  L.qo = off; off = ws_up(off + 4 * (size_t)NT);
+  L.rq = off; off = ws_up(off + rot_bytes);
+  L.rk = off; off = ws_up(off + rot_bytes);
+  L.total = off;
+  return L;
+}
+
+inline PlanDev ws_bind(char* w, const WsLayout& L) {
+  PlanDev pd{};
+  pd.counters = reinterpret_cast<int*>(w + L.hdr);
+  pd.status = pd.counters + 8;
+  pd.pairs = reinterpret_cast<unsigned long long*>(w + L.hdr + 64);
+  pd.meta = reinterpret_cast<ReqMeta*>(w + L.meta);
+  pd.boxes = reinterpret_cast<TileBox*>(w + L.box);
+  pd.krec = reinterpret_cast<KeyTileRec*>(w + L.rec);
+  pd.cls = reinterpret_cast<uint8_t*>(w + L.cls);
+  pd.klist = reinterpret_cast<uint32_t*>(w + L.kl);
+  pd.kcount = reinterpret_cast<int*>(w + L.kc);
+  pd.qcost = reinterpret_cast<int*>(w + L.qc);
+  pd.qreq = reinterpret_cast<int*>(w + L.qr);
+  pd.qorder = reinterpret_cast<int*>(w + L.qo);
+  return pd;
+}
+
+}  // namespace recattn
