@@ -50,12 +50,14 @@ def _peaks():
                 "source": "fallback"}
 
 
-def _workload(name, rank):
-    seed_kw = {}
+def _workload(name, rank, batch=None):
+    kw = {}
     if rank:
         base = {"tiny_fp32": 1001, "cadet": 1002, "sort": 1003, "mtgr": 1004}.get(name, 1005)
-        seed_kw["seed"] = base + 7919 * rank
-    return W.make(name, **seed_kw)
+        kw["seed"] = base + 7919 * rank
+    if batch:
+        kw["batch"] = batch
+    return W.make(name, **kw)
 
 
 def _config(w: W.Workload, name: str, parallelism: str):
@@ -152,7 +154,7 @@ def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
-    w = _workload(args.workload, 0)
+    w = _workload(args.workload, 0, args.batch)
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         _oracle_sample(w, per_step / 4)
@@ -199,7 +201,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
 
-    w = _workload(args.workload, rank)
+    w = _workload(args.workload, rank, args.batch)
     bf16 = w.dtype == "bf16"
     elem = 2 if bf16 else 4
 
@@ -360,6 +362,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="cadet", choices=W.NAMES)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's number of requests (small profiling cases)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

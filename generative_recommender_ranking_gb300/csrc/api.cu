@@ -217,7 +217,7 @@ REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_
   // workspace layout
   const size_t elem = params->dtype == REC_ATTN_BF16 ? 2 : 4;
   const size_t qk_bytes = (size_t)T * params->num_heads * params->head_dim * elem;
-  const WsLayout lay = ws_layout(batch, NT, NC, params->use_rope ? qk_bytes : 0);
+  const WsLayout lay = ws_layout(batch, NT, NC, params->num_heads, params->use_rope ? qk_bytes : 0);
   plan->ws_bytes = lay.total;
 
   cudaMemPool_t pool;
@@ -234,7 +234,7 @@ REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_
   if (e == cudaSuccess && batch > 0)
     e = cudaMemcpyAsync(pd.meta, meta.data(), sizeof(ReqMeta) * (size_t)batch, cudaMemcpyHostToDevice, plan->stream);
   if (e == cudaSuccess)
-    e = launch_plan(plan->mask, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t, plan->ty, batch, NT,
+    e = launch_plan(plan->mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t, plan->ty, batch, NT,
                     plan->stream);
   if (e != cudaSuccess) {
     cudaFreeAsync(plan->ws, plan->stream);
@@ -295,7 +295,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, 
   }
   AttnArgs a;
   a.meta = plan->pd.meta; a.qreq = plan->pd.qreq; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
-  a.qorder = plan->pd.qorder; a.t = plan->t; a.ty = plan->ty;
+  a.items = plan->pd.items; a.t = plan->t; a.ty = plan->ty;
   a.counters = plan->pd.counters; a.krec = plan->pd.krec;
   a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = plan->pd.status;
   a.n_items = plan->NT * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale; a.mask = plan->mask;

@@ -10,7 +10,7 @@ struct AttnArgs {
   const int* qreq;
   const int* kcount;
   const uint32_t* klist;
-  const int* qorder;
+  const int* items;  // work items (query tile * H + head), execution order
   const long long* t;
   const int8_t* ty;
   const void* q;     // rotated (or raw when RoPE is off) queries [T][H][d]
@@ -51,8 +51,9 @@ struct WorkItem {
 
 __device__ __forceinline__ WorkItem decode_item(const AttnArgs& a, long long w, bool ordered) {
   WorkItem it;
-  const long long qg = ordered ? (long long)a.qorder[w / a.heads] : w / a.heads;
-  it.h = (int)(w % a.heads);
+  const long long e = ordered ? (long long)a.items[w] : w;
+  const long long qg = e / a.heads;
+  it.h = (int)(e % a.heads);
   it.m = a.meta[a.qreq[qg]];
   it.qt = (int)(qg - it.m.tile_start);
   it.n = a.kcount[qg];

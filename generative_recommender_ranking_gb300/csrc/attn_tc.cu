@@ -8,7 +8,8 @@
 // One persistent CTA per SM runs two independent item streams, so the tensor core
 // works on one stream while the other stream's softmax runs.  12 warps:
 //   warp 0, 1     TMA producers (stream 0, 1): claim items from a global counter in
-//                 longest-first order, publish item descriptors and per-stage tile
+//                 the planner's order (heaviest items first, then request by request,
+//                 head by head), publish item descriptors and per-stage tile
 //                 info in shared memory, load Q', K', V (and, for PARTIAL tiles, the
 //                 key-tile record) with TMA / bulk copies into per-stream rings;
 //   warp 2, 3     MMA issuers (stream 0, 1): S = Q'K'^T into the stream's TMEM S
@@ -20,9 +21,12 @@
 //                 bitmaps and, for time clauses, a binary search over time-sorted
 //                 runs; FULL tiles skip the mask.  Online softmax in the exp2 domain
 //                 with a lazily updated reference maximum; O rescaled in TMEM only when
-//                 the maximum grows by more than 2^8; P rounded to bf16 and the row sum
-//                 l accumulated from the rounded values, so every output row is an
-//                 exact convex combination of the value rows it saw.
+//                 the maximum grows by more than 2^8; P rounded to bf16.  The row sum l
+//                 is the sum of exactly those rounded P values (for d = 64 the PV MMA
+//                 computes it: a block of bf16 ones is appended to V as 16 extra output
+//                 columns), so every output row is an exact convex combination of the
+//                 value rows it saw.  Row times and types come from the query tile's
+//                 planner record, bulk-copied next to Q.
 // Every wait on an mbarrier is bounded (REC_ATTN_ERR_TIMEOUT in the status word).
 #include <climits>
 
@@ -45,10 +49,20 @@ constexpr int kRecBytes = (int)sizeof(KeyTileRec);
 
 template <int D>
 struct Cfg;
+// QB: Q buffers per stream, NS: K/V stages per stream, SUM: the PV MMA also sums P
+// (a block of ones appended to V as 16 extra output columns), OC: TMEM columns of O.
 template <>
-struct Cfg<64> { static constexpr int QB = 2, NS = 2; };
+struct Cfg<64> {
+  static constexpr int QB = 2, NS = 2;
+  static constexpr bool SUM = true;
+  static constexpr int OC = 64 + 16;
+};
 template <>
-struct Cfg<128> { static constexpr int QB = 1, NS = 1; };
+struct Cfg<128> {
+  static constexpr int QB = 1, NS = 1;
+  static constexpr bool SUM = false;
+  static constexpr int OC = 128;
+};
 
 struct ItemDesc {
   long long tok0;  // first token of the query tile (global index)
@@ -74,8 +88,10 @@ struct Layout {
   static constexpr int kQ = 0;                                   // [stream][QB]
   static constexpr int kK = kQ + kStreams * QB * kQBytes;        // [stream][NS]
   static constexpr int kV = kK + kStreams * NS * kKVBytes;       // [stream][NS]
-  static constexpr int kRec = kV + kStreams * NS * kKVBytes;     // [stream][NS] KeyTileRec
-  static constexpr int kInfo = kRec + kStreams * NS * kRecBytes; // [stream][NS] StageInfo
+  static constexpr int kOnes = kV + kStreams * NS * kKVBytes;    // 128 x 64 bf16 ones (SUM only)
+  static constexpr int kRec = kOnes + (Cfg<D>::SUM ? kSlab : 0);  // [stream][NS] KeyTileRec
+  static constexpr int kQRec = kRec + kStreams * NS * kRecBytes;  // [stream][QB] KeyTileRec of the query tile
+  static constexpr int kInfo = kQRec + kStreams * QB * kRecBytes; // [stream][NS] StageInfo
   static constexpr int kItems = (kInfo + kStreams * NS * 8 + 15) & ~15;  // [stream][2] ItemDesc
   static constexpr int kBars = (kItems + kStreams * 2 * 32 + 7) & ~7;
   static constexpr int kBarsPerStream = 2 + 2 + 2 * QB + 3 * NS + 4;
@@ -250,6 +266,7 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
   uint8_t* kbuf = sm + L::kK + s * NS * L::kKVBytes;
   uint8_t* vbuf = sm + L::kV + s * NS * L::kKVBytes;
   uint8_t* rbuf = sm + L::kRec + s * NS * kRecBytes;
+  uint8_t* qrbuf = sm + L::kQRec + s * QB * kRecBytes;
   uint32_t it_cnt = 0, q_it = 0, kv_it = 0;
   bool q_used[QB], st_used[NS];
   uint32_t q_ph[QB], st_ph[NS];
@@ -277,10 +294,12 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
     if (it.n == 0) continue;
     const int qb = (int)(q_it % QB);
     if (!wait_bar(B.q_empty + qb, ((q_it / QB) & 1) ^ 1, abort_flag, a.status)) break;
-    ptx::mbar_arrive_expect_tx(B.q_full + qb, L::kQBytes);
+    ptx::mbar_arrive_expect_tx(B.q_full + qb, L::kQBytes + kRecBytes);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c)
       ptx::tma_load_2d(qbuf + qb * L::kQBytes + c * kSlab, tq, it.h * D + c * 64, (int)d->tok0, B.q_full + qb);
+    // the query tile's times and type bitmaps (its rows' metadata for the softmax)
+    ptx::bulk_load(qrbuf + qb * kRecBytes, a.krec + it.m.tile_start + it.qt, kRecBytes, B.q_full + qb);
     q_used[qb] = true; q_ph[qb] = (q_it / QB) & 1;
     ++q_it;
     for (int j = 0; j < it.n; ++j) {
@@ -321,13 +340,15 @@ __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, u
   using L = Layout<D>;
   constexpr int QB = L::QB, NS = L::NS;
   constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kTile, kTile, false, false);
-  constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kTile, D, false, true);
+  constexpr int OC = Cfg<D>::OC;
+  constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kTile, OC, false, true);
   const ItemDesc* items = reinterpret_cast<const ItemDesc*>(sm + L::kItems) + s * 2;
   const uint32_t q_addr = ptx::smem_u32(sm + L::kQ + s * QB * L::kQBytes);
   const uint32_t k_addr = ptx::smem_u32(sm + L::kK + s * NS * L::kKVBytes);
   const uint32_t v_addr = ptx::smem_u32(sm + L::kV + s * NS * L::kKVBytes);
   const uint32_t tm_s = tmem + (uint32_t)(s * kTile);
-  const uint32_t tm_o = tmem + 2u * kTile + (uint32_t)(s * D);
+  const uint32_t tm_o = tmem + 2u * kTile + (uint32_t)(s * OC);
+  const uint32_t ones_addr = ptx::smem_u32(sm + L::kOnes);
   uint32_t it_cnt = 0, q_it = 0, kv_it = 0, p_it = 0;
   for (;;) {
     const int slot = (int)(it_cnt & 1);
@@ -352,9 +373,12 @@ __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, u
         if (!wait_bar(B.v_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) goto out;
         ptx::tc_fence_after();
         const uint32_t vb = v_addr + st * L::kKVBytes;
+        // N = D (+16): the second 64-column block of B is the next V slab (D = 128) or
+        // the block of ones whose first 16 output columns give the row sum of P
+        const uint32_t lbo = Cfg<D>::SUM ? ones_addr - vb : (uint32_t)kSlab;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          ptx::umma_f16_ts(tm_o, tm_s + kk * 8, ptx::smem_desc_sw128(vb + kk * 16 * 128, kSlab, 1024), idesc_o,
+          ptx::umma_f16_ts(tm_o, tm_s + kk * 8, ptx::smem_desc_sw128(vb + kk * 16 * 128, lbo, 1024), idesc_o,
                            (j > 0 || kk > 0) ? 1u : 0u);
         ptx::umma_commit(B.kv_empty + st);
       }
@@ -392,15 +416,17 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
   const ItemDesc* items = reinterpret_cast<const ItemDesc*>(sm + L::kItems) + s * 2;
   const StageInfo* info = reinterpret_cast<const StageInfo*>(sm + L::kInfo) + s * NS;
   const KeyTileRec* recs = reinterpret_cast<const KeyTileRec*>(sm + L::kRec) + s * NS;
+  const KeyTileRec* qrecs = reinterpret_cast<const KeyTileRec*>(sm + L::kQRec) + s * L::QB;
+  constexpr int OC = Cfg<D>::OC;
   const int lane = threadIdx.x & 31;
   const int quad = (threadIdx.x >> 5) & 3;  // TMEM lanes this warp may access
   const int row = quad * 32 + lane;
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t tm_s = tmem + lane_off + (uint32_t)(s * kTile);
-  const uint32_t tm_o = tmem + lane_off + 2u * kTile + (uint32_t)(s * D);
+  const uint32_t tm_o = tmem + lane_off + 2u * kTile + (uint32_t)(s * OC);
   const float sl2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
   const int H = a.heads;
-  uint32_t it_cnt = 0, kv_it = 0, s_it = 0, o_it = 0;
+  uint32_t it_cnt = 0, kv_it = 0, s_it = 0, o_it = 0, q_it = 0;
   for (;;) {
     const int slot = (int)(it_cnt & 1);
     if (!wait_bar_warp(B.item_full + slot, (it_cnt >> 1) & 1, abort_flag, a.status)) return;
@@ -421,9 +447,17 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       }
       continue;
     }
-    long long ti = 0;
+    // this row's time and type, from the query tile's record next to Q
+    const int qb = (int)(q_it % L::QB);
+    if (!wait_bar_warp(B.q_full + qb, (q_it / L::QB) & 1, abort_flag, a.status)) return;
+    ++q_it;
+    const KeyTileRec* qr = qrecs + qb;
+    const long long ti = qr->t[row];
     int tyi = -1;
-    if (row_ok) { ti = a.t[tok]; tyi = a.ty[tok]; }
+#pragma unroll
+    for (int c = 0; c < kTypes; ++c)
+      if ((qr->typebits[c][row >> 5] >> (row & 31)) & 1u) tyi = c;
+    ptx::mbar_arrive(B.q_empty + qb);  // the Q buffer and its record may be refilled
     RowMask rm;
     row_mask_setup(a.mask, row_ok, pi, ti, tyi, rm);
     float m_ref = -INFINITY, l = 0.f;
@@ -462,10 +496,10 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       for (int c = 0; c < kTile / 2; ++c) {
         const __nv_bfloat162 pb =
             __floats2bfloat162_rn(ex2(fmaf(x[2 * c], sl2, -m_use)), ex2(fmaf(x[2 * c + 1], sl2, -m_use)));
-        rs += __low2float(pb) + __high2float(pb);
+        if (!Cfg<D>::SUM) rs += __low2float(pb) + __high2float(pb);
         pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
       }
-      l = l * corr + rs;
+      if (!Cfg<D>::SUM) l = l * corr + rs;
       // O holds PV(0..j-1): S(j) was issued after PV(j-1), so its completion implies it
       if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll
@@ -475,6 +509,13 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
 #pragma unroll
           for (int e = 0; e < 64; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
           ptx::tmem_st64(tm_o + half * 64, o);
+        }
+        if (Cfg<D>::SUM) {  // the row-sum columns
+          uint32_t o[16];
+          ptx::tmem_ld16(tm_o + D, o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+          ptx::tmem_st16(tm_o + D, o);
         }
       }
       ptx::tmem_st64(tm_s, pk);  // P(j) over the first 64 columns of S(j)
@@ -486,6 +527,11 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
     if (!wait_bar_warp(B.o_ready, o_it & 1, abort_flag, a.status)) return;
     ++o_it;
     ptx::tc_fence_after();
+    if (Cfg<D>::SUM) {
+      uint32_t o[16];
+      ptx::tmem_ld16(tm_o + D, o);
+      l = __uint_as_float(o[0]);
+    }
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int half = 0; half < D / 64; ++half) {
@@ -535,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = 0; i < QB; ++i) {
         ptx::mbar_init(B.q_full + i, 1);
-        ptx::mbar_init(B.q_empty + i, 1);
+        ptx::mbar_init(B.q_empty + i, 1 + 128);  // last S MMA done + every softmax thread read its row
       }
       for (int i = 0; i < NS; ++i) {
         ptx::mbar_init(B.k_full + i, 1);
@@ -553,6 +599,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     ptx::tmem_alloc(tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
+  }
+  if (Cfg<D>::SUM) {  // bf16 ones, read by the PV MMA as extra B columns
+    uint4* ones = reinterpret_cast<uint4*>(sm + L::kOnes);
+    for (int i = threadIdx.x; i < kSlab / 16; i += blockDim.x)
+      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    ptx::fence_proxy_async_smem();
   }
   ptx::tc_fence_before();
   __syncthreads();

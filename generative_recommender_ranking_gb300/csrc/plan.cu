@@ -88,10 +88,33 @@ __device__ __forceinline__ T warp_max(T v) {
 
 constexpr int kPlanThreads = 512;
 constexpr int kCostBins = 4096;
+constexpr int kStageTiles = 4096;
 
-__global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, PlanDev pd, const long long* offsets,
-                                                       const long long* t, const int8_t* ty,
-                                                       long long n_tiles) {
+// In-place exclusive scan of kCostBins counters by one block of kPlanThreads threads.
+__device__ void block_exclusive_scan_bins(int* hist, int* part) {
+  constexpr int per = kCostBins / kPlanThreads;
+  int local = 0;
+  for (int i = 0; i < per; ++i) local += hist[threadIdx.x * per + i];
+  part[threadIdx.x] = local;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int run = part[threadIdx.x] - local;
+  for (int i = 0; i < per; ++i) {
+    const int h = hist[threadIdx.x * per + i];
+    hist[threadIdx.x * per + i] = run;
+    run += h;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, PlanDev pd,
+                                                       const long long* offsets, const long long* t,
+                                                       const int8_t* ty, long long n_tiles) {
   const int b = blockIdx.x;
   const ReqMeta m = pd.meta[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
@@ -194,6 +217,9 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, PlanDev pd, con
   __syncthreads();
 
   // Phase 3: compact each query tile's non-SKIP key tiles (one warp per query tile).
+  __shared__ int s_rcost;
+  if (threadIdx.x == 0) s_rcost = 0;
+  __syncthreads();
   for (int qt = warp; qt < m.ntiles; qt += nwarps) {
     const uint8_t* row = pd.cls + m.cls_start + (long long)qt * m.ntiles;
     uint32_t* out = pd.klist + m.cls_start + (long long)qt * m.ntiles;
@@ -209,52 +235,121 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, PlanDev pd, con
     if (lane == 0) {
       const long long g = m.tile_start + qt;
       pd.kcount[g] = n;
-      pd.qcost[g] = 2 * nfull + 3 * (n - nfull) + 1;  // a PARTIAL tile costs ~1.5 FULL ones
+      const int cost = 2 * nfull + 3 * (n - nfull) + 1;  // a PARTIAL tile costs ~1.5 FULL ones
+      pd.qcost[g] = cost;
       pd.qreq[g] = b;
+      atomicAdd(&s_rcost, cost);
     }
   }
+  __syncthreads();
+  if (threadIdx.x == 0) pd.rcost[b] = s_rcost;
 
-  // Phase 4: the last block to finish orders all query tiles by cost, descending
-  // (counting sort; the order only affects load balance, never results).
+  // Phase 4: the last block to finish writes the work-item order.  The order only
+  // affects load balance and cache reuse, never results.
+  //  - heavy query tiles (cost above 16x the mean, e.g. a candidate tile that reads a
+  //    whole 20K history next to window-only tiles) go first, most expensive first;
+  //  - then the rest, request by request (most expensive first), inside a request
+  //    head by head, inside a head from the last query tile to the first, so the
+  //    items running at the same time share K'/V tiles in L2.
   __shared__ int s_ticket;
   __shared__ int s_hist[kCostBins];
   __shared__ int s_part[kPlanThreads];
+  __shared__ int s_qc[kStageTiles];  // per-tile costs (when n_tiles <= kStageTiles)
+  __shared__ unsigned long long s_sum;
+  __shared__ int s_max, s_nheavy;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_ticket = atomicAdd(&pd.counters[0], 1);
   __syncthreads();
   if (s_ticket != (int)gridDim.x - 1) return;
   __threadfence();
+  const int B = gridDim.x;
+  const bool staged = n_tiles <= kStageTiles;
+  if (threadIdx.x == 0) { s_sum = 0; s_max = 1; s_nheavy = 0; }
   for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
-  for (long long q = threadIdx.x; q < n_tiles; q += blockDim.x) {
-    const int c = min(__ldcg(pd.qcost + q), kCostBins - 1);
-    atomicAdd(&s_hist[kCostBins - 1 - c], 1);
+  {
+    unsigned long long part = 0;
+    for (long long q = threadIdx.x; q < n_tiles; q += blockDim.x) {
+      const int c = __ldcg(pd.qcost + q);
+      if (staged) s_qc[q] = c;
+      part += (unsigned long long)c;
+    }
+    atomicAdd(&s_sum, part);
+    int rmax = 1;
+    for (int r = threadIdx.x; r < B; r += blockDim.x) rmax = max(rmax, __ldcg(pd.rcost + r));
+    atomicMax(&s_max, rmax);
   }
   __syncthreads();
-  // exclusive scan of s_hist (kCostBins / kPlanThreads = 8 bins per thread)
-  constexpr int per = kCostBins / kPlanThreads;
-  int local = 0;
-  for (int i = 0; i < per; ++i) local += s_hist[threadIdx.x * per + i];
-  s_part[threadIdx.x] = local;
+  const long long total = (long long)s_sum;
+  auto qc = [&](long long q) { return staged ? s_qc[q] : __ldcg(pd.qcost + q); };
+  // heavy: qcost * n_tiles > 16 * total
+  auto heavy = [&](long long q) { return (long long)qc(q) * n_tiles > 16 * total; };
+  // heavy query tiles, counting-sorted by cost (descending) into the front of `items`
+  for (long long q = threadIdx.x; q < n_tiles; q += blockDim.x)
+    if (heavy(q)) {
+      atomicAdd(&s_hist[kCostBins - 1 - min(qc(q), kCostBins - 1)], 1);
+      atomicAdd(&s_nheavy, 1);
+    }
   __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int v = threadIdx.x >= off ? s_part[threadIdx.x - off] : 0;
+  const long long heavy_items = (long long)s_nheavy * heads;
+  if (heavy_items > 0) {
+    block_exclusive_scan_bins(s_hist, s_part);
+    for (long long q = threadIdx.x; q < n_tiles; q += blockDim.x)
+      if (heavy(q)) {
+        const int pos = atomicAdd(&s_hist[kCostBins - 1 - min(qc(q), kCostBins - 1)], 1);
+        for (int h = 0; h < heads; ++h) pd.items[(long long)pos * heads + h] = (int)(q * heads + h);
+      }
     __syncthreads();
-    s_part[threadIdx.x] += v;
+    for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) s_hist[i] = 0;
     __syncthreads();
   }
-  int run = s_part[threadIdx.x] - local;
-  for (int i = 0; i < per; ++i) {
-    const int h = s_hist[threadIdx.x * per + i];
-    s_hist[threadIdx.x * per + i] = run;
-    run += h;
+  // requests by cost, descending
+  const long long mx = s_max;
+  for (int r = threadIdx.x; r < B; r += blockDim.x)
+    atomicAdd(&s_hist[kCostBins - 1 - (int)((long long)__ldcg(pd.rcost + r) * (kCostBins - 1) / mx)], 1);
+  __syncthreads();
+  block_exclusive_scan_bins(s_hist, s_part);
+  for (int r = threadIdx.x; r < B; r += blockDim.x) {
+    const int key = (int)((long long)__ldcg(pd.rcost + r) * (kCostBins - 1) / mx);
+    pd.rorder[atomicAdd(&s_hist[kCostBins - 1 - key], 1)] = r;
   }
   __syncthreads();
-  for (long long q = threadIdx.x; q < n_tiles; q += blockDim.x) {
-    const int c = min(__ldcg(pd.qcost + q), kCostBins - 1);
-    const int pos = atomicAdd(&s_hist[kCostBins - 1 - c], 1);
-    pd.qorder[pos] = (int)q;
+  // light items per request (in rorder order) -> first light item of each request
+  long long carry = heavy_items;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int k = base + threadIdx.x;
+    int v = 0;
+    if (k < B) {
+      const ReqMeta rm = pd.meta[__ldcg(pd.rorder + k)];
+      v = rm.ntiles;
+      if (heavy_items > 0)
+        for (int qt = 0; qt < rm.ntiles; ++qt) v -= heavy(rm.tile_start + qt) ? 1 : 0;
+      v *= heads;
+    }
+    s_part[threadIdx.x] = v;
+    __syncthreads();
+    for (int off = 1; off < kPlanThreads; off <<= 1) {
+      const int add = threadIdx.x >= off ? s_part[threadIdx.x - off] : 0;
+      __syncthreads();
+      s_part[threadIdx.x] += add;
+      __syncthreads();
+    }
+    if (k < B) pd.roff[k] = (int)(carry + s_part[threadIdx.x] - v);
+    const int chunk_total = s_part[kPlanThreads - 1];
+    __syncthreads();
+    carry += chunk_total;
+  }
+  if (threadIdx.x == 0) pd.roff[B] = (int)carry;
+  __syncthreads();
+  // one thread per (request, head): its light query tiles, last to first
+  for (long long kh = threadIdx.x; kh < (long long)B * heads; kh += blockDim.x) {
+    const int k = (int)(kh / heads), h = (int)(kh % heads);
+    const ReqMeta rm = pd.meta[__ldcg(pd.rorder + k)];
+    const int r0 = __ldcg(pd.roff + k), nl = (__ldcg(pd.roff + k + 1) - r0) / heads;
+    long long w = r0 + (long long)h * nl;
+    for (int qt = rm.ntiles - 1; qt >= 0; --qt)
+      if (heavy_items == 0 || !heavy(rm.tile_start + qt)) pd.items[w++] = (int)((rm.tile_start + qt) * heads + h);
   }
 }
 
@@ -300,11 +395,11 @@ __global__ void __launch_bounds__(kTile) k_count_pairs(MaskP mp, PlanDev pd, con
 
 }  // namespace
 
-cudaError_t launch_plan(const MaskP& mp, const PlanDev& pd, const long long* offsets_dev,
+cudaError_t launch_plan(const MaskP& mp, int heads, const PlanDev& pd, const long long* offsets_dev,
                         const long long* t, const int8_t* ty, int batch, long long n_tiles,
                         cudaStream_t st) {
   if (batch <= 0) return cudaSuccess;
-  k_plan<<<batch, kPlanThreads, 0, st>>>(mp, pd, offsets_dev, t, ty, n_tiles);
+  k_plan<<<batch, kPlanThreads, 0, st>>>(mp, heads, pd, offsets_dev, t, ty, n_tiles);
   return cudaGetLastError();
 }
 

@@ -61,7 +61,10 @@ struct PlanDev {
   int* kcount;          // [NT]: entries in each query tile's list
   int* qcost;           // [NT]: scheduling cost of each query tile
   int* qreq;            // [NT]: request of each query tile
-  int* qorder;          // [NT]: query tiles, most expensive first
+  int* items;           // [NT*H]: work items (query tile * H + head) in execution order
+  int* rcost;           // [B]: scheduling cost of each request
+  int* rorder;          // [B]: requests, most expensive first
+  int* roff;            // [B+1]: first item of each request in `items` (in rorder order)
   int* counters;        // [8]: plan ticket, attention item counter, attention exit ticket
   int* status;          // [1]: first device error (rec_attn_status)
   unsigned long long* pairs;  // [1]: visible-pair counter

@@ -14,50 +14,96 @@ namespace recattn {
 
 namespace {
 
+// 16 bytes of a head row: 8 bf16 or 4 fp32 values, i.e. 4 or 2 rotation pairs.
 template <typename E>
-struct Pair;
+struct Chunk;
 template <>
-struct Pair<__nv_bfloat16> {
-  using V = __nv_bfloat162;
-  static __device__ __forceinline__ float2 load(const V* p) { return __bfloat1622float2(*p); }
-  static __device__ __forceinline__ void store(V* p, float a, float b) { *p = __floats2bfloat162_rn(a, b); }
+struct Chunk<__nv_bfloat16> {
+  static constexpr int kPairs = 4;
+  static __device__ __forceinline__ void load(const void* p, float (&x)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void store(void* p, const float (&x)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 };
 template <>
-struct Pair<float> {
-  using V = float2;
-  static __device__ __forceinline__ float2 load(const V* p) { return *p; }
-  static __device__ __forceinline__ void store(V* p, float a, float b) { *p = make_float2(a, b); }
+struct Chunk<float> {
+  static constexpr int kPairs = 2;
+  static __device__ __forceinline__ void load(const void* p, float (&x)[8]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+  static __device__ __forceinline__ void store(void* p, const float (&x)[8]) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  }
 };
 
-// One block per global tile; threads walk (token, pair) and loop over heads so each
-// angle's sin/cos is computed once per token and pair.
+// One block per global tile.  Thread work unit: one token and one 16-byte chunk of
+// its head row, for every head, so each angle's sin/cos is computed once per token;
+// heads are processed two at a time with all loads issued before any store.
 template <typename E>
-__global__ void __launch_bounds__(256) k_rope(RopeArgs a) {
-  using P = Pair<E>;
-  using V = typename P::V;
+__global__ void __launch_bounds__(256, 4) k_rope(RopeArgs a) {
+  using C = Chunk<E>;
+  constexpr int kPairs = C::kPairs;
+  constexpr int kHeadBatch = 2;
   const long long g = blockIdx.x;
   const ReqMeta m = a.meta[a.qreq[g]];
   const int tl = (int)(g - m.tile_start);
   const long long t_ref = a.t[m.tok_start];
-  const int half = a.head_dim >> 1;
-  const V* q = reinterpret_cast<const V*>(a.q);
-  const V* k = reinterpret_cast<const V*>(a.k);
-  V* qr = reinterpret_cast<V*>(a.qr);
-  V* kr = reinterpret_cast<V*>(a.kr);
-  for (int idx = threadIdx.x; idx < kTile * half; idx += blockDim.x) {
-    const int r = idx / half, i = idx - r * half;
-    const int pos = tl * kTile + r;
-    if (pos >= m.len) break;
-    const long long tok = m.tok_start + pos;
-    const long long dt = a.t[tok] - t_ref;
-    float s, c;
-    sincosf((float)dt * a.omega[i], &s, &c);
-    for (int h = 0; h < a.heads; ++h) {
-      const long long e = (tok * a.heads + h) * half + i;
-      const float2 x = P::load(q + e);
-      P::store(qr + e, x.x * c - x.y * s, x.x * s + x.y * c);
-      const float2 y = P::load(k + e);
-      P::store(kr + e, y.x * c - y.y * s, y.x * s + y.y * c);
+  const int chunks = a.head_dim / (2 * kPairs);
+  const int rows = min(kTile, m.len - tl * kTile);
+  const char* __restrict__ q = static_cast<const char*>(a.q);
+  const char* __restrict__ k = static_cast<const char*>(a.k);
+  char* __restrict__ qr = static_cast<char*>(a.qr);
+  char* __restrict__ kr = static_cast<char*>(a.kr);
+  const long long head_bytes = (long long)a.head_dim * (long long)sizeof(E);
+  for (int idx = threadIdx.x; idx < rows * chunks; idx += blockDim.x) {
+    const int r = idx / chunks, c = idx - r * chunks;
+    const long long tok = m.tok_start + tl * kTile + r;
+    const float dt = (float)(a.t[tok] - t_ref);  // exact int64 difference, then fp32
+    float sn[kPairs], cs[kPairs];
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
+    const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
+    for (int h0 = 0; h0 < a.heads; h0 += kHeadBatch) {
+      float x[kHeadBatch][8], y[kHeadBatch][8];
+#pragma unroll
+      for (int u = 0; u < kHeadBatch; ++u)
+        if (h0 + u < a.heads) {
+          C::load(q + row0 + (h0 + u) * head_bytes, x[u]);
+          C::load(k + row0 + (h0 + u) * head_bytes, y[u]);
+        }
+#pragma unroll
+      for (int u = 0; u < kHeadBatch; ++u) {
+#pragma unroll
+        for (int p = 0; p < kPairs; ++p) {
+          const float x0 = x[u][2 * p], x1 = x[u][2 * p + 1], y0 = y[u][2 * p], y1 = y[u][2 * p + 1];
+          x[u][2 * p] = x0 * cs[p] - x1 * sn[p];
+          x[u][2 * p + 1] = x0 * sn[p] + x1 * cs[p];
+          y[u][2 * p] = y0 * cs[p] - y1 * sn[p];
+          y[u][2 * p + 1] = y0 * sn[p] + y1 * cs[p];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kHeadBatch; ++u)
+        if (h0 + u < a.heads) {
+          C::store(qr + row0 + (h0 + u) * head_bytes, x[u]);
+          C::store(kr + row0 + (h0 + u) * head_bytes, y[u]);
+        }
     }
   }
 }

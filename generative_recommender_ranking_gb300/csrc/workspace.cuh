@@ -9,13 +9,13 @@
 namespace recattn {
 
 struct WsLayout {
-  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, qo, rq, rk, total;
+  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, it, rc, ro, rf, rq, rk, total;
 };
 
 inline size_t ws_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 // rot_bytes: bytes of one rotated [T][H][d] copy (0 when the RoPE is off).
-inline WsLayout ws_layout(long long batch, long long NT, long long NC, size_t rot_bytes) {
+inline WsLayout ws_layout(long long batch, long long NT, long long NC, long long heads, size_t rot_bytes) {
   WsLayout L;
   size_t off = 0;
   L.hdr = off; off = ws_up(off + 256);
@@ -27,7 +27,10 @@ inline WsLayout ws_layout(long long batch, long long NT, long long NC, size_t ro
   L.kc = off; off = ws_up(off + 4 * (size_t)NT);
   L.qc = off; off = ws_up(off + 4 * (size_t)NT);
   L.qr = off; off = ws_up(off + 4 * (size_t)NT);
-  L.qo = off; off = ws_up(off + 4 * (size_t)NT);
+  L.it = off; off = ws_up(off + 4 * (size_t)NT * (size_t)heads);
+  L.rc = off; off = ws_up(off + 4 * (size_t)batch);
+  L.ro = off; off = ws_up(off + 4 * (size_t)batch);
+  L.rf = off; off = ws_up(off + 4 * ((size_t)batch + 1));
   L.rq = off; off = ws_up(off + rot_bytes);
   L.rk = off; off = ws_up(off + rot_bytes);
   L.total = off;
@@ -47,7 +50,10 @@ inline PlanDev ws_bind(char* w, const WsLayout& L) {
   pd.kcount = reinterpret_cast<int*>(w + L.kc);
   pd.qcost = reinterpret_cast<int*>(w + L.qc);
   pd.qreq = reinterpret_cast<int*>(w + L.qr);
-  pd.qorder = reinterpret_cast<int*>(w + L.qo);
+  pd.items = reinterpret_cast<int*>(w + L.it);
+  pd.rcost = reinterpret_cast<int*>(w + L.rc);
+  pd.rorder = reinterpret_cast<int*>(w + L.ro);
+  pd.roff = reinterpret_cast<int*>(w + L.rf);
   return pd;
 }
 
