@@ -12,9 +12,10 @@
 //                 head by head), publish item descriptors and per-stage tile
 //                 info in shared memory, load Q', K', V (and, for PARTIAL tiles, the
 //                 key-tile record) with TMA / bulk copies into per-stream rings;
-//   warp 2, 3     MMA issuers (stream 0, 1): S = Q'K'^T into the stream's TMEM S
-//                 buffer, then O += P V with P read straight from TMEM (P overwrites
-//                 the first 64 columns of S);
+//   warp 2, 3     MMA issuers (stream 0, 1): each 128-key tile is two 64-key chunks;
+//                 S(g) = Q'K'(g)^T goes to TMEM buffer g % 2 of the stream, so S(g+1)
+//                 is computed while the softmax works on chunk g; O += P(g) V(g) reads
+//                 P straight from TMEM (P overwrites the first 32 columns of S(g));
 //   warps 4..7    softmax of stream 0, warps 8..11 softmax of stream 1: one query row
 //                 per thread (TMEM lane quadrant = warp % 4).  PARTIAL tiles build the
 //                 row's 128-bit visibility mask from position ranges, per-type key
@@ -46,6 +47,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;          // keep the reference max until it is exceeded by 2^8
 constexpr int kRecBytes = (int)sizeof(KeyTileRec);
+constexpr int kChunk = 64;                   // keys per S chunk (a 128-key tile is two chunks)
 
 template <int D>
 struct Cfg;
@@ -94,7 +96,7 @@ struct Layout {
   static constexpr int kInfo = kQRec + kStreams * QB * kRecBytes; // [stream][NS] StageInfo
   static constexpr int kItems = (kInfo + kStreams * NS * 8 + 15) & ~15;  // [stream][2] ItemDesc
   static constexpr int kBars = (kItems + kStreams * 2 * 32 + 7) & ~7;
-  static constexpr int kBarsPerStream = 2 + 2 + 2 * QB + 3 * NS + 4;
+  static constexpr int kBarsPerStream = 2 + 2 + 2 * QB + 3 * NS + 6;
   static constexpr int kTotal = kBars + kStreams * kBarsPerStream * 8 + 16;
   static constexpr int kDynamic = kTotal + 1024;  // slack to align the base to 1024 B
 };
@@ -102,13 +104,14 @@ struct Layout {
 // mbarriers of one stream
 struct SBars {
   uint64_t *item_full, *item_empty, *q_full, *q_empty, *k_full, *v_full, *kv_empty;
-  uint64_t *s_full, *p_full, *o_ready, *mma_done;
+  uint64_t *s_full, *p_full, *pv_done, *o_ready, *mma_done;  // s_full: [2], one per S buffer
   template <int D>
   __device__ void bind(uint64_t* b) {
     constexpr int QB = Cfg<D>::QB, NS = Cfg<D>::NS;
     item_full = b; item_empty = b + 2; q_full = b + 4; q_empty = q_full + QB;
     k_full = q_empty + QB; v_full = k_full + NS; kv_empty = v_full + NS;
-    s_full = kv_empty + NS; p_full = s_full + 1; o_ready = p_full + 1; mma_done = o_ready + 1;
+    s_full = kv_empty + NS; p_full = s_full + 2; pv_done = p_full + 1; o_ready = pv_done + 1;
+    mma_done = o_ready + 1;
   }
 };
 
@@ -136,6 +139,22 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, vo
                                               int* status) {
   const bool ok = wait_bar(bar, parity, abort_flag, status);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Packed fp32 pairs for the fma.rn.f32x2 instruction.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -334,13 +353,18 @@ drain:
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// Per stream, each 128-key tile is processed as two 64-key chunks.  Chunk g of the
+// stream (counted across items) has its S in TMEM buffer g % 2; its P overwrites the
+// first 32 columns of that buffer.  Issue order: S(0), S(1), then for every chunk g:
+// PV(g) once P(g) is ready, then S(g+2) into the buffer PV(g) has just read.  So while
+// the softmax works on chunk g, S(g+1) is already computed.
 template <int D>
 __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, uint32_t tmem,
                         volatile int* abort_flag) {
   using L = Layout<D>;
   constexpr int QB = L::QB, NS = L::NS;
-  constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kTile, kTile, false, false);
   constexpr int OC = Cfg<D>::OC;
+  constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kTile, kChunk, false, false);
   constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kTile, OC, false, true);
   const ItemDesc* items = reinterpret_cast<const ItemDesc*>(sm + L::kItems) + s * 2;
   const uint32_t q_addr = ptx::smem_u32(sm + L::kQ + s * QB * L::kQBytes);
@@ -349,7 +373,7 @@ __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, u
   const uint32_t tm_s = tmem + (uint32_t)(s * kTile);
   const uint32_t tm_o = tmem + 2u * kTile + (uint32_t)(s * OC);
   const uint32_t ones_addr = ptx::smem_u32(sm + L::kOnes);
-  uint32_t it_cnt = 0, q_it = 0, kv_it = 0, p_it = 0;
+  uint32_t it_cnt = 0, q_it = 0, kv_it = 0, p_it = 0, s_ch = 0;
   for (;;) {
     const int slot = (int)(it_cnt & 1);
     if (!wait_bar(B.item_full + slot, (it_cnt >> 1) & 1, abort_flag, a.status)) break;
@@ -363,39 +387,60 @@ __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, u
     ++q_it;
     ptx::tc_fence_after();
     const uint32_t qa = q_addr + qb * L::kQBytes;
-    for (int j = -1; j < n; ++j) {
-      if (j >= 0) {
-        // O += P(j) V(j), P read from TMEM
-        if (!wait_bar(B.p_full, p_it & 1, abort_flag, a.status)) goto out;
-        ++p_it;
+    const int nch = 2 * n;
+    // S(g) = Q' K'(g)^T for chunk g of this item, into buffer s_ch % 2
+    auto issue_s = [&](int g) -> bool {
+      const int j = g >> 1, c = g & 1;
+      const int st = (int)((kv_it + j) % NS);
+      if (c == 0) {
+        if (!wait_bar(B.k_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) return false;
         ptx::tc_fence_after();
-        const int st = (int)((kv_it + j) % NS);
+      }
+      const uint32_t kb = k_addr + st * L::kKVBytes + c * (kChunk * 128);
+      const uint32_t d_tmem = tm_s + (s_ch & 1) * kChunk;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
+        ptx::umma_f16(d_tmem, ptx::smem_desc_sw128(qa + off, 16, 1024), ptx::smem_desc_sw128(kb + off, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
+      }
+      ptx::umma_commit(B.s_full + (s_ch & 1));
+      ++s_ch;
+      if (g == nch - 1) ptx::umma_commit(B.q_empty + qb);  // last S of the item issued
+      return true;
+    };
+    const uint32_t ch0 = s_ch;  // global chunk index of this item's chunk 0
+    if (!issue_s(0) || !issue_s(1)) goto out;
+    for (int g = 0; g < nch; ++g) {
+      const int j = g >> 1, c = g & 1;
+      const int st = (int)((kv_it + j) % NS);
+      if (!wait_bar(B.p_full, p_it & 1, abort_flag, a.status)) goto out;
+      ++p_it;
+      ptx::tc_fence_after();
+      if (c == 0) {
         if (!wait_bar(B.v_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) goto out;
         ptx::tc_fence_after();
-        const uint32_t vb = v_addr + st * L::kKVBytes;
-        // N = D (+16): the second 64-column block of B is the next V slab (D = 128) or
-        // the block of ones whose first 16 output columns give the row sum of P
-        const uint32_t lbo = Cfg<D>::SUM ? ones_addr - vb : (uint32_t)kSlab;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          ptx::umma_f16_ts(tm_o, tm_s + kk * 8, ptx::smem_desc_sw128(vb + kk * 16 * 128, lbo, 1024), idesc_o,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::umma_commit(B.kv_empty + st);
       }
-      if (j + 1 < n) {
-        // S(j+1) = Q' K'(j+1)^T (overwrites P(j) after the PV MMA above has read it)
-        const int st = (int)((kv_it + j + 1) % NS);
-        if (!wait_bar(B.k_full + st, ((kv_it + j + 1) / NS) & 1, abort_flag, a.status)) goto out;
-        ptx::tc_fence_after();
-        const uint32_t kb = k_addr + st * L::kKVBytes;
+      // O += P(g) V(g): P from TMEM, V rows of this chunk; the second 64-column block
+      // of B is the next V slab (D = 128) or the block of ones whose first 16 output
+      // columns give the row sum of P (D = 64)
+      const uint32_t vb = v_addr + st * L::kKVBytes;
+      const uint32_t lbo = Cfg<D>::SUM ? ones_addr - vb : (uint32_t)kSlab;
+      const uint32_t pa = tm_s + ((ch0 + g) & 1) * kChunk;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-          ptx::umma_f16(tm_s, ptx::smem_desc_sw128(qa + off, 16, 1024), ptx::smem_desc_sw128(kb + off, 16, 1024),
-                        idesc_s, kk > 0 ? 1u : 0u);
-        }
-        ptx::umma_commit(B.s_full);
-        if (j + 2 == n) ptx::umma_commit(B.q_empty + qb);  // last S of the item issued
+      for (int kk = 0; kk < kChunk / 16; ++kk)
+        ptx::umma_f16_ts(tm_o, pa + kk * 8,
+                         ptx::smem_desc_sw128(vb + c * (kChunk * 128) + kk * 16 * 128, lbo, 1024), idesc_o,
+                         (g > 0 || kk > 0) ? 1u : 0u);
+      ptx::umma_commit(B.pv_done);
+      if (c == 1) ptx::umma_commit(B.kv_empty + st);
+      if (NS >= 2) {
+        if (g + 2 < nch && !issue_s(g + 2)) goto out;
+      } else if (c == 1) {
+        // one K/V stage: the next tile's K can only land after this tile's last PV,
+        // so both of its S chunks are issued here
+        if (g + 1 < nch && !issue_s(g + 1)) goto out;
+        if (g + 2 < nch && !issue_s(g + 2)) goto out;
       }
     }
     ptx::umma_commit(B.o_ready);
@@ -426,7 +471,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
   const uint32_t tm_o = tmem + lane_off + 2u * kTile + (uint32_t)(s * OC);
   const float sl2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
   const int H = a.heads;
-  uint32_t it_cnt = 0, kv_it = 0, s_it = 0, o_it = 0, q_it = 0;
+  uint32_t it_cnt = 0, kv_it = 0, ch = 0, o_it = 0, q_it = 0;
   for (;;) {
     const int slot = (int)(it_cnt & 1);
     if (!wait_bar_warp(B.item_full + slot, (it_cnt >> 1) & 1, abort_flag, a.status)) return;
@@ -468,60 +513,74 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       // the stage's tile info and key record (written by the producer / bulk copy)
       if (!wait_bar_warp(B.k_full + st, kph, abort_flag, a.status)) return;
       const StageInfo inf = info[st];
-      if (!wait_bar_warp(B.s_full, s_it & 1, abort_flag, a.status)) return;
-      ++s_it;
-      ptx::tc_fence_after();
-      uint32_t sr[kTile];
-      ptx::tmem_ld128(tm_s, sr);
-      float x[kTile];
+      const bool partial = inf.cls != REC_ATTN_TILE_FULL;
+      uint32_t vm[4] = {~0u, ~0u, ~0u, ~0u};
+      if (partial) build_mask(rm, recs + st, inf.kt * kTile, vm);
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t buf = ch & 1;
+        if (!wait_bar_warp(B.s_full + buf, (ch >> 1) & 1, abort_flag, a.status)) return;
+        ptx::tc_fence_after();
+        uint32_t sr[kChunk];
+        ptx::tmem_ld64(tm_s + buf * kChunk, sr);
+        float x[kChunk];
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) x[c] = __uint_as_float(sr[c]);
-      if (inf.cls != REC_ATTN_TILE_FULL) {
-        uint32_t vm[4];
-        build_mask(rm, recs + st, inf.kt * kTile, vm);
+        for (int e = 0; e < kChunk; ++e) x[e] = __uint_as_float(sr[e]);
+        if (partial) {
+          const uint32_t w0 = c ? vm[2] : vm[0], w1 = c ? vm[3] : vm[1];
 #pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (!((vm[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
-      }
-      float mx = x[0];
-#pragma unroll
-      for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, x[c]);
-      const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
-      const float m_new = (m_tile > m_ref + kRescaleLog2) ? m_tile : m_ref;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float corr = ex2(m_ref - m_use);  // 0 when m_ref = -inf, 1 when unchanged
-      uint32_t pk[kTile / 2];
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < kTile / 2; ++c) {
-        const __nv_bfloat162 pb =
-            __floats2bfloat162_rn(ex2(fmaf(x[2 * c], sl2, -m_use)), ex2(fmaf(x[2 * c + 1], sl2, -m_use)));
-        if (!Cfg<D>::SUM) rs += __low2float(pb) + __high2float(pb);
-        pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
-      }
-      if (!Cfg<D>::SUM) l = l * corr + rs;
-      // O holds PV(0..j-1): S(j) was issued after PV(j-1), so its completion implies it
-      if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
-        for (int half = 0; half < D / 64; ++half) {
-          uint32_t o[64];
-          ptx::tmem_ld64(tm_o + half * 64, o);
-#pragma unroll
-          for (int e = 0; e < 64; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          ptx::tmem_st64(tm_o + half * 64, o);
+          for (int e = 0; e < kChunk; ++e)
+            if (!(((e < 32 ? w0 : w1) >> (e & 31)) & 1u)) x[e] = -INFINITY;
         }
-        if (Cfg<D>::SUM) {  // the row-sum columns
-          uint32_t o[16];
-          ptx::tmem_ld16(tm_o + D, o);
+        float mx = x[0];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          ptx::tmem_st16(tm_o + D, o);
+        for (int e = 1; e < kChunk; ++e) mx = fmaxf(mx, x[e]);
+        const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
+        const float m_new = (m_tile > m_ref + kRescaleLog2) ? m_tile : m_ref;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float corr = ex2(m_ref - m_use);  // 0 when m_ref = -inf, 1 when unchanged
+        uint32_t pk[kChunk / 2];
+        float rs = 0.f;
+        const unsigned long long sl2x2 = pack2(sl2, sl2), negm2 = pack2(-m_use, -m_use);
+#pragma unroll
+        for (int e = 0; e < kChunk / 2; ++e) {
+          float y0, y1;
+          unpack2(ffma2(pack2(x[2 * e], x[2 * e + 1]), sl2x2, negm2), y0, y1);
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(ex2(y0), ex2(y1));
+          if (!Cfg<D>::SUM) rs += __low2float(pb) + __high2float(pb);
+          pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
         }
+        if (!Cfg<D>::SUM) l = l * corr + rs;
+        // Every PV completion is waited for in order (one phase per chunk, so the
+        // parity wait is exact); O may only be rescaled once PV(ch-1) has landed, and
+        // PV(ch-1) was issued as soon as P(ch-1) was ready, so this rarely waits.
+        if (ch > 0) {
+          if (!wait_bar_warp(B.pv_done, (ch - 1) & 1, abort_flag, a.status)) return;
+          ptx::tc_fence_after();
+        }
+        if ((j > 0 || c > 0) && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll
+          for (int half = 0; half < D / 64; ++half) {
+            uint32_t o[64];
+            ptx::tmem_ld64(tm_o + half * 64, o);
+#pragma unroll
+            for (int e = 0; e < 64; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            ptx::tmem_st64(tm_o + half * 64, o);
+          }
+          if (Cfg<D>::SUM) {  // the row-sum columns
+            uint32_t o[16];
+            ptx::tmem_ld16(tm_o + D, o);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            ptx::tmem_st16(tm_o + D, o);
+          }
+        }
+        ptx::tmem_st32(tm_s + buf * kChunk, pk);  // P over the first 32 columns of S
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(B.p_full);
+        m_ref = m_new;
+        ++ch;
       }
-      ptx::tmem_st64(tm_s, pk);  // P(j) over the first 64 columns of S(j)
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(B.p_full);
-      m_ref = m_new;
     }
     // epilogue: O / l
     if (!wait_bar_warp(B.o_ready, o_it & 1, abort_flag, a.status)) return;
@@ -589,7 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(B.kv_empty + i, 1);
       }
       ptx::mbar_init(B.s_full, 1);
+      ptx::mbar_init(B.s_full + 1, 1);
       ptx::mbar_init(B.p_full, 128);
+      ptx::mbar_init(B.pv_done, 1);
       ptx::mbar_init(B.o_ready, 1);
       ptx::mbar_init(B.mma_done, 1);
     }
@@ -612,7 +673,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    ptx::setmaxnreg_dec<56>();
     const int s = warp & 1;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
@@ -621,7 +681,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       else run_mma<D>(a, sm, s, B, tmem, abort_flag);
     }
   } else {
-    ptx::setmaxnreg_inc<224>();
     const int s = (warp - 4) >> 2;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
