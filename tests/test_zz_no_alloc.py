@@ -73,8 +73,8 @@ def test_noalloc_state_does_not_leak_between_batches():
 
 
 def test_noalloc_rejects_batches_beyond_its_workspace():
-    # 2 x T x H x d x 2 bytes of rotated Q/K alone exceed the static array
-    T = bd.NOALLOC_SCRATCH_BYTES // (8 * 64 * 2) // 2 + 128
+    # the rotated K alone (T x H x d x 2 bytes) exceeds the static array
+    T = bd.NOALLOC_SCRATCH_BYTES // (8 * 64 * 2) + 1024
     w = W.Workload("big", 8, 64, "bf16", np.array([0, T], dtype=np.int64),
                    np.zeros(T, np.int64), np.ones(T, np.int8), None, None, None)
     dev = torch.zeros(1, dtype=torch.int64, device="cuda")
