@@ -40,6 +40,12 @@ struct rec_attn_plan_s {
   // cached TMA descriptors for the last (q', k', v) pointers
   const void* map_src[3] = {nullptr, nullptr, nullptr};
   CUtensorMap maps[3];
+  // Planning runs on a library side stream (after the caller's stream has produced the
+  // offsets, times and types: ev_in), so the RoPE prologue of rec_attn_fwd, on the
+  // caller's stream, overlaps the planning kernel.  The prologue waits only for the
+  // request-table upload (ev_meta); the attention kernel waits for the planner (ev_plan).
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_in = nullptr, ev_meta = nullptr, ev_plan = nullptr;
   // optional kernel timing: events around the RoPE prologue and the attention kernel
   bool timing = false;
   bool timed = false;
@@ -50,6 +56,20 @@ namespace {
 
 std::mutex g_pool_mu;
 std::map<int, cudaMemPool_t> g_pools;
+std::map<int, cudaStream_t> g_side;
+
+// Library-owned non-blocking stream per device for the RoPE prologue.
+cudaError_t side_stream_for(int device, cudaStream_t* out) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  auto it = g_side.find(device);
+  if (it != g_side.end()) { *out = it->second; return cudaSuccess; }
+  cudaStream_t st;
+  cudaError_t e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return e;
+  g_side[device] = st;
+  *out = st;
+  return cudaSuccess;
+}
 
 rec_attn_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return REC_ATTN_OK;
@@ -230,14 +250,32 @@ REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_
   plan->qrot = params->use_rope ? w + lay.rq : nullptr;
   plan->krot = params->use_rope ? w + lay.rk : nullptr;
 
-  e = cudaMemsetAsync(w + lay.hdr, 0, 256, plan->stream);
-  if (e == cudaSuccess && batch > 0)
-    e = cudaMemcpyAsync(pd.meta, meta.data(), sizeof(ReqMeta) * (size_t)batch, cudaMemcpyHostToDevice, plan->stream);
-  if (e == cudaSuccess)
-    e = launch_plan(plan->mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t, plan->ty, batch, NT,
-                    plan->stream);
+  for (cudaEvent_t* ev : {&plan->ev_in, &plan->ev_meta, &plan->ev_plan})
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = side_stream_for(plan->device, &plan->side);
+  // the side stream starts after the caller's stream reaches this point (inputs ready,
+  // workspace allocated)
+  if (e == cudaSuccess) e = cudaEventRecord(plan->ev_in, plan->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->side, plan->ev_in, 0);
   if (e != cudaSuccess) {
     cudaFreeAsync(plan->ws, plan->stream);
+    for (cudaEvent_t ev : {plan->ev_in, plan->ev_meta, plan->ev_plan})
+      if (ev) cudaEventDestroy(ev);
+    delete plan;
+    return from_cuda(e);
+  }
+  e = cudaMemsetAsync(w + lay.hdr, 0, 256, plan->side);
+  if (e == cudaSuccess && batch > 0)
+    e = cudaMemcpyAsync(pd.meta, meta.data(), sizeof(ReqMeta) * (size_t)batch, cudaMemcpyHostToDevice, plan->side);
+  if (e == cudaSuccess) e = cudaEventRecord(plan->ev_meta, plan->side);
+  if (e == cudaSuccess)
+    e = launch_plan(plan->mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t, plan->ty, batch, NT,
+                    plan->side);
+  if (e == cudaSuccess) e = cudaEventRecord(plan->ev_plan, plan->side);
+  if (e != cudaSuccess) {
+    cudaStreamWaitEvent(plan->stream, plan->ev_plan, 0);
+    cudaFreeAsync(plan->ws, plan->stream);
+    for (cudaEvent_t ev : {plan->ev_in, plan->ev_meta, plan->ev_plan}) cudaEventDestroy(ev);
     delete plan;
     return from_cuda(e);
   }
@@ -273,24 +311,32 @@ REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, 
 
   const void* qs = q;
   const void* ks = k;
-  if (plan->timing) {
-    plan->timed = false;
-    e = cudaEventRecord(plan->ev[0], st);
-    if (e != cudaSuccess) return from_cuda(e);
-  }
   if (p.use_rope) {
+    e = cudaStreamWaitEvent(st, plan->ev_meta, 0);  // the request table (not the planner)
+    if (e == cudaSuccess && plan->timing) {
+      plan->timed = false;
+      e = cudaEventRecord(plan->ev[0], st);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
     RopeArgs ra;
-    ra.meta = plan->pd.meta; ra.qreq = plan->pd.qreq; ra.t = plan->t;
+    ra.meta = plan->pd.meta; ra.batch = plan->batch; ra.t = plan->t;
     ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
     ra.heads = p.num_heads; ra.head_dim = p.head_dim;
     std::memcpy(ra.omega, plan->omega, sizeof ra.omega);
     e = launch_rope(ra, p.dtype, plan->NT, st);
+    if (e == cudaSuccess && plan->timing) e = cudaEventRecord(plan->ev[1], st);
     if (e != cudaSuccess) return from_cuda(e);
     qs = plan->qrot; ks = plan->krot;
+  } else if (plan->timing) {
+    plan->timed = false;
+    e = cudaEventRecord(plan->ev[0], st);
+    if (e == cudaSuccess) e = cudaEventRecord(plan->ev[1], st);
+    if (e != cudaSuccess) return from_cuda(e);
   }
+  e = cudaStreamWaitEvent(st, plan->ev_plan, 0);
+  if (e != cudaSuccess) return from_cuda(e);
   if (plan->timing) {
-    e = cudaEventRecord(plan->ev[1], st);
-    if (e == cudaSuccess) e = cudaEventRecord(plan->ev[2], st);
+    e = cudaEventRecord(plan->ev[2], st);
     if (e != cudaSuccess) return from_cuda(e);
   }
   AttnArgs a;
@@ -319,8 +365,13 @@ REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, 
 
 REC_ATTN_API void rec_attn_free(rec_attn_plan_t* plan) {
   if (!plan) return;
-  if (plan->ws) cudaFreeAsync(plan->ws, plan->stream);
+  if (plan->ws) {
+    cudaStreamWaitEvent(plan->stream, plan->ev_plan, 0);  // planning may still run on the side stream
+    cudaFreeAsync(plan->ws, plan->stream);
+  }
   for (cudaEvent_t ev : plan->ev)
+    if (ev) cudaEventDestroy(ev);
+  for (cudaEvent_t ev : {plan->ev_in, plan->ev_meta, plan->ev_plan})
     if (ev) cudaEventDestroy(ev);
   delete plan;
 }
@@ -355,14 +406,17 @@ REC_ATTN_API rec_attn_status rec_attn_tile_classes(rec_attn_plan_t* plan, uint8_
   if (!host_out) return REC_ATTN_OK;
   if (capacity < (size_t)plan->NC) return REC_ATTN_ERR_INVALID_ARG;
   if (plan->NC == 0) return REC_ATTN_OK;
-  cudaError_t e = cudaMemcpyAsync(host_out, plan->pd.cls, (size_t)plan->NC, cudaMemcpyDeviceToHost, plan->stream);
+  cudaError_t e = cudaStreamWaitEvent(plan->stream, plan->ev_plan, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(host_out, plan->pd.cls, (size_t)plan->NC, cudaMemcpyDeviceToHost, plan->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(plan->stream);
   return from_cuda(e);
 }
 
 REC_ATTN_API rec_attn_status rec_attn_visible_pairs(rec_attn_plan_t* plan, uint64_t* host_out) {
   if (!plan || !host_out) return REC_ATTN_ERR_INVALID_ARG;
-  cudaError_t e = cudaMemsetAsync(plan->pd.pairs, 0, sizeof(unsigned long long), plan->stream);
+  cudaError_t e = cudaStreamWaitEvent(plan->stream, plan->ev_plan, 0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(plan->pd.pairs, 0, sizeof(unsigned long long), plan->stream);
   if (e == cudaSuccess) e = launch_count_pairs(plan->mask, plan->pd, plan->t, plan->ty, plan->NT, plan->stream);
   unsigned long long n = 0;
   if (e == cudaSuccess) e = cudaMemcpyAsync(&n, plan->pd.pairs, sizeof n, cudaMemcpyDeviceToHost, plan->stream);
@@ -374,7 +428,8 @@ REC_ATTN_API rec_attn_status rec_attn_visible_pairs(rec_attn_plan_t* plan, uint6
 REC_ATTN_API rec_attn_status rec_attn_device_status(rec_attn_plan_t* plan, int32_t* status_out) {
   if (!plan || !status_out) return REC_ATTN_ERR_INVALID_ARG;
   int s = 0;
-  cudaError_t e = cudaMemcpyAsync(&s, plan->pd.status, sizeof s, cudaMemcpyDeviceToHost, plan->stream);
+  cudaError_t e = cudaStreamWaitEvent(plan->stream, plan->ev_plan, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&s, plan->pd.status, sizeof s, cudaMemcpyDeviceToHost, plan->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(plan->stream);
   if (e == cudaSuccess) *status_out = s;
   return from_cuda(e);

@@ -30,7 +30,7 @@ struct AttnArgs {
 // Arguments of the time-RoPE prologue.
 struct RopeArgs {
   const ReqMeta* meta;
-  const int* qreq;         // request of each global tile
+  int batch;               // requests in meta (the prologue needs nothing the planner writes)
   const long long* t;
   const void* q;
   const void* k;

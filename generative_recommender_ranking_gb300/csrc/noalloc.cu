@@ -189,7 +189,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   const void* ks = k;
   if (params->use_rope) {
     RopeArgs ra;
-    ra.meta = pd.meta; ra.qreq = pd.qreq; ra.t = t;
+    ra.meta = pd.meta; ra.batch = batch; ra.t = t;
     ra.q = q; ra.k = k; ra.qr = w + lay.rq; ra.kr = w + lay.rk;
     ra.heads = params->num_heads; ra.head_dim = params->head_dim;
     for (int i = 0; i < kMaxPairs; ++i)
