@@ -104,7 +104,11 @@ typedef struct rec_attn_plan_s rec_attn_plan_t; /* opaque */
  *   offsets_dev     device int64[B+1], same values.
  *   timestamps_dev  device int64[T] seconds, T = offsets[B]; |t| < 2^62.
  *   types_dev       device int8[T], each in 0..3.
- *   stream          cudaStream_t for the planning kernels.
+ *   stream          cudaStream_t the inputs are produced on.  The planning work (a
+ *                   request-table upload and one kernel) runs on a library-owned stream
+ *                   that first waits for `stream`; every later call on the plan orders
+ *                   itself after that work, so a rec_attn_fwd on `stream` overlaps its
+ *                   time-RoPE prologue with the planning kernel.
  *   plan_out        receives the plan.
  * The device arrays must stay valid and unchanged while the plan is used.  The
  * plan owns a device workspace (per-tile statistics, tile classes, per-query-tile
@@ -142,9 +146,9 @@ rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, const void* k
 
 /*
  * rec_attn_free -- release a plan (NULL-safe).  The workspace returns to the
- * library pool in stream order on the stream of the plan's last use, so work
- * already enqueued there may still run; callers that used other streams must
- * synchronize them first.
+ * library pool in stream order on the stream of the plan's last use (after the
+ * planning work), so work already enqueued there may still run; callers that used
+ * other streams must synchronize them first.
  */
 void rec_attn_free(rec_attn_plan_t* plan);
 
