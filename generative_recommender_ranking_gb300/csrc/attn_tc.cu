@@ -236,7 +236,10 @@ __device__ __forceinline__ void build_mask(const RowMask& rm, const KeyTileRec* 
   vm[0] = vm[1] = vm[2] = vm[3] = 0u;
 #pragma unroll
   for (int c = 0; c < kTypes; ++c) {
-    const int n = rec->run_n[c];
+    // the record comes from the planner; its run is still clamped to the tile so no
+    // value in it can index outside the record
+    const int rl = min(max(rec->run_lo[c], 0), kTile - 1);
+    const int n = min(max(rec->run_n[c], 0), kTile - rl);
     const int lo = rm.plo[c] - k0, hi = rm.phi[c] - k0;
     if (n == 0 || lo > hi || hi < 0 || lo >= kTile) continue;
     uint32_t r[4];
@@ -247,7 +250,6 @@ __device__ __forceinline__ void build_mask(const RowMask& rm, const KeyTileRec* 
       const long long thr = rm.thr[c];
       if (rec->sorted[c]) {
         // keys of this type form a run with non-decreasing times: count t_j <= thr
-        const int rl = rec->run_lo[c];
         int first = 0, len = n;
         while (len > 0) {
           const int half = len >> 1;
