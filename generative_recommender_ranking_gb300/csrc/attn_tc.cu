@@ -12,22 +12,21 @@
 //                 head by head), publish item descriptors and per-stage tile
 //                 info in shared memory, load Q', K', V (and, for PARTIAL tiles, the
 //                 key-tile record) with TMA / bulk copies into per-stream rings;
-//   warp 2, 3     MMA issuers (stream 0, 1): each 128-key tile is two 64-key chunks;
-//                 S(g) = Q'K'(g)^T goes to TMEM buffer g % 2 of the stream, so S(g+1)
-//                 is computed while the softmax works on chunk g; O += P(g) V(g) reads
-//                 P straight from TMEM (P overwrites the first 32 columns of S(g));
+//   warp 2, 3     MMA issuers (stream 0, 1).  d = 64: S = Q'K'^T over a whole 128-key
+//                 tile (N = 128), issued as soon as the softmax has read the previous
+//                 S; P has TMEM columns of its own and O += P V is issued per 64-key
+//                 half.  d = 128: each tile is two 64-key chunks with S double-buffered
+//                 and P written over the first columns of its chunk's S;
 //   warps 4..7    softmax of stream 0, warps 8..11 softmax of stream 1: one query row
 //                 per thread (TMEM lane quadrant = warp % 4).  PARTIAL tiles build the
 //                 row's 128-bit visibility mask from position ranges, per-type key
 //                 bitmaps and, for time clauses, a binary search over time-sorted
 //                 runs; FULL tiles skip the mask.  Online softmax in the exp2 domain
 //                 with a lazily updated reference maximum; O rescaled in TMEM only when
-//                 the maximum grows by more than 2^8; P rounded to bf16.  The row sum l
-//                 is the sum of exactly those rounded P values (for d = 64 the PV MMA
-//                 computes it: a block of bf16 ones is appended to V as 16 extra output
-//                 columns), so every output row is an exact convex combination of the
-//                 value rows it saw.  Row times and types come from the query tile's
-//                 planner record, bulk-copied next to Q.
+//                 the maximum grows by more than 2^8, and only then does the softmax
+//                 wait for the PV that precedes it.  P rounded to bf16; the row sum l
+//                 is the fp32 sum of the unrounded exponentials.  Row times and types
+//                 come from the query tile's planner record, bulk-copied next to Q.
 // Every wait on an mbarrier is bounded (REC_ATTN_ERR_TIMEOUT in the status word).
 #include <climits>
 
@@ -41,7 +40,6 @@ namespace recattn {
 namespace {
 
 constexpr int kStreams = 2;
-constexpr int kThreads = 384;
 constexpr int kSlab = kTile * 128;           // 128 rows x 128 B: one 64-column swizzle slab
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
@@ -51,20 +49,44 @@ constexpr int kChunk = 64;                   // keys per S chunk (a 128-key tile
 
 template <int D>
 struct Cfg;
-// QB: Q buffers per stream, NS: K/V stages per stream, SUM: the PV MMA also sums P
-// (a block of ones appended to V as 16 extra output columns), OC: TMEM columns of O.
+// QB: Q buffers per stream, NS: K/V stages per stream, WIDE: S over the whole 128-key
+// tile with P in TMEM columns of its own (else two 64-key chunks, P over S).
 template <>
 struct Cfg<64> {
   static constexpr int QB = 2, NS = 2;
-  static constexpr bool SUM = true;
-  static constexpr int OC = 64 + 16;
+  static constexpr bool WIDE = true;
 };
 template <>
 struct Cfg<128> {
   static constexpr int QB = 1, NS = 1;
-  static constexpr bool SUM = false;
-  static constexpr int OC = 128;
+  static constexpr bool WIDE = false;
 };
+// per stream one producer warp and one MMA-issuer warp, then two softmax warpgroups
+constexpr int kRoleWarps = 2 * kStreams;
+constexpr int kThreads = 32 * (kRoleWarps + 8);
+
+// TMEM columns of one stream (lane base included by the caller).
+//   WIDE:    [stream] S 128 | P 64 (bf16 pairs) | O D      -> 2 x 256 for D = 64
+//   chunked: S [stream][2 chunks][64], then O [stream][D]   -> 256 + 2 x 128 for D = 128
+struct TmemMap {
+  uint32_t s, p, o;
+};
+template <int D>
+__device__ __forceinline__ TmemMap tmem_map(uint32_t base, int s) {
+  TmemMap m;
+  if (Cfg<D>::WIDE) {
+    m.s = base + (uint32_t)(s * (kTile + kTile / 2 + D));
+    m.p = m.s + kTile;
+    m.o = m.p + kTile / 2;
+  } else {
+    m.s = base + (uint32_t)(s * kTile);
+    m.p = 0;
+    m.o = base + 2u * kTile + (uint32_t)(s * D);
+  }
+  return m;
+}
+static_assert(kStreams * (kTile + kTile / 2 + 64) <= (int)kTmemCols, "WIDE TMEM map");
+static_assert(2 * kTile + kStreams * 128 <= (int)kTmemCols, "chunked TMEM map");
 
 struct ItemDesc {
   long long tok0;  // first token of the query tile (global index)
@@ -90,27 +112,33 @@ struct Layout {
   static constexpr int kQ = 0;                                   // [stream][QB]
   static constexpr int kK = kQ + kStreams * QB * kQBytes;        // [stream][NS]
   static constexpr int kV = kK + kStreams * NS * kKVBytes;       // [stream][NS]
-  static constexpr int kOnes = kV + kStreams * NS * kKVBytes;    // 128 x 64 bf16 ones (SUM only)
-  static constexpr int kRec = kOnes + (Cfg<D>::SUM ? kSlab : 0);  // [stream][NS] KeyTileRec
+  static constexpr int kRec = kV + kStreams * NS * kKVBytes;      // [stream][NS] KeyTileRec
   static constexpr int kQRec = kRec + kStreams * NS * kRecBytes;  // [stream][QB] KeyTileRec of the query tile
   static constexpr int kInfo = kQRec + kStreams * QB * kRecBytes; // [stream][NS] StageInfo
   static constexpr int kItems = (kInfo + kStreams * NS * 8 + 15) & ~15;  // [stream][2] ItemDesc
   static constexpr int kBars = (kItems + kStreams * 2 * 32 + 7) & ~7;
-  static constexpr int kBarsPerStream = 2 + 2 + 2 * QB + 3 * NS + 6;
+  static constexpr int kBarsPerStream = 2 + 2 + 2 * QB + 4 * NS + 9;
   static constexpr int kTotal = kBars + kStreams * kBarsPerStream * 8 + 16;
   static constexpr int kDynamic = kTotal + 1024;  // slack to align the base to 1024 B
 };
 
 // mbarriers of one stream
 struct SBars {
-  uint64_t *item_full, *item_empty, *q_full, *q_empty, *k_full, *v_full, *kv_empty;
-  uint64_t *s_full, *p_full, *pv_done, *o_ready, *mma_done;  // s_full: [2], one per S buffer
+  // k_free[st]: the softmax has seen S of the stage's tile complete (so K was read)
+  // and has read the stage's tile info and key record; v_empty[st]: the tile's last
+  // PV completed.  K and V of a stage are refilled independently.
+  uint64_t *item_full, *item_empty, *q_full, *q_empty, *k_full, *v_full, *k_free, *v_empty;
+  // s_full, p_full, pv_done: [2] each.  Chunked: indexed by the stream's chunk count
+  // mod 2.  WIDE: s_full[0] only (one S buffer), s_free when the softmax has read S,
+  // p_full / pv_done indexed by the 64-key half of the tile.
+  uint64_t *s_full, *s_free, *p_full, *pv_done, *o_ready, *mma_done;
   template <int D>
   __device__ void bind(uint64_t* b) {
     constexpr int QB = Cfg<D>::QB, NS = Cfg<D>::NS;
     item_full = b; item_empty = b + 2; q_full = b + 4; q_empty = q_full + QB;
-    k_full = q_empty + QB; v_full = k_full + NS; kv_empty = v_full + NS;
-    s_full = kv_empty + NS; p_full = s_full + 2; pv_done = p_full + 1; o_ready = pv_done + 1;
+    k_full = q_empty + QB; v_full = k_full + NS; k_free = v_full + NS; v_empty = k_free + NS;
+    s_full = v_empty + NS; s_free = s_full + 2; p_full = s_free + 1; pv_done = p_full + 2;
+    o_ready = pv_done + 2;
     mma_done = o_ready + 1;
   }
 };
@@ -155,6 +183,19 @@ __device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsign
   unsigned long long r;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
+}
+
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// max(a, b, c) in one instruction (NaN operands are ignored, as with fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -289,10 +330,10 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
   uint8_t* rbuf = sm + L::kRec + s * NS * kRecBytes;
   uint8_t* qrbuf = sm + L::kQRec + s * QB * kRecBytes;
   uint32_t it_cnt = 0, q_it = 0, kv_it = 0;
-  bool q_used[QB], st_used[NS];
-  uint32_t q_ph[QB], st_ph[NS];
+  bool q_used[QB], k_used[NS], v_used[NS];
+  uint32_t q_ph[QB], k_ph[NS], v_ph[NS];
   for (int i = 0; i < QB; ++i) { q_used[i] = false; q_ph[i] = 0; }
-  for (int i = 0; i < NS; ++i) { st_used[i] = false; st_ph[i] = 0; }
+  for (int i = 0; i < NS; ++i) { k_used[i] = v_used[i] = false; k_ph[i] = v_ph[i] = 0; }
   for (;;) {
     const long long w = atomicAdd(a.counters + 1, 1);
     const int slot = (int)(it_cnt & 1);
@@ -328,7 +369,7 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
       const int kt = (int)(e & 0xffffffu), cl = (int)(e >> 24);
       const int st = (int)(kv_it % NS);
       const uint32_t ph = (kv_it / NS) & 1;
-      if (!wait_bar(B.kv_empty + st, ph ^ 1, abort_flag, a.status)) goto drain;
+      if (!wait_bar(B.k_free + st, ph ^ 1, abort_flag, a.status)) goto drain;
       info[st].kt = kt;
       info[st].cls = cl;
       const bool partial = cl != REC_ATTN_TILE_FULL;
@@ -338,11 +379,13 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
       for (int c = 0; c < D / 64; ++c)
         ptx::tma_load_2d(kbuf + st * L::kKVBytes + c * kSlab, tk, it.h * D + c * 64, y, B.k_full + st);
       if (partial) ptx::bulk_load(rbuf + st * kRecBytes, a.krec + it.m.tile_start + kt, kRecBytes, B.k_full + st);
+      k_used[st] = true; k_ph[st] = ph;
+      if (!wait_bar(B.v_empty + st, ph ^ 1, abort_flag, a.status)) goto drain;
       ptx::mbar_arrive_expect_tx(B.v_full + st, L::kKVBytes);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
         ptx::tma_load_2d(vbuf + st * L::kKVBytes + c * kSlab, tv, it.h * D + c * 64, y, B.v_full + st);
-      st_used[st] = true; st_ph[st] = ph;
+      v_used[st] = true; v_ph[st] = ph;
       ++kv_it;
     }
   }
@@ -350,31 +393,39 @@ drain:
   // every load issued must land before the CTA exits (only waits after an abort)
   for (int i = 0; i < QB; ++i)
     if (q_used[i]) drain_bar(B.q_full + i, q_ph[i]);
-  for (int i = 0; i < NS; ++i)
-    if (st_used[i]) { drain_bar(B.k_full + i, st_ph[i]); drain_bar(B.v_full + i, st_ph[i]); }
+  for (int i = 0; i < NS; ++i) {
+    if (k_used[i]) drain_bar(B.k_full + i, k_ph[i]);
+    if (v_used[i]) drain_bar(B.v_full + i, v_ph[i]);
+  }
 }
 
 // ------------------------------------------------------------------ MMA issuer
-// Per stream, each 128-key tile is processed as two 64-key chunks.  Chunk g of the
-// stream (counted across items) has its S in TMEM buffer g % 2; its P overwrites the
-// first 32 columns of that buffer.  Issue order: S(0), S(1), then for every chunk g:
-// PV(g) once P(g) is ready, then S(g+2) into the buffer PV(g) has just read.  So while
-// the softmax works on chunk g, S(g+1) is already computed.
+// Per stream, one thread issues every MMA; tiles are counted across the stream's items.
+//
+// WIDE (d = 64): S(t) = Q' K'(t)^T over the whole 128-key tile (N = 128) into the
+// stream's single S buffer.  S(t+1) is issued as soon as the softmax has read S(t)
+// into registers (s_free), so it runs while the softmax computes exponentials.  P(t)
+// has its own 64 TMEM columns, one 32-column half per 64-key chunk; O += P_c(t) V_c(t)
+// is issued per chunk once that half of P is written (p_full[c]).
+//
+// Chunked (d = 128, where a separate P does not fit next to O): each tile is two
+// 64-key chunks; chunk g of the stream has its S in buffer g % 2 and its P overwrites
+// the first 32 columns of that buffer.  Issue order: S(0), S(1), then for every chunk
+// g: PV(g) once P(g) is ready, then S(g+2) into the buffer PV(g) has just read (the
+// tensor core runs one thread's MMAs in order).
 template <int D>
 __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, uint32_t tmem,
                         volatile int* abort_flag) {
   using L = Layout<D>;
   constexpr int QB = L::QB, NS = L::NS;
-  constexpr int OC = Cfg<D>::OC;
-  constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kTile, kChunk, false, false);
-  constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kTile, OC, false, true);
+  constexpr bool WIDE = Cfg<D>::WIDE;
+  constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kTile, WIDE ? kTile : kChunk, false, false);
+  constexpr uint32_t idesc_o = ptx::idesc_bf16_f32(kTile, D, false, true);
   const ItemDesc* items = reinterpret_cast<const ItemDesc*>(sm + L::kItems) + s * 2;
   const uint32_t q_addr = ptx::smem_u32(sm + L::kQ + s * QB * L::kQBytes);
   const uint32_t k_addr = ptx::smem_u32(sm + L::kK + s * NS * L::kKVBytes);
   const uint32_t v_addr = ptx::smem_u32(sm + L::kV + s * NS * L::kKVBytes);
-  const uint32_t tm_s = tmem + (uint32_t)(s * kTile);
-  const uint32_t tm_o = tmem + 2u * kTile + (uint32_t)(s * OC);
-  const uint32_t ones_addr = ptx::smem_u32(sm + L::kOnes);
+  const TmemMap tm = tmem_map<D>(tmem, s);
   uint32_t it_cnt = 0, q_it = 0, kv_it = 0, p_it = 0, s_ch = 0;
   for (;;) {
     const int slot = (int)(it_cnt & 1);
@@ -389,60 +440,101 @@ __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, u
     ++q_it;
     ptx::tc_fence_after();
     const uint32_t qa = q_addr + qb * L::kQBytes;
-    const int nch = 2 * n;
-    // S(g) = Q' K'(g)^T for chunk g of this item, into buffer s_ch % 2
-    auto issue_s = [&](int g) -> bool {
-      const int j = g >> 1, c = g & 1;
-      const int st = (int)((kv_it + j) % NS);
-      if (c == 0) {
+    if constexpr (WIDE) {
+      // S(j) of this item; s_ch counts the stream's S tiles
+      auto issue_s = [&](int j) -> bool {
+        const int st = (int)((kv_it + j) % NS);
+        if (s_ch > 0 && !wait_bar(B.s_free, (s_ch - 1) & 1, abort_flag, a.status)) return false;
         if (!wait_bar(B.k_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) return false;
         ptx::tc_fence_after();
-      }
-      const uint32_t kb = k_addr + st * L::kKVBytes + c * (kChunk * 128);
-      const uint32_t d_tmem = tm_s + (s_ch & 1) * kChunk;
+        const uint32_t kb = k_addr + st * L::kKVBytes;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
-        ptx::umma_f16(d_tmem, ptx::smem_desc_sw128(qa + off, 16, 1024), ptx::smem_desc_sw128(kb + off, 16, 1024),
-                      idesc_s, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
+          ptx::umma_f16(tm.s, ptx::smem_desc_sw128(qa + off, 16, 1024), ptx::smem_desc_sw128(kb + off, 16, 1024),
+                        idesc_s, kk > 0 ? 1u : 0u);
+        }
+        ptx::umma_commit(B.s_full);
+        ++s_ch;
+        if (j == n - 1) ptx::umma_commit(B.q_empty + qb);  // last S of the item issued
+        return true;
+      };
+      if (!issue_s(0)) goto out;
+      for (int j = 0; j < n; ++j) {
+        if (j + 1 < n && !issue_s(j + 1)) goto out;
+        const int st = (int)((kv_it + j) % NS);
+        const uint32_t vb = v_addr + st * L::kKVBytes;
+        const uint32_t pc = p_it++;  // the stream's PV tile count
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          if (!wait_bar(B.p_full + c, pc & 1, abort_flag, a.status)) goto out;
+          ptx::tc_fence_after();
+          if (c == 0) {
+            if (!wait_bar(B.v_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) goto out;
+            ptx::tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < kChunk / 16; ++kk)
+            ptx::umma_f16_ts(tm.o, tm.p + c * (kChunk / 2) + kk * 8,
+                             ptx::smem_desc_sw128(vb + (c * kChunk + kk * 16) * 128, kSlab, 1024), idesc_o,
+                             (j > 0 || c > 0 || kk > 0) ? 1u : 0u);
+          ptx::umma_commit(B.pv_done + c);
+        }
+        ptx::umma_commit(B.v_empty + st);
       }
-      ptx::umma_commit(B.s_full + (s_ch & 1));
-      ++s_ch;
-      if (g == nch - 1) ptx::umma_commit(B.q_empty + qb);  // last S of the item issued
-      return true;
-    };
-    const uint32_t ch0 = s_ch;  // global chunk index of this item's chunk 0
-    if (!issue_s(0) || !issue_s(1)) goto out;
-    for (int g = 0; g < nch; ++g) {
-      const int j = g >> 1, c = g & 1;
-      const int st = (int)((kv_it + j) % NS);
-      if (!wait_bar(B.p_full, p_it & 1, abort_flag, a.status)) goto out;
-      ++p_it;
-      ptx::tc_fence_after();
-      if (c == 0) {
-        if (!wait_bar(B.v_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) goto out;
+    } else {
+      const int nch = 2 * n;
+      // S(g) = Q' K'(g)^T for chunk g of this item, into buffer s_ch % 2
+      auto issue_s = [&](int g) -> bool {
+        const int j = g >> 1, c = g & 1;
+        const int st = (int)((kv_it + j) % NS);
+        if (c == 0) {
+          if (!wait_bar(B.k_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) return false;
+          ptx::tc_fence_after();
+        }
+        const uint32_t kb = k_addr + st * L::kKVBytes + c * (kChunk * 128);
+        const uint32_t d_tmem = tm.s + (s_ch & 1) * kChunk;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
+          ptx::umma_f16(d_tmem, ptx::smem_desc_sw128(qa + off, 16, 1024), ptx::smem_desc_sw128(kb + off, 16, 1024),
+                        idesc_s, kk > 0 ? 1u : 0u);
+        }
+        ptx::umma_commit(B.s_full + (s_ch & 1));
+        ++s_ch;
+        if (g == nch - 1) ptx::umma_commit(B.q_empty + qb);  // last S of the item issued
+        return true;
+      };
+      const uint32_t ch0 = s_ch;  // global chunk index of this item's chunk 0
+      if (!issue_s(0) || !issue_s(1)) goto out;
+      for (int g = 0; g < nch; ++g) {
+        const int j = g >> 1, c = g & 1;
+        const int st = (int)((kv_it + j) % NS);
+        const uint32_t pc = p_it++;  // the stream's chunk count
+        if (!wait_bar(B.p_full + (pc & 1), (pc >> 1) & 1, abort_flag, a.status)) goto out;
         ptx::tc_fence_after();
-      }
-      // O += P(g) V(g): P from TMEM, V rows of this chunk; the second 64-column block
-      // of B is the next V slab (D = 128) or the block of ones whose first 16 output
-      // columns give the row sum of P (D = 64)
-      const uint32_t vb = v_addr + st * L::kKVBytes;
-      const uint32_t lbo = Cfg<D>::SUM ? ones_addr - vb : (uint32_t)kSlab;
-      const uint32_t pa = tm_s + ((ch0 + g) & 1) * kChunk;
+        if (c == 0) {
+          if (!wait_bar(B.v_full + st, ((kv_it + j) / NS) & 1, abort_flag, a.status)) goto out;
+          ptx::tc_fence_after();
+        }
+        // O += P(g) V(g): P from TMEM, V rows of this chunk (both 64-column slabs)
+        const uint32_t vb = v_addr + st * L::kKVBytes;
+        const uint32_t pa = tm.s + ((ch0 + g) & 1) * kChunk;
 #pragma unroll
-      for (int kk = 0; kk < kChunk / 16; ++kk)
-        ptx::umma_f16_ts(tm_o, pa + kk * 8,
-                         ptx::smem_desc_sw128(vb + c * (kChunk * 128) + kk * 16 * 128, lbo, 1024), idesc_o,
-                         (g > 0 || kk > 0) ? 1u : 0u);
-      ptx::umma_commit(B.pv_done);
-      if (c == 1) ptx::umma_commit(B.kv_empty + st);
-      if (NS >= 2) {
-        if (g + 2 < nch && !issue_s(g + 2)) goto out;
-      } else if (c == 1) {
-        // one K/V stage: the next tile's K can only land after this tile's last PV,
-        // so both of its S chunks are issued here
-        if (g + 1 < nch && !issue_s(g + 1)) goto out;
-        if (g + 2 < nch && !issue_s(g + 2)) goto out;
+        for (int kk = 0; kk < kChunk / 16; ++kk)
+          ptx::umma_f16_ts(tm.o, pa + kk * 8,
+                           ptx::smem_desc_sw128(vb + c * (kChunk * 128) + kk * 16 * 128, kSlab, 1024), idesc_o,
+                           (g > 0 || kk > 0) ? 1u : 0u);
+        ptx::umma_commit(B.pv_done + (pc & 1));
+        if (c == 1) ptx::umma_commit(B.v_empty + st);
+        if (NS >= 2) {
+          if (g + 2 < nch && !issue_s(g + 2)) goto out;
+        } else if (c == 1) {
+          // one K/V stage: the next tile's K can only land after this tile's last PV,
+          // so both of its S chunks are issued here
+          if (g + 1 < nch && !issue_s(g + 1)) goto out;
+          if (g + 2 < nch && !issue_s(g + 2)) goto out;
+        }
       }
     }
     ptx::umma_commit(B.o_ready);
@@ -455,24 +547,85 @@ out:
 }
 
 // ------------------------------------------------------------------ softmax
+// One 64-key chunk of a row: masked scores, lazy reference-max update, P = 2^(x*sl2 - m)
+// rounded to bf16 (packed pairs), the fp32 sum of the exponentials, and the factor
+// (corr, needed when resc) by which O and l must be scaled before P is added.
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[kChunk], bool partial, uint32_t w0, uint32_t w1,
+                                              float sl2, float& m_ref, uint32_t (&pk)[kChunk / 2], float& corr,
+                                              bool& resc, float& rs) {
+  float x[kChunk];
+#pragma unroll
+  for (int e = 0; e < kChunk; ++e) x[e] = __uint_as_float(sr[e]);
+  if (partial) {
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e)
+      if (!(((e < 32 ? w0 : w1) >> (e & 31)) & 1u)) x[e] = -INFINITY;
+  }
+  // row maximum as a depth-4 tree of three-input maxima (21 + 7 + 3 + 1)
+  static_assert(kChunk == 64, "the max tree covers 64 scores");
+  float m1[22], m2[8];
+#pragma unroll
+  for (int i = 0; i < 21; ++i) m1[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  m1[21] = x[63];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
+  m2[7] = m1[21];
+  const float mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+  const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
+  const float m_new = (m_tile > m_ref + kRescaleLog2) ? m_tile : m_ref;
+  const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+  // O (and l) need scaling only when a finite running max moved; while it is -inf
+  // every P so far was exactly 0, so O and l are 0
+  resc = m_new != m_ref && m_ref != -INFINITY;
+  corr = resc ? ex2(m_ref - m_use) : 1.f;
+  const unsigned long long sl2x2 = pack2(sl2, sl2), negm2 = pack2(-m_use, -m_use);
+  unsigned long long acc0 = 0ull, acc1 = 0ull;  // packed partial sums (+0.0f pairs)
+#pragma unroll
+  for (int e = 0; e < kChunk / 2; ++e) {
+    float y0, y1;
+    unpack2(ffma2(pack2(x[2 * e], x[2 * e + 1]), sl2x2, negm2), y0, y1);
+    const float e0 = ex2(y0), e1 = ex2(y1);
+    const __nv_bfloat162 pb = __floats2bfloat162_rn(e0, e1);
+    pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
+    if (e & 1) acc1 = fadd2(acc1, pack2(e0, e1));
+    else acc0 = fadd2(acc0, pack2(e0, e1));
+  }
+  float r0, r1, r2, r3;
+  unpack2(acc0, r0, r1);
+  unpack2(acc1, r2, r3);
+  rs = (r0 + r1) + (r2 + r3);
+  m_ref = m_new;
+}
+
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t tm_o, float corr) {
+#pragma unroll
+  for (int half = 0; half < D / 64; ++half) {
+    uint32_t o[64];
+    ptx::tmem_ld64(tm_o + half * 64, o);
+#pragma unroll
+    for (int e = 0; e < 64; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+    ptx::tmem_st64(tm_o + half * 64, o);
+  }
+}
+
 template <int D>
 __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, uint32_t tmem,
                             volatile int* abort_flag) {
   using L = Layout<D>;
   constexpr int NS = L::NS;
+  constexpr bool WIDE = Cfg<D>::WIDE;
   const ItemDesc* items = reinterpret_cast<const ItemDesc*>(sm + L::kItems) + s * 2;
   const StageInfo* info = reinterpret_cast<const StageInfo*>(sm + L::kInfo) + s * NS;
   const KeyTileRec* recs = reinterpret_cast<const KeyTileRec*>(sm + L::kRec) + s * NS;
   const KeyTileRec* qrecs = reinterpret_cast<const KeyTileRec*>(sm + L::kQRec) + s * L::QB;
-  constexpr int OC = Cfg<D>::OC;
   const int lane = threadIdx.x & 31;
   const int quad = (threadIdx.x >> 5) & 3;  // TMEM lanes this warp may access
   const int row = quad * 32 + lane;
-  const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const uint32_t tm_s = tmem + lane_off + (uint32_t)(s * kTile);
-  const uint32_t tm_o = tmem + lane_off + 2u * kTile + (uint32_t)(s * OC);
+  const TmemMap tm = tmem_map<D>(tmem + ((uint32_t)(quad * 32) << 16), s);
   const float sl2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
   const int H = a.heads;
+  // ch: the stream's S chunk count (chunked) or S tile count (WIDE)
   uint32_t it_cnt = 0, kv_it = 0, ch = 0, o_it = 0, q_it = 0;
   for (;;) {
     const int slot = (int)(it_cnt & 1);
@@ -508,6 +661,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
     RowMask rm;
     row_mask_setup(a.mask, row_ok, pi, ti, tyi, rm);
     float m_ref = -INFINITY, l = 0.f;
+    bool p1_pending = false;
     for (int j = 0; j < d.n; ++j) {
       const int st = (int)(kv_it % NS);
       const uint32_t kph = (kv_it / NS) & 1;
@@ -518,86 +672,95 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       const bool partial = inf.cls != REC_ATTN_TILE_FULL;
       uint32_t vm[4] = {~0u, ~0u, ~0u, ~0u};
       if (partial) build_mask(rm, recs + st, inf.kt * kTile, vm);
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t buf = ch & 1;
-        if (!wait_bar_warp(B.s_full + buf, (ch >> 1) & 1, abort_flag, a.status)) return;
+      if constexpr (WIDE) {
+        const uint32_t t = ch++;
+        if (!wait_bar_warp(B.s_full, t & 1, abort_flag, a.status)) return;
+        ptx::mbar_arrive(B.k_free + st);  // S(t) has read K; info and record were read above
         ptx::tc_fence_after();
-        uint32_t sr[kChunk];
-        ptx::tmem_ld64(tm_s + buf * kChunk, sr);
-        float x[kChunk];
-#pragma unroll
-        for (int e = 0; e < kChunk; ++e) x[e] = __uint_as_float(sr[e]);
-        if (partial) {
-          const uint32_t w0 = c ? vm[2] : vm[0], w1 = c ? vm[3] : vm[1];
-#pragma unroll
-          for (int e = 0; e < kChunk; ++e)
-            if (!(((e < 32 ? w0 : w1) >> (e & 31)) & 1u)) x[e] = -INFINITY;
+        uint32_t sr[kChunk], pk[kChunk / 2];
+        float corr, rs;
+        bool resc;
+        ptx::tmem_ld64_async(tm.s, sr);
+        ptx::tmem_wait_ld(sr);
+        if (p1_pending) {  // publish the previous tile's P half 1, stored while this S loaded
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(B.p_full + 1);
+          p1_pending = false;
         }
-        float mx = x[0];
-#pragma unroll
-        for (int e = 1; e < kChunk; ++e) mx = fmaxf(mx, x[e]);
-        const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
-        const float m_new = (m_tile > m_ref + kRescaleLog2) ? m_tile : m_ref;
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float corr = ex2(m_ref - m_use);  // 0 when m_ref = -inf, 1 when unchanged
-        uint32_t pk[kChunk / 2];
-        float rs = 0.f;
-        const unsigned long long sl2x2 = pack2(sl2, sl2), negm2 = pack2(-m_use, -m_use);
-#pragma unroll
-        for (int e = 0; e < kChunk / 2; ++e) {
-          float y0, y1;
-          unpack2(ffma2(pack2(x[2 * e], x[2 * e + 1]), sl2x2, negm2), y0, y1);
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(ex2(y0), ex2(y1));
-          if (!Cfg<D>::SUM) rs += __low2float(pb) + __high2float(pb);
-          pk[e] = *reinterpret_cast<const uint32_t*>(&pb);
-        }
-        if (!Cfg<D>::SUM) l = l * corr + rs;
-        // Every PV completion is waited for in order (one phase per chunk, so the
-        // parity wait is exact); O may only be rescaled once PV(ch-1) has landed, and
-        // PV(ch-1) was issued as soon as P(ch-1) was ready, so this rarely waits.
-        if (ch > 0) {
-          if (!wait_bar_warp(B.pv_done, (ch - 1) & 1, abort_flag, a.status)) return;
+        softmax_chunk(sr, partial, vm[0], vm[1], sl2, m_ref, pk, corr, resc, rs);
+        l = l * corr + rs;
+        // P half c may be overwritten once PV_c(t-1) has read it; O may be rescaled
+        // once every earlier PV has landed.  Each pv_done[c] completes once per tile
+        // and PV_c(t) needs P half c of tile t, so every parity wait here is exact.
+        if (t > 0 && !wait_bar_warp(B.pv_done + 0, (t - 1) & 1, abort_flag, a.status)) return;
+        if (__any_sync(0xffffffffu, resc)) {
+          if (!wait_bar_warp(B.pv_done + 1, (t - 1) & 1, abort_flag, a.status)) return;
           ptx::tc_fence_after();
+          rescale_o<D>(tm.o, corr);
         }
-        if ((j > 0 || c > 0) && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
-          for (int half = 0; half < D / 64; ++half) {
-            uint32_t o[64];
-            ptx::tmem_ld64(tm_o + half * 64, o);
-#pragma unroll
-            for (int e = 0; e < 64; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-            ptx::tmem_st64(tm_o + half * 64, o);
-          }
-          if (Cfg<D>::SUM) {  // the row-sum columns
-            uint32_t o[16];
-            ptx::tmem_ld16(tm_o + D, o);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-            ptx::tmem_st16(tm_o + D, o);
-          }
-        }
-        ptx::tmem_st32(tm_s + buf * kChunk, pk);  // P over the first 32 columns of S
+        ptx::tc_fence_after();
+        ptx::tmem_st32_async(tm.p, pk);
+        ptx::tmem_ld64_async(tm.s + kChunk, sr);  // the second half loads while P half 0 stores
+        ptx::tmem_wait_ld(sr);
+        ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(B.p_full);
-        m_ref = m_new;
-        ++ch;
+        ptx::mbar_arrive(B.p_full + 0);
+        ptx::mbar_arrive(B.s_free);  // S(t) is in registers: S(t+1) may overwrite it
+        softmax_chunk(sr, partial, vm[2], vm[3], sl2, m_ref, pk, corr, resc, rs);
+        l = l * corr + rs;
+        if (t > 0 && !wait_bar_warp(B.pv_done + 1, (t - 1) & 1, abort_flag, a.status)) return;
+        if (__any_sync(0xffffffffu, resc)) {
+          if (!wait_bar_warp(B.pv_done + 0, t & 1, abort_flag, a.status)) return;
+          ptx::tc_fence_after();
+          rescale_o<D>(tm.o, corr);
+        }
+        ptx::tc_fence_after();
+        ptx::tmem_st32_async(tm.p + kChunk / 2, pk);
+        p1_pending = true;  // published after the next S load, or before the epilogue
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t buf = ch & 1;
+          if (!wait_bar_warp(B.s_full + buf, (ch >> 1) & 1, abort_flag, a.status)) return;
+          if (c == 1) ptx::mbar_arrive(B.k_free + st);  // both S chunks have read K
+          ptx::tc_fence_after();
+          uint32_t sr[kChunk], pk[kChunk / 2];
+          float corr, rs;
+          bool resc;
+          ptx::tmem_ld64(tm.s + buf * kChunk, sr);
+          softmax_chunk(sr, partial, c ? vm[2] : vm[0], c ? vm[3] : vm[1], sl2, m_ref, pk, corr, resc, rs);
+          l = l * corr + rs;
+          // O may only be rescaled once PV(ch-1) has landed.  The two pv_done barriers
+          // alternate by chunk, and PV(ch+1) cannot start before P(ch+1) exists, so the
+          // barrier of chunk ch-1 is at most at that chunk's phase: the parity wait is
+          // exact although most chunks never wait on it.
+          if (__any_sync(0xffffffffu, resc)) {
+            if (!wait_bar_warp(B.pv_done + ((ch - 1) & 1), ((ch - 1) >> 1) & 1, abort_flag, a.status)) return;
+            ptx::tc_fence_after();
+            rescale_o<D>(tm.o, corr);
+          }
+          ptx::tmem_st32(tm.s + buf * kChunk, pk);  // P over the first 32 columns of S
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(B.p_full + (ch & 1));
+          ++ch;
+        }
       }
+    }
+    if (p1_pending) {
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(B.p_full + 1);
     }
     // epilogue: O / l
     if (!wait_bar_warp(B.o_ready, o_it & 1, abort_flag, a.status)) return;
     ++o_it;
     ptx::tc_fence_after();
-    if (Cfg<D>::SUM) {
-      uint32_t o[16];
-      ptx::tmem_ld16(tm_o + D, o);
-      l = __uint_as_float(o[0]);
-    }
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int half = 0; half < D / 64; ++half) {
       uint32_t o[64];
-      ptx::tmem_ld64(tm_o + half * 64, o);
+      ptx::tmem_ld64(tm.o + half * 64, o);
       if (row_ok) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -647,12 +810,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < NS; ++i) {
         ptx::mbar_init(B.k_full + i, 1);
         ptx::mbar_init(B.v_full + i, 1);
-        ptx::mbar_init(B.kv_empty + i, 1);
+        ptx::mbar_init(B.k_free + i, 128);
+        ptx::mbar_init(B.v_empty + i, 1);
       }
       ptx::mbar_init(B.s_full, 1);
       ptx::mbar_init(B.s_full + 1, 1);
-      ptx::mbar_init(B.p_full, 128);
-      ptx::mbar_init(B.pv_done, 1);
+      ptx::mbar_init(B.s_free, 128);
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(B.p_full + i, 128);
+        ptx::mbar_init(B.pv_done + i, 1);
+      }
       ptx::mbar_init(B.o_ready, 1);
       ptx::mbar_init(B.mma_done, 1);
     }
@@ -663,18 +830,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (Cfg<D>::SUM) {  // bf16 ones, read by the PV MMA as extra B columns
-    uint4* ones = reinterpret_cast<uint4*>(sm + L::kOnes);
-    for (int i = threadIdx.x; i < kSlab / 16; i += blockDim.x)
-      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    ptx::fence_proxy_async_smem();
-  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < kRoleWarps) {
     const int s = warp & 1;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
@@ -683,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       else run_mma<D>(a, sm, s, B, tmem, abort_flag);
     }
   } else {
-    const int s = (warp - 4) >> 2;
+    const int s = (warp - kRoleWarps) >> 2;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
     run_softmax<D>(a, sm, s, B, tmem, abort_flag);
