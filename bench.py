@@ -50,6 +50,27 @@ def _peaks():
                 "source": "fallback"}
 
 
+def _traffic(workload: str):
+    """DRAM bytes (read + write) of one attention launch from the committed ncu capture,
+    or None when the capture is for another workload or the kernel sources have changed
+    since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "k_attn_tc_dram_traffic.json")
+    try:
+        import hashlib
+        with open(path) as f:
+            d = json.load(f)
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != d["sources_sha256"] or workload not in d["workloads"]:
+            return None
+        x = d["workloads"][workload]
+        return float(x["dram_bytes_read"] + x["dram_bytes_write"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def _workload(name, rank, batch=None):
     kw = {}
     if rank:
@@ -313,15 +334,17 @@ def run_ours(args):
     bytes_attn = 4.0 * tokens * w.num_heads * w.head_dim * elem + 9.0 * tokens
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
     attn_gbs = bytes_attn / (attn_ms * 1e-3) / 1e9
+    # full-size default batch only: the capture was taken on that launch
+    traffic = _traffic(args.workload) if (args.batch is None and world == 1) else None
     hbm_bound = (flops / bytes_attn) < (pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9))
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": attn_gbs / pk["hbm_gbs"], "traffic": None,
+                "frac": attn_gbs / pk["hbm_gbs"], "traffic": traffic,
                 "kernel": "k_attn_tc (masked softmax attention)", "peak_source": pk["source"],
                 "algorithmic_bytes_per_launch": bytes_attn, "ms_per_launch": attn_ms}
     else:
         roof = {"bound": "tensor", "achieved": attn_tflops, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": attn_tflops / pk["bf16_tflops"], "traffic": None,
+                "unit": "TFLOP/s", "frac": attn_tflops / pk["bf16_tflops"], "traffic": traffic,
                 "kernel": "k_attn_tc (masked softmax attention)", "peak_source": pk["source"],
                 "algorithmic_flops_per_launch": flops, "ms_per_launch": attn_ms}
     line = {
