@@ -67,6 +67,31 @@ class Params:
                          float(self.softmax_scale))
 
 
+class OrcFused(ctypes.Structure):
+    _fields_ = [
+        ("q_norm_w", ctypes.c_void_p),
+        ("k_norm_w", ctypes.c_void_p),
+        ("norm_eps", ctypes.c_double),
+        ("q_gate", ctypes.c_void_p),
+        ("k_gate", ctypes.c_void_p),
+        ("out_gate", ctypes.c_void_p),
+    ]
+
+
+@dataclass
+class Fused:
+    """Fused prologue/epilogue inputs: QK-RMSNorm gains [H, d] (None = no norm on
+    that side), its epsilon, and sigmoid-gate pre-activations [T, H, d] in the I/O
+    dtype (None = no gate) for Q, K and the attention output."""
+
+    q_norm_w: np.ndarray | None = None
+    k_norm_w: np.ndarray | None = None
+    norm_eps: float = 1e-6
+    q_gate: np.ndarray | None = None
+    k_gate: np.ndarray | None = None
+    out_gate: np.ndarray | None = None
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no CUDA); returns the library path."""
     os.makedirs(_BUILD, exist_ok=True)
@@ -102,6 +127,14 @@ def lib() -> ctypes.CDLL:
         L.orc_attention.argtypes = [P, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, vp,
                                     ctypes.c_int64, vp, vp, vp, ctypes.c_int32]
         L.orc_attention.restype = ctypes.c_int
+        L.orc_attention_fused.argtypes = [P, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, vp,
+                                          ctypes.POINTER(OrcFused), ctypes.c_int64, vp, vp, vp,
+                                          ctypes.c_int32]
+        L.orc_attention_fused.restype = ctypes.c_int
+        L.orc_rmsnorm.argtypes = [vp, vp, ctypes.c_int, ctypes.c_double, vp]
+        L.orc_rmsnorm.restype = None
+        L.orc_sigmoid.argtypes = [ctypes.c_double]
+        L.orc_sigmoid.restype = ctypes.c_double
         L.orc_tile_classes.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp]
         L.orc_tile_classes.restype = ctypes.c_int64
         _lib = L
@@ -151,6 +184,20 @@ def rope(p: Params, t: int, x) -> np.ndarray:
     return y
 
 
+def rmsnorm(x, w, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * w over one vector."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    assert x.shape == w.shape and x.ndim == 1
+    y = np.zeros_like(x)
+    lib().orc_rmsnorm(_ptr(x), _ptr(w), x.shape[0], float(eps), _ptr(y))
+    return y
+
+
+def sigmoid(x: float) -> float:
+    return float(lib().orc_sigmoid(float(x)))
+
+
 def tile_classes(p: Params, offsets, t, ty) -> np.ndarray:
     offsets, t, ty = _c64(offsets), _c64(t), _c8(ty)
     cp = p.c()
@@ -162,7 +209,7 @@ def tile_classes(p: Params, offsets, t, ty) -> np.ndarray:
 
 
 def attention(p: Params, offsets, t, ty, q, k, v, rows=None, threads: int | None = None,
-              with_lse: bool = False):
+              with_lse: bool = False, fused: Fused | None = None):
     """fp64 attention outputs for `rows` (sorted global token indices; None = all).
 
     q, k, v: [T, H, d] arrays, either float32 or uint16 holding bf16 bit patterns
@@ -190,10 +237,28 @@ def attention(p: Params, offsets, t, ty, q, k, v, rows=None, threads: int | None
     if threads is None:
         threads = os.cpu_count() or 1
     cp = p.c()
-    rc = lib().orc_attention(ctypes.byref(cp), len(offsets) - 1, _ptr(offsets), _ptr(t), _ptr(ty),
-                             dtype, _ptr(q), _ptr(k), _ptr(v), n_rows,
-                             None if rows_arr is None else _ptr(rows_arr), _ptr(out), _ptr(lse),
-                             int(threads))
+    keep = []  # arrays whose buffers the C call reads
+
+    def arr(a, dt, shape):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a, dtype=dt)
+        assert a.shape == shape, (a.shape, shape)
+        keep.append(a)
+        return _ptr(a)
+
+    fp = None
+    if fused is not None:
+        T = int(offsets[-1])
+        gate_dt = np.uint16 if dtype == 0 else np.float32
+        fc = OrcFused(arr(fused.q_norm_w, np.float64, (H, d)), arr(fused.k_norm_w, np.float64, (H, d)),
+                      float(fused.norm_eps), arr(fused.q_gate, gate_dt, (T, H, d)),
+                      arr(fused.k_gate, gate_dt, (T, H, d)), arr(fused.out_gate, gate_dt, (T, H, d)))
+        fp = ctypes.byref(fc)
+    rc = lib().orc_attention_fused(ctypes.byref(cp), len(offsets) - 1, _ptr(offsets), _ptr(t), _ptr(ty),
+                                   dtype, _ptr(q), _ptr(k), _ptr(v), fp, n_rows,
+                                   None if rows_arr is None else _ptr(rows_arr), _ptr(out), _ptr(lse),
+                                   int(threads))
     if rc != 0:
         raise ValueError(f"orc_attention rejected its arguments (rc={rc})")
     out, lse = out[:n_rows], lse[:n_rows]

@@ -23,6 +23,14 @@
  *     LazFormer Eq. 19-21 (causal window + global history, target -> history,
  *     target self only); MTGR hybrid dynamic mask (static part fully visible,
  *     real-time block causal, targets see real-time events before them).
+ *   - Fused prologue / epilogue steps (orc_attention_fused): QK-RMSNorm, the
+ *     normalisation of each query and key head vector before the scores are formed
+ *     (SORT review page, section 3.3.2 "Attention Gate & QK Norm"; TM20K review
+ *     page, the QK Norm added after the query/key projections); the sigmoid gates
+ *     on the projected Q and K (CADET review page, section on time encoding and
+ *     self-gating: a per-dimension coefficient in (0, 1) multiplied back onto the
+ *     vector); and the attention output gate, an elementwise sigmoid gate on the
+ *     attention output (SORT section 3.3.2).  Order: norm, then gate, then RoPE.
  *   - The tile classification (orc_tile_classes) is NOT a definition from the
  *     pages: it is the bounding-box interval rule this project uses to skip fully
  *     masked 128x128 tiles (the pages' "mask preload check" of SORT section 4.1 and
@@ -120,6 +128,21 @@ void orc_rope(const orc_params* p, int64_t t, const double* x, double* y) {
 }
 
 /* ------------------------------------------------------------------------- */
+/* QK-RMSNorm and sigmoid gates                                               */
+/* ------------------------------------------------------------------------- */
+
+/* y = x / sqrt(mean(x^2) + eps) * w, over one head vector of length d. */
+void orc_rmsnorm(const double* x, const double* w, int d, double eps, double* y) {
+  double ss = 0.0;
+  for (int e = 0; e < d; ++e) ss += x[e] * x[e];
+  const double r = 1.0 / sqrt(ss / d + eps);
+  for (int e = 0; e < d; ++e) y[e] = x[e] * r * w[e];
+}
+
+/* The logistic function 1 / (1 + e^-x). */
+double orc_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* ------------------------------------------------------------------------- */
 /* Attention                                                                  */
 /* ------------------------------------------------------------------------- */
 
@@ -148,9 +171,31 @@ typedef struct {
   const int64_t* row_hi;
   double* out; /* [n_rows][H][d] */
   double* lse; /* [n_rows][H] or NULL */
+  const orc_fused* f; /* NULL: plain attention */
   int64_t n_units;
   int64_t next_unit; /* atomic work counter over (request, head) */
 } attn_job;
+
+/* One query (is_q) or key head vector of global token g: loaded, then QK-RMSNorm,
+ * then the sigmoid gate, then the time-RoPE, in that order.  tmp holds d doubles. */
+static void prep_row(const attn_job* J, int is_q, int64_t g, int32_t h, double* tmp, double* y) {
+  const orc_params* p = J->p;
+  const int H = p->num_heads, d = p->head_dim;
+  const int64_t base = (g * H + h) * (int64_t)d;
+  for (int e = 0; e < d; ++e) tmp[e] = load_elem(J->dtype, is_q ? J->q : J->k, base + e);
+  if (J->f) {
+    const double* w = is_q ? J->f->q_norm_w : J->f->k_norm_w;
+    const void* gate = is_q ? J->f->q_gate : J->f->k_gate;
+    if (w) {
+      orc_rmsnorm(tmp, w + (int64_t)h * d, d, J->f->norm_eps, y);
+      memcpy(tmp, y, sizeof(double) * d);
+    }
+    if (gate)
+      for (int e = 0; e < d; ++e) tmp[e] *= orc_sigmoid(load_elem(J->dtype, gate, base + e));
+  }
+  if (p->use_rope) orc_rope(p, J->t[g], tmp, y);
+  else memcpy(y, tmp, sizeof(double) * d);
+}
 
 static void attn_unit(attn_job* J, int32_t b, int32_t h, double* krot, double* vrow,
                       double* qin, double* qrot, double* s, uint8_t* vis) {
@@ -160,17 +205,10 @@ static void attn_unit(attn_job* J, int32_t b, int32_t h, double* krot, double* v
   const double scale = p->softmax_scale > 0 ? p->softmax_scale : 1.0 / sqrt((double)d);
   (void)vrow;
   /* rotated keys of this request and head */
-  for (int64_t j = 0; j < L; ++j) {
-    for (int e = 0; e < d; ++e)
-      qin[e] = load_elem(J->dtype, J->k, ((base + j) * H + h) * (int64_t)d + e);
-    if (p->use_rope) orc_rope(p, J->t[base + j], qin, krot + j * d);
-    else memcpy(krot + j * d, qin, sizeof(double) * d);
-  }
+  for (int64_t j = 0; j < L; ++j) prep_row(J, 0, base + j, h, qin, krot + j * d);
   for (int64_t r = J->row_lo[b]; r < J->row_hi[b]; ++r) {
     const int64_t gi = J->rows[r], i = gi - base;
-    for (int e = 0; e < d; ++e) qin[e] = load_elem(J->dtype, J->q, (gi * H + h) * (int64_t)d + e);
-    if (p->use_rope) orc_rope(p, J->t[gi], qin, qrot);
-    else memcpy(qrot, qin, sizeof(double) * d);
+    prep_row(J, 1, gi, h, qin, qrot);
     /* one row of the mask and of the scores */
     double m = -INFINITY;
     int any = 0;
@@ -198,6 +236,9 @@ static void attn_unit(attn_job* J, int32_t b, int32_t h, double* krot, double* v
       for (int e = 0; e < d; ++e)
         o[e] += w * load_elem(J->dtype, J->v, ((base + j) * H + h) * (int64_t)d + e);
     }
+    if (J->f && J->f->out_gate) /* attention output gate */
+      for (int e = 0; e < d; ++e)
+        o[e] *= orc_sigmoid(load_elem(J->dtype, J->f->out_gate, (gi * H + h) * (int64_t)d + e));
     if (J->lse) J->lse[r * H + h] = m + log(den);
   }
 }
@@ -230,6 +271,16 @@ int orc_attention(const orc_params* p, int32_t B, const int64_t* offsets,
                   const void* q, const void* k, const void* v,
                   int64_t n_rows, const int64_t* rows, double* out, double* lse,
                   int32_t n_threads) {
+  return orc_attention_fused(p, B, offsets, t, ty, dtype, q, k, v, NULL, n_rows, rows, out, lse,
+                             n_threads);
+}
+
+int orc_attention_fused(const orc_params* p, int32_t B, const int64_t* offsets,
+                        const int64_t* t, const int8_t* ty, int32_t dtype,
+                        const void* q, const void* k, const void* v, const orc_fused* f,
+                        int64_t n_rows, const int64_t* rows, double* out, double* lse,
+                        int32_t n_threads) {
+  if (f && !(f->norm_eps >= 0.0)) return -1;
   if (!p || B < 0 || !offsets || p->num_heads <= 0 || p->head_dim <= 0 || (p->head_dim & 1))
     return -1;
   if (dtype != ORC_BF16 && dtype != ORC_FP32) return -1;
@@ -256,7 +307,7 @@ int orc_attention(const orc_params* p, int32_t B, const int64_t* offsets,
     while (r < n_rows && rows[r] < offsets[b + 1]) ++r;
     hi[b] = r;
   }
-  attn_job J = {p, B, offsets, t, ty, dtype, q, k, v, rows, lo, hi, out, lse,
+  attn_job J = {p, B, offsets, t, ty, dtype, q, k, v, rows, lo, hi, out, lse, f,
                 (int64_t)B * p->num_heads, 0};
   if (n_threads < 1) n_threads = 1;
   if (n_threads == 1) {

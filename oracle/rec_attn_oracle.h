@@ -47,6 +47,28 @@ int orc_attention(const orc_params* p, int32_t B, const int64_t* offsets,
                   const void* q, const void* k, const void* v,
                   int64_t n_rows, const int64_t* rows, double* out, double* lse,
                   int32_t n_threads);
+/* Fused inputs: QK-RMSNorm gains (fp64 [H][d], NULL = no norm of that side),
+ * its epsilon, and sigmoid-gate pre-activations in the I/O dtype ([T][H][d],
+ * NULL = no gate) for Q, K and the attention output. */
+typedef struct {
+  const double* q_norm_w;
+  const double* k_norm_w;
+  double norm_eps;
+  const void* q_gate;
+  const void* k_gate;
+  const void* out_gate;
+} orc_fused;
+/* y = x / sqrt(mean(x^2) + eps) * w over one head vector of length d. */
+void orc_rmsnorm(const double* x, const double* w, int d, double eps, double* y);
+/* 1 / (1 + e^-x). */
+double orc_sigmoid(double x);
+/* orc_attention with the fused steps: q and k rows are normalised (if a gain is
+ * given), gated, then rotated; outputs are gated.  f == NULL is orc_attention. */
+int orc_attention_fused(const orc_params* p, int32_t B, const int64_t* offsets,
+                        const int64_t* t, const int8_t* ty, int32_t dtype,
+                        const void* q, const void* k, const void* v, const orc_fused* f,
+                        int64_t n_rows, const int64_t* rows, double* out, double* lse,
+                        int32_t n_threads);
 /* Tile classes (SKIP/PARTIAL/FULL) of every (q-tile, k-tile) pair of every
  * request, request-major then q-tile then k-tile; returns the count written.
  * cls may be NULL to query the count. */
