@@ -250,11 +250,28 @@ def run_ours(args):
     flops = 4.0 * w.head_dim * w.num_heads * pairs
     tokens = w.total_tokens
 
+    fused_dev = {}
+    if args.fused:
+        fi = W.fused_inputs(w)
+        for name in ("q_norm_w", "k_norm_w", "q_gate", "k_gate", "out_gate"):
+            a = getattr(fi, name)
+            fused_dev[name] = (host(a) if a.dtype == np.uint16 else torch.from_numpy(a)).to(dev)
+        fused_eps = fi.norm_eps
+
+    def fwd(p, q_, k_, v_):
+        if args.fused:
+            bd.rec_attn_fwd_fused(p, q_, k_, v_, out, None, stream, q_norm_weight=fused_dev["q_norm_w"],
+                                  k_norm_weight=fused_dev["k_norm_w"], norm_eps=fused_eps,
+                                  q_gate=fused_dev["q_gate"], k_gate=fused_dev["k_gate"],
+                                  out_gate=fused_dev["out_gate"])
+        else:
+            bd.rec_attn_fwd(p, q_, k_, v_, out, None, stream)
+
     def step(timed=False):
         p = bd.rec_attn_plan(params, off_h, off_d, t, ty, stream)
         if timed:
             bd.rec_attn_enable_timing(p)
-        bd.rec_attn_fwd(p, q, k, v, out, None, stream)
+        fwd(p, q, k, v)
         return p
 
     # grow the library's workspace pool to K live plans first, so no timed step
@@ -303,21 +320,25 @@ def run_ours(args):
               for _ in range(args.steps)]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dt, dty, doff = torch.empty_like(t), torch.empty_like(ty), torch.empty_like(off_d)
+    copies = [(dq, hq), (dk, hk), (dv, hv), (dt, ht), (dty, hty), (doff, hoff)]
+    # fused: the per-token gate pre-activations travel with Q/K/V (the gains are weights)
+    copies += [(fused_dev[n], fused_dev[n].cpu().pin_memory()) for n in ("q_gate", "k_gate", "out_gate")
+               if n in fused_dev]
     for i in range(args.steps + 1):
         flush.zero_()
         if i > 0:
             e2e_ev[i - 1][0].record(stream)
-        for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (dt, ht), (dty, hty), (doff, hoff)):
+        for d_, h_ in copies:
             d_.copy_(h_, non_blocking=True)
         p = bd.rec_attn_plan(params, off_h, doff, dt, dty, stream)
-        bd.rec_attn_fwd(p, dq, dk, dv, out, None, stream)
+        fwd(p, dq, dk, dv)
         hout.copy_(out, non_blocking=True)
         if i > 0:
             e2e_ev[i - 1][1].record(stream)
         bd.rec_attn_free(p)
     torch.cuda.synchronize(dev)
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, ht, hty, hoff))
+    h2d = sum(h_.numel() * h_.element_size() for _, h_ in copies)
     d2h = hout.numel() * hout.element_size()
 
     # slowest rank's times, total work of all ranks
@@ -331,11 +352,11 @@ def run_ours(args):
     pk = _peaks()
     ms_step = total_ms / args.steps
     value = all_flops * args.steps / (total_ms * 1e-3) / 1e12
-    bytes_attn = 4.0 * tokens * w.num_heads * w.head_dim * elem + 9.0 * tokens
+    bytes_attn = (5.0 if args.fused else 4.0) * tokens * w.num_heads * w.head_dim * elem + 9.0 * tokens
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
     attn_gbs = bytes_attn / (attn_ms * 1e-3) / 1e9
     # full-size default batch only: the capture was taken on that launch
-    traffic = _traffic(args.workload) if (args.batch is None and world == 1) else None
+    traffic = _traffic(args.workload) if (args.batch is None and world == 1 and not args.fused) else None
     hbm_bound = (flops / bytes_attn) < (pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9))
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -352,7 +373,8 @@ def run_ours(args):
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "fp32",
         "data": "synthetic (seeded generators standing in for the pages' private logs)",
-        "config": _config(w, args.workload, f"dp{world} (requests sharded, no collective)"),
+        "config": dict(_config(w, args.workload, f"dp{world} (requests sharded, no collective)"),
+                       **({"fused": "QK-RMSNorm + Q/K sigmoid gates + output gate"} if args.fused else {})),
         "tokens_per_s": all_tokens * args.steps / (total_ms * 1e-3),
         "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
         "visible_pairs_per_head": pairs,
@@ -389,6 +411,8 @@ def main(argv=None):
                     help="override the workload's number of requests (small profiling cases)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="time rec_attn_fwd_fused with QK-RMSNorm, Q/K gates and the output gate on")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)

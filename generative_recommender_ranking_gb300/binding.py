@@ -43,6 +43,18 @@ class RecAttnParams(ctypes.Structure):
     ]
 
 
+class RecAttnFused(ctypes.Structure):
+    """rec_attn_fused: QK-RMSNorm gains, epsilon and sigmoid-gate pre-activations."""
+    _fields_ = [
+        ("q_norm_weight", ctypes.c_void_p),
+        ("k_norm_weight", ctypes.c_void_p),
+        ("norm_eps", ctypes.c_float),
+        ("q_gate", ctypes.c_void_p),
+        ("k_gate", ctypes.c_void_p),
+        ("out_gate", ctypes.c_void_p),
+    ]
+
+
 class RecAttnError(RuntimeError):
     def __init__(self, fn: str, code: int):
         self.code = code
@@ -70,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.rec_attn_plan.restype = ctypes.c_int
         L.rec_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.rec_attn_fwd.restype = ctypes.c_int
+        L.rec_attn_fwd_fused.argtypes = [vp, vp, vp, vp, ctypes.POINTER(RecAttnFused), vp, vp, vp]
+        L.rec_attn_fwd_fused.restype = ctypes.c_int
         L.rec_attn_free.argtypes = [vp]
         L.rec_attn_free.restype = None
         L.rec_attn_tile_classes.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
@@ -154,6 +168,18 @@ def rec_attn_fwd(plan: Plan, q, k, v, out, lse=None, stream=None) -> None:
     code = lib().rec_attn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                               _stream(stream))
     _check("rec_attn_fwd", code)
+
+
+def rec_attn_fwd_fused(plan: Plan, q, k, v, out, lse=None, stream=None, q_norm_weight=None,
+                       k_norm_weight=None, norm_eps: float = 1e-6, q_gate=None, k_gate=None,
+                       out_gate=None) -> None:
+    """rec_attn_fwd with QK-RMSNorm (float32 [H, d] gains), Q/K sigmoid gates and the
+    attention output gate ([T, H, d] pre-activations in the I/O dtype); None = off."""
+    f = RecAttnFused(_ptr(q_norm_weight), _ptr(k_norm_weight), float(norm_eps), _ptr(q_gate),
+                     _ptr(k_gate), _ptr(out_gate))
+    code = lib().rec_attn_fwd_fused(plan.handle, _ptr(q), _ptr(k), _ptr(v), ctypes.byref(f), _ptr(out),
+                                    _ptr(lse), _stream(stream))
+    _check("rec_attn_fwd_fused", code)
 
 
 def rec_attn_free(plan: Plan) -> None:

@@ -33,6 +33,7 @@ struct rec_attn_plan_s {
   PlanDev pd{};
   void* qrot = nullptr;
   void* krot = nullptr;
+  void* qk_extra = nullptr;  // Q'/K' buffers of a plan without the RoPE, made on the first fused call
   const long long* t = nullptr;
   const int8_t* ty = nullptr;
   MaskP mask{};
@@ -283,8 +284,11 @@ REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_
   return REC_ATTN_OK;
 }
 
-REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
-                                          void* out, float* lse, void* stream) {
+namespace {
+
+// The forward of rec_attn_fwd and rec_attn_fwd_fused (f == nullptr: no fused step).
+rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                         const rec_attn_fused* f, void* out, float* lse, void* stream) {
   if (!plan) return REC_ATTN_ERR_INVALID_ARG;
   const rec_attn_params& p = plan->p;
   const long long T = plan->T;
@@ -300,6 +304,16 @@ REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, 
       return REC_ATTN_ERR_INVALID_ARG;
     if (lse && (overlaps(lse, (size_t)T * p.num_heads * 4, out, bytes)))
       return REC_ATTN_ERR_INVALID_ARG;
+    if (f) {
+      if (!(f->norm_eps >= 0.f) || !std::isfinite(f->norm_eps)) return REC_ATTN_ERR_INVALID_ARG;
+      const void* gates[3] = {f->q_gate, f->k_gate, f->out_gate};
+      for (const void* g : gates)
+        if (reinterpret_cast<uintptr_t>(g) & 15u) return REC_ATTN_ERR_INVALID_ARG;
+      if (overlaps(out, bytes, f->out_gate, f->out_gate ? bytes : 0)) return REC_ATTN_ERR_INVALID_ARG;
+      const float* ws[2] = {f->q_norm_weight, f->k_norm_weight};
+      for (const float* w : ws)
+        if (reinterpret_cast<uintptr_t>(w) & 3u) return REC_ATTN_ERR_INVALID_ARG;
+    }
   }
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -311,7 +325,40 @@ REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, 
 
   const void* qs = q;
   const void* ks = k;
-  if (p.use_rope) {
+  const bool fuse_qk = f && (f->q_norm_weight || f->k_norm_weight || f->q_gate || f->k_gate);
+  if (fuse_qk) {
+    // fused QK-RMSNorm / gates, then the rotation (if the plan has one), into Q'/K'
+    if (!plan->qrot) {
+      if (!plan->qk_extra) {
+        const size_t elem = p.dtype == REC_ATTN_BF16 ? 2 : 4;
+        const size_t qk_bytes = ((size_t)T * p.num_heads * p.head_dim * elem + 255) & ~(size_t)255;
+        cudaMemPool_t pool;
+        e = pool_for(plan->device, &pool);
+        if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&plan->qk_extra, 2 * qk_bytes, pool, st);
+        if (e != cudaSuccess) { plan->qk_extra = nullptr; return from_cuda(e); }
+        plan->krot = static_cast<char*>(plan->qk_extra) + qk_bytes;
+      }
+      plan->qrot = plan->qk_extra;
+    }
+    e = cudaStreamWaitEvent(st, plan->ev_meta, 0);
+    if (e == cudaSuccess && plan->timing) {
+      plan->timed = false;
+      e = cudaEventRecord(plan->ev[0], st);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    RopeArgs ra;
+    ra.meta = plan->pd.meta; ra.batch = plan->batch; ra.t = plan->t;
+    ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
+    ra.heads = p.num_heads; ra.head_dim = p.head_dim;
+    std::memcpy(ra.omega, plan->omega, sizeof ra.omega);  // all zero without the RoPE
+    FusedArgs fa;
+    fa.q_norm_w = f->q_norm_weight; fa.k_norm_w = f->k_norm_weight; fa.eps = f->norm_eps;
+    fa.q_gate = f->q_gate; fa.k_gate = f->k_gate;
+    e = launch_rope_fused(ra, fa, p.dtype, plan->NT, st);
+    if (e == cudaSuccess && plan->timing) e = cudaEventRecord(plan->ev[1], st);
+    if (e != cudaSuccess) return from_cuda(e);
+    qs = plan->qrot; ks = plan->krot;
+  } else if (p.use_rope) {
     e = cudaStreamWaitEvent(st, plan->ev_meta, 0);  // the request table (not the planner)
     if (e == cudaSuccess && plan->timing) {
       plan->timed = false;
@@ -344,6 +391,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, 
   a.items = plan->pd.items; a.t = plan->t; a.ty = plan->ty;
   a.counters = plan->pd.counters; a.krec = plan->pd.krec;
   a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = plan->pd.status;
+  a.out_gate = f ? f->out_gate : nullptr;
   a.n_items = plan->NT * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale; a.mask = plan->mask;
   if (p.dtype == REC_ATTN_FP32) {
     e = launch_attn_simt(a, p.head_dim, st);
@@ -363,12 +411,27 @@ REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, 
   return finish_timing(plan, st, e);
 }
 
+}  // namespace
+
+REC_ATTN_API rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                                          void* out, float* lse, void* stream) {
+  return fwd_impl(plan, q, k, v, nullptr, out, lse, stream);
+}
+
+REC_ATTN_API rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const void* q, const void* k,
+                                                const void* v, const rec_attn_fused* fused, void* out,
+                                                float* lse, void* stream) {
+  if (!fused) return REC_ATTN_ERR_INVALID_ARG;
+  return fwd_impl(plan, q, k, v, fused, out, lse, stream);
+}
+
 REC_ATTN_API void rec_attn_free(rec_attn_plan_t* plan) {
   if (!plan) return;
   if (plan->ws) {
     cudaStreamWaitEvent(plan->stream, plan->ev_plan, 0);  // planning may still run on the side stream
     cudaFreeAsync(plan->ws, plan->stream);
   }
+  if (plan->qk_extra) cudaFreeAsync(plan->qk_extra, plan->stream);
   for (cudaEvent_t ev : plan->ev)
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : {plan->ev_in, plan->ev_meta, plan->ev_plan})

@@ -17,6 +17,7 @@ struct AttnArgs {
   const void* k;     // rotated keys
   const void* v;
   void* out;
+  const void* out_gate;  // optional [T][H][d] in the I/O dtype: O <- O * sigmoid(out_gate)
   float* lse;        // optional [T][H]
   int* status;
   int* counters;     // [1]: dynamic item counter, [2]: exit ticket (both reset at kernel end)
@@ -39,6 +40,18 @@ struct RopeArgs {
   int heads, head_dim;
   float omega[kMaxPairs];  // rad per second, pair i
 };
+
+// Fused steps of the prologue, applied before the rotation: QK-RMSNorm
+// (x / sqrt(mean(x^2) + eps) * w[h]) and then the sigmoid gate x * sigmoid(g).
+struct FusedArgs {
+  const float* q_norm_w;  // [H][d] or null
+  const float* k_norm_w;
+  float eps;
+  const void* q_gate;     // [T][H][d] in the I/O dtype, or null
+  const void* k_gate;
+};
+
+__device__ __forceinline__ float sigmoidf_fast(float x) { return 1.f / (1.f + __expf(-x)); }
 
 // One work item: (query tile, head).
 struct WorkItem {

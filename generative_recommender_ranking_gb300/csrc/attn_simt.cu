@@ -85,8 +85,14 @@ __global__ void __launch_bounds__(kTile) k_attn_simt(AttnArgs a) {
   if (!row_ok) return;
   float* dst = static_cast<float*>(a.out) + (tok * H + it.h) * D;
   const float inv = l > 0.f ? 1.f / l : 0.f;
+  if (a.out_gate) {  // the attention output gate, O * sigmoid(g)
+    const float* g = static_cast<const float*>(a.out_gate) + (tok * H + it.h) * D;
 #pragma unroll
-  for (int e = 0; e < D; ++e) dst[e] = o[e] * inv;
+    for (int e = 0; e < D; ++e) dst[e] = o[e] * inv * sigmoidf_fast(g[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < D; ++e) dst[e] = o[e] * inv;
+  }
   if (a.lse) a.lse[tok * H + it.h] = l > 0.f ? mrun + logf(l) : -INFINITY;
 }
 

@@ -762,13 +762,30 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       uint32_t o[64];
       ptx::tmem_ld64(tm.o + half * 64, o);
       if (row_ok) {
+        // the attention output gate, O * sigmoid(g), when the caller passed one
+        const uint4* grow = a.out_gate ? reinterpret_cast<const uint4*>(
+                                             static_cast<const __nv_bfloat16*>(a.out_gate) + (tok * H + d.h) * D + half * 64)
+                                       : nullptr;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
+          float sc[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sc[e] = inv;
+          if (grow) {
+            const uint4 gv = grow[c];
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+              sc[2 * e] *= sigmoidf_fast(gf.x);
+              sc[2 * e + 1] *= sigmoidf_fast(gf.y);
+            }
+          }
           uint32_t wv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(__uint_as_float(o[c * 8 + 2 * e]) * inv,
-                                                            __uint_as_float(o[c * 8 + 2 * e + 1]) * inv);
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(__uint_as_float(o[c * 8 + 2 * e]) * sc[2 * e],
+                                                            __uint_as_float(o[c * 8 + 2 * e + 1]) * sc[2 * e + 1]);
             wv[e] = *reinterpret_cast<const uint32_t*>(&pb);
           }
           reinterpret_cast<uint4*>(orow + half * 64)[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);

@@ -13,6 +13,8 @@ cudaError_t launch_plan(const MaskP& mp, int heads, const PlanDev& pd, const lon
 cudaError_t launch_count_pairs(const MaskP& mp, const PlanDev& pd, const long long* t,
                                const int8_t* ty, long long n_tiles, cudaStream_t st);
 cudaError_t launch_rope(const RopeArgs& a, int dtype, long long n_tiles, cudaStream_t st);
+cudaError_t launch_rope_fused(const RopeArgs& a, const FusedArgs& f, int dtype, long long n_tiles,
+                              cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs& a, int head_dim, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                            const CUtensorMap& v, int head_dim, int grid, cudaStream_t st);

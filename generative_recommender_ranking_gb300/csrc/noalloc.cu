@@ -206,6 +206,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   a.meta = pd.meta; a.qreq = pd.qreq; a.kcount = pd.kcount; a.klist = pd.klist; a.items = pd.items;
   a.counters = pd.counters; a.krec = pd.krec;
   a.t = t; a.ty = types_dev; a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = pd.status;
+  a.out_gate = nullptr;
   a.n_items = NT * params->num_heads; a.heads = params->num_heads;
   a.scale = params->softmax_scale > 0.f ? params->softmax_scale : 1.f / std::sqrt((float)params->head_dim);
   a.mask = mask;

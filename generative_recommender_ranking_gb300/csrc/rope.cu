@@ -121,7 +121,111 @@ __global__ void __launch_bounds__(256, 4) k_rope(RopeArgs a) {
   }
 }
 
+// Sum of v over the `group` consecutive lanes that hold one head row (group is a
+// power of two dividing 32 and every lane of the warp takes part).
+__device__ __forceinline__ float group_sum(float v, int group) {
+  for (int off = group >> 1; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// x <- x / sqrt(mean over the head row of x^2 + eps) * w, then x <- x * sigmoid(g):
+// the fused QK-RMSNorm and sigmoid gate of one 16-byte chunk of a head row.
+template <typename E>
+__device__ __forceinline__ void norm_gate(float (&x)[8], bool act, const float* w, float eps, const void* gate,
+                                          long long off_bytes, int e0, int chunks, int d) {
+  using C = Chunk<E>;
+  constexpr int kElems = 2 * C::kPairs;
+  if (w) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < kElems; ++e) ss = fmaf(x[e], x[e], ss);
+    ss = group_sum(ss, chunks);
+    const float r = rsqrtf(ss / (float)d + eps);
+    if (act) {
+#pragma unroll
+      for (int e = 0; e < kElems; ++e) x[e] *= r * w[e0 + e];
+    }
+  }
+  if (gate && act) {
+    float g[8];
+    C::load(static_cast<const char*>(gate) + off_bytes, g);
+#pragma unroll
+    for (int e = 0; e < kElems; ++e) x[e] *= sigmoidf_fast(g[e]);
+  }
+}
+
+// The prologue with the fused steps: per (token, head) row, QK-RMSNorm and the
+// sigmoid gate on Q and K, then the rotation (omega all zero: none).  Every lane of
+// a warp runs every iteration (inactive lanes carry zeros), so the row sums can use
+// warp shuffles over the lanes of one row.
+template <typename E>
+__global__ void __launch_bounds__(256, 4) k_rope_fused(RopeArgs a, FusedArgs f) {
+  using C = Chunk<E>;
+  constexpr int kPairs = C::kPairs;
+  const long long g = blockIdx.x;
+  __shared__ int s_req;
+  if (threadIdx.x == 0) {
+    int lo = 0, hi = a.batch;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (a.meta[mid].tile_start <= g) lo = mid;
+      else hi = mid;
+    }
+    s_req = lo;
+  }
+  __syncthreads();
+  const ReqMeta m = a.meta[s_req];
+  const int tl = (int)(g - m.tile_start);
+  const long long t_ref = a.t[m.tok_start];
+  const int chunks = a.head_dim / (2 * kPairs);
+  const int rows = min(kTile, m.len - tl * kTile);
+  const int total = rows * chunks;
+  const int lane = threadIdx.x & 31;
+  const long long head_bytes = (long long)a.head_dim * (long long)sizeof(E);
+  for (int base = threadIdx.x - lane; base < total; base += blockDim.x) {
+    const int idx = base + lane;
+    const bool act = idx < total;
+    const int r = act ? idx / chunks : 0, c = act ? idx - r * chunks : 0;
+    const long long tok = m.tok_start + tl * kTile + r;
+    const float dt = act ? (float)(a.t[tok] - t_ref) : 0.f;
+    float sn[kPairs], cs[kPairs];
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
+    const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
+    for (int h = 0; h < a.heads; ++h) {
+      const long long off = row0 + h * head_bytes;
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (act) {
+        C::load(static_cast<const char*>(a.q) + off, x);
+        C::load(static_cast<const char*>(a.k) + off, y);
+      }
+      const int e0 = h * a.head_dim + c * 2 * kPairs;
+      norm_gate<E>(x, act, f.q_norm_w, f.eps, f.q_gate, off, e0, chunks, a.head_dim);
+      norm_gate<E>(y, act, f.k_norm_w, f.eps, f.k_gate, off, e0, chunks, a.head_dim);
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        const float x0 = x[2 * p], x1 = x[2 * p + 1], y0 = y[2 * p], y1 = y[2 * p + 1];
+        x[2 * p] = x0 * cs[p] - x1 * sn[p];
+        x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
+        y[2 * p] = y0 * cs[p] - y1 * sn[p];
+        y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
+      }
+      if (act) {
+        C::store(static_cast<char*>(a.qr) + off, x);
+        C::store(static_cast<char*>(a.kr) + off, y);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rope_fused(const RopeArgs& a, const FusedArgs& f, int dtype, long long n_tiles, cudaStream_t st) {
+  if (n_tiles <= 0) return cudaSuccess;
+  if (dtype == REC_ATTN_BF16) k_rope_fused<__nv_bfloat16><<<(unsigned)n_tiles, 256, 0, st>>>(a, f);
+  else k_rope_fused<float><<<(unsigned)n_tiles, 256, 0, st>>>(a, f);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope(const RopeArgs& a, int dtype, long long n_tiles, cudaStream_t st) {
   if (n_tiles <= 0) return cudaSuccess;

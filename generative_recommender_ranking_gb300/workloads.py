@@ -236,3 +236,30 @@ def make(name: str, **kw) -> Workload:
 
 
 NAMES = ("tiny_fp32", "cadet", "sort", "mtgr", "tm20k_full", "tm20k_window")
+
+
+@dataclass
+class FusedInputs:
+    """Inputs of the fused steps: QK-RMSNorm gains [H, d] (float32) and sigmoid-gate
+    pre-activations [T, H, d] (bf16 bits or float32, like Q/K/V)."""
+
+    q_norm_w: np.ndarray
+    k_norm_w: np.ndarray
+    q_gate: np.ndarray
+    k_gate: np.ndarray
+    out_gate: np.ndarray
+    norm_eps: float = 1e-6
+
+
+def fused_inputs(w: Workload, seed: int = 2001) -> FusedInputs:
+    """Seeded gains ~ U(0.5, 1.5) and gate pre-activations ~ N(0, 1.5^2) for a workload."""
+    rng = np.random.default_rng(seed)
+    T, H, d = w.total_tokens, w.num_heads, w.head_dim
+    gains = lambda: rng.uniform(0.5, 1.5, size=(H, d)).astype(np.float32)
+    qn, kn = gains(), gains()
+
+    def gate():
+        g = (rng.standard_normal(size=(T, H, d)) * 1.5).astype(np.float32)
+        return round_to_bf16_bits(g) if w.dtype == "bf16" else g
+
+    return FusedInputs(qn, kn, gate(), gate(), gate())

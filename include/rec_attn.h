@@ -145,6 +145,49 @@ rec_attn_status rec_attn_fwd(rec_attn_plan_t* plan, const void* q, const void* k
                              const void* v, void* out, float* lse, void* stream);
 
 /*
+ * Fused prologue / epilogue steps of rec_attn_fwd_fused.  Each pointer may be NULL,
+ * which turns that step off; a struct of NULLs computes what rec_attn_fwd computes.
+ *
+ *   QK-RMSNorm (SORT review page, section 3.3.2 "Attention Gate & QK Norm"; TM20K
+ *   review page, the QK Norm after the query/key projections): every query and key
+ *   head vector x becomes x / sqrt(mean(x^2) + norm_eps) * w[h], w a device
+ *   float[H][d] gain (q_norm_weight, k_norm_weight), 4-byte aligned.
+ *
+ *   Q / K sigmoid gates (CADET review page, section on time encoding and
+ *   self-gating: a per-dimension coefficient in (0, 1) multiplied onto the
+ *   projected Q and K): x <- x * sigmoid(g), g a device [T][H][d] array of gate
+ *   pre-activations in params->dtype (q_gate, k_gate), 16-byte aligned.
+ *
+ *   Order on Q and K: norm, then gate, then the time-RoPE (if params->use_rope).
+ *
+ *   Attention output gate (SORT section 3.3.2): O <- O * sigmoid(g), g = out_gate,
+ *   a device [T][H][d] array in params->dtype, 16-byte aligned, not aliasing out.
+ *
+ * Arithmetic is fp32; Q' and K' are rounded once to params->dtype.
+ */
+typedef struct {
+  const float* q_norm_weight; /* [H][d] or NULL */
+  const float* k_norm_weight; /* [H][d] or NULL */
+  float norm_eps;             /* >= 0 (e.g. 1e-6) */
+  const void* q_gate;         /* [T][H][d] or NULL */
+  const void* k_gate;         /* [T][H][d] or NULL */
+  const void* out_gate;       /* [T][H][d] or NULL */
+} rec_attn_fused;
+
+/*
+ * rec_attn_fwd_fused -- rec_attn_fwd with the fused steps above.  Arguments, layout
+ * and asynchrony as for rec_attn_fwd; `fused` is read on the host during the call.
+ * When a Q/K step is on and the plan was made without the RoPE, the first such call
+ * takes 2 * T * H * d elements of Q'/K' workspace from the library's memory pool on
+ * `stream` (released with the plan).
+ * Errors: INVALID_ARG (those of rec_attn_fwd, NULL fused, negative or non-finite
+ * norm_eps, misaligned weights or gates, out_gate aliasing out), CUDA, OOM.
+ */
+rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const void* q, const void* k,
+                                   const void* v, const rec_attn_fused* fused, void* out,
+                                   float* lse, void* stream);
+
+/*
  * rec_attn_free -- release a plan (NULL-safe).  The workspace returns to the
  * library pool in stream order on the stream of the plan's last use (after the
  * planning work), so work already enqueued there may still run; callers that used

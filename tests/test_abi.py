@@ -91,6 +91,8 @@ def test_host_validation_rejects_bad_arguments(L):
 
 def test_null_plan_calls(L):
     assert L.rec_attn_fwd(None, 1, 1, 1, 1, None, None) == bd.ERR_INVALID_ARG
+    f = bd.RecAttnFused(None, None, 1e-6, None, None, None)
+    assert L.rec_attn_fwd_fused(None, 1, 1, 1, ctypes.byref(f), 1, None, None) == bd.ERR_INVALID_ARG
     n = ctypes.c_size_t()
     assert L.rec_attn_tile_classes(None, None, 0, ctypes.byref(n)) == bd.ERR_INVALID_ARG
     c = ctypes.c_uint64()
