@@ -135,6 +135,10 @@ def lib() -> ctypes.CDLL:
         L.orc_rmsnorm.restype = None
         L.orc_sigmoid.argtypes = [ctypes.c_double]
         L.orc_sigmoid.restype = ctypes.c_double
+        L.orc_query_keep.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+        L.orc_query_keep.restype = ctypes.c_int64
+        L.orc_kept_rows.argtypes = [ctypes.c_int32, vp, vp, ctypes.c_int64, vp]
+        L.orc_kept_rows.restype = ctypes.c_int64
         L.orc_tile_classes.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp]
         L.orc_tile_classes.restype = ctypes.c_int64
         _lib = L
@@ -196,6 +200,22 @@ def rmsnorm(x, w, eps: float) -> np.ndarray:
 
 def sigmoid(x: float) -> float:
     return float(lib().orc_sigmoid(float(x)))
+
+
+def query_keep(hist_len: int, n_min: int, layer: int, n_layers: int) -> int:
+    """LazFormer Eq. 22: history queries kept at layer `layer` (1-based) of `n_layers`."""
+    return int(lib().orc_query_keep(int(hist_len), int(n_min), int(layer), int(n_layers)))
+
+
+def kept_rows(offsets, ty, keep: int) -> np.ndarray:
+    """Sorted global rows a pruned layer computes: all non-user tokens and the last
+    `keep` user tokens of each request (keep < 0: every token)."""
+    offsets, ty = _c64(offsets), _c8(ty)
+    B = len(offsets) - 1
+    n = lib().orc_kept_rows(B, _ptr(offsets), _ptr(ty), int(keep), None)
+    rows = np.zeros(max(n, 1), dtype=np.int64)
+    lib().orc_kept_rows(B, _ptr(offsets), _ptr(ty), int(keep), _ptr(rows))
+    return rows[:n]
 
 
 def tile_classes(p: Params, offsets, t, ty) -> np.ndarray:

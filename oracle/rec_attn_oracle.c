@@ -31,6 +31,13 @@
  *     self-gating: a per-dimension coefficient in (0, 1) multiplied back onto the
  *     vector); and the attention output gate, an elementwise sigmoid gate on the
  *     attention output (SORT section 3.3.2).  Order: norm, then gate, then RoPE.
+ *   - Query pruning (orc_kept_rows, orc_query_keep): only some queries are
+ *     computed; every key stays.  SORT review page, section 3.2.2 (queries are
+ *     pruned on the user side only, history and profile; candidates are never
+ *     dropped); LazFormer review page, Eq. 22 (layer l keeps the most recent N_l
+ *     history tokens and every target, N_l falling linearly from the history length
+ *     to N_min) and the target-attention (TA) variant of the TM20K review page, in
+ *     which only targets query the history (N_l = 0).
  *   - The tile classification (orc_tile_classes) is NOT a definition from the
  *     pages: it is the bounding-box interval rule this project uses to skip fully
  *     masked 128x128 tiles (the pages' "mask preload check" of SORT section 4.1 and
@@ -320,6 +327,52 @@ int orc_attention_fused(const orc_params* p, int32_t B, const int64_t* offsets,
   }
   free(lo); free(hi); free(all_rows);
   return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Query pruning                                                              */
+/* ------------------------------------------------------------------------- */
+
+/* LazFormer Eq. 22: N_l = min(Lh, max(N_min, Round[Lh - (l-1)/(L-1) (Lh - N_min)]))
+ * for layer l of L (1-based); Round is round-half-away-from-zero.  A single layer
+ * keeps the whole history. */
+int64_t orc_query_keep(int64_t hist_len, int64_t n_min, int32_t layer, int32_t n_layers) {
+  if (hist_len < 0 || n_min < 0 || n_layers < 1 || layer < 1 || layer > n_layers) return -1;
+  if (n_layers == 1) return hist_len;
+  const double x = (double)hist_len - (double)(layer - 1) / (double)(n_layers - 1) * (double)(hist_len - n_min);
+  int64_t r = (int64_t)floor(fabs(x) + 0.5);
+  if (x < 0) r = -r;
+  if (r < n_min) r = n_min;
+  if (r > hist_len) r = hist_len;
+  return r;
+}
+
+/* Rows a pruned layer computes, as sorted global token indices: in each request,
+ * every token that is not a user token (real-time events, candidates) and the last
+ * `keep` user tokens (GLOBAL or HIST) by position; keep < 0 keeps every token.
+ * Returns the number of rows (rows may be NULL to count). */
+int64_t orc_kept_rows(int32_t B, const int64_t* offsets, const int8_t* ty, int64_t keep, int64_t* rows) {
+  int64_t n = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t s = offsets[b], e = offsets[b + 1];
+    int64_t seen = 0; /* user tokens at or after the current position */
+    int64_t first_kept = s; /* the first kept user token's global index */
+    if (keep >= 0) {
+      first_kept = e;
+      for (int64_t g = e - 1; g >= s; --g)
+        if (is_user(ty[g])) {
+          if (seen == keep) break;
+          ++seen;
+          first_kept = g;
+        }
+    }
+    for (int64_t g = s; g < e; ++g)
+      if (!is_user(ty[g]) || g >= first_kept) {
+        if (rows) rows[n] = g;
+        ++n;
+      }
+  }
+  return n;
 }
 
 /* ------------------------------------------------------------------------- */

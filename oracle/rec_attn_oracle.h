@@ -69,6 +69,12 @@ int orc_attention_fused(const orc_params* p, int32_t B, const int64_t* offsets,
                         const void* q, const void* k, const void* v, const orc_fused* f,
                         int64_t n_rows, const int64_t* rows, double* out, double* lse,
                         int32_t n_threads);
+/* LazFormer Eq. 22 per-layer query budget N_l (round half away from zero);
+ * -1 on invalid arguments. */
+int64_t orc_query_keep(int64_t hist_len, int64_t n_min, int32_t layer, int32_t n_layers);
+/* Rows of a pruned layer (sorted global indices): every non-user token and the last
+ * `keep` user tokens of each request (keep < 0: all).  Returns the count. */
+int64_t orc_kept_rows(int32_t B, const int64_t* offsets, const int8_t* ty, int64_t keep, int64_t* rows);
 /* Tile classes (SKIP/PARTIAL/FULL) of every (q-tile, k-tile) pair of every
  * request, request-major then q-tile then k-tile; returns the count written.
  * cls may be NULL to query the count. */
