@@ -146,9 +146,10 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def _oracle_sample(w: W.Workload, budget_s: float):
-    """Time the fp64 oracle on the first requests of the workload (all heads)
-    until about `budget_s` seconds of work; returns (seconds, visible pairs, requests)."""
+def _oracle_sample(w: W.Workload, budget_s: float, keep: int = -1):
+    """Time the fp64 oracle on the first requests of the workload (all heads; with
+    query pruning, the computed rows only) until about `budget_s` seconds of work;
+    returns (seconds, visible pairs, requests, threads)."""
     import oracle
     oracle.build()
     p = oracle.Params(w.num_heads, w.head_dim, **w.mask, **w.rope)
@@ -160,10 +161,17 @@ def _oracle_sample(w: W.Workload, budget_s: float):
         s, e = int(w.offsets[done]), int(w.offsets[done + n])
         off = w.offsets[done:done + n + 1] - s
         sl = slice(s, e)
+        rows = None if keep < 0 else oracle.kept_rows(off, w.types[sl], keep)
         t0 = time.perf_counter()
-        oracle.attention(p, off, w.t[sl], w.types[sl], w.q[sl], w.k[sl], w.v[sl], threads=threads)
+        oracle.attention(p, off, w.t[sl], w.types[sl], w.q[sl], w.k[sl], w.v[sl], rows=rows, threads=threads)
         secs += time.perf_counter() - t0
-        pairs += oracle.visible_pairs(p, off, w.t[sl], w.types[sl])
+        if rows is None:
+            pairs += oracle.visible_pairs(p, off, w.t[sl], w.types[sl])
+        else:
+            for b in range(n):
+                bs, be = int(off[b]), int(off[b + 1])
+                r = rows[(rows >= bs) & (rows < be)] - bs
+                pairs += int(oracle.mask(p, w.t[sl][bs:be], w.types[sl][bs:be])[r].sum())
         done += n
         chunk *= 2
     return secs, pairs, done, threads
@@ -178,11 +186,11 @@ def run_reference(args):
     w = _workload(args.workload, 0, args.batch)
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        _oracle_sample(w, per_step / 4)
+        _oracle_sample(w, per_step / 4, args.keep_user_queries)
     tot_s, tot_pairs, reqs = 0.0, 0, []
     threads = 1
     for _ in range(args.steps):
-        s, pairs, n, threads = _oracle_sample(w, per_step)
+        s, pairs, n, threads = _oracle_sample(w, per_step, args.keep_user_queries)
         tot_s += s
         tot_pairs += pairs
         reqs.append(n)
@@ -242,8 +250,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    def mkplan(off_d_, t_, ty_, st=None):
+        if args.keep_user_queries >= 0:
+            return bd.rec_attn_plan_query_pruned(params, args.keep_user_queries, off_h, off_d_, t_, ty_, st)
+        return bd.rec_attn_plan(params, off_h, off_d_, t_, ty_, st)
+
     # exact visible pairs (FLOP accounting) from the library's own counter
-    plan = bd.rec_attn_plan(params, off_h, off_d, t, ty)
+    plan = mkplan(off_d, t, ty)
     pairs = bd.rec_attn_visible_pairs(plan)
     cls = bd.rec_attn_tile_classes(plan)
     bd.rec_attn_free(plan)
@@ -268,7 +281,7 @@ def run_ours(args):
             bd.rec_attn_fwd(p, q_, k_, v_, out, None, stream)
 
     def step(timed=False):
-        p = bd.rec_attn_plan(params, off_h, off_d, t, ty, stream)
+        p = mkplan(off_d, t, ty, stream)
         if timed:
             bd.rec_attn_enable_timing(p)
         fwd(p, q, k, v)
@@ -276,7 +289,7 @@ def run_ours(args):
 
     # grow the library's workspace pool to K live plans first, so no timed step
     # waits on a driver allocation
-    pre = [bd.rec_attn_plan(params, off_h, off_d, t, ty, stream) for _ in range(args.steps)]
+    pre = [mkplan(off_d, t, ty, stream) for _ in range(args.steps)]
     for p_ in pre:
         bd.rec_attn_free(p_)
     for _ in range(max(args.warmup, 3)):
@@ -330,7 +343,7 @@ def run_ours(args):
             e2e_ev[i - 1][0].record(stream)
         for d_, h_ in copies:
             d_.copy_(h_, non_blocking=True)
-        p = bd.rec_attn_plan(params, off_h, doff, dt, dty, stream)
+        p = mkplan(doff, dt, dty, stream)
         fwd(p, dq, dk, dv)
         hout.copy_(out, non_blocking=True)
         if i > 0:
@@ -374,7 +387,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if bf16 else "fp32",
         "data": "synthetic (seeded generators standing in for the pages' private logs)",
         "config": dict(_config(w, args.workload, f"dp{world} (requests sharded, no collective)"),
-                       **({"fused": "QK-RMSNorm + Q/K sigmoid gates + output gate"} if args.fused else {})),
+                       **({"fused": "QK-RMSNorm + Q/K sigmoid gates + output gate"} if args.fused else {}),
+                       **({"keep_user_queries": args.keep_user_queries} if args.keep_user_queries >= 0 else {})),
         "tokens_per_s": all_tokens * args.steps / (total_ms * 1e-3),
         "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
         "visible_pairs_per_head": pairs,
@@ -390,7 +404,7 @@ def run_ours(args):
         "wall_s_timed_region": wall,
     }
     if world == 1 and not args.no_cpu_baseline:
-        secs, cpairs, nreq, threads = _oracle_sample(w, args.cpu_budget)
+        secs, cpairs, nreq, threads = _oracle_sample(w, args.cpu_budget, args.keep_user_queries)
         cval = 4.0 * w.head_dim * w.num_heads * cpairs / secs / 1e12
         line["cpu_baseline"] = {"value": cval, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                 "sample": f"first {nreq} of {w.batch} requests, all heads ({secs:.1f} s)"}
@@ -405,7 +419,10 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="cadet", choices=W.NAMES)
+    ap.add_argument("--workload", default="cadet", choices=W.NAMES + W.EXTRA_NAMES)
+    ap.add_argument("--keep-user-queries", type=int, default=-1,
+                    help="query pruning: compute every non-user query and the last N user queries of "
+                         "each request (-1: all; 0: target attention)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's number of requests (small profiling cases)")

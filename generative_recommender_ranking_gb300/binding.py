@@ -80,6 +80,11 @@ def lib() -> ctypes.CDLL:
         L.rec_attn_plan.argtypes = [ctypes.POINTER(RecAttnParams), i32, vp, vp, vp, vp, vp,
                                     ctypes.POINTER(vp)]
         L.rec_attn_plan.restype = ctypes.c_int
+        L.rec_attn_plan_query_pruned.argtypes = [ctypes.POINTER(RecAttnParams), i32, i32, vp, vp, vp, vp, vp,
+                                                 ctypes.POINTER(vp)]
+        L.rec_attn_plan_query_pruned.restype = ctypes.c_int
+        L.rec_attn_query_keep.argtypes = [i64, i64, i32, i32]
+        L.rec_attn_query_keep.restype = i64
         L.rec_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp]
         L.rec_attn_fwd.restype = ctypes.c_int
         L.rec_attn_fwd_fused.argtypes = [vp, vp, vp, vp, ctypes.POINTER(RecAttnFused), vp, vp, vp]
@@ -162,6 +167,25 @@ def rec_attn_plan(params: RecAttnParams, offsets_host, offsets_dev, timestamps_d
                                _ptr(timestamps_dev), _ptr(types_dev), _stream(stream), ctypes.byref(h))
     _check("rec_attn_plan", code)
     return Plan(h.value, B, int(off_h[-1]) if B > 0 else 0, (offsets_dev, timestamps_dev, types_dev))
+
+
+def rec_attn_plan_query_pruned(params: RecAttnParams, keep_user_queries: int, offsets_host, offsets_dev,
+                               timestamps_dev, types_dev, stream=None) -> Plan:
+    """rec_attn_plan for a layer that computes every non-user query and the last
+    `keep_user_queries` user queries of each request (-1: all)."""
+    off_h = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int64))
+    B = len(off_h) - 1
+    h = ctypes.c_void_p()
+    code = lib().rec_attn_plan_query_pruned(ctypes.byref(params), int(keep_user_queries), B, _ptr(off_h),
+                                            _ptr(offsets_dev), _ptr(timestamps_dev), _ptr(types_dev),
+                                            _stream(stream), ctypes.byref(h))
+    _check("rec_attn_plan_query_pruned", code)
+    return Plan(h.value, B, int(off_h[-1]) if B > 0 else 0, (offsets_dev, timestamps_dev, types_dev))
+
+
+def rec_attn_query_keep(hist_len: int, n_min: int, layer: int, n_layers: int) -> int:
+    """LazFormer Eq. 22 per-layer query budget (host-only)."""
+    return int(lib().rec_attn_query_keep(int(hist_len), int(n_min), int(layer), int(n_layers)))
 
 
 def rec_attn_fwd(plan: Plan, q, k, v, out, lse=None, stream=None) -> None:

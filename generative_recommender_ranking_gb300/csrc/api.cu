@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -182,10 +183,11 @@ REC_ATTN_API const char* rec_attn_status_string(rec_attn_status s) {
   return "unknown status";
 }
 
-REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_t batch,
-                                           const int64_t* offsets_host, const int64_t* offsets_dev,
-                                           const int64_t* timestamps_dev, const int8_t* types_dev, void* stream,
-                                           rec_attn_plan_t** plan_out) {
+namespace {
+
+rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queries, int32_t batch,
+                          const int64_t* offsets_host, const int64_t* offsets_dev, const int64_t* timestamps_dev,
+                          const int8_t* types_dev, void* stream, rec_attn_plan_t** plan_out) {
   if (!plan_out) return REC_ATTN_ERR_INVALID_ARG;
   *plan_out = nullptr;
   rec_attn_status st = check_params(params);
@@ -223,6 +225,7 @@ REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_
   plan->t = reinterpret_cast<const long long*>(timestamps_dev);
   plan->ty = types_dev;
   plan->mask.use_delay = params->use_delay;
+  plan->mask.keep_user = keep_user_queries < 0 ? -1 : keep_user_queries;
   plan->mask.delay = params->use_delay ? params->delay_s : 0;
   plan->mask.window = params->window;
   plan->mask.bidir = params->hist_bidirectional;
@@ -282,6 +285,37 @@ REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_
   }
   *plan_out = plan;
   return REC_ATTN_OK;
+}
+
+}  // namespace
+
+REC_ATTN_API rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_t batch,
+                                           const int64_t* offsets_host, const int64_t* offsets_dev,
+                                           const int64_t* timestamps_dev, const int8_t* types_dev, void* stream,
+                                           rec_attn_plan_t** plan_out) {
+  return plan_impl(params, -1, batch, offsets_host, offsets_dev, timestamps_dev, types_dev, stream, plan_out);
+}
+
+REC_ATTN_API rec_attn_status rec_attn_plan_query_pruned(const rec_attn_params* params, int32_t keep_user_queries,
+                                                        int32_t batch, const int64_t* offsets_host,
+                                                        const int64_t* offsets_dev, const int64_t* timestamps_dev,
+                                                        const int8_t* types_dev, void* stream,
+                                                        rec_attn_plan_t** plan_out) {
+  if (plan_out) *plan_out = nullptr;
+  if (keep_user_queries < -1) return REC_ATTN_ERR_INVALID_ARG;
+  return plan_impl(params, keep_user_queries, batch, offsets_host, offsets_dev, timestamps_dev, types_dev, stream,
+                   plan_out);
+}
+
+REC_ATTN_API int64_t rec_attn_query_keep(int64_t hist_len, int64_t n_min, int32_t layer, int32_t n_layers) {
+  if (hist_len < 0 || n_min < 0 || n_layers < 1 || layer < 1 || layer > n_layers) return -1;
+  if (n_layers == 1) return hist_len;
+  // N_l = min(Lh, max(N_min, Round[Lh - (l - 1) / (L - 1) * (Lh - N_min)])), exact in
+  // integers: Round[x / q] with x = Lh (L-1) - (l-1)(Lh - N_min), q = L - 1, half away from 0
+  const long long q = n_layers - 1;
+  const long long x = hist_len * q - (long long)(layer - 1) * (hist_len - n_min);
+  const long long r = x >= 0 ? (2 * x + q) / (2 * q) : -((-2 * x + q) / (2 * q));
+  return std::min<long long>(hist_len, std::max<long long>(n_min, r));
 }
 
 namespace {
@@ -389,7 +423,7 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
   AttnArgs a;
   a.meta = plan->pd.meta; a.qreq = plan->pd.qreq; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
   a.items = plan->pd.items; a.t = plan->t; a.ty = plan->ty;
-  a.counters = plan->pd.counters; a.krec = plan->pd.krec;
+  a.counters = plan->pd.counters; a.krec = plan->pd.krec; a.qkeep = plan->pd.qkeep;
   a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = plan->pd.status;
   a.out_gate = f ? f->out_gate : nullptr;
   a.n_items = plan->NT * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale; a.mask = plan->mask;

@@ -22,6 +22,7 @@ struct AttnArgs {
   int* status;
   int* counters;     // [1]: dynamic item counter, [2]: exit ticket (both reset at kernel end)
   const KeyTileRec* krec;
+  const int* qkeep;  // [B] first kept user position of each request (query pruning)
   long long n_items; // query tiles x heads
   int heads;
   float scale;       // softmax scale (natural-log domain)
@@ -58,7 +59,8 @@ struct WorkItem {
   ReqMeta m;
   int qt;            // query tile index inside the request
   int h;
-  int n;             // non-SKIP key tiles
+  int n;             // non-SKIP key tiles; -1: every row of the tile is pruned
+  int keep;          // first kept user position of the request (query pruning)
   const uint32_t* list;
 };
 
@@ -67,9 +69,11 @@ __device__ __forceinline__ WorkItem decode_item(const AttnArgs& a, long long w, 
   const long long e = ordered ? (long long)a.items[w] : w;
   const long long qg = e / a.heads;
   it.h = (int)(e % a.heads);
-  it.m = a.meta[a.qreq[qg]];
+  const int b = a.qreq[qg];
+  it.m = a.meta[b];
   it.qt = (int)(qg - it.m.tile_start);
   it.n = a.kcount[qg];
+  it.keep = a.qkeep[b];
   it.list = a.klist + it.m.cls_start + (long long)it.qt * it.m.ntiles;
   return it;
 }

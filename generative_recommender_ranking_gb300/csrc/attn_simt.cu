@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(kTile) k_attn_simt(AttnArgs a) {
   float (*s_k)[D + 1] = reinterpret_cast<float (*)[D + 1]>(s_ty + kTile);
   float (*s_v)[D] = reinterpret_cast<float (*)[D]>(&s_k[kTile][0]);
   const WorkItem it = decode_item(a, blockIdx.x, false);
+  if (it.n < 0) return;  // every query of the tile is pruned
   const int r = threadIdx.x, pi = it.qt * kTile + r;
   const bool row_ok = pi < it.m.len;
   const long long tok = it.m.tok_start + pi;
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kTile) k_attn_simt(AttnArgs a) {
       for (int e = 0; e < D; ++e) o[e] = fmaf(p, s_v[c][e], o[e]);
     }
   }
-  if (!row_ok) return;
+  if (!row_ok || !query_kept(tyi, pi, it.keep)) return;
   float* dst = static_cast<float*>(a.out) + (tok * H + it.h) * D;
   const float inv = l > 0.f ? 1.f / l : 0.f;
   if (a.out_gate) {  // the attention output gate, O * sigmoid(g)

@@ -93,9 +93,9 @@ struct ItemDesc {
   int pos0;        // request-local position of the tile's first row
   int rows;        // valid rows in the tile
   int h;
-  int n;           // non-SKIP key tiles
+  int n;           // non-SKIP key tiles; -1: every query of the tile is pruned
   int end;         // 1: the stream is done
-  int pad;
+  int keep;        // first kept user position of the request (query pruning)
 };
 static_assert(sizeof(ItemDesc) == 32, "");
 
@@ -351,9 +351,10 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
     d->rows = min(kTile, it.m.len - it.qt * kTile);
     d->h = it.h;
     d->n = it.n;
+    d->keep = it.keep;
     d->end = 0;
     ptx::mbar_arrive(B.item_full + slot);
-    if (it.n == 0) continue;
+    if (it.n <= 0) continue;
     const int qb = (int)(q_it % QB);
     if (!wait_bar(B.q_empty + qb, ((q_it / QB) & 1) ^ 1, abort_flag, a.status)) break;
     ptx::mbar_arrive_expect_tx(B.q_full + qb, L::kQBytes + kRecBytes);
@@ -434,7 +435,7 @@ __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, u
     const int end = items[slot].end, n = items[slot].n;
     ptx::mbar_arrive(B.item_empty + slot);
     if (end) break;
-    if (n == 0) continue;
+    if (n <= 0) continue;
     const int qb = (int)(q_it % QB);
     if (!wait_bar(B.q_full + qb, (q_it / QB) & 1, abort_flag, a.status)) break;
     ++q_it;
@@ -638,8 +639,8 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
     const int pi = d.pos0 + row;
     const long long tok = d.tok0 + row;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (tok * H + d.h) * D;
-    if (d.n == 0) {
-      if (row_ok) {
+    if (d.n <= 0) {  // no visible key tile: zero rows; -1: a tile of pruned queries
+      if (d.n == 0 && row_ok && query_kept(a.ty[tok], pi, d.keep)) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
@@ -658,6 +659,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
     for (int c = 0; c < kTypes; ++c)
       if ((qr->typebits[c][row >> 5] >> (row & 31)) & 1u) tyi = c;
     ptx::mbar_arrive(B.q_empty + qb);  // the Q buffer and its record may be refilled
+    const bool out_ok = row_ok && query_kept(tyi, pi, d.keep);  // pruned rows are computed, not written
     RowMask rm;
     row_mask_setup(a.mask, row_ok, pi, ti, tyi, rm);
     float m_ref = -INFINITY, l = 0.f;
@@ -761,7 +763,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
     for (int half = 0; half < D / 64; ++half) {
       uint32_t o[64];
       ptx::tmem_ld64(tm.o + half * 64, o);
-      if (row_ok) {
+      if (out_ok) {
         // the attention output gate, O * sigmoid(g), when the caller passed one
         const uint4* grow = a.out_gate ? reinterpret_cast<const uint4*>(
                                              static_cast<const __nv_bfloat16*>(a.out_gate) + (tok * H + d.h) * D + half * 64)
@@ -792,7 +794,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
         }
       }
     }
-    if (row_ok && a.lse) {
+    if (out_ok && a.lse) {
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       a.lse[tok * H + d.h] = l > 0.f ? (m_use + __log2f(l)) * 0.6931471805599453f : -INFINITY;
     }

@@ -180,6 +180,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   mask.delay = params->use_delay ? params->delay_s : 0;
   mask.window = params->window;
   mask.bidir = params->hist_bidirectional;
+  mask.keep_user = -1;  // every query
   const long long* t = reinterpret_cast<const long long*>(timestamps_dev);
   if (e == cudaSuccess)
     e = launch_plan(mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), t, types_dev, batch, NT, s);
@@ -204,7 +205,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   }
   AttnArgs a;
   a.meta = pd.meta; a.qreq = pd.qreq; a.kcount = pd.kcount; a.klist = pd.klist; a.items = pd.items;
-  a.counters = pd.counters; a.krec = pd.krec;
+  a.counters = pd.counters; a.krec = pd.krec; a.qkeep = pd.qkeep;
   a.t = t; a.ty = types_dev; a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = pd.status;
   a.out_gate = nullptr;
   a.n_items = NT * params->num_heads; a.heads = params->num_heads;

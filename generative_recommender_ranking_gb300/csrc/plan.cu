@@ -190,6 +190,36 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   }
   __syncthreads();
 
+  // Query pruning: the position of the first kept user token, i.e. the keep_user-th
+  // user token (GLOBAL or HIST) counted from the end of the request (0: every query).
+  __shared__ int s_keep;
+  if (threadIdx.x == 0) {
+    int pos = 0;
+    if (mp.keep_user >= 0) {
+      pos = m.len;  // no user token kept unless found below
+      int need = mp.keep_user;
+      for (int tl = m.ntiles - 1; tl >= 0 && need > 0; --tl) {
+        const TileBox* bx = pd.boxes + (m.tile_start + tl) * kTypes;
+        const int nu = bx[REC_ATTN_GLOBAL].cnt + bx[REC_ATTN_HIST].cnt;
+        if (nu < need) {
+          need -= nu;
+          if (nu > 0) pos = tl * kTile;  // every user token of the tile is kept
+          continue;
+        }
+        // the need-th user token from the tile's end
+        const KeyTileRec* rec = pd.krec + (m.tile_start + tl);
+        for (int c = kTile - 1; c >= 0; --c) {
+          const int w = c >> 5, bit = c & 31;
+          const bool u = ((rec->typebits[REC_ATTN_GLOBAL][w] | rec->typebits[REC_ATTN_HIST][w]) >> bit) & 1u;
+          if (u && --need == 0) { pos = tl * kTile + c; break; }
+        }
+        need = 0;
+      }
+    }
+    s_keep = pos;
+    pd.qkeep[b] = pos;
+  }
+
   // Phase 2: class of every (query tile, key tile) pair of the request.
   const long long npairs = (long long)m.ntiles * m.ntiles;
   for (long long idx = threadIdx.x; idx < npairs; idx += blockDim.x) {
@@ -221,6 +251,20 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   if (threadIdx.x == 0) s_rcost = 0;
   __syncthreads();
   for (int qt = warp; qt < m.ntiles; qt += nwarps) {
+    // a query tile whose every token is a user token before the first kept one
+    // computes nothing: no key list, no cost, the kernels skip it
+    const TileBox* qbx = pd.boxes + (m.tile_start + qt) * kTypes;
+    const bool pruned = min(m.len, (qt + 1) * kTile) <= s_keep && qbx[REC_ATTN_RT].cnt == 0 &&
+                        qbx[REC_ATTN_CAND].cnt == 0;
+    if (pruned) {
+      if (lane == 0) {
+        const long long g = m.tile_start + qt;
+        pd.kcount[g] = -1;
+        pd.qcost[g] = 0;
+        pd.qreq[g] = b;
+      }
+      continue;
+    }
     const uint8_t* row = pd.cls + m.cls_start + (long long)qt * m.ntiles;
     uint32_t* out = pd.klist + m.cls_start + (long long)qt * m.ntiles;
     int n = 0, nfull = 0;
@@ -366,10 +410,10 @@ __global__ void __launch_bounds__(kTile) k_count_pairs(MaskP mp, PlanDev pd, con
   __shared__ unsigned long long s_sum;
   if (r == 0) s_sum = 0;
   __syncthreads();
-  const bool row_ok = pi < m.len;
   long long ti = 0;
   int tyi = -1;
-  if (row_ok) { ti = t[m.tok_start + pi]; tyi = ty[m.tok_start + pi]; }
+  if (pi < m.len) { ti = t[m.tok_start + pi]; tyi = ty[m.tok_start + pi]; }
+  const bool row_ok = pi < m.len && query_kept(tyi, pi, pd.qkeep[b]);
   bool thr_ok; long long thr;
   delay_bound(ti, mp.delay, thr_ok, thr);
   unsigned long long cnt = 0;

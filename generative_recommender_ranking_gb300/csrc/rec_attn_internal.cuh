@@ -47,7 +47,7 @@ struct MaskP {
   int use_delay;
   int window;
   int bidir;
-  int pad;
+  int keep_user;  // query pruning: user queries kept per request, counted from the end; < 0: all
   long long delay;
 };
 
@@ -65,6 +65,7 @@ struct PlanDev {
   int* rcost;           // [B]: scheduling cost of each request
   int* rorder;          // [B]: requests, most expensive first
   int* roff;            // [B+1]: first item of each request in `items` (in rorder order)
+  int* qkeep;           // [B]: query pruning: user tokens before this position compute nothing
   int* counters;        // [8]: plan ticket, attention item counter, attention exit ticket
   int* status;          // [1]: first device error (rec_attn_status)
   unsigned long long* pairs;  // [1]: visible-pair counter
@@ -74,6 +75,12 @@ struct PlanDev {
 __device__ __forceinline__ void set_status(int* st, int code) { atomicCAS(st, 0, code); }
 
 __device__ __forceinline__ bool is_user(int ty) { return ty == REC_ATTN_GLOBAL || ty == REC_ATTN_HIST; }
+
+// Whether a query row is computed under query pruning: every non-user token, and the
+// user tokens at or after the request's first kept user position.
+__device__ __forceinline__ bool query_kept(int ty, int pos, int keep_pos) {
+  return !is_user(ty) || pos >= keep_pos;
+}
 
 // vis(i, j) for two tokens of one request.  `thr_ok`/`thr` encode the exact delay
 // bound of the query (t_i - delta): thr_ok is false when t_i - delta lies below the

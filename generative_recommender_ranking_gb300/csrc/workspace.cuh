@@ -9,7 +9,7 @@
 namespace recattn {
 
 struct WsLayout {
-  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, it, rc, ro, rf, rq, rk, total;
+  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, it, rc, ro, rf, qk, rq, rk, total;
 };
 
 inline size_t ws_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -31,6 +31,7 @@ inline WsLayout ws_layout(long long batch, long long NT, long long NC, long long
   L.rc = off; off = ws_up(off + 4 * (size_t)batch);
   L.ro = off; off = ws_up(off + 4 * (size_t)batch);
   L.rf = off; off = ws_up(off + 4 * ((size_t)batch + 1));
+  L.qk = off; off = ws_up(off + 4 * (size_t)batch);
   L.rq = off; off = ws_up(off + rot_bytes);
   L.rk = off; off = ws_up(off + rot_bytes);
   L.total = off;
@@ -54,6 +55,7 @@ inline PlanDev ws_bind(char* w, const WsLayout& L) {
   pd.rcost = reinterpret_cast<int*>(w + L.rc);
   pd.rorder = reinterpret_cast<int*>(w + L.ro);
   pd.roff = reinterpret_cast<int*>(w + L.rf);
+  pd.qkeep = reinterpret_cast<int*>(w + L.qk);
   return pd;
 }
 

@@ -218,8 +218,30 @@ def tm20k(variant="full", batch=16, n_hist=20000, n_global=64, window=512, seed=
                     dict(_ROPE))
 
 
+def cadet_serving(batch=16, n_hist=4096, n_cand=500, seed=1006, heads=4, head_dim=64):
+    """CADET serving: one user history of n_hist events (gaps log-normal, median 3 h,
+    clipped to [1 s, 28 d], span <= 1 year) with n_cand candidates appended, stamped
+    at request time.  History causal + delta_delay = 3600 s, candidates see the
+    history and themselves only.  Q/K/V ~ N(0,1)/sqrt(d), bf16."""
+    rng = np.random.default_rng(seed)
+    H, d = heads, head_dim
+    ts, tys = [], []
+    for _ in range(batch):
+        t0 = _epoch(rng)
+        g = _lognormal_gaps(rng, n_hist + 1, 10800.0, 2.5, YEAR, clip=(1.0, 28 * DAY))
+        c = t0 + np.round(np.cumsum(g)).astype(np.int64)
+        ts.append(np.concatenate([c[:n_hist], np.full(n_cand, c[n_hist], dtype=np.int64)]))
+        tys.append(np.array([HIST] * n_hist + [CAND] * n_cand, dtype=np.int8))
+    t, ty = np.concatenate(ts), np.concatenate(tys)
+    q, k, v = _qkv(rng, len(t), H, d, "bf16", scale=1.0 / np.sqrt(d))
+    return Workload("cadet_serving", H, d, "bf16", _pack([n_hist + n_cand] * batch), t, ty, q, k, v,
+                    dict(use_delay=True, delay_s=3600, window=0, hist_bidirectional=False),
+                    dict(_ROPE))
+
+
 def make(name: str, **kw) -> Workload:
-    """Workload by name: tiny_fp32, cadet, sort, mtgr, tm20k_full, tm20k_window."""
+    """Workload by name: tiny_fp32, cadet, sort, mtgr, tm20k_full, tm20k_window,
+    cadet_serving."""
     if name == "tiny_fp32":
         return tiny_fp32(**kw)
     if name == "cadet":
@@ -232,10 +254,14 @@ def make(name: str, **kw) -> Workload:
         return tm20k("full", **kw)
     if name == "tm20k_window":
         return tm20k("window", **kw)
+    if name == "cadet_serving":
+        return cadet_serving(**kw)
     raise KeyError(name)
 
 
 NAMES = ("tiny_fp32", "cadet", "sort", "mtgr", "tm20k_full", "tm20k_window")
+# serving-side workloads (query pruning / target attention), outside the five configs
+EXTRA_NAMES = ("cadet_serving",)
 
 
 @dataclass

@@ -128,6 +128,43 @@ rec_attn_status rec_attn_plan(const rec_attn_params* params, int32_t batch,
                               void* stream, rec_attn_plan_t** plan_out);
 
 /*
+ * rec_attn_plan_query_pruned -- rec_attn_plan for a layer that computes only some
+ * queries (query pruning); every token stays a key.
+ *
+ *   keep_user_queries  -1: every query (same as rec_attn_plan).  N >= 0: in each
+ *             request the computed queries are every token that is not a user token
+ *             (REC_ATTN_RT, REC_ATTN_CAND) and the last N user tokens (REC_ATTN_GLOBAL,
+ *             REC_ATTN_HIST) by position.  SORT review page, section 3.2.2 (Query
+ *             Pruning cuts the user side, history and profile, layer by layer and never
+ *             drops a candidate); LazFormer review page, Eq. 22 (the next layer keeps the
+ *             most recent N_l history tokens and every target; rec_attn_query_keep gives
+ *             N_l); N = 0 is target attention (only targets query the history, TM20K
+ *             review page) and the candidate-only pass of M-FALCON serving.
+ *
+ * rec_attn_fwd on such a plan writes out (and lse) only at the computed rows; the rows
+ * of pruned queries are left as they were.  Query tiles with no computed row are not
+ * scheduled.  rec_attn_visible_pairs counts the pairs of computed rows only.  Tile
+ * classes are those of the full mask.  Other arguments, errors and ownership as for
+ * rec_attn_plan; INVALID_ARG also for keep_user_queries < -1.
+ */
+rec_attn_status rec_attn_plan_query_pruned(const rec_attn_params* params, int32_t keep_user_queries,
+                                           int32_t batch, const int64_t* offsets_host,
+                                           const int64_t* offsets_dev, const int64_t* timestamps_dev,
+                                           const int8_t* types_dev, void* stream,
+                                           rec_attn_plan_t** plan_out);
+
+/*
+ * rec_attn_query_keep -- LazFormer Eq. 22: user queries kept at layer `layer`
+ * (1-based) of an `n_layers`-layer stack, N_l = min(hist_len, max(n_min,
+ * Round[hist_len - (layer - 1) / (n_layers - 1) * (hist_len - n_min)])), Round to the
+ * nearest integer with halves away from zero (computed exactly in integers).  One
+ * layer keeps hist_len.  Host-only, no CUDA call.  Returns -1 for negative lengths,
+ * n_layers < 1 or layer outside 1..n_layers.  (The page's defaults: 1152 compressed
+ * history tokens, n_min = 128.)
+ */
+int64_t rec_attn_query_keep(int64_t hist_len, int64_t n_min, int32_t layer, int32_t n_layers);
+
+/*
  * rec_attn_fwd -- attention forward for a planned batch.
  *
  *   q, k, v   device [T][H][d] row-major, contiguous, in params->dtype (bf16 bit
