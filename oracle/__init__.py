@@ -135,6 +135,9 @@ def lib() -> ctypes.CDLL:
         L.orc_rmsnorm.restype = None
         L.orc_sigmoid.argtypes = [ctypes.c_double]
         L.orc_sigmoid.restype = ctypes.c_double
+        L.orc_attention_bwd.argtypes = [P, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp,
+                                        vp, vp, vp, ctypes.c_int32]
+        L.orc_attention_bwd.restype = ctypes.c_int
         L.orc_query_keep.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
         L.orc_query_keep.restype = ctypes.c_int64
         L.orc_kept_rows.argtypes = [ctypes.c_int32, vp, vp, ctypes.c_int64, vp]
@@ -283,3 +286,27 @@ def attention(p: Params, offsets, t, ty, q, k, v, rows=None, threads: int | None
         raise ValueError(f"orc_attention rejected its arguments (rc={rc})")
     out, lse = out[:n_rows], lse[:n_rows]
     return (out, lse) if with_lse else out
+
+
+def attention_bwd(p: Params, offsets, t, ty, q, k, v, dout, threads: int | None = None):
+    """fp64 gradients (dq, dk, dv), each [T, H, d], of attention() for the upstream
+    gradient dout; q, k, v, dout are float32 or uint16 bf16 bits (one dtype)."""
+    offsets, t, ty = _c64(offsets), _c64(t), _c8(ty)
+    q, k, v, dout = (np.ascontiguousarray(a) for a in (q, k, v, dout))
+    if q.dtype == np.uint16:
+        dtype = 0
+    elif q.dtype == np.float32:
+        dtype = 1
+    else:
+        raise TypeError("q/k/v/dout must be float32 or uint16 (bf16 bits)")
+    assert k.dtype == q.dtype and v.dtype == q.dtype and dout.dtype == q.dtype
+    assert int(offsets[0]) == 0
+    shape = q.shape
+    dq, dk, dv = (np.zeros(shape, dtype=np.float64) for _ in range(3))
+    cp = p.c()
+    rc = lib().orc_attention_bwd(ctypes.byref(cp), len(offsets) - 1, _ptr(offsets), _ptr(t), _ptr(ty), dtype,
+                                 _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 int(threads or os.cpu_count() or 1))
+    if rc != 0:
+        raise ValueError(f"orc_attention_bwd rejected its arguments (rc={rc})")
+    return dq, dk, dv

@@ -31,6 +31,12 @@
  *     self-gating: a per-dimension coefficient in (0, 1) multiplied back onto the
  *     vector); and the attention output gate, an elementwise sigmoid gate on the
  *     attention output (SORT section 3.3.2).  Order: norm, then gate, then RoPE.
+ *   - Backward pass (orc_attention_bwd): the gradients of the attention above
+ *     with respect to Q, K and V, written out by the chain rule on the materialised
+ *     probabilities (dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dO * O)),
+ *     dQ~ = scale dS K~, dK~ = scale dS^T Q~, then the inverse rotation).  The pages
+ *     train these models (TM20K section 2.1, LazFormer's FlexAttention training)
+ *     but print no backward formula; this is the derivative of the definition.
  *   - Query pruning (orc_kept_rows, orc_query_keep): only some queries are
  *     computed; every key stays.  SORT review page, section 3.2.2 (queries are
  *     pruned on the user side only, history and profile; candidates are never
@@ -326,6 +332,149 @@ int orc_attention_fused(const orc_params* p, int32_t B, const int64_t* offsets,
     free(th);
   }
   free(lo); free(hi); free(all_rows);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Backward pass                                                              */
+/* ------------------------------------------------------------------------- */
+
+/* y = R(t)^T x: the inverse of orc_rope (rotation by the negative angle). */
+static void rope_inverse(const orc_params* p, int64_t t, const double* x, double* y) {
+  const int d = p->head_dim;
+  for (int i = 0; i < d / 2; ++i) {
+    double omega = p->phi_min / p->dt_max_s * pow(p->rope_base, 2.0 * i / d);
+    double a = (double)t * omega;
+    double c = cos(a), s = sin(a);
+    y[2 * i] = x[2 * i] * c + x[2 * i + 1] * s;
+    y[2 * i + 1] = -x[2 * i] * s + x[2 * i + 1] * c;
+  }
+}
+
+typedef struct {
+  const orc_params* p;
+  int32_t B;
+  const int64_t *offsets, *t;
+  const int8_t* ty;
+  int dtype;
+  const void *q, *k, *v, *dout;
+  double *dq, *dk, *dv; /* [T][H][d] */
+  int64_t n_units, next_unit;
+} bwd_job;
+
+static void bwd_unit(bwd_job* J, int32_t b, int32_t h) {
+  const orc_params* p = J->p;
+  const int H = p->num_heads, d = p->head_dim;
+  const int64_t base = J->offsets[b], L = J->offsets[b + 1] - base;
+  if (L <= 0) return;
+  const double scale = p->softmax_scale > 0 ? p->softmax_scale : 1.0 / sqrt((double)d);
+  double* qr = (double*)malloc(sizeof(double) * (size_t)L * d);  /* rotated queries */
+  double* kr = (double*)malloc(sizeof(double) * (size_t)L * d);  /* rotated keys */
+  double* vv = (double*)malloc(sizeof(double) * (size_t)L * d);
+  double* go = (double*)malloc(sizeof(double) * (size_t)L * d);  /* dO */
+  double* P = (double*)calloc((size_t)L * L, sizeof(double));    /* probabilities, 0 where masked */
+  double* gq = (double*)calloc((size_t)L * d, sizeof(double));   /* dQ~ */
+  double* gk = (double*)calloc((size_t)L * d, sizeof(double));   /* dK~ */
+  double* tmp = (double*)malloc(sizeof(double) * d);
+  for (int64_t i = 0; i < L; ++i) {
+    const int64_t off = ((base + i) * H + h) * (int64_t)d;
+    for (int e = 0; e < d; ++e) {
+      tmp[e] = load_elem(J->dtype, J->q, off + e);
+      vv[i * d + e] = load_elem(J->dtype, J->v, off + e);
+      go[i * d + e] = load_elem(J->dtype, J->dout, off + e);
+    }
+    if (p->use_rope) orc_rope(p, J->t[base + i], tmp, qr + i * d);
+    else memcpy(qr + i * d, tmp, sizeof(double) * d);
+    for (int e = 0; e < d; ++e) tmp[e] = load_elem(J->dtype, J->k, off + e);
+    if (p->use_rope) orc_rope(p, J->t[base + i], tmp, kr + i * d);
+    else memcpy(kr + i * d, tmp, sizeof(double) * d);
+  }
+  /* forward probabilities row by row */
+  for (int64_t i = 0; i < L; ++i) {
+    double m = -INFINITY;
+    double* Pi = P + i * L;
+    for (int64_t j = 0; j < L; ++j) {
+      if (!orc_visible(p, i, J->t[base + i], J->ty[base + i], j, J->t[base + j], J->ty[base + j])) {
+        Pi[j] = -INFINITY;
+        continue;
+      }
+      double acc = 0.0;
+      for (int e = 0; e < d; ++e) acc += qr[i * d + e] * kr[j * d + e];
+      Pi[j] = scale * acc;
+      if (Pi[j] > m) m = Pi[j];
+    }
+    if (m == -INFINITY) { /* no visible key: O = 0, no gradient flows */
+      for (int64_t j = 0; j < L; ++j) Pi[j] = 0.0;
+      continue;
+    }
+    double den = 0.0;
+    for (int64_t j = 0; j < L; ++j) den += (Pi[j] == -INFINITY) ? 0.0 : exp(Pi[j] - m);
+    for (int64_t j = 0; j < L; ++j) Pi[j] = (Pi[j] == -INFINITY) ? 0.0 : exp(Pi[j] - m) / den;
+  }
+  /* dV = P^T dO; D_i = sum_j P_ij dP_ij; dS = P (dP - D); dQ~ = scale dS K~; dK~ = scale dS^T Q~ */
+  for (int64_t i = 0; i < L; ++i) {
+    const double* Pi = P + i * L;
+    double Di = 0.0;
+    for (int64_t j = 0; j < L; ++j) {
+      if (Pi[j] == 0.0) continue;
+      double dp = 0.0;
+      for (int e = 0; e < d; ++e) dp += go[i * d + e] * vv[j * d + e];
+      Di += Pi[j] * dp;
+    }
+    for (int64_t j = 0; j < L; ++j) {
+      if (Pi[j] == 0.0) continue;
+      double dp = 0.0;
+      for (int e = 0; e < d; ++e) dp += go[i * d + e] * vv[j * d + e];
+      const double ds = Pi[j] * (dp - Di);
+      for (int e = 0; e < d; ++e) {
+        J->dv[((base + j) * H + h) * (int64_t)d + e] += Pi[j] * go[i * d + e];
+        gq[i * d + e] += scale * ds * kr[j * d + e];
+        gk[j * d + e] += scale * ds * qr[i * d + e];
+      }
+    }
+  }
+  /* back through the rotation */
+  for (int64_t i = 0; i < L; ++i) {
+    double* dqo = J->dq + ((base + i) * H + h) * (int64_t)d;
+    double* dko = J->dk + ((base + i) * H + h) * (int64_t)d;
+    if (p->use_rope) {
+      rope_inverse(p, J->t[base + i], gq + i * d, dqo);
+      rope_inverse(p, J->t[base + i], gk + i * d, dko);
+    } else {
+      memcpy(dqo, gq + i * d, sizeof(double) * d);
+      memcpy(dko, gk + i * d, sizeof(double) * d);
+    }
+  }
+  free(qr); free(kr); free(vv); free(go); free(P); free(gq); free(gk); free(tmp);
+}
+
+static void* bwd_worker(void* arg) {
+  bwd_job* J = (bwd_job*)arg;
+  for (;;) {
+    int64_t u = __atomic_fetch_add(&J->next_unit, 1, __ATOMIC_RELAXED);
+    if (u >= J->n_units) break;
+    bwd_unit(J, (int32_t)(u / J->p->num_heads), (int32_t)(u % J->p->num_heads));
+  }
+  return NULL;
+}
+
+int orc_attention_bwd(const orc_params* p, int32_t B, const int64_t* offsets, const int64_t* t,
+                      const int8_t* ty, int32_t dtype, const void* q, const void* k, const void* v,
+                      const void* dout, double* dq, double* dk, double* dv, int32_t n_threads) {
+  if (!p || B < 0 || !offsets || p->num_heads <= 0 || p->head_dim <= 0 || (p->head_dim & 1)) return -1;
+  if (dtype != ORC_BF16 && dtype != ORC_FP32) return -1;
+  for (int32_t b = 0; b < B; ++b)
+    if (offsets[b + 1] < offsets[b]) return -1;
+  const int64_t n = (offsets[B] - offsets[0]) * p->num_heads * (int64_t)p->head_dim;
+  memset(dq, 0, sizeof(double) * (size_t)n);
+  memset(dk, 0, sizeof(double) * (size_t)n);
+  memset(dv, 0, sizeof(double) * (size_t)n);
+  bwd_job J = {p, B, offsets, t, ty, dtype, q, k, v, dout, dq, dk, dv, (int64_t)B * p->num_heads, 0};
+  if (n_threads < 1) n_threads = 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)n_threads);
+  for (int i = 0; i < n_threads; ++i) pthread_create(&th[i], NULL, bwd_worker, &J);
+  for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+  free(th);
   return 0;
 }
 

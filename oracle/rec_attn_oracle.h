@@ -69,6 +69,12 @@ int orc_attention_fused(const orc_params* p, int32_t B, const int64_t* offsets,
                         const void* q, const void* k, const void* v, const orc_fused* f,
                         int64_t n_rows, const int64_t* rows, double* out, double* lse,
                         int32_t n_threads);
+/* Gradients of orc_attention (no fused steps) for the upstream gradient dout
+ * ([T][H][d] in dtype): dq, dk, dv [T][H][d] fp64 (arrays must be offsets[0]-based
+ * at 0).  Each (request, head) materialises its L x L probabilities.  Returns 0 or -1. */
+int orc_attention_bwd(const orc_params* p, int32_t B, const int64_t* offsets, const int64_t* t,
+                      const int8_t* ty, int32_t dtype, const void* q, const void* k, const void* v,
+                      const void* dout, double* dq, double* dk, double* dv, int32_t n_threads);
 /* LazFormer Eq. 22 per-layer query budget N_l (round half away from zero);
  * -1 on invalid arguments. */
 int64_t orc_query_keep(int64_t hist_len, int64_t n_min, int32_t layer, int32_t n_layers);
