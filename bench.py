@@ -35,6 +35,9 @@ from generative_recommender_ranking_gb300 import workloads as W  # noqa: E402
 
 METRIC = "masked-attn fwd TFLOP/s over visible pairs, % of GB300 bf16 peak; tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+# CUDA-core fp32 peak of a GB300 from its unit counts: 152 SMs x 128 FMA lanes x 2 FLOP
+# x 2070 MHz (the backward pass runs there)
+FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def _peaks():
@@ -260,8 +263,14 @@ def run_ours(args):
     pairs = bd.rec_attn_visible_pairs(plan)
     cls = bd.rec_attn_tile_classes(plan)
     bd.rec_attn_free(plan)
-    flops = 4.0 * w.head_dim * w.num_heads * pairs
+    flops_fwd = 4.0 * w.head_dim * w.num_heads * pairs
+    flops = flops_fwd * (3.5 if args.backward else 1.0)  # backward: 10 d per pair (2.5x forward)
     tokens = w.total_tokens
+    if args.backward:
+        lse_buf = torch.empty((tokens, w.num_heads), dtype=torch.float32, device=dev)
+        gen = torch.Generator(device="cpu").manual_seed(77)
+        dout = torch.randn(q.shape, generator=gen, dtype=torch.float32).to(q.dtype).to(dev)
+        dq_, dk_, dv_ = (torch.empty_like(q) for _ in range(3))
 
     fused_dev = {}
     if args.fused:
@@ -277,13 +286,24 @@ def run_ours(args):
                                   k_norm_weight=fused_dev["k_norm_w"], norm_eps=fused_eps,
                                   q_gate=fused_dev["q_gate"], k_gate=fused_dev["k_gate"],
                                   out_gate=fused_dev["out_gate"])
+        elif args.backward:
+            bd.rec_attn_fwd(p, q_, k_, v_, out, lse_buf, stream)
+            if bwd_events is not None:
+                bwd_events[-1][0].record(stream)
+            bd.rec_attn_bwd(p, q_, k_, v_, out, lse_buf, dout, dq_, dk_, dv_, stream)
+            if bwd_events is not None:
+                bwd_events[-1][1].record(stream)
         else:
             bd.rec_attn_fwd(p, q_, k_, v_, out, None, stream)
+
+    bwd_events = None  # per timed step: CUDA events around the backward call
 
     def step(timed=False):
         p = mkplan(off_d, t, ty, stream)
         if timed:
             bd.rec_attn_enable_timing(p)
+            if args.backward:
+                bwd_events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
         fwd(p, q, k, v)
         return p
 
@@ -300,6 +320,8 @@ def run_ours(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     plans = []
+    if args.backward:
+        bwd_events = []
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     if world > 1:
         dist.barrier()
@@ -325,6 +347,8 @@ def run_ours(args):
         raise RuntimeError(f"device status {status}: {bd.rec_attn_status_string(status)}")
     total_ms = float(sum(step_ms))
     attn_ms = statistics.mean(x[1] for x in kt)
+    bwd_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in bwd_events) if args.backward else 0.0
+    bwd_events = None  # the end-to-end leg below records none
     rope_ms = statistics.mean(x[0] for x in kt)
 
     # ---- end to end through the C-ABI with host buffers (H2D inputs, D2H output)
@@ -366,11 +390,11 @@ def run_ours(args):
     ms_step = total_ms / args.steps
     value = all_flops * args.steps / (total_ms * 1e-3) / 1e12
     bytes_attn = (5.0 if args.fused else 4.0) * tokens * w.num_heads * w.head_dim * elem + 9.0 * tokens
-    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    attn_tflops = flops_fwd / (attn_ms * 1e-3) / 1e12
     attn_gbs = bytes_attn / (attn_ms * 1e-3) / 1e9
     # full-size default batch only: the capture was taken on that launch
     traffic = _traffic(args.workload) if (args.batch is None and world == 1 and not args.fused) else None
-    hbm_bound = (flops / bytes_attn) < (pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9))
+    hbm_bound = (flops_fwd / bytes_attn) < (pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9))
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": attn_gbs / pk["hbm_gbs"], "traffic": traffic,
@@ -380,7 +404,18 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": attn_tflops, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": attn_tflops / pk["bf16_tflops"], "traffic": traffic,
                 "kernel": "k_attn_tc (masked softmax attention)", "peak_source": pk["source"],
-                "algorithmic_flops_per_launch": flops, "ms_per_launch": attn_ms}
+                "algorithmic_flops_per_launch": flops_fwd, "ms_per_launch": attn_ms}
+    if args.backward:
+        # the backward kernels dominate the step; they run on the CUDA cores in fp32
+        fp32_peak = FP32_FMA_PEAK_TFLOPS
+        bwd_tflops = 2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": bwd_tflops, "peak": fp32_peak, "unit": "TFLOP/s",
+                "frac": bwd_tflops / fp32_peak, "traffic": None,
+                "kernel": "k_bwd_delta + k_bwd_dq + k_bwd_dkv (backward, CUDA cores, fp32)",
+                "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2070 MHz",
+                "algorithmic_flops_per_launch": 2.5 * flops_fwd, "ms_per_launch": bwd_ms,
+                "forward_attention": {"achieved": attn_tflops, "unit": "TFLOP/s",
+                                      "frac": attn_tflops / pk["bf16_tflops"], "ms_per_launch": attn_ms}}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
@@ -388,18 +423,22 @@ def run_ours(args):
         "data": "synthetic (seeded generators standing in for the pages' private logs)",
         "config": dict(_config(w, args.workload, f"dp{world} (requests sharded, no collective)"),
                        **({"fused": "QK-RMSNorm + Q/K sigmoid gates + output gate"} if args.fused else {}),
-                       **({"keep_user_queries": args.keep_user_queries} if args.keep_user_queries >= 0 else {})),
+                       **({"keep_user_queries": args.keep_user_queries} if args.keep_user_queries >= 0 else {}),
+                       **({"pass": "forward + backward (FLOPs 14 d per visible pair and head)"}
+                          if args.backward else {})),
         "tokens_per_s": all_tokens * args.steps / (total_ms * 1e-3),
         "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
         "visible_pairs_per_head": pairs,
         "tile_classes": {"skip": int((cls == 0).sum()), "partial": int((cls == 1).sum()),
                          "full": int((cls == 2).sum())},
         "kernel_ms": {"attention": attn_ms, "rope": rope_ms, "plan_and_overhead": ms_step - attn_ms - rope_ms},
-        "fwd_only_tflops": flops / ((attn_ms + rope_ms) * 1e-3) / 1e12,
+        "fwd_only_tflops": flops_fwd / ((attn_ms + rope_ms) * 1e-3) / 1e12,
+        **({"backward_ms": bwd_ms, "backward_tflops": 2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12}
+           if args.backward else {}),
         "roofline": roof,
         "e2e": {"value": all_flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (7 if args.backward else 3) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
@@ -428,6 +467,9 @@ def main(argv=None):
                     help="override the workload's number of requests (small profiling cases)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="one step = plan + forward + backward (training); FLOPs 4d (forward) + 10d "
+                         "(backward) per visible pair and head")
     ap.add_argument("--fused", action="store_true",
                     help="time rec_attn_fwd_fused with QK-RMSNorm, Q/K gates and the output gate on")
     args = ap.parse_args(argv)

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.rec_attn_fwd.restype = ctypes.c_int
         L.rec_attn_fwd_fused.argtypes = [vp, vp, vp, vp, ctypes.POINTER(RecAttnFused), vp, vp, vp]
         L.rec_attn_fwd_fused.restype = ctypes.c_int
+        L.rec_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.rec_attn_bwd.restype = ctypes.c_int
         L.rec_attn_free.argtypes = [vp]
         L.rec_attn_free.restype = None
         L.rec_attn_tile_classes.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
@@ -204,6 +206,13 @@ def rec_attn_fwd_fused(plan: Plan, q, k, v, out, lse=None, stream=None, q_norm_w
     code = lib().rec_attn_fwd_fused(plan.handle, _ptr(q), _ptr(k), _ptr(v), ctypes.byref(f), _ptr(out),
                                     _ptr(lse), _stream(stream))
     _check("rec_attn_fwd_fused", code)
+
+
+def rec_attn_bwd(plan: Plan, q, k, v, out, lse, dout, dq, dk, dv, stream=None) -> None:
+    """Gradients dq, dk, dv of rec_attn_fwd for the upstream gradient dout."""
+    code = lib().rec_attn_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                              _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream))
+    _check("rec_attn_bwd", code)
 
 
 def rec_attn_free(plan: Plan) -> None:

@@ -35,6 +35,7 @@ struct rec_attn_plan_s {
   void* qrot = nullptr;
   void* krot = nullptr;
   void* qk_extra = nullptr;  // Q'/K' buffers of a plan without the RoPE, made on the first fused call
+  float* bwd_delta = nullptr;  // [T][H] workspace of the backward pass, made on its first call
   const long long* t = nullptr;
   const int8_t* ty = nullptr;
   MaskP mask{};
@@ -459,6 +460,73 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const voi
   return fwd_impl(plan, q, k, v, fused, out, lse, stream);
 }
 
+REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                                          const void* out, const float* lse, const void* dout, void* dq,
+                                          void* dk, void* dv, void* stream) {
+  if (!plan) return REC_ATTN_ERR_INVALID_ARG;
+  const rec_attn_params& p = plan->p;
+  const long long T = plan->T;
+  const bool dim_ok = p.dtype == REC_ATTN_BF16 ? p.head_dim == 64 : (p.head_dim == 32 || p.head_dim == 64);
+  if (!dim_ok || plan->mask.keep_user >= 0) return REC_ATTN_ERR_UNSUPPORTED;
+  if (T > 0) {
+    const void* ptrs[8] = {q, k, v, out, dout, dq, dk, dv};
+    for (const void* x : ptrs)
+      if (!x || (reinterpret_cast<uintptr_t>(x) & 15u)) return REC_ATTN_ERR_INVALID_ARG;
+    if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return REC_ATTN_ERR_INVALID_ARG;
+    const size_t elem = p.dtype == REC_ATTN_BF16 ? 2 : 4;
+    const size_t bytes = (size_t)T * p.num_heads * p.head_dim * elem;
+    const void* ins[6] = {q, k, v, out, dout, lse};
+    const size_t in_bytes[6] = {bytes, bytes, bytes, bytes, bytes, (size_t)T * p.num_heads * 4};
+    void* outs[3] = {dq, dk, dv};
+    for (int o = 0; o < 3; ++o) {
+      for (int i = 0; i < 6; ++i)
+        if (overlaps(outs[o], bytes, ins[i], in_bytes[i])) return REC_ATTN_ERR_INVALID_ARG;
+      for (int o2 = o + 1; o2 < 3; ++o2)
+        if (overlaps(outs[o], bytes, outs[o2], bytes)) return REC_ATTN_ERR_INVALID_ARG;
+    }
+  }
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (dev != plan->device) return REC_ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  plan->stream = st;
+  if (T == 0) return REC_ATTN_OK;
+  if (!plan->bwd_delta) {
+    cudaMemPool_t pool;
+    e = pool_for(plan->device, &pool);
+    if (e == cudaSuccess)
+      e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&plan->bwd_delta),
+                                  (size_t)T * p.num_heads * sizeof(float), pool, st);
+    if (e != cudaSuccess) { plan->bwd_delta = nullptr; return from_cuda(e); }
+  }
+  const void* qs = q;
+  const void* ks = k;
+  if (p.use_rope) {  // Q' and K' again, into the plan's workspace
+    e = cudaStreamWaitEvent(st, plan->ev_meta, 0);
+    if (e != cudaSuccess) return from_cuda(e);
+    RopeArgs ra;
+    ra.meta = plan->pd.meta; ra.batch = plan->batch; ra.t = plan->t;
+    ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
+    ra.heads = p.num_heads; ra.head_dim = p.head_dim;
+    std::memcpy(ra.omega, plan->omega, sizeof ra.omega);
+    e = launch_rope(ra, p.dtype, plan->NT, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    qs = plan->qrot; ks = plan->krot;
+  }
+  e = cudaStreamWaitEvent(st, plan->ev_plan, 0);
+  if (e != cudaSuccess) return from_cuda(e);
+  BwdArgs a;
+  a.meta = plan->pd.meta; a.batch = plan->batch; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
+  a.cls = plan->pd.cls; a.t = plan->t; a.ty = plan->ty;
+  a.q = qs; a.k = ks; a.v = v; a.out = out; a.dout = dout; a.lse = lse; a.delta = plan->bwd_delta;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.rows = T * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale;
+  a.rotate = p.use_rope; a.mask = plan->mask;
+  std::memcpy(a.omega, plan->omega, sizeof a.omega);
+  return from_cuda(launch_attn_bwd(a, p.dtype, p.head_dim, plan->NT, st));
+}
+
 REC_ATTN_API void rec_attn_free(rec_attn_plan_t* plan) {
   if (!plan) return;
   if (plan->ws) {
@@ -466,6 +534,7 @@ REC_ATTN_API void rec_attn_free(rec_attn_plan_t* plan) {
     cudaFreeAsync(plan->ws, plan->stream);
   }
   if (plan->qk_extra) cudaFreeAsync(plan->qk_extra, plan->stream);
+  if (plan->bwd_delta) cudaFreeAsync(plan->bwd_delta, plan->stream);
   for (cudaEvent_t ev : plan->ev)
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : {plan->ev_in, plan->ev_meta, plan->ev_plan})

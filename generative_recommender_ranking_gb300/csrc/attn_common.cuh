@@ -42,6 +42,33 @@ struct RopeArgs {
   float omega[kMaxPairs];  // rad per second, pair i
 };
 
+// Arguments of the backward kernels.
+struct BwdArgs {
+  const ReqMeta* meta;
+  int batch;
+  const int* kcount;       // per query tile: entries in its key-tile list
+  const uint32_t* klist;   // per query tile: non-SKIP key tiles (kt | class << 24)
+  const uint8_t* cls;      // per request: ntiles x ntiles class matrix
+  const long long* t;
+  const int8_t* ty;
+  const void* q;           // rotated queries Q' (or raw without the RoPE) [T][H][d]
+  const void* k;           // rotated keys K'
+  const void* v;
+  const void* out;         // forward output O
+  const void* dout;        // upstream gradient dO
+  const float* lse;        // forward log-sum-exp [T][H]
+  float* delta;            // workspace [T][H]: <dO, O> per row
+  void* dq;                // outputs [T][H][d] (w.r.t. the unrotated Q, K)
+  void* dk;
+  void* dv;
+  long long rows;          // T * H
+  int heads;
+  float scale;
+  int rotate;              // 1: undo the time-RoPE on dQ', dK'
+  MaskP mask;
+  float omega[kMaxPairs];  // rad per second, pair i
+};
+
 // Fused steps of the prologue, applied before the rotation: QK-RMSNorm
 // (x / sqrt(mean(x^2) + eps) * w[h]) and then the sigmoid gate x * sigmoid(g).
 struct FusedArgs {

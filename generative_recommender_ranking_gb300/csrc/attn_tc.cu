@@ -610,7 +610,9 @@ __device__ __forceinline__ void rescale_o(uint32_t tm_o, float corr) {
   }
 }
 
-template <int D>
+// GATE: the attention output gate is applied in the epilogue (a separate
+// instantiation, so the plain epilogue carries none of its code).
+template <int D, bool GATE>
 __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, uint32_t tmem,
                             volatile int* abort_flag) {
   using L = Layout<D>;
@@ -660,6 +662,15 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       if ((qr->typebits[c][row >> 5] >> (row & 31)) & 1u) tyi = c;
     ptx::mbar_arrive(B.q_empty + qb);  // the Q buffer and its record may be refilled
     const bool out_ok = row_ok && query_kept(tyi, pi, d.keep);  // pruned rows are computed, not written
+    uint4 gpre[8];  // GATE: the gate of the row's first 64 columns, loaded while the item runs
+    if constexpr (GATE) {
+      if (out_ok) {
+        const uint4* g0 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out_gate) +
+                                                         (tok * H + d.h) * D);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) gpre[c] = g0[c];
+      }
+    }
     RowMask rm;
     row_mask_setup(a.mask, row_ok, pi, ti, tyi, rm);
     float m_ref = -INFINITY, l = 0.f;
@@ -754,7 +765,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       ptx::tc_fence_before();
       ptx::mbar_arrive(B.p_full + 1);
     }
-    // epilogue: O / l
+    // epilogue: O / l (times sigmoid of the output gate)
     if (!wait_bar_warp(B.o_ready, o_it & 1, abort_flag, a.status)) return;
     ++o_it;
     ptx::tc_fence_after();
@@ -764,17 +775,15 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       uint32_t o[64];
       ptx::tmem_ld64(tm.o + half * 64, o);
       if (out_ok) {
-        // the attention output gate, O * sigmoid(g), when the caller passed one
-        const uint4* grow = a.out_gate ? reinterpret_cast<const uint4*>(
-                                             static_cast<const __nv_bfloat16*>(a.out_gate) + (tok * H + d.h) * D + half * 64)
-                                       : nullptr;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           float sc[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) sc[e] = inv;
-          if (grow) {
-            const uint4 gv = grow[c];
+          if constexpr (GATE) {
+            const uint4 gv = half == 0 ? gpre[c]
+                                       : reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out_gate) +
+                                                                        (tok * H + d.h) * D + half * 64)[c];
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -802,7 +811,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
   }
 }
 
-template <int D>
+template <int D, bool GATE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -854,7 +863,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // gated d = 64: registers move from the role warpgroup (warps 0-3) to the two softmax
+  // warpgroups; launched with 168 per thread (checked on the host): 128*56 + 256*224
+  // = 384*168
+  constexpr bool kSplitRegs = GATE && D == 64;
   if (warp < kRoleWarps) {
+    if constexpr (kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     const int s = warp & 1;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
@@ -863,10 +877,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       else run_mma<D>(a, sm, s, B, tmem, abort_flag);
     }
   } else {
+    if constexpr (kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
     const int s = (warp - kRoleWarps) >> 2;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
-    run_softmax<D>(a, sm, s, B, tmem, abort_flag);
+    run_softmax<D, GATE>(a, sm, s, B, tmem, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -885,15 +900,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int D, bool GATE>
+cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                     int grid, cudaStream_t st) {
+  using L = Layout<D>;
+  static_assert(L::kDynamic <= 227 * 1024, "shared memory budget");
+  cudaError_t e =
+      cudaFuncSetAttribute(k_attn_tc<D, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
+  if (e != cudaSuccess) return e;
+  if (GATE && D == 64) {
+    // the register split inside the kernel needs 384 x 168 registers at launch; with
+    // fewer, setmaxnreg.inc could never be granted, so refuse to launch instead
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, k_attn_tc<D, GATE>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * kThreads < 128 * 56 + 256 * 224) return cudaErrorInvalidConfiguration;
+  }
+  k_attn_tc<D, GATE><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, int grid,
                    cudaStream_t st) {
-  using L = Layout<D>;
-  static_assert(L::kDynamic <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(k_attn_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
-  if (e != cudaSuccess) return e;
-  k_attn_tc<D><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
-  return cudaGetLastError();
+  return a.out_gate ? launch_t<D, true>(a, q, k, v, grid, st) : launch_t<D, false>(a, q, k, v, grid, st);
 }
 
 }  // namespace

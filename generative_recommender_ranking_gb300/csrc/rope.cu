@@ -129,12 +129,12 @@ __device__ __forceinline__ float group_sum(float v, int group) {
 }
 
 // x <- x / sqrt(mean over the head row of x^2 + eps) * w, then x <- x * sigmoid(g):
-// the fused QK-RMSNorm and sigmoid gate of one 16-byte chunk of a head row.
+// the fused QK-RMSNorm and sigmoid gate of one 16-byte chunk of a head row (g holds
+// the chunk's gate pre-activations when `gated`).
 template <typename E>
-__device__ __forceinline__ void norm_gate(float (&x)[8], bool act, const float* w, float eps, const void* gate,
-                                          long long off_bytes, int e0, int chunks, int d) {
-  using C = Chunk<E>;
-  constexpr int kElems = 2 * C::kPairs;
+__device__ __forceinline__ void norm_gate(float (&x)[8], bool act, const float* w, float eps, bool gated,
+                                          const float (&g)[8], int e0, int chunks, int d) {
+  constexpr int kElems = 2 * Chunk<E>::kPairs;
   if (w) {
     float ss = 0.f;
 #pragma unroll
@@ -146,9 +146,7 @@ __device__ __forceinline__ void norm_gate(float (&x)[8], bool act, const float* 
       for (int e = 0; e < kElems; ++e) x[e] *= r * w[e0 + e];
     }
   }
-  if (gate && act) {
-    float g[8];
-    C::load(static_cast<const char*>(gate) + off_bytes, g);
+  if (gated) {
 #pragma unroll
     for (int e = 0; e < kElems; ++e) x[e] *= sigmoidf_fast(g[e]);
   }
@@ -192,16 +190,21 @@ __global__ void __launch_bounds__(256, 4) k_rope_fused(RopeArgs a, FusedArgs f) 
 #pragma unroll
     for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
     const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
+    const bool qg = f.q_gate != nullptr, kg = f.k_gate != nullptr;
     for (int h = 0; h < a.heads; ++h) {
       const long long off = row0 + h * head_bytes;
-      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (act) {
+      float x[8], y[8], gx[8], gy[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = y[e] = gx[e] = gy[e] = 0.f;
+      if (act) {  // every load of the head row chunk before any arithmetic
         C::load(static_cast<const char*>(a.q) + off, x);
         C::load(static_cast<const char*>(a.k) + off, y);
+        if (qg) C::load(static_cast<const char*>(f.q_gate) + off, gx);
+        if (kg) C::load(static_cast<const char*>(f.k_gate) + off, gy);
       }
       const int e0 = h * a.head_dim + c * 2 * kPairs;
-      norm_gate<E>(x, act, f.q_norm_w, f.eps, f.q_gate, off, e0, chunks, a.head_dim);
-      norm_gate<E>(y, act, f.k_norm_w, f.eps, f.k_gate, off, e0, chunks, a.head_dim);
+      norm_gate<E>(x, act, f.q_norm_w, f.eps, qg, gx, e0, chunks, a.head_dim);
+      norm_gate<E>(y, act, f.k_norm_w, f.eps, kg, gy, e0, chunks, a.head_dim);
 #pragma unroll
       for (int p = 0; p < kPairs; ++p) {
         const float x0 = x[2 * p], x1 = x[2 * p + 1], y0 = y[2 * p], y1 = y[2 * p + 1];

@@ -225,6 +225,28 @@ rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const void* q, const v
                                    float* lse, void* stream);
 
 /*
+ * rec_attn_bwd -- gradients of rec_attn_fwd with respect to q, k and v, for the
+ * upstream gradient dout (training: the TM20K and LazFormer review pages train these
+ * models end to end; the pages print no backward formula, so this is the derivative
+ * of the forward's definition).
+ *
+ *   q, k, v   the forward's inputs (the time-RoPE is applied again inside).
+ *   out, lse  the forward's output and log-sum-exp (lse is required here).
+ *   dout      device [T][H][d] in params->dtype: dLoss/dout.
+ *   dq, dk, dv  device [T][H][d] in params->dtype, written in full; they may not
+ *             alias any input or each other.  All tensors 16-byte aligned.
+ * The plan must be the forward's (same offsets, times, types, params) and made by
+ * rec_attn_plan (not query-pruned).  Supported: bf16 with head_dim 64, fp32 with
+ * head_dim 32 or 64 (else UNSUPPORTED).  The first call takes T * H floats of
+ * workspace from the library pool on `stream` (released with the plan).  CUDA cores,
+ * fp32 arithmetic; gradients are rounded once to params->dtype.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM.
+ */
+rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                             const void* out, const float* lse, const void* dout, void* dq, void* dk,
+                             void* dv, void* stream);
+
+/*
  * rec_attn_free -- release a plan (NULL-safe).  The workspace returns to the
  * library pool in stream order on the stream of the plan's last use (after the
  * planning work), so work already enqueued there may still run; callers that used

@@ -1,0 +1,100 @@
+"""Backward pass on the GPU (rec_attn_bwd) vs the fp64 oracle backward, through the
+C-ABI, on the same inputs and upstream gradient.
+
+Tolerance per gradient tensor (derived in the design doc from the roundings the GPU makes:
+Q', K', O and the gradients themselves in bf16): relative Frobenius error <= 1e-2 and
+max-abs error <= 2e-2 * max|reference| for bf16; 1e-5 and 1e-4 for fp32.  Blind
+query rows and unread keys must get exactly zero gradients."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as gu
+import oracle
+from generative_recommender_ranking_gb300 import binding as bd
+from generative_recommender_ranking_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gu.ensure_built()
+
+
+CASES = {
+    "tiny_fp32": lambda: W.tiny_fp32(batch=3, n_hist=200, n_cand=20),
+    "cadet": lambda: W.cadet(batch=3, n_pairs=150),
+    "sort": lambda: W.sort(batch=2, n_hist=400, n_cand=40, window=96),
+    "mtgr": lambda: W.mtgr(batch=3, hist=(150, 300), rt=(20, 60), cand=(10, 30)),
+    "tm20k_window": lambda: W.tm20k("window", batch=1, n_hist=1000),
+}
+
+
+def _grad_inputs(w, seed=11):
+    rng = np.random.default_rng(seed)
+    g = rng.standard_normal(w.q.shape).astype(np.float32)
+    return W.round_to_bf16_bits(g) if w.dtype == "bf16" else g
+
+
+def _tol(w):
+    return (1e-2, 2e-2) if w.dtype == "bf16" else (1e-5, 1e-4)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "cadet", "sort", "mtgr", "tm20k_window"])
+def test_backward_parity(name):
+    w = CASES[name]()
+    tens = gu.device_inputs(w)
+    plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    try:
+        out = torch.empty_like(tens["q"])
+        lse = torch.empty((w.total_tokens, w.num_heads), dtype=torch.float32, device=out.device)
+        bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out, lse)
+        g_host = _grad_inputs(w)
+        dout = gu.device_inputs(W.Workload(**{**w.__dict__, "q": g_host}))["q"]
+        dq, dk, dv = (torch.full_like(tens["q"], float("nan")) for _ in range(3))
+        bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], out, lse, dout, dq, dk, dv)
+        torch.cuda.synchronize()
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
+    ref = oracle.attention_bwd(gu.oracle_params(w), w.offsets, w.t, w.types, w.q, w.k, w.v, g_host)
+    rel_tol, max_tol = _tol(w)
+    op = gu.oracle_params(w)
+    for what, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        x = gu.to_f64(got)
+        assert np.isfinite(x).all(), f"{what}: unwritten or non-finite values"
+        rel = np.linalg.norm(x - r) / max(np.linalg.norm(r), 1e-30)
+        mx = np.max(np.abs(x - r))
+        assert rel <= rel_tol and mx <= max_tol * max(np.max(np.abs(r)), 1e-30), (name, what, rel, mx)
+        # exact zeros where no gradient flows
+        for b in range(w.batch):
+            s, e = int(w.offsets[b]), int(w.offsets[b + 1])
+            m = oracle.mask(op, w.t[s:e], w.types[s:e])
+            if what == "dq":
+                assert np.all(x[s:e][m.sum(1) == 0] == 0.0)
+            else:
+                assert np.all(x[s:e][m.sum(0) == 0] == 0.0)
+
+
+def test_backward_rejects_pruned_plans_and_bad_pointers():
+    w = CASES["cadet"]()
+    tens = gu.device_inputs(w)
+    plan = bd.rec_attn_plan_query_pruned(gu.params_for(w), 10, tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    x = torch.empty_like(tens["q"])
+    lse = torch.empty((w.total_tokens, w.num_heads), dtype=torch.float32, device=x.device)
+    try:
+        with pytest.raises(bd.RecAttnError):
+            bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], x, lse, x, *(torch.empty_like(x) for _ in range(3)))
+    finally:
+        bd.rec_attn_free(plan)
+    plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    try:
+        dq = torch.empty_like(x)
+        with pytest.raises(bd.RecAttnError):  # a gradient aliasing an input
+            bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], x, lse, x, tens["q"], dq, torch.empty_like(x))
+        with pytest.raises(bd.RecAttnError):  # lse is required
+            bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], x, None, x, dq, torch.empty_like(x),
+                            torch.empty_like(x))
+    finally:
+        bd.rec_attn_free(plan)
