@@ -138,6 +138,9 @@ def lib() -> ctypes.CDLL:
         L.orc_attention_bwd.argtypes = [P, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp,
                                         vp, vp, vp, ctypes.c_int32]
         L.orc_attention_bwd.restype = ctypes.c_int
+        L.orc_compress.argtypes = [ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, ctypes.c_int32,
+                                   ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp]
+        L.orc_compress.restype = ctypes.c_int64
         L.orc_query_keep.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
         L.orc_query_keep.restype = ctypes.c_int64
         L.orc_kept_rows.argtypes = [ctypes.c_int32, vp, vp, ctypes.c_int64, vp]
@@ -310,3 +313,35 @@ def attention_bwd(p: Params, offsets, t, ty, q, k, v, dout, threads: int | None 
     if rc != 0:
         raise ValueError(f"orc_attention_bwd rejected its arguments (rc={rc})")
     return dq, dk, dv
+
+
+def compress(offsets, hist_begin, hist_len, segments, x=None, t=None, ty=None):
+    """History compression.  segments: [(length or -1, group size), ...] from the most
+    recent; x: [T, width] float32 or bf16 bits.  Returns (out_offsets, out_x fp64,
+    out_t, out_ty), or only out_offsets when x is None."""
+    offsets, hb, hl = _c64(offsets), _c64(hist_begin), _c64(hist_len)
+    B = len(offsets) - 1
+    sl = _c64([s_[0] for s_ in segments])
+    sg = np.ascontiguousarray([s_[1] for s_ in segments], dtype=np.int32)
+    out_off = np.zeros(B + 1, dtype=np.int64)
+    L = lib()
+    if x is None:
+        n = L.orc_compress(B, _ptr(offsets), _ptr(hb), _ptr(hl), len(segments), _ptr(sl), _ptr(sg), 0, 1,
+                           None, None, None, _ptr(out_off), None, None, None)
+        if n < 0:
+            raise ValueError("orc_compress rejected its arguments")
+        return out_off
+    x = np.ascontiguousarray(x)
+    dtype = 0 if x.dtype == np.uint16 else 1
+    width = int(np.prod(x.shape[1:]))
+    t, ty = _c64(t), _c8(ty)
+    n = L.orc_compress(B, _ptr(offsets), _ptr(hb), _ptr(hl), len(segments), _ptr(sl), _ptr(sg), dtype, width,
+                       None, None, None, _ptr(out_off), None, None, None)
+    if n < 0:
+        raise ValueError("orc_compress rejected its arguments")
+    ox = np.zeros((max(n, 1), width), dtype=np.float64)
+    ot = np.zeros(max(n, 1), dtype=np.int64)
+    oty = np.zeros(max(n, 1), dtype=np.int8)
+    L.orc_compress(B, _ptr(offsets), _ptr(hb), _ptr(hl), len(segments), _ptr(sl), _ptr(sg), dtype, width,
+                   _ptr(x), _ptr(t), _ptr(ty), _ptr(out_off), _ptr(ox), _ptr(ot), _ptr(oty))
+    return out_off, ox[:n].reshape((n,) + x.shape[1:]), ot[:n], oty[:n]

@@ -37,6 +37,12 @@
  *     dQ~ = scale dS K~, dK~ = scale dS^T Q~, then the inverse rotation).  The pages
  *     train these models (TM20K section 2.1, LazFormer's FlexAttention training)
  *     but print no backward formula; this is the derivative of the definition.
+ *   - History compression (orc_compress): the history is merged by summing groups
+ *     of consecutive tokens, the group size set per recency segment.  LazFormer
+ *     review page, Eq. 16-18 (keep the most recent l tokens, sum the rest in groups
+ *     of g, the last group partial) and its Table 6 configurations; TM20K review
+ *     page, PATM (position segments with merge factors, zero-padded sums) and LPTM
+ *     (sum of adjacent history pairs, targets never merged).
  *   - Query pruning (orc_kept_rows, orc_query_keep): only some queries are
  *     computed; every key stays.  SORT review page, section 3.2.2 (queries are
  *     pruned on the user side only, history and profile; candidates are never
@@ -476,6 +482,93 @@ int orc_attention_bwd(const orc_params* p, int32_t B, const int64_t* offsets, co
   for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
   free(th);
   return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* History compression                                                        */
+/* ------------------------------------------------------------------------- */
+
+/* Groups of one request's history of Lh tokens under the segment spec: segment i
+ * (i = 0 the most recent) covers the next seg_len[i] tokens going back in time
+ * (seg_len < 0: all the rest) and merges them in groups of seg_group[i], the oldest
+ * group of a segment being the partial one.  Writes the groups oldest first as
+ * [first, last) history indices (0 = oldest) and returns their count; lo/hi may be
+ * NULL to count. */
+static int64_t history_groups(int64_t Lh, int32_t n_seg, const int64_t* seg_len, const int32_t* seg_group,
+                              int64_t* lo, int64_t* hi) {
+  int64_t n = 0, rank = 0; /* rank: tokens already covered, counted from the newest */
+  /* segments are laid out from the newest; the output wants the oldest first, so
+   * collect per segment and emit in reverse at the end */
+  int64_t nseg_groups[64];
+  int64_t seg_start[64], seg_m[64];
+  int32_t used = 0;
+  for (int32_t i = 0; i < n_seg && rank < Lh && i < 64; ++i) {
+    const int64_t room = Lh - rank;
+    const int64_t m = (seg_len[i] < 0 || seg_len[i] > room) ? room : seg_len[i];
+    const int64_t g = seg_group[i];
+    seg_start[used] = rank;
+    seg_m[used] = m;
+    nseg_groups[used] = (m + g - 1) / g;
+    ++used;
+    rank += m;
+  }
+  if (rank < Lh) return -1; /* the spec does not cover the whole history */
+  for (int32_t u = used - 1; u >= 0; --u) {
+    const int32_t g = seg_group[u];
+    for (int64_t q = nseg_groups[u] - 1; q >= 0; --q) { /* q = 0 is the newest group */
+      const int64_t r0 = seg_start[u] + q * g;                        /* newest rank in it */
+      const int64_t r1 = seg_start[u] + ((q + 1) * g < seg_m[u] ? (q + 1) * g : seg_m[u]); /* past oldest */
+      if (lo) { lo[n] = Lh - r1; hi[n] = Lh - r0; }
+      ++n;
+    }
+  }
+  return n;
+}
+
+int64_t orc_compress(int32_t B, const int64_t* offsets, const int64_t* hist_begin, const int64_t* hist_len,
+                     int32_t n_seg, const int64_t* seg_len, const int32_t* seg_group, int32_t dtype, int64_t width,
+                     const void* x, const int64_t* t, const int8_t* ty, int64_t* out_offsets, double* out_x,
+                     int64_t* out_t, int8_t* out_ty) {
+  if (B < 0 || !offsets || n_seg < 1 || n_seg > 64 || width < 1) return -1;
+  for (int32_t i = 0; i < n_seg; ++i)
+    if (seg_group[i] < 1) return -1;
+  int64_t n_out = 0;
+  if (out_offsets) out_offsets[0] = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t s = offsets[b], L = offsets[b + 1] - s, hb = hist_begin[b], Lh = hist_len[b];
+    if (L < 0 || hb < 0 || Lh < 0 || hb + Lh > L) return -1;
+    const int64_t G = history_groups(Lh, n_seg, seg_len, seg_group, NULL, NULL);
+    if (G < 0) return -1;
+    int64_t* glo = (int64_t*)malloc(sizeof(int64_t) * (size_t)(G > 0 ? G : 1));
+    int64_t* ghi = (int64_t*)malloc(sizeof(int64_t) * (size_t)(G > 0 ? G : 1));
+    history_groups(Lh, n_seg, seg_len, seg_group, glo, ghi);
+    const int64_t Lo = L - Lh + G;
+    if (out_x) {
+      int64_t o = n_out;
+      for (int64_t p = 0; p < hb; ++p, ++o) { /* tokens before the history */
+        for (int64_t e = 0; e < width; ++e) out_x[o * width + e] = load_elem(dtype, x, (s + p) * width + e);
+        out_t[o] = t[s + p]; out_ty[o] = ty[s + p];
+      }
+      for (int64_t gi = 0; gi < G; ++gi, ++o) { /* merged groups: sums, latest time */
+        int64_t tmax = INT64_MIN;
+        for (int64_t e = 0; e < width; ++e) out_x[o * width + e] = 0.0;
+        for (int64_t j = glo[gi]; j < ghi[gi]; ++j) {
+          const int64_t g = s + hb + j;
+          for (int64_t e = 0; e < width; ++e) out_x[o * width + e] += load_elem(dtype, x, g * width + e);
+          if (t[g] > tmax) tmax = t[g];
+        }
+        out_t[o] = tmax; out_ty[o] = TY_HIST;
+      }
+      for (int64_t p = hb + Lh; p < L; ++p, ++o) { /* tokens after the history */
+        for (int64_t e = 0; e < width; ++e) out_x[o * width + e] = load_elem(dtype, x, (s + p) * width + e);
+        out_t[o] = t[s + p]; out_ty[o] = ty[s + p];
+      }
+    }
+    free(glo); free(ghi);
+    n_out += Lo;
+    if (out_offsets) out_offsets[b + 1] = n_out;
+  }
+  return n_out;
 }
 
 /* ------------------------------------------------------------------------- */

@@ -75,6 +75,17 @@ int orc_attention_fused(const orc_params* p, int32_t B, const int64_t* offsets,
 int orc_attention_bwd(const orc_params* p, int32_t B, const int64_t* offsets, const int64_t* t,
                       const int8_t* ty, int32_t dtype, const void* q, const void* k, const void* v,
                       const void* dout, double* dq, double* dk, double* dv, int32_t n_threads);
+/* History compression: in request b the tokens [hist_begin[b], hist_begin[b] +
+ * hist_len[b]) (time-ordered history) are replaced by sums of groups of consecutive
+ * tokens; recency segment i (0 = newest) covers seg_len[i] tokens (< 0: the rest)
+ * with groups of seg_group[i], the oldest group of a segment partial.  Merged tokens
+ * keep time order, take the latest member time and type HIST.  x: [T][width] in dtype;
+ * out_x fp64.  out arrays may be NULL (out_offsets too) to count.  Returns the total
+ * output rows or -1. */
+int64_t orc_compress(int32_t B, const int64_t* offsets, const int64_t* hist_begin, const int64_t* hist_len,
+                     int32_t n_seg, const int64_t* seg_len, const int32_t* seg_group, int32_t dtype, int64_t width,
+                     const void* x, const int64_t* t, const int8_t* ty, int64_t* out_offsets, double* out_x,
+                     int64_t* out_t, int8_t* out_ty);
 /* LazFormer Eq. 22 per-layer query budget N_l (round half away from zero);
  * -1 on invalid arguments. */
 int64_t orc_query_keep(int64_t hist_len, int64_t n_min, int32_t layer, int32_t n_layers);
