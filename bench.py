@@ -35,6 +35,12 @@ from generative_recommender_ranking_gb300 import workloads as W  # noqa: E402
 
 METRIC = "masked-attn fwd TFLOP/s over visible pairs, % of GB300 bf16 peak; tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+# history-compression settings: recency segments (length or -1, group size), newest first
+COMPRESS_SPECS = {
+    "lazformer_keep1024_g8": [(1024, 1), (-1, 8)],
+    "lptm_pairs": [(-1, 2)],
+    "patm_bands": [(1000, 1), (4000, 2), (5000, 3), (-1, 4)],
+}
 # CUDA-core fp32 peak of a GB300 from its unit counts: 152 SMs x 128 FMA lanes x 2 FLOP
 # x 2070 MHz (the backward pass runs there)
 FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
@@ -212,6 +218,63 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+
+def run_compress(args):
+    """--compress: history compression of the workload's K rows ([T, H*d]), HBM-bound."""
+    import torch
+    from generative_recommender_ranking_gb300 import binding as bd
+    from generative_recommender_ranking_gb300 import build as bld
+    bld.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = _workload(args.workload, 0, args.batch)
+    segs = COMPRESS_SPECS[args.compress]
+    hb, hl = [], []
+    for b in range(w.batch):
+        s0, e0 = int(w.offsets[b]), int(w.offsets[b + 1])
+        idx = np.nonzero(w.types[s0:e0] == W.HIST)[0]
+        hb.append(int(idx[0]) if len(idx) else 0)
+        hl.append(len(idx))
+    T = w.total_tokens
+    raw = w.k.reshape(T, -1)
+    x = (torch.from_numpy(raw.view(np.int16)).view(torch.bfloat16) if raw.dtype == np.uint16
+         else torch.from_numpy(raw)).to(dev)
+    t = torch.from_numpy(w.t).to(dev)
+    ty = torch.from_numpy(w.types).to(dev)
+    out_off = bd.rec_attn_compress_lengths(w.offsets, hb, hl, segs)
+    n = int(out_off[-1])
+    x_out = torch.empty((n, x.shape[1]), dtype=x.dtype, device=dev)
+    t_out = torch.empty(n, dtype=torch.int64, device=dev)
+    ty_out = torch.empty(n, dtype=torch.int8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    call = lambda: bd.rec_attn_compress(w.offsets, hb, hl, segs, x, t, ty, x_out, t_out, ty_out, stream)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    elem = x.element_size()
+    nbytes = (T + n) * x.shape[1] * elem + 9.0 * (T + n)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    pk = _peaks()
+    print(json.dumps({
+        "metric": "history compression GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "dtype": w.dtype,
+        "data": "synthetic", "config": {"workload": args.workload, "rows_in": T, "rows_out": n,
+                                        "width": int(x.shape[1]), "segments": segs,
+                                        "l2": "flushed between timed steps (256 MiB write)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "k_compress",
+                     "peak_source": pk["source"], "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": ms},
+        "gpu_launches": args.steps}), flush=True)
+    return 0
+
 
 def run_ours(args):
     import torch
@@ -467,12 +530,16 @@ def main(argv=None):
                     help="override the workload's number of requests (small profiling cases)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compress", default=None, choices=sorted(COMPRESS_SPECS),
+                    help="time history compression of the workload's key rows instead (HBM-bound)")
     ap.add_argument("--backward", action="store_true",
                     help="one step = plan + forward + backward (training); FLOPs 4d (forward) + 10d "
                          "(backward) per visible pair and head")
     ap.add_argument("--fused", action="store_true",
                     help="time rec_attn_fwd_fused with QK-RMSNorm, Q/K gates and the output gate on")
     args = ap.parse_args(argv)
+    if args.compress:
+        return run_compress(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

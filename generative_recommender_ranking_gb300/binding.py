@@ -91,6 +91,10 @@ def lib() -> ctypes.CDLL:
         L.rec_attn_fwd_fused.restype = ctypes.c_int
         L.rec_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.rec_attn_bwd.restype = ctypes.c_int
+        L.rec_attn_compress_lengths.argtypes = [i32, vp, vp, vp, i32, vp, vp, vp]
+        L.rec_attn_compress_lengths.restype = ctypes.c_int
+        L.rec_attn_compress.argtypes = [i32, vp, vp, vp, i32, vp, vp, i32, i64, vp, vp, vp, vp, vp, vp, vp]
+        L.rec_attn_compress.restype = ctypes.c_int
         L.rec_attn_free.argtypes = [vp]
         L.rec_attn_free.restype = None
         L.rec_attn_tile_classes.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
@@ -213,6 +217,42 @@ def rec_attn_bwd(plan: Plan, q, k, v, out, lse, dout, dq, dk, dv, stream=None) -
     code = lib().rec_attn_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
                               _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream))
     _check("rec_attn_bwd", code)
+
+
+def _segments(segments):
+    sl = np.ascontiguousarray([int(a) for a, _ in segments], dtype=np.int64)
+    sg = np.ascontiguousarray([int(g) for _, g in segments], dtype=np.int32)
+    return sl, sg
+
+
+def rec_attn_compress_lengths(offsets_host, hist_begin, hist_len, segments) -> np.ndarray:
+    """Output offsets of history compression; segments = [(length or -1, group), ...]
+    from the most recent."""
+    off = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int64))
+    hb = np.ascontiguousarray(np.asarray(hist_begin, dtype=np.int64))
+    hl = np.ascontiguousarray(np.asarray(hist_len, dtype=np.int64))
+    sl, sg = _segments(segments)
+    out = np.zeros(len(off), dtype=np.int64)
+    _check("rec_attn_compress_lengths",
+           lib().rec_attn_compress_lengths(len(off) - 1, _ptr(off), _ptr(hb), _ptr(hl), len(sl), _ptr(sl), _ptr(sg),
+                                           _ptr(out)))
+    return out
+
+
+def rec_attn_compress(offsets_host, hist_begin, hist_len, segments, x, timestamps, types, x_out, t_out, ty_out,
+                      stream=None) -> None:
+    """History compression of device rows x [T, width] (bf16 or float32) into x_out."""
+    off = np.ascontiguousarray(np.asarray(offsets_host, dtype=np.int64))
+    hb = np.ascontiguousarray(np.asarray(hist_begin, dtype=np.int64))
+    hl = np.ascontiguousarray(np.asarray(hist_len, dtype=np.int64))
+    sl, sg = _segments(segments)
+    import torch
+    dtype = BF16 if x.dtype == torch.bfloat16 else FP32
+    width = x[0].numel() if x.shape[0] > 0 else int(np.prod(x.shape[1:]))
+    code = lib().rec_attn_compress(len(off) - 1, _ptr(off), _ptr(hb), _ptr(hl), len(sl), _ptr(sl), _ptr(sg), dtype,
+                                   int(width), _ptr(x), _ptr(timestamps), _ptr(types), _ptr(x_out), _ptr(t_out),
+                                   _ptr(ty_out), _stream(stream))
+    _check("rec_attn_compress", code)
 
 
 def rec_attn_free(plan: Plan) -> None:

@@ -527,6 +527,107 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   return from_cuda(launch_attn_bwd(a, p.dtype, p.head_dim, plan->NT, st));
 }
 
+namespace {
+
+// Output lengths of history compression (host arithmetic, checked): per request, the
+// groups of each recency segment, ceil(covered / group).
+rec_attn_status compress_layout(int32_t batch, const int64_t* offsets_host, const int64_t* hist_begin_host,
+                                const int64_t* hist_len_host, int32_t n_segments, const int64_t* seg_len,
+                                const int32_t* seg_group, std::vector<CompressReq>* reqs, int64_t* out_offsets) {
+  if (batch < 0 || (batch > 0 && (!offsets_host || !hist_begin_host || !hist_len_host)))
+    return REC_ATTN_ERR_INVALID_ARG;
+  if (n_segments < 1 || n_segments > kMaxSegments || !seg_len || !seg_group) return REC_ATTN_ERR_INVALID_ARG;
+  bool unbounded = false;
+  for (int i = 0; i < n_segments; ++i) {
+    if (seg_group[i] < 1) return REC_ATTN_ERR_INVALID_ARG;
+    if (seg_len[i] < 0) unbounded = true;
+  }
+  if (batch > 0 && offsets_host[0] != 0) return REC_ATTN_ERR_INVALID_ARG;
+  long long out = 0;
+  if (out_offsets) out_offsets[0] = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const long long len = offsets_host[b + 1] - offsets_host[b];
+    const long long hb = hist_begin_host[b], hl = hist_len_host[b];
+    if (len < 0 || hb < 0 || hl < 0 || hb + hl > len) return REC_ATTN_ERR_INVALID_ARG;
+    long long covered = 0, groups = 0;
+    for (int i = 0; i < n_segments && covered < hl; ++i) {
+      const long long room = hl - covered;
+      const long long m = (seg_len[i] < 0 || seg_len[i] > room) ? room : seg_len[i];
+      groups += (m + seg_group[i] - 1) / seg_group[i];
+      covered += m;
+    }
+    if (covered < hl && !unbounded) return REC_ATTN_ERR_INVALID_ARG;  // the segments must cover the history
+    CompressReq r;
+    r.in_start = offsets_host[b]; r.len = len; r.hist_begin = hb; r.hist_len = hl;
+    r.out_start = out; r.out_len = len - hl + groups;
+    out += r.out_len;
+    if (reqs) reqs->push_back(r);
+    if (out_offsets) out_offsets[b + 1] = out;
+  }
+  return REC_ATTN_OK;
+}
+
+}  // namespace
+
+REC_ATTN_API rec_attn_status rec_attn_compress_lengths(int32_t batch, const int64_t* offsets_host,
+                                                       const int64_t* hist_begin_host, const int64_t* hist_len_host,
+                                                       int32_t n_segments, const int64_t* seg_len,
+                                                       const int32_t* seg_group, int64_t* out_offsets_host) {
+  if (!out_offsets_host) return REC_ATTN_ERR_INVALID_ARG;
+  return compress_layout(batch, offsets_host, hist_begin_host, hist_len_host, n_segments, seg_len, seg_group,
+                         nullptr, out_offsets_host);
+}
+
+REC_ATTN_API rec_attn_status rec_attn_compress(int32_t batch, const int64_t* offsets_host,
+                                               const int64_t* hist_begin_host, const int64_t* hist_len_host,
+                                               int32_t n_segments, const int64_t* seg_len, const int32_t* seg_group,
+                                               int32_t dtype, int64_t width, const void* x,
+                                               const int64_t* timestamps, const int8_t* types, void* x_out,
+                                               int64_t* timestamps_out, int8_t* types_out, void* stream) {
+  if (dtype != REC_ATTN_BF16 && dtype != REC_ATTN_FP32) return REC_ATTN_ERR_INVALID_ARG;
+  const size_t elem = dtype == REC_ATTN_BF16 ? 2 : 4;
+  if (width < 1 || ((size_t)width * elem) % 16 != 0) return REC_ATTN_ERR_INVALID_ARG;
+  std::vector<CompressReq> reqs;
+  reqs.reserve((size_t)(batch > 0 ? batch : 0));
+  rec_attn_status stt = compress_layout(batch, offsets_host, hist_begin_host, hist_len_host, n_segments, seg_len,
+                                        seg_group, &reqs, nullptr);
+  if (stt != REC_ATTN_OK) return stt;
+  const long long rows_out = reqs.empty() ? 0 : reqs.back().out_start + reqs.back().out_len;
+  const long long rows_in = batch > 0 ? offsets_host[batch] : 0;
+  if (rows_out == 0) return REC_ATTN_OK;
+  const void* ptrs[5] = {x, timestamps, types, x_out, timestamps_out};
+  for (const void* p : ptrs)
+    if (!p) return REC_ATTN_ERR_INVALID_ARG;
+  if (!types_out || (reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_out) & 15u) ||
+      (reinterpret_cast<uintptr_t>(timestamps) & 7u) || (reinterpret_cast<uintptr_t>(timestamps_out) & 7u))
+    return REC_ATTN_ERR_INVALID_ARG;
+  if (overlaps(x_out, (size_t)rows_out * width * elem, x, (size_t)rows_in * width * elem))
+    return REC_ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  cudaMemPool_t pool;
+  if (e == cudaSuccess) e = pool_for(dev, &pool);
+  void* dreq = nullptr;
+  const size_t req_bytes = sizeof(CompressReq) * reqs.size();
+  if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&dreq, req_bytes, pool, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  // pageable source: the copy is staged before the call returns, so reqs may go away
+  e = cudaMemcpyAsync(dreq, reqs.data(), req_bytes, cudaMemcpyHostToDevice, st);
+  CompressArgs a;
+  a.req = static_cast<const CompressReq*>(dreq);
+  a.batch = batch; a.n_seg = n_segments; a.rows_out = rows_out;
+  for (int i = 0; i < kMaxSegments; ++i) {
+    a.seg_len[i] = i < n_segments ? seg_len[i] : 0;
+    a.seg_group[i] = i < n_segments ? seg_group[i] : 1;
+  }
+  a.width = width; a.x = x; a.t = reinterpret_cast<const long long*>(timestamps); a.ty = types;
+  a.x_out = x_out; a.t_out = reinterpret_cast<long long*>(timestamps_out); a.ty_out = types_out;
+  if (e == cudaSuccess) e = launch_compress(a, dtype, st);
+  cudaError_t e2 = cudaFreeAsync(dreq, st);
+  return from_cuda(e != cudaSuccess ? e : e2);
+}
+
 REC_ATTN_API void rec_attn_free(rec_attn_plan_t* plan) {
   if (!plan) return;
   if (plan->ws) {

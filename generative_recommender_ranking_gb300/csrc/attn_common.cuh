@@ -79,7 +79,13 @@ struct FusedArgs {
   const void* k_gate;
 };
 
-__device__ __forceinline__ float sigmoidf_fast(float x) { return 1.f / (1.f + __expf(-x)); }
+// sigmoid(x) = (1 + tanh(x / 2)) / 2, one hardware tanh (relative error about 2^-11,
+// below the bf16 rounding that follows) and one FMA.
+__device__ __forceinline__ float sigmoidf_fast(float x) {
+  float th;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * x));
+  return fmaf(0.5f, th, 0.5f);
+}
 
 // One work item: (query tile, head).
 struct WorkItem {

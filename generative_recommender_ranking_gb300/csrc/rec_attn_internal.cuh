@@ -71,6 +71,29 @@ struct PlanDev {
   unsigned long long* pairs;  // [1]: visible-pair counter
 };
 
+// History compression: one request of the batch, and the kernel arguments.
+constexpr int kMaxSegments = 8;
+struct CompressReq {
+  long long in_start, len;         // input rows of the request
+  long long hist_begin, hist_len;  // request-local history range
+  long long out_start, out_len;    // output rows of the request
+};
+struct CompressArgs {
+  const CompressReq* req;
+  int batch;
+  int n_seg;
+  long long rows_out;
+  long long seg_len[kMaxSegments];  // recency segments from the newest (< 0: the rest)
+  int seg_group[kMaxSegments];
+  long long width;                  // elements per row
+  const void* x;
+  const long long* t;
+  const int8_t* ty;
+  void* x_out;
+  long long* t_out;
+  int8_t* ty_out;
+};
+
 // Record a device-side error; the first error wins.
 __device__ __forceinline__ void set_status(int* st, int code) { atomicCAS(st, 0, code); }
 

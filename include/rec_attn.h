@@ -247,6 +247,40 @@ rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, const void* k
                              void* dv, void* stream);
 
 /*
+ * History compression (LazFormer review page, Eq. 16-18 and Table 6; TM20K review page,
+ * PATM and LPTM): in request b the history rows [hist_begin[b], hist_begin[b] +
+ * hist_len[b]) (request-local, time-ordered) are replaced by sums of groups of
+ * consecutive rows.  Recency segment i (i = 0 the newest) covers the next seg_len[i]
+ * history rows going back in time (seg_len[i] < 0: all the rest) in groups of
+ * seg_group[i] >= 1; the oldest group of a segment is the partial one.  The segments
+ * must cover every history (an unbounded one does).  Output rows keep time order:
+ * the rows before the history, the merged groups (oldest first; timestamp = the latest
+ * member's, type REC_ATTN_HIST), the rows after it.  Examples: LazFormer "keep 1024,
+ * groups of 8" is {(1024, 1), (-1, 8)}; LPTM is {(-1, 2)}; PATM's four position bands
+ * are {(1000, 1), (4000, 2), (5000, 3), (-1, 4)}.  At most 8 segments.
+ *
+ * rec_attn_compress_lengths -- host only: out_offsets_host[0..batch] of the output.
+ * rec_attn_compress -- x: device [T][width] rows in dtype (width * element size a
+ *   multiple of 16 bytes, 16-byte aligned); timestamps int64 [T], types int8 [T];
+ *   x_out / timestamps_out / types_out: device outputs sized by the lengths above (x_out
+ *   may not overlap x).  Sums in fp32, rounded once.  offsets, hist ranges and segments
+ *   are host arrays read during the call; a small request table is staged through the
+ *   library pool on `stream`.  Asynchronous.
+ * Errors: INVALID_ARG (negative or inconsistent ranges, uncovered history, bad segments,
+ * alignment, NULL pointers), CUDA.
+ */
+rec_attn_status rec_attn_compress_lengths(int32_t batch, const int64_t* offsets_host,
+                                          const int64_t* hist_begin_host, const int64_t* hist_len_host,
+                                          int32_t n_segments, const int64_t* seg_len,
+                                          const int32_t* seg_group, int64_t* out_offsets_host);
+rec_attn_status rec_attn_compress(int32_t batch, const int64_t* offsets_host,
+                                  const int64_t* hist_begin_host, const int64_t* hist_len_host,
+                                  int32_t n_segments, const int64_t* seg_len, const int32_t* seg_group,
+                                  int32_t dtype, int64_t width, const void* x, const int64_t* timestamps,
+                                  const int8_t* types, void* x_out, int64_t* timestamps_out,
+                                  int8_t* types_out, void* stream);
+
+/*
  * rec_attn_free -- release a plan (NULL-safe).  The workspace returns to the
  * library pool in stream order on the stream of the plan's last use (after the
  * planning work), so work already enqueued there may still run; callers that used
