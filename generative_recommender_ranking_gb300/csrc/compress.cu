@@ -26,7 +26,6 @@ template <typename E>
 struct Vec;
 template <>
 struct Vec<__nv_bfloat16> {
-  static constexpr int kElems = 8;
   static __device__ __forceinline__ void add(const void* p, float (&acc)[8]) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -49,7 +48,6 @@ struct Vec<__nv_bfloat16> {
 };
 template <>
 struct Vec<float> {
-  static constexpr int kElems = 4;
   static __device__ __forceinline__ void add(const void* p, float (&acc)[8]) {
     const float4 v = *reinterpret_cast<const float4*>(p);
     acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
