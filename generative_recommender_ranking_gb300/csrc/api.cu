@@ -272,6 +272,13 @@ rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queri
   e = cudaMemsetAsync(w + lay.hdr, 0, 256, plan->side);
   if (e == cudaSuccess && batch > 0)
     e = cudaMemcpyAsync(pd.meta, meta.data(), sizeof(ReqMeta) * (size_t)batch, cudaMemcpyHostToDevice, plan->side);
+  if (e == cudaSuccess && NT > 0) {
+    // the request of every tile, so the prologue needs no search over the table
+    std::vector<int> treq((size_t)NT);
+    for (int32_t b = 0; b < batch; ++b)
+      for (int i = 0; i < meta[b].ntiles; ++i) treq[(size_t)(meta[b].tile_start + i)] = b;
+    e = cudaMemcpyAsync(pd.treq, treq.data(), sizeof(int) * (size_t)NT, cudaMemcpyHostToDevice, plan->side);
+  }
   if (e == cudaSuccess) e = cudaEventRecord(plan->ev_meta, plan->side);
   if (e == cudaSuccess)
     e = launch_plan(plan->mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t, plan->ty, batch, NT,
@@ -382,7 +389,7 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
     }
     if (e != cudaSuccess) return from_cuda(e);
     RopeArgs ra;
-    ra.meta = plan->pd.meta; ra.batch = plan->batch; ra.t = plan->t;
+    ra.meta = plan->pd.meta; ra.tile_req = plan->pd.treq; ra.batch = plan->batch; ra.t = plan->t;
     ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
     ra.heads = p.num_heads; ra.head_dim = p.head_dim;
     std::memcpy(ra.omega, plan->omega, sizeof ra.omega);  // all zero without the RoPE
@@ -401,7 +408,7 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
     }
     if (e != cudaSuccess) return from_cuda(e);
     RopeArgs ra;
-    ra.meta = plan->pd.meta; ra.batch = plan->batch; ra.t = plan->t;
+    ra.meta = plan->pd.meta; ra.tile_req = plan->pd.treq; ra.batch = plan->batch; ra.t = plan->t;
     ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
     ra.heads = p.num_heads; ra.head_dim = p.head_dim;
     std::memcpy(ra.omega, plan->omega, sizeof ra.omega);
@@ -506,7 +513,7 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
     e = cudaStreamWaitEvent(st, plan->ev_meta, 0);
     if (e != cudaSuccess) return from_cuda(e);
     RopeArgs ra;
-    ra.meta = plan->pd.meta; ra.batch = plan->batch; ra.t = plan->t;
+    ra.meta = plan->pd.meta; ra.tile_req = plan->pd.treq; ra.batch = plan->batch; ra.t = plan->t;
     ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
     ra.heads = p.num_heads; ra.head_dim = p.head_dim;
     std::memcpy(ra.omega, plan->omega, sizeof ra.omega);

@@ -32,6 +32,7 @@ struct AttnArgs {
 // Arguments of the time-RoPE prologue.
 struct RopeArgs {
   const ReqMeta* meta;
+  const int* tile_req;     // [NT] request of each tile (uploaded with the request table)
   int batch;               // requests in meta (the prologue needs nothing the planner writes)
   const long long* t;
   const void* q;

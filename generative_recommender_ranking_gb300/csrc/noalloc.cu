@@ -175,6 +175,25 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
     }
     e = cudaMemcpyAsync(pd.meta + b0, chunk, sizeof(ReqMeta) * n, cudaMemcpyHostToDevice, s);
   }
+  // the request of every tile, uploaded the same way
+  {
+    int tchunk[2048];
+    int nfill = 0;
+    long long tdone = 0;
+    for (int32_t b = 0; b < batch && e == cudaSuccess; ++b) {
+      const long long nt = (offsets_host[b + 1] - offsets_host[b] + kTile - 1) / kTile;
+      for (long long i = 0; i < nt && e == cudaSuccess; ++i) {
+        tchunk[nfill++] = b;
+        if (nfill == 2048) {
+          e = cudaMemcpyAsync(pd.treq + tdone, tchunk, sizeof(int) * nfill, cudaMemcpyHostToDevice, s);
+          tdone += nfill;
+          nfill = 0;
+        }
+      }
+    }
+    if (e == cudaSuccess && nfill > 0)
+      e = cudaMemcpyAsync(pd.treq + tdone, tchunk, sizeof(int) * nfill, cudaMemcpyHostToDevice, s);
+  }
   MaskP mask{};
   mask.use_delay = params->use_delay;
   mask.delay = params->use_delay ? params->delay_s : 0;
@@ -190,7 +209,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   const void* ks = k;
   if (params->use_rope) {
     RopeArgs ra;
-    ra.meta = pd.meta; ra.batch = batch; ra.t = t;
+    ra.meta = pd.meta; ra.tile_req = pd.treq; ra.batch = batch; ra.t = t;
     ra.q = q; ra.k = k; ra.qr = w + lay.rq; ra.kr = w + lay.rk;
     ra.heads = params->num_heads; ra.head_dim = params->head_dim;
     for (int i = 0; i < kMaxPairs; ++i)

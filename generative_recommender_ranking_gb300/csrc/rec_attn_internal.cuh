@@ -66,6 +66,7 @@ struct PlanDev {
   int* rorder;          // [B]: requests, most expensive first
   int* roff;            // [B+1]: first item of each request in `items` (in rorder order)
   int* qkeep;           // [B]: query pruning: user tokens before this position compute nothing
+  int* treq;            // [NT]: request of each tile (uploaded with the request table)
   int* counters;        // [8]: plan ticket, attention item counter, attention exit ticket
   int* status;          // [1]: first device error (rec_attn_status)
   unsigned long long* pairs;  // [1]: visible-pair counter

@@ -61,20 +61,7 @@ __global__ void __launch_bounds__(256, 4) k_rope(RopeArgs a) {
   constexpr int kPairs = C::kPairs;
   constexpr int kHeadBatch = 2;
   const long long g = blockIdx.x;
-  // the request owning tile g: the last one whose first tile is <= g (an empty request
-  // shares its first tile index with the next non-empty one, which comes after it)
-  __shared__ int s_req;
-  if (threadIdx.x == 0) {
-    int lo = 0, hi = a.batch;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (a.meta[mid].tile_start <= g) lo = mid;
-      else hi = mid;
-    }
-    s_req = lo;
-  }
-  __syncthreads();
-  const ReqMeta m = a.meta[s_req];
+  const ReqMeta m = a.meta[a.tile_req[g]];
   const int tl = (int)(g - m.tile_start);
   const long long t_ref = a.t[m.tok_start];
   const int chunks = a.head_dim / (2 * kPairs);
@@ -161,18 +148,7 @@ __global__ void __launch_bounds__(256, 4) k_rope_fused(RopeArgs a, FusedArgs f) 
   using C = Chunk<E>;
   constexpr int kPairs = C::kPairs;
   const long long g = blockIdx.x;
-  __shared__ int s_req;
-  if (threadIdx.x == 0) {
-    int lo = 0, hi = a.batch;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (a.meta[mid].tile_start <= g) lo = mid;
-      else hi = mid;
-    }
-    s_req = lo;
-  }
-  __syncthreads();
-  const ReqMeta m = a.meta[s_req];
+  const ReqMeta m = a.meta[a.tile_req[g]];
   const int tl = (int)(g - m.tile_start);
   const long long t_ref = a.t[m.tok_start];
   const int chunks = a.head_dim / (2 * kPairs);

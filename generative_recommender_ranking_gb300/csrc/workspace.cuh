@@ -9,7 +9,7 @@
 namespace recattn {
 
 struct WsLayout {
-  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, it, rc, ro, rf, qk, rq, rk, total;
+  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, it, rc, ro, rf, qk, tr, rq, rk, total;
 };
 
 inline size_t ws_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -32,6 +32,7 @@ inline WsLayout ws_layout(long long batch, long long NT, long long NC, long long
   L.ro = off; off = ws_up(off + 4 * (size_t)batch);
   L.rf = off; off = ws_up(off + 4 * ((size_t)batch + 1));
   L.qk = off; off = ws_up(off + 4 * (size_t)batch);
+  L.tr = off; off = ws_up(off + 4 * (size_t)NT);
   L.rq = off; off = ws_up(off + rot_bytes);
   L.rk = off; off = ws_up(off + rot_bytes);
   L.total = off;
@@ -56,6 +57,7 @@ inline PlanDev ws_bind(char* w, const WsLayout& L) {
   pd.rorder = reinterpret_cast<int*>(w + L.ro);
   pd.roff = reinterpret_cast<int*>(w + L.rf);
   pd.qkeep = reinterpret_cast<int*>(w + L.qk);
+  pd.treq = reinterpret_cast<int*>(w + L.tr);
   return pd;
 }
 
