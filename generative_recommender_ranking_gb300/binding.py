@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
         L.rec_attn_compress_lengths.restype = ctypes.c_int
         L.rec_attn_compress.argtypes = [i32, vp, vp, vp, i32, vp, vp, i32, i64, vp, vp, vp, vp, vp, vp, vp]
         L.rec_attn_compress.restype = ctypes.c_int
+        L.rec_attn_check_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.POINTER(i32), vp]
+        L.rec_attn_check_wait_timeout.restype = ctypes.c_int
         L.rec_attn_free.argtypes = [vp]
         L.rec_attn_free.restype = None
         L.rec_attn_tile_classes.argtypes = [vp, vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]
@@ -253,6 +255,15 @@ def rec_attn_compress(offsets_host, hist_begin, hist_len, segments, x, timestamp
                                    int(width), _ptr(x), _ptr(timestamps), _ptr(types), _ptr(x_out), _ptr(t_out),
                                    _ptr(ty_out), _stream(stream))
     _check("rec_attn_compress", code)
+
+
+def rec_attn_check_wait_timeout(limit_ms: int = 50, stream=None) -> int:
+    """Run the kernels' bounded wait on a barrier nothing arrives at; returns the
+    status word it wrote (ERR_TIMEOUT when the failure detection works)."""
+    st = ctypes.c_int32()
+    _check("rec_attn_check_wait_timeout", lib().rec_attn_check_wait_timeout(int(limit_ms), ctypes.byref(st),
+                                                                             _stream(stream)))
+    return int(st.value)
 
 
 def rec_attn_free(plan: Plan) -> None:

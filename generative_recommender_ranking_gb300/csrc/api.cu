@@ -635,6 +635,29 @@ REC_ATTN_API rec_attn_status rec_attn_compress(int32_t batch, const int64_t* off
   return from_cuda(e != cudaSuccess ? e : e2);
 }
 
+REC_ATTN_API rec_attn_status rec_attn_check_wait_timeout(uint32_t limit_ms, int32_t* status_out, void* stream) {
+  if (!status_out || limit_ms < 1 || limit_ms > 10000) return REC_ATTN_ERR_INVALID_ARG;
+  *status_out = REC_ATTN_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  cudaMemPool_t pool;
+  if (e == cudaSuccess) e = pool_for(dev, &pool);
+  void* d = nullptr;
+  if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&d, sizeof(int), pool, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  int h = 0;
+  e = cudaMemsetAsync(d, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = launch_wait_timeout(static_cast<int*>(d), (unsigned long long)limit_ms * 1000000ull, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof(int), cudaMemcpyDeviceToHost, st);
+  cudaError_t e2 = cudaFreeAsync(d, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = e2;
+  if (e != cudaSuccess) return from_cuda(e);
+  *status_out = h;
+  return REC_ATTN_OK;
+}
+
 REC_ATTN_API void rec_attn_free(rec_attn_plan_t* plan) {
   if (!plan) return;
   if (plan->ws) {

@@ -34,6 +34,7 @@
 
 #include "attn_common.cuh"
 #include "ptx_sm103.cuh"
+#include "wait.cuh"
 
 namespace recattn {
 
@@ -144,19 +145,7 @@ struct SBars {
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (ptx::globaltimer() - t0 > kWaitNs) {
-      *abort_flag = 1;
-      set_status(status, REC_ATTN_ERR_TIMEOUT);
-      return false;
-    }
-  }
+  return bounded_wait(bar, parity, abort_flag, status, kWaitNs);
 }
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = ptx::globaltimer();

@@ -21,7 +21,10 @@ template <>
 struct Chunk<__nv_bfloat16> {
   static constexpr int kPairs = 4;
   static __device__ __forceinline__ void load(const void* p, float (&x)[8]) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    unpack(*reinterpret_cast<const uint4*>(p), x);
+  }
+  // the 16 raw bytes of a chunk, as values
+  static __device__ __forceinline__ void unpack(const uint4 v, float (&x)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -44,8 +47,10 @@ template <>
 struct Chunk<float> {
   static constexpr int kPairs = 2;
   static __device__ __forceinline__ void load(const void* p, float (&x)[8]) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    unpack(*reinterpret_cast<const uint4*>(p), x);
+  }
+  static __device__ __forceinline__ void unpack(const uint4 v, float (&x)[8]) {
+    x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y); x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
   }
   static __device__ __forceinline__ void store(void* p, const float (&x)[8]) {
     *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
@@ -54,12 +59,12 @@ struct Chunk<float> {
 
 // One block per global tile.  Thread work unit: one token and one 16-byte chunk of
 // its head row, for every head, so each angle's sin/cos is computed once per token;
-// heads are processed two at a time with all loads issued before any store.
+// heads are processed four at a time with the eight 16-byte loads in flight together
+// (kept raw until used, so the registers stay within the four-blocks-per-SM budget).
 template <typename E>
 __global__ void __launch_bounds__(256, 4) k_rope(RopeArgs a) {
   using C = Chunk<E>;
   constexpr int kPairs = C::kPairs;
-  constexpr int kHeadBatch = 2;
   const long long g = blockIdx.x;
   const ReqMeta m = a.meta[a.tile_req[g]];
   const int tl = (int)(g - m.tile_start);
@@ -79,31 +84,31 @@ __global__ void __launch_bounds__(256, 4) k_rope(RopeArgs a) {
 #pragma unroll
     for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
     const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
-    for (int h0 = 0; h0 < a.heads; h0 += kHeadBatch) {
-      float x[kHeadBatch][8], y[kHeadBatch][8];
+    for (int h0 = 0; h0 < a.heads; h0 += 4) {
+      uint4 rq[4], rk[4];  // raw 16-byte chunks of four heads, all loads in flight together
 #pragma unroll
-      for (int u = 0; u < kHeadBatch; ++u)
+      for (int u = 0; u < 4; ++u)
         if (h0 + u < a.heads) {
-          C::load(q + row0 + (h0 + u) * head_bytes, x[u]);
-          C::load(k + row0 + (h0 + u) * head_bytes, y[u]);
+          rq[u] = *reinterpret_cast<const uint4*>(q + row0 + (h0 + u) * head_bytes);
+          rk[u] = *reinterpret_cast<const uint4*>(k + row0 + (h0 + u) * head_bytes);
         }
 #pragma unroll
-      for (int u = 0; u < kHeadBatch; ++u) {
+      for (int u = 0; u < 4; ++u) {
+        if (h0 + u >= a.heads) break;
+        float x[8], y[8];
+        C::unpack(rq[u], x);
+        C::unpack(rk[u], y);
 #pragma unroll
         for (int p = 0; p < kPairs; ++p) {
-          const float x0 = x[u][2 * p], x1 = x[u][2 * p + 1], y0 = y[u][2 * p], y1 = y[u][2 * p + 1];
-          x[u][2 * p] = x0 * cs[p] - x1 * sn[p];
-          x[u][2 * p + 1] = x0 * sn[p] + x1 * cs[p];
-          y[u][2 * p] = y0 * cs[p] - y1 * sn[p];
-          y[u][2 * p + 1] = y0 * sn[p] + y1 * cs[p];
+          const float x0 = x[2 * p], x1 = x[2 * p + 1], y0 = y[2 * p], y1 = y[2 * p + 1];
+          x[2 * p] = x0 * cs[p] - x1 * sn[p];
+          x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
+          y[2 * p] = y0 * cs[p] - y1 * sn[p];
+          y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
         }
+        C::store(qr + row0 + (h0 + u) * head_bytes, x);
+        C::store(kr + row0 + (h0 + u) * head_bytes, y);
       }
-#pragma unroll
-      for (int u = 0; u < kHeadBatch; ++u)
-        if (h0 + u < a.heads) {
-          C::store(qr + row0 + (h0 + u) * head_bytes, x[u]);
-          C::store(kr + row0 + (h0 + u) * head_bytes, y[u]);
-        }
     }
   }
 }
@@ -144,7 +149,7 @@ __device__ __forceinline__ void norm_gate(float (&x)[8], bool act, const float* 
 // a warp runs every iteration (inactive lanes carry zeros), so the row sums can use
 // warp shuffles over the lanes of one row.
 template <typename E>
-__global__ void __launch_bounds__(256, 4) k_rope_fused(RopeArgs a, FusedArgs f) {
+__global__ void __launch_bounds__(256, 3) k_rope_fused(RopeArgs a, FusedArgs f) {
   using C = Chunk<E>;
   constexpr int kPairs = C::kPairs;
   const long long g = blockIdx.x;
@@ -167,31 +172,46 @@ __global__ void __launch_bounds__(256, 4) k_rope_fused(RopeArgs a, FusedArgs f) 
     for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
     const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
     const bool qg = f.q_gate != nullptr, kg = f.k_gate != nullptr;
-    for (int h = 0; h < a.heads; ++h) {
-      const long long off = row0 + h * head_bytes;
-      float x[8], y[8], gx[8], gy[8];
+    // two heads at a time: their q, k and gate chunks (up to eight 16-byte loads) in flight
+    // together, kept raw until used
+    for (int h0 = 0; h0 < a.heads; h0 += 2) {
+      uint4 rq[2], rk[2], rgq[2], rgk[2];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = y[e] = gx[e] = gy[e] = 0.f;
-      if (act) {  // every load of the head row chunk before any arithmetic
-        C::load(static_cast<const char*>(a.q) + off, x);
-        C::load(static_cast<const char*>(a.k) + off, y);
-        if (qg) C::load(static_cast<const char*>(f.q_gate) + off, gx);
-        if (kg) C::load(static_cast<const char*>(f.k_gate) + off, gy);
+      for (int u = 0; u < 2; ++u) {
+        rq[u] = rk[u] = rgq[u] = rgk[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (act && h0 + u < a.heads) {
+          const long long off = row0 + (h0 + u) * head_bytes;
+          rq[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.q) + off);
+          rk[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.k) + off);
+          if (qg) rgq[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(f.q_gate) + off);
+          if (kg) rgk[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(f.k_gate) + off);
+        }
       }
-      const int e0 = h * a.head_dim + c * 2 * kPairs;
-      norm_gate<E>(x, act, f.q_norm_w, f.eps, qg, gx, e0, chunks, a.head_dim);
-      norm_gate<E>(y, act, f.k_norm_w, f.eps, kg, gy, e0, chunks, a.head_dim);
 #pragma unroll
-      for (int p = 0; p < kPairs; ++p) {
-        const float x0 = x[2 * p], x1 = x[2 * p + 1], y0 = y[2 * p], y1 = y[2 * p + 1];
-        x[2 * p] = x0 * cs[p] - x1 * sn[p];
-        x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
-        y[2 * p] = y0 * cs[p] - y1 * sn[p];
-        y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
-      }
-      if (act) {
-        C::store(static_cast<char*>(a.qr) + off, x);
-        C::store(static_cast<char*>(a.kr) + off, y);
+      for (int u = 0; u < 2; ++u) {
+        if (h0 + u >= a.heads) break;  // uniform across the block
+        const int h = h0 + u;
+        const long long off = row0 + h * head_bytes;
+        float x[8], y[8], gx[8], gy[8];
+        C::unpack(rq[u], x);
+        C::unpack(rk[u], y);
+        C::unpack(rgq[u], gx);
+        C::unpack(rgk[u], gy);
+        const int e0 = h * a.head_dim + c * 2 * kPairs;
+        norm_gate<E>(x, act, f.q_norm_w, f.eps, qg, gx, e0, chunks, a.head_dim);
+        norm_gate<E>(y, act, f.k_norm_w, f.eps, kg, gy, e0, chunks, a.head_dim);
+#pragma unroll
+        for (int p = 0; p < kPairs; ++p) {
+          const float x0 = x[2 * p], x1 = x[2 * p + 1], y0 = y[2 * p], y1 = y[2 * p + 1];
+          x[2 * p] = x0 * cs[p] - x1 * sn[p];
+          x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
+          y[2 * p] = y0 * cs[p] - y1 * sn[p];
+          y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
+        }
+        if (act) {
+          C::store(static_cast<char*>(a.qr) + off, x);
+          C::store(static_cast<char*>(a.kr) + off, y);
+        }
       }
     }
   }

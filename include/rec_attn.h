@@ -281,6 +281,18 @@ rec_attn_status rec_attn_compress(int32_t batch, const int64_t* offsets_host,
                                   int8_t* types_out, void* stream);
 
 /*
+ * rec_attn_check_wait_timeout -- self-check of the failure detection inside the
+ * pipelined kernels (the pages have no counterpart: it guards this implementation).
+ * Every wait of a kernel on an mbarrier is bounded; on expiry it records
+ * REC_ATTN_ERR_TIMEOUT in the status word and the CTA stops instead of hanging.  This
+ * call runs the same wait on a barrier that nothing arrives at, with a limit of
+ * limit_ms (1..10000), and returns the status word the kernel wrote in *status_out
+ * (REC_ATTN_ERR_TIMEOUT when the mechanism works).  The device stays usable.
+ * Synchronizes `stream`.  Errors: INVALID_ARG, CUDA.
+ */
+rec_attn_status rec_attn_check_wait_timeout(uint32_t limit_ms, int32_t* status_out, void* stream);
+
+/*
  * rec_attn_free -- release a plan (NULL-safe).  The workspace returns to the
  * library pool in stream order on the stream of the plan's last use (after the
  * planning work), so work already enqueued there may still run; callers that used

@@ -100,6 +100,10 @@ def test_null_plan_calls(L):
     s = ctypes.c_int32()
     assert L.rec_attn_device_status(None, ctypes.byref(s)) == bd.ERR_INVALID_ARG
     L.rec_attn_free(None)  # NULL-safe
+    st = ctypes.c_int32()
+    assert L.rec_attn_check_wait_timeout(0, ctypes.byref(st), None) == bd.ERR_INVALID_ARG
+    assert L.rec_attn_check_wait_timeout(20000, ctypes.byref(st), None) == bd.ERR_INVALID_ARG
+    assert L.rec_attn_check_wait_timeout(50, None, None) == bd.ERR_INVALID_ARG
 
 
 def test_valid_plan_without_gpu_reports_cuda_error(L):

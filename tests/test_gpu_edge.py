@@ -147,3 +147,16 @@ def test_longest_request_sampled():
         assert bd.rec_attn_device_status(plan) == bd.OK
     finally:
         bd.rec_attn_free(plan)
+
+
+def test_bounded_wait_times_out_and_the_device_stays_usable():
+    # the kernels' bounded mbarrier wait, on a barrier nothing arrives at, must give up
+    # with REC_ATTN_ERR_TIMEOUT in the status word after its limit (50 ms here)
+    assert bd.rec_attn_check_wait_timeout(50) == bd.ERR_TIMEOUT
+    w = W.sort(batch=1, n_hist=200, n_cand=10, window=64)
+    out, _, plan = gu.run_gpu(w)
+    try:
+        assert bd.rec_attn_device_status(plan) == bd.OK
+        assert not torch.isnan(out).any()
+    finally:
+        bd.rec_attn_free(plan)
