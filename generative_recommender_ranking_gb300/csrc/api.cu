@@ -270,14 +270,15 @@ rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queri
     return from_cuda(e);
   }
   e = cudaMemsetAsync(w + lay.hdr, 0, 256, plan->side);
-  if (e == cudaSuccess && batch > 0)
-    e = cudaMemcpyAsync(pd.meta, meta.data(), sizeof(ReqMeta) * (size_t)batch, cudaMemcpyHostToDevice, plan->side);
-  if (e == cudaSuccess && NT > 0) {
-    // the request of every tile, so the prologue needs no search over the table
-    std::vector<int> treq((size_t)NT);
+  if (e == cudaSuccess && batch > 0) {
+    // the request table and the request of every tile (so the prologue needs no search),
+    // laid out as in the workspace and uploaded in one copy
+    std::vector<char> up(lay.tr - lay.meta + sizeof(int) * (size_t)NT);
+    std::memcpy(up.data(), meta.data(), sizeof(ReqMeta) * (size_t)batch);
+    int* treq = reinterpret_cast<int*>(up.data() + (lay.tr - lay.meta));
     for (int32_t b = 0; b < batch; ++b)
-      for (int i = 0; i < meta[b].ntiles; ++i) treq[(size_t)(meta[b].tile_start + i)] = b;
-    e = cudaMemcpyAsync(pd.treq, treq.data(), sizeof(int) * (size_t)NT, cudaMemcpyHostToDevice, plan->side);
+      for (int i = 0; i < meta[b].ntiles; ++i) treq[meta[b].tile_start + i] = b;
+    e = cudaMemcpyAsync(pd.meta, up.data(), up.size(), cudaMemcpyHostToDevice, plan->side);
   }
   if (e == cudaSuccess) e = cudaEventRecord(plan->ev_meta, plan->side);
   if (e == cudaSuccess)

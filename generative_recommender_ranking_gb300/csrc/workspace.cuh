@@ -20,6 +20,7 @@ inline WsLayout ws_layout(long long batch, long long NT, long long NC, long long
   size_t off = 0;
   L.hdr = off; off = ws_up(off + 256);
   L.meta = off; off = ws_up(off + sizeof(ReqMeta) * (size_t)batch);
+  L.tr = off; off = ws_up(off + 4 * (size_t)NT);  // right after the table: both go up in one copy
   L.box = off; off = ws_up(off + sizeof(TileBox) * kTypes * (size_t)NT);
   L.rec = off; off = ws_up(off + sizeof(KeyTileRec) * (size_t)NT);
   L.cls = off; off = ws_up(off + (size_t)NC);
@@ -32,7 +33,6 @@ inline WsLayout ws_layout(long long batch, long long NT, long long NC, long long
   L.ro = off; off = ws_up(off + 4 * (size_t)batch);
   L.rf = off; off = ws_up(off + 4 * ((size_t)batch + 1));
   L.qk = off; off = ws_up(off + 4 * (size_t)batch);
-  L.tr = off; off = ws_up(off + 4 * (size_t)NT);
   L.rq = off; off = ws_up(off + rot_bytes);
   L.rk = off; off = ws_up(off + rot_bytes);
   L.total = off;

@@ -160,3 +160,28 @@ def test_bounded_wait_times_out_and_the_device_stays_usable():
         assert not torch.isnan(out).any()
     finally:
         bd.rec_attn_free(plan)
+
+
+@pytest.mark.parametrize("case", ["sorted", "unsorted_within_tile", "unsorted_across_tiles", "interleaved_types"])
+def test_time_clauses_with_and_without_sorted_runs(case):
+    # The planner turns a time clause into a position bound only when the key type's
+    # tokens form one contiguous run with non-decreasing times; every other layout
+    # must take the per-key time path and give the same result as the oracle.
+    rng = np.random.default_rng(21)
+    lengths = [300, 260]
+    T = sum(lengths)
+    t = W.EPOCH + np.sort(rng.integers(0, 30 * 86400, size=T)).astype(np.int64)
+    types = np.full(T, W.HIST, dtype=np.int8)
+    for b, (s, n) in enumerate(zip([0, 300], lengths)):
+        types[s + n - 40:s + n - 20] = W.RT
+        types[s + n - 20:s + n] = W.CAND
+        t[s + n - 20:s + n] = t[s + n - 21] + 10
+    if case == "unsorted_within_tile":
+        t[10], t[11] = t[11] + 7200, t[10]
+    elif case == "unsorted_across_tiles":
+        t[127], t[128] = t[128] + 7200, t[127]
+    elif case == "interleaved_types":
+        types[50:60] = W.RT  # real-time events inside the history: RT no longer one run
+    w = _custom(lengths, t=t, types=types, mask=dict(use_delay=True, delay_s=3600, window=0,
+                                                     hist_bidirectional=False))
+    _check_all(w)
