@@ -42,7 +42,7 @@ COMPRESS_SPECS = {
     "patm_bands": [(1000, 1), (4000, 2), (5000, 3), (-1, 4)],
 }
 # CUDA-core fp32 peak of a GB300 from its unit counts: 152 SMs x 128 FMA lanes x 2 FLOP
-# x 2070 MHz (the backward pass runs there)
+# x 2070 MHz (the fp32 backward pass runs there)
 FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
@@ -469,16 +469,26 @@ def run_ours(args):
                 "kernel": "k_attn_tc (masked softmax attention)", "peak_source": pk["source"],
                 "algorithmic_flops_per_launch": flops_fwd, "ms_per_launch": attn_ms}
     if args.backward:
-        # the backward kernels dominate the step; they run on the CUDA cores in fp32
-        fp32_peak = FP32_FMA_PEAK_TFLOPS
+        # the backward kernels dominate the step: bf16 runs on the tensor cores (dQ and
+        # dK/dV modes of k_bwd_tc), fp32 on the CUDA cores
         bwd_tflops = 2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12
-        roof = {"bound": "alu", "achieved": bwd_tflops, "peak": fp32_peak, "unit": "TFLOP/s",
-                "frac": bwd_tflops / fp32_peak, "traffic": None,
-                "kernel": "k_bwd_delta + k_bwd_dq + k_bwd_dkv (backward, CUDA cores, fp32)",
-                "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2070 MHz",
-                "algorithmic_flops_per_launch": 2.5 * flops_fwd, "ms_per_launch": bwd_ms,
-                "forward_attention": {"achieved": attn_tflops, "unit": "TFLOP/s",
-                                      "frac": attn_tflops / pk["bf16_tflops"], "ms_per_launch": attn_ms}}
+        fwd_part = {"achieved": attn_tflops, "unit": "TFLOP/s", "frac": attn_tflops / pk["bf16_tflops"],
+                    "ms_per_launch": attn_ms}
+        if bf16:
+            roof = {"bound": "tensor", "achieved": bwd_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": bwd_tflops / pk["bf16_tflops"], "traffic": None,
+                    "kernel": "k_bwd_delta + k_bwd_tc<dQ> + k_bwd_tc<dK,dV> (backward, tensor cores)",
+                    "peak_source": pk["source"],
+                    "algorithmic_flops_per_launch": 2.5 * flops_fwd, "ms_per_launch": bwd_ms,
+                    "forward_attention": fwd_part}
+        else:
+            fp32_peak = FP32_FMA_PEAK_TFLOPS
+            roof = {"bound": "alu", "achieved": bwd_tflops, "peak": fp32_peak, "unit": "TFLOP/s",
+                    "frac": bwd_tflops / fp32_peak, "traffic": None,
+                    "kernel": "k_bwd_delta + k_bwd_dq + k_bwd_dkv (backward, CUDA cores, fp32)",
+                    "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2070 MHz",
+                    "algorithmic_flops_per_launch": 2.5 * flops_fwd, "ms_per_launch": bwd_ms,
+                    "forward_attention": fwd_part}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,

@@ -526,13 +526,24 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   if (e != cudaSuccess) return from_cuda(e);
   BwdArgs a;
   a.meta = plan->pd.meta; a.batch = plan->batch; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
+  a.items = plan->pd.items; a.qreq = plan->pd.qreq; a.krec = plan->pd.krec;
+  a.n_items = plan->NT * p.num_heads;
+  a.status = plan->pd.status;
   a.cls = plan->pd.cls; a.t = plan->t; a.ty = plan->ty;
   a.q = qs; a.k = ks; a.v = v; a.out = out; a.dout = dout; a.lse = lse; a.delta = plan->bwd_delta;
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.rows = T * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale;
   a.rotate = p.use_rope; a.mask = plan->mask;
   std::memcpy(a.omega, plan->omega, sizeof a.omega);
-  return from_cuda(launch_attn_bwd(a, p.dtype, p.head_dim, plan->NT, st));
+  e = launch_bwd_delta(a, p.dtype, p.head_dim, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (p.dtype == REC_ATTN_FP32) return from_cuda(launch_attn_bwd_simt(a, p.head_dim, plan->NT, st));
+  CUtensorMap maps[4];  // Q', K', V, dO
+  const void* srcs[4] = {qs, ks, v, dout};
+  const long long cols = (long long)p.num_heads * p.head_dim;
+  for (int i = 0; i < 4; ++i)
+    if (!encode_map(&maps[i], srcs[i], T, cols)) return REC_ATTN_ERR_CUDA;
+  return from_cuda(launch_attn_bwd_tc(a, maps, plan->num_sms, st));
 }
 
 namespace {

@@ -1,5 +1,6 @@
-// attn_bwd.cu -- backward pass of the masked time-RoPE softmax attention (CUDA cores,
-// fp32 arithmetic), for head_dim <= 64.
+// attn_bwd.cu -- backward pass of the masked time-RoPE softmax attention on the CUDA
+// cores (fp32 inputs, head_dim 32 or 64), and the row term D of both backward paths
+// (the bf16 path runs on the tensor cores: attn_bwd_tc.cu).
 //
 // Gradients of O = Softmax(QK^T/sqrt(d) + M) V (TM20K review page, section 2.1;
 // LazFormer review page, Eq. 19-21) through the time-RoPE (CADET review page, time
@@ -10,7 +11,7 @@
 // and dQ = R(t_i)^T dQ', dK = R(t_j)^T dK' (the rotation is orthogonal).
 //
 // Three kernels walk the planner's tile lists, so SKIP tiles cost nothing here either:
-//   k_bwd_delta  D_i per (token, head);
+//   k_bwd_delta  D_i per (token, head), fp32 or bf16 rows;
 //   k_bwd_dq     one block per (query tile, head), d/32 threads per query row, over the
 //                query tile's non-SKIP key tiles (K', V and key metadata staged in
 //                shared memory);
@@ -44,15 +45,12 @@ template <>
 __device__ __forceinline__ void st_elem<float>(void* base, long long i, float x) {
   static_cast<float*>(base)[i] = x;
 }
-template <>
-__device__ __forceinline__ void st_elem<__nv_bfloat16>(void* base, long long i, float x) {
-  static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
-}
 
 // Each row (query or key) is handled by kSplit = D / 32 neighbouring threads; part p
-// of a row holds its dims p, p + kSplit, p + 2 kSplit, ... (32 of them), so the
-// threads of a warp read consecutive shared-memory words and dot products need
-// log2(kSplit) shuffles.
+// of a row holds its 32 contiguous dims [32 p, 32 p + 32), so a thread reads its share
+// of a staged row with 16-byte shared-memory loads (all threads of a part read the same
+// address: a broadcast), a rotation pair never straddles two threads, and dot products
+// need log2(kSplit) shuffles.
 template <int D>
 struct Split {
   static constexpr int kSplit = D / 32;
@@ -67,27 +65,24 @@ __device__ __forceinline__ float part_sum(float v) {
 }
 
 // y <- R(t)^T y over adjacent pairs (the inverse of the prologue's rotation), on the
-// 32 dims this thread holds (dim = e * S + part).
-template <int S>
+// 32 dims [32 part, 32 part + 32) this thread holds: pairs 16 part .. 16 part + 15.
 __device__ __forceinline__ void rotate_back(float (&y)[32], int part, float dt, const float* omega) {
-  if constexpr (S == 1) {
 #pragma unroll
-    for (int p = 0; p < 16; ++p) {
-      float sn, cs;
-      sincosf(dt * omega[p], &sn, &cs);
-      const float a = y[2 * p], b = y[2 * p + 1];
-      y[2 * p] = a * cs + b * sn;
-      y[2 * p + 1] = -a * sn + b * cs;
-    }
-  } else {
-    static_assert(S == 2, "two threads per row: part 0 holds the even dims, part 1 the odd ones");
+  for (int p = 0; p < 16; ++p) {
+    float sn, cs;
+    sincosf(dt * omega[16 * part + p], &sn, &cs);
+    const float u = y[2 * p], w = y[2 * p + 1];
+    y[2 * p] = u * cs + w * sn;
+    y[2 * p + 1] = -u * sn + w * cs;
+  }
+}
+
+// 32 contiguous floats of a staged shared-memory row, as eight 16-byte loads.
+__device__ __forceinline__ void lds32(const float* p, float (&x)[32]) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      float sn, cs;
-      sincosf(dt * omega[e], &sn, &cs);  // dims 2e (part 0) and 2e + 1 (part 1) form pair e
-      const float other = __shfl_xor_sync(0xffffffffu, y[e], 1);
-      y[e] = part == 0 ? y[e] * cs + other * sn : -other * sn + y[e] * cs;
-    }
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = reinterpret_cast<const float4*>(p)[i];
+    x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
   }
 }
 
@@ -114,7 +109,9 @@ __global__ void __launch_bounds__(128) k_bwd_delta(BwdArgs a) {
 
 template <int D>
 struct BwdSmem {
-  float a[kTile][D + 1], b[kTile][D + 1];  // K', V (dQ kernel) or Q' * scale, dO (dK/dV kernel)
+  // K', V (dQ kernel) or Q' * scale, dO (dK/dV kernel); rows padded to keep 16-byte alignment
+  __align__(16) float a[kTile][D + 4];
+  __align__(16) float b[kTile][D + 4];
   long long t[kTile];
   int ty[kTile];
   float lse[kTile], dlt[kTile];
@@ -142,8 +139,8 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dq(BwdArgs a) {
   if (row_ok) {
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      q[e] = ld_elem<E>(a.q, row * D + e * S + part) * a.scale;
-      go[e] = ld_elem<E>(a.dout, row * D + e * S + part);
+      q[e] = ld_elem<E>(a.q, row * D + 32 * part + e) * a.scale;
+      go[e] = ld_elem<E>(a.dout, row * D + 32 * part + e);
     }
     ti = a.t[tok];
     tyi = a.ty[tok];
@@ -179,23 +176,26 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dq(BwdArgs a) {
       bool vis = live;
       if (vis && cl != REC_ATTN_TILE_FULL)
         vis = vis_pred(a.mask, pi, ti, tyi, thr_ok, thr, kt * kTile + c, sm.t[c], sm.ty[c]);
+      float kc[32], vc[32];
+      lds32(&sm.a[c][32 * part], kc);
+      lds32(&sm.b[c][32 * part], vc);
       float s = 0.f, dp = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        s = fmaf(q[e], sm.a[c][e * S + part], s);
-        dp = fmaf(go[e], sm.b[c][e * S + part], dp);
+        s = fmaf(q[e], kc[e], s);
+        dp = fmaf(go[e], vc[e], dp);
       }
       s = part_sum<S>(s);
       dp = part_sum<S>(dp);
       const float ds = vis ? __expf(s - lse) * (dp - dlt) * a.scale : 0.f;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) acc[e] = fmaf(ds, sm.a[c][e * S + part], acc[e]);
+      for (int e = 0; e < 32; ++e) acc[e] = fmaf(ds, kc[e], acc[e]);
     }
   }
-  if (a.rotate) rotate_back<S>(acc, part, (float)(ti - a.t[m.tok_start]), a.omega);
   if (!row_ok) return;
+  if (a.rotate) rotate_back(acc, part, (float)(ti - a.t[m.tok_start]), a.omega);
 #pragma unroll
-  for (int e = 0; e < 32; ++e) st_elem<E>(a.dq, row * D + e * S + part, acc[e]);
+  for (int e = 0; e < 32; ++e) st_elem<E>(a.dq, row * D + 32 * part + e, acc[e]);
 }
 
 // dK, dV: block = (key tile g, head h); kSplit threads per key row.
@@ -219,8 +219,8 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dkv(BwdArgs a) {
   if (row_ok) {
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      k[e] = ld_elem<E>(a.k, row * D + e * S + part);
-      v[e] = ld_elem<E>(a.v, row * D + e * S + part);
+      k[e] = ld_elem<E>(a.k, row * D + 32 * part + e);
+      v[e] = ld_elem<E>(a.v, row * D + 32 * part + e);
     }
     tj = a.t[tok];
     tyj = a.ty[tok];
@@ -256,11 +256,14 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dkv(BwdArgs a) {
         delay_bound(sm.t[c], a.mask.delay, thr_ok, thr);
         vis = vis_pred(a.mask, qt * kTile + c, sm.t[c], sm.ty[c], thr_ok, thr, pj, tj, tyj);
       }
+      float qc[32], gc[32];
+      lds32(&sm.a[c][32 * part], qc);
+      lds32(&sm.b[c][32 * part], gc);
       float s = 0.f, dp = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        s = fmaf(sm.a[c][e * S + part], k[e], s);
-        dp = fmaf(sm.b[c][e * S + part], v[e], dp);
+        s = fmaf(qc[e], k[e], s);
+        dp = fmaf(gc[e], v[e], dp);
       }
       s = part_sum<S>(s);
       dp = part_sum<S>(dp);
@@ -268,27 +271,29 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dkv(BwdArgs a) {
       const float ds = p * (dp - sm.dlt[c]);  // sm.a already carries the scale
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        dv[e] = fmaf(p, sm.b[c][e * S + part], dv[e]);
-        dk[e] = fmaf(ds, sm.a[c][e * S + part], dk[e]);
+        dv[e] = fmaf(p, gc[e], dv[e]);
+        dk[e] = fmaf(ds, qc[e], dk[e]);
       }
     }
   }
-  if (a.rotate) rotate_back<S>(dk, part, (float)(tj - a.t[m.tok_start]), a.omega);
   if (!row_ok) return;
+  if (a.rotate) rotate_back(dk, part, (float)(tj - a.t[m.tok_start]), a.omega);
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
-    st_elem<E>(a.dk, row * D + e * S + part, dk[e]);
-    st_elem<E>(a.dv, row * D + e * S + part, dv[e]);
+    st_elem<E>(a.dk, row * D + 32 * part + e, dk[e]);
+    st_elem<E>(a.dv, row * D + 32 * part + e, dv[e]);
   }
 }
 
 template <typename E, int D>
+cudaError_t launch_delta_t(const BwdArgs& a, cudaStream_t st) {
+  if (a.rows <= 0) return cudaSuccess;
+  k_bwd_delta<E, D><<<(unsigned)((a.rows + 127) / 128), 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename E, int D>
 cudaError_t launch_bwd_t(const BwdArgs& a, long long n_tiles, cudaStream_t st) {
-  if (a.rows > 0) {
-    k_bwd_delta<E, D><<<(unsigned)((a.rows + 127) / 128), 128, 0, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   if (n_tiles <= 0) return cudaSuccess;
   const dim3 grid((unsigned)n_tiles, (unsigned)a.heads);
   const int smem = (int)sizeof(BwdSmem<D>);
@@ -304,13 +309,19 @@ cudaError_t launch_bwd_t(const BwdArgs& a, long long n_tiles, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_attn_bwd(const BwdArgs& a, int dtype, int head_dim, long long n_tiles, cudaStream_t st) {
+cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, int head_dim, cudaStream_t st) {
   if (dtype == REC_ATTN_BF16) {
-    if (head_dim == 64) return launch_bwd_t<__nv_bfloat16, 64>(a, n_tiles, st);
+    if (head_dim == 64) return launch_delta_t<__nv_bfloat16, 64>(a, st);
   } else {
-    if (head_dim == 32) return launch_bwd_t<float, 32>(a, n_tiles, st);
-    if (head_dim == 64) return launch_bwd_t<float, 64>(a, n_tiles, st);
+    if (head_dim == 32) return launch_delta_t<float, 32>(a, st);
+    if (head_dim == 64) return launch_delta_t<float, 64>(a, st);
   }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_bwd_simt(const BwdArgs& a, int head_dim, long long n_tiles, cudaStream_t st) {
+  if (head_dim == 32) return launch_bwd_t<float, 32>(a, n_tiles, st);
+  if (head_dim == 64) return launch_bwd_t<float, 64>(a, n_tiles, st);
   return cudaErrorInvalidValue;
 }
 

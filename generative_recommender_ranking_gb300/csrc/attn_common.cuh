@@ -47,6 +47,11 @@ struct RopeArgs {
 struct BwdArgs {
   const ReqMeta* meta;
   int batch;
+  const int* items;        // work items (query tile * H + head), the planner's execution order
+  const int* qreq;         // request of each tile
+  const KeyTileRec* krec;  // per tile: type bitmaps and times (tensor-core kernels' masks)
+  long long n_items;       // tiles x heads
+  int* status;             // device status word (first error wins)
   const int* kcount;       // per query tile: entries in its key-tile list
   const uint32_t* klist;   // per query tile: non-SKIP key tiles (kt | class << 24)
   const uint8_t* cls;      // per request: ntiles x ntiles class matrix

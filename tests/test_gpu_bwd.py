@@ -28,6 +28,12 @@ CASES = {
     "sort": lambda: W.sort(batch=2, n_hist=400, n_cand=40, window=96),
     "mtgr": lambda: W.mtgr(batch=3, hist=(150, 300), rt=(20, 60), cand=(10, 30)),
     "tm20k_window": lambda: W.tm20k("window", batch=1, n_hist=1000),
+    # more (tile, head) items than the tensor-core kernels' 2 x 152 persistent CTAs, so
+    # every CTA runs several items (accumulators, rings and barrier phases carried over)
+    "cadet_many": lambda: W.cadet(batch=128, n_pairs=150),
+    "sort_full_len": lambda: W.sort(batch=4),
+    "mtgr_many": lambda: W.mtgr(batch=16),
+    "tm20k_window_6k": lambda: W.tm20k("window", batch=1, n_hist=6000),
 }
 
 
@@ -41,7 +47,7 @@ def _tol(w):
     return (1e-2, 2e-2) if w.dtype == "bf16" else (1e-5, 1e-4)
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "cadet", "sort", "mtgr", "tm20k_window"])
+@pytest.mark.parametrize("name", list(CASES))
 def test_backward_parity(name):
     w = CASES[name]()
     tens = gu.device_inputs(w)
