@@ -35,7 +35,10 @@ struct rec_attn_plan_s {
   void* qrot = nullptr;
   void* krot = nullptr;
   void* qk_extra = nullptr;  // Q'/K' buffers of a plan without the RoPE, made on the first fused call
-  float* bwd_delta = nullptr;  // [T][H] workspace of the backward pass, made on its first call
+  // workspace of the backward pass, made on its first call: fp32 path D [T][H];
+  // bf16 path the item descriptors, transposed tile lists (built once) and row constants
+  void* bwd_ws = nullptr;
+  bool bwd_sched = false;
   const long long* t = nullptr;
   const int8_t* ty = nullptr;
   MaskP mask{};
@@ -500,14 +503,19 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   plan->stream = st;
   if (T == 0) return REC_ATTN_OK;
-  if (!plan->bwd_delta) {
+  const bool tc = p.dtype == REC_ATTN_BF16;
+  const long long n_items = plan->NT * p.num_heads;
+  // bf16 workspace: descriptors [2][n_items] | row constants [H][NT][128] | lists [NC]
+  const size_t off_rowc = (size_t)2 * n_items * sizeof(BwdItemDesc);
+  const size_t off_ql = off_rowc + (size_t)plan->NT * p.num_heads * kTile * sizeof(float2);
+  const size_t ws_bytes = tc ? off_ql + (size_t)plan->NC * sizeof(uint32_t) : (size_t)T * p.num_heads * sizeof(float);
+  if (!plan->bwd_ws) {
     cudaMemPool_t pool;
     e = pool_for(plan->device, &pool);
-    if (e == cudaSuccess)
-      e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&plan->bwd_delta),
-                                  (size_t)T * p.num_heads * sizeof(float), pool, st);
-    if (e != cudaSuccess) { plan->bwd_delta = nullptr; return from_cuda(e); }
+    if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&plan->bwd_ws, ws_bytes, pool, st);
+    if (e != cudaSuccess) { plan->bwd_ws = nullptr; return from_cuda(e); }
   }
+  char* bws = static_cast<char*>(plan->bwd_ws);
   const void* qs = q;
   const void* ks = k;
   if (p.use_rope) {  // Q' and K' again, into the plan's workspace
@@ -530,14 +538,31 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   a.n_items = plan->NT * p.num_heads;
   a.status = plan->pd.status;
   a.cls = plan->pd.cls; a.t = plan->t; a.ty = plan->ty;
-  a.q = qs; a.k = ks; a.v = v; a.out = out; a.dout = dout; a.lse = lse; a.delta = plan->bwd_delta;
+  a.q = qs; a.k = ks; a.v = v; a.out = out; a.dout = dout; a.lse = lse;
+  a.delta = tc ? nullptr : reinterpret_cast<float*>(bws);
+  a.n_tiles = plan->NT;
+  a.desc = tc ? reinterpret_cast<const BwdItemDesc*>(bws) : nullptr;
+  a.rowc = tc ? reinterpret_cast<float2*>(bws + off_rowc) : nullptr;
+  a.qlist = tc ? reinterpret_cast<const uint32_t*>(bws + off_ql) : nullptr;
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.rows = T * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale;
   a.rotate = p.use_rope; a.mask = plan->mask;
   std::memcpy(a.omega, plan->omega, sizeof a.omega);
-  e = launch_bwd_delta(a, p.dtype, p.head_dim, st);
-  if (e != cudaSuccess) return from_cuda(e);
-  if (p.dtype == REC_ATTN_FP32) return from_cuda(launch_attn_bwd_simt(a, p.head_dim, plan->NT, st));
+  if (!tc) {
+    e = launch_bwd_delta(a, p.dtype, p.head_dim, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(launch_attn_bwd_simt(a, p.head_dim, plan->NT, st));
+  }
+  if (!plan->bwd_sched) {  // the plan's masks never change: its backward schedule is built once
+    BwdSchedArgs sa;
+    sa.meta = plan->pd.meta; sa.qreq = plan->pd.qreq; sa.items = plan->pd.items; sa.kcount = plan->pd.kcount;
+    sa.cls = plan->pd.cls; sa.t = plan->t; sa.n_tiles = plan->NT; sa.n_items = n_items; sa.heads = p.num_heads;
+    sa.desc = reinterpret_cast<BwdItemDesc*>(bws);
+    sa.qlist = reinterpret_cast<uint32_t*>(bws + off_ql);
+    e = launch_bwd_schedule(sa, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    plan->bwd_sched = true;
+  }
   CUtensorMap maps[4];  // Q', K', V, dO
   const void* srcs[4] = {qs, ks, v, dout};
   const long long cols = (long long)p.num_heads * p.head_dim;
@@ -677,7 +702,7 @@ REC_ATTN_API void rec_attn_free(rec_attn_plan_t* plan) {
     cudaFreeAsync(plan->ws, plan->stream);
   }
   if (plan->qk_extra) cudaFreeAsync(plan->qk_extra, plan->stream);
-  if (plan->bwd_delta) cudaFreeAsync(plan->bwd_delta, plan->stream);
+  if (plan->bwd_ws) cudaFreeAsync(plan->bwd_ws, plan->stream);
   for (cudaEvent_t ev : plan->ev)
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : {plan->ev_in, plan->ev_meta, plan->ev_plan})

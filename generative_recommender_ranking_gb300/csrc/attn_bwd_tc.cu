@@ -27,11 +27,16 @@
 // TMEM columns:  DQ   S[0] 0..63 | S[1] 64..127 | dP 128..191 | dQ 192..255
 //                DKV  S^T 0..63 | dP^T 64..127 | dV 128..191 | dK 192..255
 // The accumulators stay in TMEM across an item's tiles; the epilogue scales, undoes
-// the rotation and writes bf16 rows.  PARTIAL tiles take the forward's per-row
+// the rotation and writes bf16 rows.  Everything a compute thread needs besides TMEM
+// comes through shared memory with the tiles: the planner's records of the item's tile
+// and the streamed tiles (times, type bitmaps) and the rows' constants
+// {lse * log2(e), D} (k_bwd_rowc, tile-padded so that a bulk copy moves a tile's
+// 128 rows), and the item descriptors (k_bwd_schedule, once per plan) are loaded one
+// item ahead.  PARTIAL tiles take the forward's per-row
 // visibility bits (row_mask.cuh), built from the key tile's planner record; in DKV
 // each thread first acts as a row of the query tile, builds that row's bits against
 // the item's key tile, and the warps transpose the bits into per-key columns with
-// ballots.  FULL tiles skip the mask.  The MMAs of one thread run in issue order, so
+// shuffles.  FULL tiles skip the mask.  The MMAs of one thread run in issue order, so
 // an MMA that overwrites TMEM columns an earlier MMA reads needs no wait.  Every
 // mbarrier wait is bounded (REC_ATTN_ERR_TIMEOUT in the status word).
 #include <cuda_bf16.h>
@@ -72,19 +77,22 @@ enum : int {
 };
 
 // Byte offsets from the 1024-aligned base of dynamic shared memory.
+constexpr int kRowB = kTile * 8;  // {lse2, D} of a tile's rows
 struct BL {
   static constexpr int kRes = 0;                             // [2] resident tiles
   static constexpr int kStr = kRes + 2 * kTileBytes;         // [kNS][2] streamed tiles
-  static constexpr int kSRec = kStr + 2 * kNS * kTileBytes;  // DQ: [kNS] streamed key-tile records
-  static constexpr int kRRec = kSRec + kNS * kRecB;          // DKV: the item's key-tile record
-  static constexpr int kCol = kRRec + kRecB;                 // DKV: [128 keys] 128 query bits
-  static constexpr int kLse = kCol + kTile * 16;             // DKV: [128] lse * log2(e) of the query tile
-  static constexpr int kDlt = kLse + kTile * 4;              // DKV: [128] D of the query tile
-  static constexpr int kBarsOff = kDlt + kTile * 4;
+  static constexpr int kSRec = kStr + 2 * kNS * kTileBytes;  // [kNS] records of the streamed tiles
+  static constexpr int kSRow = kSRec + kNS * kRecB;          // DKV: [kNS] row constants of the query tiles
+  static constexpr int kRRec = kSRow + kNS * kRowB;          // record of the item's tile
+  static constexpr int kRRow = kRRec + kRecB;                // DQ: row constants of the query tile
+  static constexpr int kCol = kRRow + kRowB;                 // DKV: [128 keys] 128 query bits
+  static constexpr int kBarsOff = kCol + kTile * 16;
   static constexpr int kTotal = kBarsOff + kNumBars * 8 + 16;  // + abort flag and TMEM slot
   static constexpr int kDynamic = kTotal + 1024;               // slack to align the base
 };
-static_assert(BL::kSRec % 16 == 0 && BL::kRRec % 16 == 0 && BL::kCol % 16 == 0, "bulk-copy alignment");
+static_assert(BL::kSRec % 16 == 0 && BL::kSRow % 16 == 0 && BL::kRRec % 16 == 0 && BL::kRRow % 16 == 0 &&
+                  BL::kCol % 16 == 0,
+              "bulk-copy alignment");
 static_assert(BL::kBarsOff % 8 == 0, "mbarrier alignment");
 static_assert(2 * (BL::kDynamic + 1024) <= 228 * 1024, "two CTAs per SM");
 
@@ -102,100 +110,105 @@ __device__ __forceinline__ void bw_drain(uint64_t* bar, uint32_t parity) {
     if (ptx::globaltimer() - t0 > kWaitNsB / 4) return;
 }
 
-// One work item: the tile whose rows this CTA owns (DQ: query tile, DKV: key tile)
-// and its streamed tiles.
-struct BItem {
-  ReqMeta m;
-  int h;
-  int tile;  // request-local
-  int n;     // streamed (non-SKIP) tiles
+// Item descriptors, one item ahead: the next descriptor's three 16-byte loads are in
+// flight while the current item runs.
+struct DescPipe {
+  const uint4* base;
+  long long n, w;
+  uint4 nx[3];
+  __device__ __forceinline__ void init(const BwdArgs& a, bool dkv) {
+    base = reinterpret_cast<const uint4*>(a.desc + (dkv ? a.n_items : 0));
+    n = a.n_items;
+    w = blockIdx.x;
+    if (w < n) fetch(w);
+  }
+  __device__ __forceinline__ void fetch(long long i) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) nx[k] = base[3 * i + k];
+  }
+  __device__ __forceinline__ bool more() const { return w < n; }
+  // the current descriptor; starts the next one's loads
+  __device__ __forceinline__ BwdItemDesc take() {
+    BwdItemDesc d;
+    d.tok_start = (long long)(((unsigned long long)nx[0].y << 32) | nx[0].x);
+    d.t_ref = (long long)(((unsigned long long)nx[0].w << 32) | nx[0].z);
+    d.list = (long long)(((unsigned long long)nx[1].y << 32) | nx[1].x);
+    d.len = (int)nx[1].z;
+    d.tile = (int)nx[1].w;
+    d.tile_start = (int)nx[2].x;
+    d.h = (int)nx[2].y;
+    d.n = (int)nx[2].z;
+    d.pad = 0;
+    w += gridDim.x;
+    if (w < n) fetch(w);
+    return d;
+  }
 };
 
-template <bool DKV>
-__device__ __forceinline__ BItem decode_bitem(const BwdArgs& a, long long w) {
-  BItem it;
-  const long long e = a.items[w];
-  const long long g = e / a.heads;
-  it.h = (int)(e % a.heads);
-  it.m = a.meta[a.qreq[g]];
-  const int qt = (int)(g - it.m.tile_start);
-  if constexpr (!DKV) {
-    it.tile = qt;
-    it.n = max(a.kcount[g], 0);
-  } else {
-    it.tile = it.m.ntiles - 1 - qt;
-    const uint8_t* col = a.cls + it.m.cls_start + it.tile;
-    int n = 0;
-    for (int r = 0; r < it.m.ntiles; ++r) n += col[(long long)r * it.m.ntiles] != REC_ATTN_TILE_SKIP;
-    it.n = n;
-  }
-  return it;
-}
-
-// The streamed tiles of an item in order: request-local tile index and class.
-template <bool DKV>
+// The streamed tiles of an item, in order: request-local tile index and class.
 struct Cursor {
-  const uint32_t* list;  // DQ: the query tile's key-tile list
-  const uint8_t* col;    // DKV: column `tile` of the request's class matrix
-  int ntiles, r;
-  __device__ __forceinline__ void init(const BwdArgs& a, const BItem& it) {
-    ntiles = it.m.ntiles;
+  const uint32_t* list;
+  int r;
+  __device__ __forceinline__ void init(const uint32_t* base, const BwdItemDesc& d) {
+    list = base + d.list;
     r = 0;
-    if constexpr (!DKV) list = a.klist + it.m.cls_start + (long long)it.tile * it.m.ntiles;
-    else col = a.cls + it.m.cls_start + it.tile;
   }
   __device__ __forceinline__ void next(int& tile, int& cls) {
-    if constexpr (!DKV) {
-      const uint32_t e = list[r++];
-      tile = (int)(e & 0xffffffu);
-      cls = (int)(e >> 24);
-    } else {
-      while (r < ntiles - 1 && col[(long long)r * ntiles] == REC_ATTN_TILE_SKIP) ++r;
-      tile = r;
-      cls = col[(long long)r * ntiles];
-      ++r;
-    }
+    const uint32_t e = list[r++];
+    tile = (int)(e & 0xffffffu);
+    cls = (int)(e >> 24);
   }
 };
 
 // ------------------------------------------------------------------ producer
 // maps: resident pair res[0], res[1]; streamed pair str[0], str[1].
+//   DQ:  resident Q', dO + the query tile's record and row constants; streamed K', V
+//        (+ the key tile's record when the tile is PARTIAL).
+//   DKV: resident K', V + the key tile's record; streamed Q', dO + the query tile's
+//        record and row constants.
 template <bool DKV>
 __device__ void bwd_producer(const BwdArgs& a, const void* const (&res)[2], const void* const (&str)[2],
                              uint8_t* sm, uint64_t* bars, volatile int* abort_flag) {
+  const uint32_t* lists = DKV ? a.qlist : a.klist;
   uint32_t it_n = 0, s_it = 0;
   bool res_used = false, str_used[kNS];
   uint32_t res_ph = 0, str_ph[kNS];
   for (int i = 0; i < kNS; ++i) { str_used[i] = false; str_ph[i] = 0; }
-  for (long long w = blockIdx.x; w < a.n_items; w += gridDim.x) {
-    const BItem it = decode_bitem<DKV>(a, w);
-    if (it.n <= 0) continue;
+  DescPipe dp;
+  dp.init(a, DKV);
+  while (dp.more()) {
+    const BwdItemDesc d = dp.take();
+    if (d.n <= 0) continue;
     if (!bw_wait(bars + kResEmpty, (it_n & 1) ^ 1, abort_flag, a.status)) goto drain;
     {
-      const int x = it.h * kD;
-      const int y = (int)(it.m.tok_start + (long long)it.tile * kTile);
-      ptx::mbar_arrive_expect_tx(bars + kResFull, 2 * kTileBytes + (DKV ? kRecB : 0));
+      const int x = d.h * kD;
+      const long long g = (long long)d.tile_start + d.tile;
+      const float2* rows_h = a.rowc + (long long)d.h * a.n_tiles * kTile;  // head h's row constants
+      ptx::mbar_arrive_expect_tx(bars + kResFull, 2 * kTileBytes + kRecB + (DKV ? 0 : kRowB));
+      const int y = (int)(d.tok_start + (long long)d.tile * kTile);
       ptx::tma_load_2d(sm + BL::kRes, res[0], x, y, bars + kResFull);
       ptx::tma_load_2d(sm + BL::kRes + kTileBytes, res[1], x, y, bars + kResFull);
-      if (DKV) ptx::bulk_load(sm + BL::kRRec, a.krec + it.m.tile_start + it.tile, kRecB, bars + kResFull);
+      ptx::bulk_load(sm + BL::kRRec, a.krec + g, kRecB, bars + kResFull);
+      if (!DKV) ptx::bulk_load(sm + BL::kRRow, rows_h + g * kTile, kRowB, bars + kResFull);
       res_used = true;
       res_ph = it_n & 1;
       ++it_n;
-      Cursor<DKV> cur;
-      cur.init(a, it);
-      for (int j = 0; j < it.n; ++j) {
+      Cursor cur;
+      cur.init(lists, d);
+      for (int j = 0; j < d.n; ++j) {
         int tile, cls;
         cur.next(tile, cls);
         const int st = (int)(s_it % kNS);
         const uint32_t ph = (s_it / kNS) & 1;
         if (!bw_wait(bars + kStrEmpty + st, ph ^ 1, abort_flag, a.status)) goto drain;
-        const bool rec = !DKV && cls != REC_ATTN_TILE_FULL;  // DQ masks PARTIAL tiles with the key record
-        const int ys = (int)(it.m.tok_start + (long long)tile * kTile);
-        ptx::mbar_arrive_expect_tx(bars + kStrFull + st, 2 * kTileBytes + (rec ? kRecB : 0));
+        const long long gs = (long long)d.tile_start + tile;
+        const bool rec = DKV || cls != REC_ATTN_TILE_FULL;  // DQ reads a key record on PARTIAL tiles only
+        const int ys = (int)(d.tok_start + (long long)tile * kTile);
+        ptx::mbar_arrive_expect_tx(bars + kStrFull + st, 2 * kTileBytes + (rec ? kRecB : 0) + (DKV ? kRowB : 0));
         ptx::tma_load_2d(sm + BL::kStr + (2 * st) * kTileBytes, str[0], x, ys, bars + kStrFull + st);
         ptx::tma_load_2d(sm + BL::kStr + (2 * st + 1) * kTileBytes, str[1], x, ys, bars + kStrFull + st);
-        if (rec)
-          ptx::bulk_load(sm + BL::kSRec + st * kRecB, a.krec + it.m.tile_start + tile, kRecB, bars + kStrFull + st);
+        if (rec) ptx::bulk_load(sm + BL::kSRec + st * kRecB, a.krec + gs, kRecB, bars + kStrFull + st);
+        if (DKV) ptx::bulk_load(sm + BL::kSRow + st * kRowB, rows_h + gs * kTile, kRowB, bars + kStrFull + st);
         str_used[st] = true;
         str_ph[st] = ph;
         ++s_it;
@@ -234,8 +247,10 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
   const uint32_t str = ptx::smem_u32(sm + BL::kStr);
   constexpr uint32_t kHalfBytes = kStep * 128;  // 64 rows of a tile
   uint32_t it_n = 0, s_it = 0, step = 0;
-  for (long long w = blockIdx.x; w < a.n_items; w += gridDim.x) {
-    const BItem it = decode_bitem<DKV>(a, w);
+  DescPipe dp;
+  dp.init(a, DKV);
+  while (dp.more()) {
+    const BwdItemDesc it = dp.take();
     if (it.n <= 0) continue;
     if (!bw_wait(bars + kResFull, it_n & 1, abort_flag, a.status)) goto out;
     if (it_n > 0 && !bw_wait(bars + kAccEmpty, (it_n - 1) & 1, abort_flag, a.status)) goto out;
@@ -319,7 +334,9 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// One output row: x * scale, then (rotate) R(dt)^T over adjacent pairs, as bf16.
+// One output row: x * scale, then (rotate) R(dt)^T over adjacent pairs, as bf16.  The
+// angles (at most a few tens of radians) take the hardware sine and cosine: their
+// error, about 1e-5 rad here, is far below the bf16 rounding of the result.
 __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t (&acc)[64], float scale, bool rotate,
                                          float dt, const float* omega) {
   uint32_t w[32];
@@ -328,7 +345,7 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t (&a
     float u = __uint_as_float(acc[2 * p]) * scale, v = __uint_as_float(acc[2 * p + 1]) * scale;
     if (rotate) {
       float sn, cs;
-      sincosf(dt * omega[p], &sn, &cs);
+      __sincosf(dt * omega[p], &sn, &cs);
       const float u2 = u * cs + v * sn;
       v = -u * sn + v * cs;
       u = u2;
@@ -360,6 +377,15 @@ __device__ __forceinline__ void ds_chunk(const uint32_t (&r)[64], uint32_t bits,
   }
 }
 
+// A row's time and type from a tile record (type -1 past the request end).
+__device__ __forceinline__ void rec_row(const KeyTileRec* rec, int row, long long& t, int& ty) {
+  t = rec->t[row];
+  ty = -1;
+#pragma unroll
+  for (int c = 0; c < kTypes; ++c)
+    if ((rec->typebits[c][row >> 5] >> (row & 31)) & 1u) ty = c;
+}
+
 // DQ: thread = query row of the item's tile.
 __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t tmem,
                                volatile int* abort_flag) {
@@ -367,34 +393,36 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
   const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
   const float sl2 = a.scale * kLog2e;
   const KeyTileRec* srec = reinterpret_cast<const KeyTileRec*>(sm + BL::kSRec);
+  const KeyTileRec* rrec = reinterpret_cast<const KeyTileRec*>(sm + BL::kRRec);
+  const float2* rrow = reinterpret_cast<const float2*>(sm + BL::kRRow);
   const int H = a.heads;
   uint32_t it_n = 0, s_it = 0, step = 0;
-  for (long long w = blockIdx.x; w < a.n_items; w += gridDim.x) {
-    const BItem it = decode_bitem<false>(a, w);
+  DescPipe dp;
+  dp.init(a, false);
+  while (dp.more()) {
+    const BwdItemDesc it = dp.take();
     const int pi = it.tile * kTile + row;
-    const bool row_ok = pi < it.m.len;
-    const long long tok = it.m.tok_start + pi, grow = tok * H + it.h;
+    const bool row_ok = pi < it.len;
+    const long long tok = it.tok_start + pi, grow = tok * H + it.h;
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + grow * kD;
     if (it.n <= 0) {  // no visible key tile
       if (row_ok) zero_row(dst);
       continue;
     }
-    long long ti = 0;
-    int tyi = -1;
-    float lse2 = 0.f, dlt = 0.f;
-    bool live = false;  // a row that sees no key (lse = -inf) contributes nothing
-    if (row_ok) {
-      ti = a.t[tok];
-      tyi = a.ty[tok];
-      const float l = a.lse[grow];
-      dlt = a.delta[grow];
-      live = l != -INFINITY;
-      lse2 = live ? l * kLog2e : 0.f;
-    }
+    // the row's time, type and constants, loaded with Q'
+    if (!bw_wait_warp(bars + kResFull, it_n & 1, abort_flag, a.status)) return;
+    long long ti;
+    int tyi;
+    rec_row(rrec, row, ti, tyi);
+    const float2 rc = rrow[row];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bars + kResEmpty);
+    const bool live = row_ok && rc.x != -INFINITY;  // a row that sees no key contributes nothing
+    const float lse2 = live ? rc.x : 0.f, dlt = rc.y;
     RowMask rm;
     row_mask_setup(a.mask, live, pi, ti, tyi, rm);
-    Cursor<false> cur;
-    cur.init(a, it);
+    Cursor cur;
+    cur.init(a.klist, it);
     for (int j = 0; j < it.n; ++j) {
       int kt, cls;
       cur.next(kt, cls);
@@ -437,8 +465,21 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
-    if (row_ok) store_row(dst, acc, a.scale, a.rotate != 0, (float)(ti - a.t[it.m.tok_start]), a.omega);
+    if (row_ok) store_row(dst, acc, a.scale, a.rotate != 0, (float)(ti - it.t_ref), a.omega);
   }
+}
+
+// Transpose of the 32 x 32 bit matrix held one row per lane: afterwards lane b holds
+// bit l = bit b of lane l's input.  Five rounds swap the off-diagonal blocks of width
+// 16, 8, 4, 2 and 1 between lanes l and l ^ j.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint32_t m = j == 16 ? 0x0000ffffu : j == 8 ? 0x00ff00ffu : j == 4 ? 0x0f0f0f0fu : j == 2 ? 0x33333333u : 0x55555555u;
+    const uint32_t p = __shfl_xor_sync(0xffffffffu, x, j);
+    x = (lane & j) ? ((x & ~m) | ((p & ~m) >> j)) : ((x & m) | ((p & m) << j));
+  }
+  return x;
 }
 
 // The 128 compute threads meet (bounded); `n` counts the uses of the barrier.
@@ -455,43 +496,42 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
   const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
   const float sl2 = a.scale * kLog2e;
   const KeyTileRec* rrec = reinterpret_cast<const KeyTileRec*>(sm + BL::kRRec);
+  const KeyTileRec* srec = reinterpret_cast<const KeyTileRec*>(sm + BL::kSRec);
+  const float2* srow = reinterpret_cast<const float2*>(sm + BL::kSRow);
   uint32_t* colS = reinterpret_cast<uint32_t*>(sm + BL::kCol);
-  float* lseS = reinterpret_cast<float*>(sm + BL::kLse);
-  float* dltS = reinterpret_cast<float*>(sm + BL::kDlt);
   const int H = a.heads;
-  uint32_t it_n = 0, step = 0, grp = 0;
-  for (long long w = blockIdx.x; w < a.n_items; w += gridDim.x) {
-    const BItem it = decode_bitem<true>(a, w);
+  uint32_t it_n = 0, s_it = 0, step = 0, grp = 0;
+  DescPipe dp;
+  dp.init(a, true);
+  while (dp.more()) {
+    const BwdItemDesc it = dp.take();
     const int pj = it.tile * kTile + row;
-    const bool key_ok = pj < it.m.len;
-    const long long tokk = it.m.tok_start + pj, growk = tokk * H + it.h;
+    const bool key_ok = pj < it.len;
+    const long long growk = (it.tok_start + pj) * H + it.h;
     __nv_bfloat16* dkr = static_cast<__nv_bfloat16*>(a.dk) + growk * kD;
     __nv_bfloat16* dvr = static_cast<__nv_bfloat16*>(a.dv) + growk * kD;
     if (it.n <= 0) {  // no query sees this key tile
       if (key_ok) { zero_row(dkr); zero_row(dvr); }
       continue;
     }
-    const long long tj = key_ok ? a.t[tokk] : 0;
     if (!bw_wait_warp(bars + kResFull, it_n & 1, abort_flag, a.status)) return;  // the key tile's record
-    Cursor<true> cur;
-    cur.init(a, it);
+    const long long tj = rrec->t[row];
+    Cursor cur;
+    cur.init(a.qlist, it);
     for (int j = 0; j < it.n; ++j) {
       int qt, cls;
       cur.next(qt, cls);
+      const int st = (int)(s_it % kNS);
+      const uint32_t ph = (s_it / kNS) & 1;
+      ++s_it;
+      if (!bw_wait_warp(bars + kStrFull + st, ph, abort_flag, a.status)) return;
       // as query row `row` of query tile qt: its visibility bits over the key tile
+      const float2* rows = srow + st * kTile;
       const int qi = qt * kTile + row;
-      const bool q_ok = qi < it.m.len;
-      const long long tokq = it.m.tok_start + qi, growq = tokq * H + it.h;
-      long long tq = 0;
-      int tyq = -1;
-      float lq = -INFINITY, dq = 0.f;
-      if (q_ok) {
-        tq = a.t[tokq];
-        tyq = a.ty[tokq];
-        lq = a.lse[growq];
-        dq = a.delta[growq];
-      }
-      const bool live = q_ok && lq != -INFINITY;
+      long long tq;
+      int tyq;
+      rec_row(srec + st, row, tq, tyq);
+      const bool live = qi < it.len && rows[row].x != -INFINITY;
       const uint32_t f = live ? ~0u : 0u;
       uint32_t vm[4] = {f, f, f, f};
       if (cls != REC_ATTN_TILE_FULL) {
@@ -503,20 +543,13 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + kResEmpty);
       }
-      // lane b keeps the bits of key 32 w + b over this warp's 32 queries
-      uint32_t colw[4] = {0u, 0u, 0u, 0u};
+      // lane b takes the bits of key 32 w + b over this warp's 32 queries
+      uint32_t colw[4];
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd)
-#pragma unroll
-        for (int b = 0; b < 32; ++b) {
-          const uint32_t bal = __ballot_sync(0xffffffffu, (vm[wd] >> b) & 1u);
-          colw[wd] = lane == b ? bal : colw[wd];
-        }
+      for (int wd = 0; wd < 4; ++wd) colw[wd] = transpose32(vm[wd], lane);
       if (!group_sync(bars + kGroup, grp, abort_flag, a.status)) return;  // last tile's readers are done
 #pragma unroll
       for (int wd = 0; wd < 4; ++wd) colS[(32 * wd + lane) * 4 + quad] = colw[wd];
-      lseS[row] = live ? lq * kLog2e : 0.f;
-      dltS[row] = dq;
       if (!group_sync(bars + kGroup, grp, abort_flag, a.status)) return;
       const uint4 cm = reinterpret_cast<const uint4*>(colS)[row];
 #pragma unroll 1
@@ -526,37 +559,38 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         const uint32_t wb[2] = {hh ? cm.z : cm.x, hh ? cm.w : cm.y};  // this step's 64 queries
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t r[64], pp[16], pd[16];
+          uint32_t r[64], pk[16];
           ptx::tmem_ld32x2_async(tl + 32 * c, tl + 64 + 32 * c, r);
-          const float4* l4 = reinterpret_cast<const float4*>(lseS + hh * kStep + c * 32);
-          const float4* d4 = reinterpret_cast<const float4*>(dltS + hh * kStep + c * 32);
+          // {lse2, D} of the chunk's 32 queries, two per 16-byte load (broadcast)
+          const float4* q4 = reinterpret_cast<const float4*>(rows + hh * kStep + c * 32);
           const uint32_t bits = wb[c];
           ptx::tmem_wait_ld(r);
+          float p[32];
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const float4 lv = l4[g], dv = d4[g];
-            const float lsv[4] = {lv.x, lv.y, lv.z, lv.w}, dsv[4] = {dv.x, dv.y, dv.z, dv.w};
-            float p[4], s[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int e = 4 * g + u;
-              const float x = ex2(fmaf(__uint_as_float(r[e]), sl2, -lsv[u]));
-              p[u] = ((bits >> e) & 1u) ? x : 0.f;
-              s[u] = p[u] * (__uint_as_float(r[32 + e]) - dsv[u]);
-            }
-            pp[2 * g] = bf16x2(p[0], p[1]);
-            pp[2 * g + 1] = bf16x2(p[2], p[3]);
-            pd[2 * g] = bf16x2(s[0], s[1]);
-            pd[2 * g + 1] = bf16x2(s[2], s[3]);
+          for (int g = 0; g < 16; ++g) {
+            const float4 k2 = q4[g];
+            const float x0 = ex2(fmaf(__uint_as_float(r[2 * g]), sl2, -k2.x));
+            const float x1 = ex2(fmaf(__uint_as_float(r[2 * g + 1]), sl2, -k2.z));
+            p[2 * g] = ((bits >> (2 * g)) & 1u) ? x0 : 0.f;
+            p[2 * g + 1] = ((bits >> (2 * g + 1)) & 1u) ? x1 : 0.f;
+            pk[g] = bf16x2(p[2 * g], p[2 * g + 1]);
           }
-          ptx::tmem_st16_async(tl + 16 * c, pp);       // P^T over S^T columns already read
-          ptx::tmem_st16_async(tl + 64 + 16 * c, pd);  // dS^T over dP^T columns already read
+          ptx::tmem_st16_async(tl + 16 * c, pk);  // P^T over S^T columns already read
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {
+            const float4 k2 = q4[g];
+            pk[g] = bf16x2(p[2 * g] * (__uint_as_float(r[32 + 2 * g]) - k2.y),
+                           p[2 * g + 1] * (__uint_as_float(r[32 + 2 * g + 1]) - k2.w));
+          }
+          ptx::tmem_st16_async(tl + 64 + 16 * c, pk);  // dS^T over dP^T columns already read
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + kXReady);
       }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bars + kStrEmpty + st);  // the stage's record and constants were read
     }
     if (!bw_wait_warp(bars + kAccFull, it_n & 1, abort_flag, a.status)) return;
     ++it_n;
@@ -568,8 +602,92 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
-    if (key_ok) store_row(dkr, acc, a.scale, a.rotate != 0, (float)(tj - a.t[it.m.tok_start]), a.omega);
+    if (key_ok) store_row(dkr, acc, a.scale, a.rotate != 0, (float)(tj - it.t_ref), a.omega);
   }
+}
+
+// ------------------------------------------------------------------ row constants
+// Block = (tile g, head h): D_i = <dO_i, O_i> for the tile's 128 rows, eight threads per
+// row (16 bytes of dO and O each, coalesced), written with lse * log2(e) as one float2
+// per row into the tile-padded table; rows past the request end and rows that see no
+// key get -inf.
+__global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
+  const long long g = blockIdx.x;
+  const int h = blockIdx.y, H = a.heads;
+  const ReqMeta m = a.meta[a.qreq[g]];
+  const int tile = (int)(g - m.tile_start);
+  const int sub = threadIdx.x & 7;
+  float2* out = a.rowc + ((long long)h * a.n_tiles + g) * kTile;
+#pragma unroll 1
+  for (int r = threadIdx.x >> 3; r < kTile; r += 32) {
+    const int p = tile * kTile + r;
+    const bool ok = p < m.len;
+    const long long row = (m.tok_start + p) * H + h;
+    float acc = 0.f;
+    if (ok) {
+      const uint4 x = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + row * kD)[sub];
+      const uint4 y = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out) + row * kD)[sub];
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[i]));
+        const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[i]));
+        acc = fmaf(fx.x, fy.x, fmaf(fx.y, fy.y, acc));
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (sub == 0) {
+      const float l = ok ? a.lse[row] : -INFINITY;
+      out[r] = make_float2(l == -INFINITY ? -INFINITY : l * kLog2e, acc);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ schedule
+// Threads [0, n_tiles): the transposed tile lists -- for key tile g, the query tiles
+// of its request whose class against it is not SKIP, in order.  Threads
+// [n_tiles, n_tiles + n_items): the descriptors of item w for both modes (DKV: the
+// mirrored key tile of the item's query tile).
+__global__ void __launch_bounds__(128) k_bwd_schedule(BwdSchedArgs s) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < s.n_tiles) {
+    const ReqMeta m = s.meta[s.qreq[i]];
+    const int kt = (int)(i - m.tile_start);
+    const uint8_t* col = s.cls + m.cls_start + kt;
+    uint32_t* out = s.qlist + m.cls_start + (long long)kt * m.ntiles;
+    int n = 0;
+    for (int qt = 0; qt < m.ntiles; ++qt) {
+      const int c = col[(long long)qt * m.ntiles];
+      if (c != REC_ATTN_TILE_SKIP) out[n++] = (uint32_t)qt | ((uint32_t)c << 24);
+    }
+    return;
+  }
+  const long long w = i - s.n_tiles;
+  if (w >= s.n_items) return;
+  const long long e = s.items[w];
+  const long long g = e / s.heads;
+  const ReqMeta m = s.meta[s.qreq[g]];
+  const int qt = (int)(g - m.tile_start), kt = m.ntiles - 1 - qt;
+  BwdItemDesc d;
+  d.tok_start = m.tok_start;
+  d.t_ref = s.t[m.tok_start];
+  d.len = m.len;
+  d.tile_start = (int)m.tile_start;
+  d.h = (int)(e % s.heads);
+  d.pad = 0;
+  d.list = m.cls_start + (long long)qt * m.ntiles;
+  d.tile = qt;
+  d.n = max(s.kcount[g], 0);
+  s.desc[w] = d;
+  const uint8_t* col = s.cls + m.cls_start + kt;
+  int n = 0;
+  for (int r = 0; r < m.ntiles; ++r) n += col[(long long)r * m.ntiles] != REC_ATTN_TILE_SKIP;
+  d.list = m.cls_start + (long long)kt * m.ntiles;
+  d.tile = kt;
+  d.n = n;
+  s.desc[s.n_items + w] = d;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -586,10 +704,10 @@ __global__ void __launch_bounds__(kThreadsB, 2)
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     ptx::mbar_init(bars + kResFull, 1);
-    ptx::mbar_init(bars + kResEmpty, DKV ? 1 + 4 : 1);  // DKV: the compute warps read the key record
+    ptx::mbar_init(bars + kResEmpty, 1 + 4);  // MMAs done + the compute warps read the record
     for (int i = 0; i < kNS; ++i) {
       ptx::mbar_init(bars + kStrFull + i, 1);
-      ptx::mbar_init(bars + kStrEmpty + i, DKV ? 1 : 1 + 4);  // DQ: the compute warps read the key record
+      ptx::mbar_init(bars + kStrEmpty + i, 1 + 4);  // MMAs done + the compute warps read the record
     }
     ptx::mbar_init(bars + kSyFull, 1);
     ptx::mbar_init(bars + kXReady, 4);
@@ -640,11 +758,21 @@ cudaError_t launch_mode(const CUtensorMap (&maps)[4], const BwdArgs& a, int grid
 
 }  // namespace
 
+cudaError_t launch_bwd_schedule(const BwdSchedArgs& s, cudaStream_t st) {
+  const long long n = s.n_tiles + s.n_items;
+  if (n <= 0) return cudaSuccess;
+  k_bwd_schedule<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(s);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap (&maps)[4], int num_sms, cudaStream_t st) {
   if (a.n_items <= 0) return cudaSuccess;
+  k_bwd_rowc<<<dim3((unsigned)a.n_tiles, (unsigned)a.heads), 256, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const long long cap = 2LL * num_sms;  // two CTAs per SM
   const int grid = (int)(a.n_items < cap ? a.n_items : cap);
-  cudaError_t e = launch_mode<false>(maps, a, grid, st);
+  e = launch_mode<false>(maps, a, grid, st);
   if (e != cudaSuccess) return e;
   return launch_mode<true>(maps, a, grid, st);
 }

@@ -43,6 +43,21 @@ struct RopeArgs {
   float omega[kMaxPairs];  // rad per second, pair i
 };
 
+// One backward work item as the tensor-core kernels read it (one 48-byte record per
+// item and mode, written once per plan by k_bwd_schedule).
+struct BwdItemDesc {
+  long long tok_start;  // first token of the item's request (global)
+  long long t_ref;      // its time: the rotation's reference
+  long long list;       // offset of the item's streamed-tile list (kt or qt | class << 24)
+  int len;              // request length
+  int tile;             // request-local tile whose rows the item owns
+  int tile_start;       // global index of the request's first tile
+  int h;
+  int n;                // streamed tiles
+  int pad;
+};
+static_assert(sizeof(BwdItemDesc) == 48, "three 16-byte loads");
+
 // Arguments of the backward kernels.
 struct BwdArgs {
   const ReqMeta* meta;
@@ -52,6 +67,11 @@ struct BwdArgs {
   const KeyTileRec* krec;  // per tile: type bitmaps and times (tensor-core kernels' masks)
   long long n_items;       // tiles x heads
   int* status;             // device status word (first error wins)
+  long long n_tiles;
+  // tensor-core path (bf16): per-plan schedule and per-call row constants
+  const BwdItemDesc* desc;  // [2][n_items]: dQ items, then dK/dV items (mirrored key tiles)
+  const uint32_t* qlist;    // per key tile: query tiles with a non-SKIP class (qt | class << 24)
+  float2* rowc;             // [H][n_tiles][128]: {lse * log2(e) (-inf: the row sees no key), D}
   const int* kcount;       // per query tile: entries in its key-tile list
   const uint32_t* klist;   // per query tile: non-SKIP key tiles (kt | class << 24)
   const uint8_t* cls;      // per request: ntiles x ntiles class matrix
@@ -73,6 +93,20 @@ struct BwdArgs {
   int rotate;              // 1: undo the time-RoPE on dQ', dK'
   MaskP mask;
   float omega[kMaxPairs];  // rad per second, pair i
+};
+
+// Arguments of the backward schedule kernel (run once per plan).
+struct BwdSchedArgs {
+  const ReqMeta* meta;
+  const int* qreq;
+  const int* items;
+  const int* kcount;
+  const uint8_t* cls;
+  const long long* t;
+  long long n_tiles, n_items;
+  int heads;
+  BwdItemDesc* desc;
+  uint32_t* qlist;
 };
 
 // Fused steps of the prologue, applied before the rotation: QK-RMSNorm
