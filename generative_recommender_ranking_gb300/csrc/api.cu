@@ -537,6 +537,7 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   a.items = plan->pd.items; a.qreq = plan->pd.qreq; a.krec = plan->pd.krec;
   a.n_items = plan->NT * p.num_heads;
   a.status = plan->pd.status;
+  a.counters = plan->pd.counters;
   a.cls = plan->pd.cls; a.t = plan->t; a.ty = plan->ty;
   a.q = qs; a.k = ks; a.v = v; a.out = out; a.dout = dout; a.lse = lse;
   a.delta = tc ? nullptr : reinterpret_cast<float*>(bws);

@@ -12,7 +12,8 @@
 // Both modes share one persistent kernel shape: two CTAs per SM (256 TMEM columns
 // each) and six warps -- warp 0 loads with TMA, one thread of warp 1 issues every MMA,
 // warps 2..5 are the compute warpgroup (one TMEM lane, i.e. one tile row, per
-// thread).  CTAs walk the planner's (tile, head) items with a static stride; mode DKV
+// thread).  The producer claims the planner's (tile, head) items from a global counter
+// and publishes each item's descriptor in shared memory for the other roles; mode DKV
 // visits key tiles in the mirrored order of the query tiles, so under causal masks
 // both modes start with their heaviest items.  Per item the resident operand pair
 // stays in shared memory (DQ: Q', dO; DKV: K', V) and the streamed pair (DQ: K', V of
@@ -31,8 +32,8 @@
 // comes through shared memory with the tiles: the planner's records of the item's tile
 // and the streamed tiles (times, type bitmaps) and the rows' constants
 // {lse * log2(e), D} (k_bwd_rowc, tile-padded so that a bulk copy moves a tile's
-// 128 rows), and the item descriptors (k_bwd_schedule, once per plan) are loaded one
-// item ahead.  PARTIAL tiles take the forward's per-row
+// 128 rows), and the item descriptors (k_bwd_schedule, once per plan) come from the
+// producer.  PARTIAL tiles take the forward's per-row
 // visibility bits (row_mask.cuh), built from the key tile's planner record; in DKV
 // each thread first acts as a row of the query tile, builds that row's bits against
 // the item's key tile, and the warps transpose the bits into per-key columns with
@@ -69,10 +70,13 @@ enum : int {
   kStrEmpty = kStrFull + kNS,
   kSyFull = kStrEmpty + kNS,  // the step's two score MMAs completed
   kXReady,                    // the compute warps wrote the step's bf16 operands
+  kDpFree,                    // DQ: the compute warps loaded the step's dP
   kAccFull,                   // the item's last accumulating MMA completed
   kAccEmpty,                  // the compute warps read the accumulators
   kGroup,                     // DKV: barrier of the 128 compute threads
-  kMmaDone,
+  kItemFull,                  // [2] the producer published an item descriptor
+  kItemEmpty = kItemFull + 2, // [2] the MMA issuer and the compute warps copied it
+  kMmaDone = kItemEmpty + 2,
   kNumBars
 };
 
@@ -85,8 +89,9 @@ struct BL {
   static constexpr int kSRow = kSRec + kNS * kRecB;          // DKV: [kNS] row constants of the query tiles
   static constexpr int kRRec = kSRow + kNS * kRowB;          // record of the item's tile
   static constexpr int kRRow = kRRec + kRecB;                // DQ: row constants of the query tile
-  static constexpr int kCol = kRRow + kRowB;                 // DKV: [128 keys] 128 query bits
-  static constexpr int kBarsOff = kCol + kTile * 16;
+  static constexpr int kCol = kRRow + kRowB;                 // DKV: [2][128 keys] 128 query bits
+  static constexpr int kItems = kCol + 2 * kTile * 16;       // [2] published item descriptors
+  static constexpr int kBarsOff = kItems + 2 * 64;
   static constexpr int kTotal = kBarsOff + kNumBars * 8 + 16;  // + abort flag and TMEM slot
   static constexpr int kDynamic = kTotal + 1024;               // slack to align the base
 };
@@ -110,40 +115,51 @@ __device__ __forceinline__ void bw_drain(uint64_t* bar, uint32_t parity) {
     if (ptx::globaltimer() - t0 > kWaitNsB / 4) return;
 }
 
-// Item descriptors, one item ahead: the next descriptor's three 16-byte loads are in
-// flight while the current item runs.
-struct DescPipe {
-  const uint4* base;
-  long long n, w;
-  uint4 nx[3];
-  __device__ __forceinline__ void init(const BwdArgs& a, bool dkv) {
-    base = reinterpret_cast<const uint4*>(a.desc + (dkv ? a.n_items : 0));
-    n = a.n_items;
-    w = blockIdx.x;
-    if (w < n) fetch(w);
-  }
-  __device__ __forceinline__ void fetch(long long i) {
-#pragma unroll
-    for (int k = 0; k < 3; ++k) nx[k] = base[3 * i + k];
-  }
-  __device__ __forceinline__ bool more() const { return w < n; }
-  // the current descriptor; starts the next one's loads
-  __device__ __forceinline__ BwdItemDesc take() {
-    BwdItemDesc d;
-    d.tok_start = (long long)(((unsigned long long)nx[0].y << 32) | nx[0].x);
-    d.t_ref = (long long)(((unsigned long long)nx[0].w << 32) | nx[0].z);
-    d.list = (long long)(((unsigned long long)nx[1].y << 32) | nx[1].x);
-    d.len = (int)nx[1].z;
-    d.tile = (int)nx[1].w;
-    d.tile_start = (int)nx[2].x;
-    d.h = (int)nx[2].y;
-    d.n = (int)nx[2].z;
-    d.pad = 0;
-    w += gridDim.x;
-    if (w < n) fetch(w);
-    return d;
-  }
+// A published item: its descriptor (as three 16-byte words) and the end flag.
+struct ItemSlot {
+  uint4 d[3];
+  int end;
+  int pad[3];
 };
+static_assert(sizeof(ItemSlot) == 64, "");
+
+__device__ __forceinline__ BwdItemDesc unpack_desc(const uint4 (&nx)[3]) {
+  BwdItemDesc d;
+  d.tok_start = (long long)(((unsigned long long)nx[0].y << 32) | nx[0].x);
+  d.t_ref = (long long)(((unsigned long long)nx[0].w << 32) | nx[0].z);
+  d.list = (long long)(((unsigned long long)nx[1].y << 32) | nx[1].x);
+  d.len = (int)nx[1].z;
+  d.tile = (int)nx[1].w;
+  d.tile_start = (int)nx[2].x;
+  d.h = (int)nx[2].y;
+  d.n = (int)nx[2].z;
+  d.pad = 0;
+  return d;
+}
+
+// Consumer side of the item slots: the next item's descriptor, or false at the end
+// (or after an abort).  warp_arrive: the compute warps arrive once per warp.
+__device__ __forceinline__ bool next_item(uint8_t* sm, uint64_t* bars, uint32_t& it_cnt, bool warp_arrive,
+                                          BwdItemDesc& d, volatile int* abort_flag, int* status) {
+  const int slot = (int)(it_cnt & 1);
+  const uint32_t ph = (it_cnt >> 1) & 1;
+  ++it_cnt;
+  const bool ok = warp_arrive ? bw_wait_warp(bars + kItemFull + slot, ph, abort_flag, status)
+                              : bw_wait(bars + kItemFull + slot, ph, abort_flag, status);
+  if (!ok) return false;
+  const ItemSlot* is = reinterpret_cast<const ItemSlot*>(sm + BL::kItems) + slot;
+  const uint4 nx[3] = {is->d[0], is->d[1], is->d[2]};
+  const int end = is->end;
+  if (warp_arrive) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bars + kItemEmpty + slot);
+  } else {
+    ptx::mbar_arrive(bars + kItemEmpty + slot);
+  }
+  if (end) return false;
+  d = unpack_desc(nx);
+  return true;
+}
 
 // The streamed tiles of an item, in order: request-local tile index and class.
 struct Cursor {
@@ -170,15 +186,33 @@ template <bool DKV>
 __device__ void bwd_producer(const BwdArgs& a, const void* const (&res)[2], const void* const (&str)[2],
                              uint8_t* sm, uint64_t* bars, volatile int* abort_flag) {
   const uint32_t* lists = DKV ? a.qlist : a.klist;
-  uint32_t it_n = 0, s_it = 0;
+  uint32_t it_n = 0, s_it = 0, it_cnt = 0;
   bool res_used = false, str_used[kNS];
   uint32_t res_ph = 0, str_ph[kNS];
   for (int i = 0; i < kNS; ++i) { str_used[i] = false; str_ph[i] = 0; }
-  DescPipe dp;
-  dp.init(a, DKV);
-  while (dp.more()) {
-    const BwdItemDesc d = dp.take();
+  const uint4* descs = reinterpret_cast<const uint4*>(a.desc + (DKV ? a.n_items : 0));
+  ItemSlot* slots = reinterpret_cast<ItemSlot*>(sm + BL::kItems);
+  int* counter = a.counters + (DKV ? 5 : 3);
+  for (;;) {
+    const long long w = atomicAdd(counter, 1);
+    const int slot = (int)(it_cnt & 1);
+    if (!bw_wait(bars + kItemEmpty + slot, ((it_cnt >> 1) & 1) ^ 1, abort_flag, a.status)) goto drain;
+    ++it_cnt;
+    if (w >= a.n_items) {
+      slots[slot].end = 1;
+      ptx::mbar_arrive(bars + kItemFull + slot);
+      break;
+    }
+    uint4 nx[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) nx[k] = descs[3 * w + k];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) slots[slot].d[k] = nx[k];
+    slots[slot].end = 0;
+    ptx::mbar_arrive(bars + kItemFull + slot);  // release: the slot's contents reach the waiters
+    const BwdItemDesc d = unpack_desc(nx);
     if (d.n <= 0) continue;
+
     if (!bw_wait(bars + kResEmpty, (it_n & 1) ^ 1, abort_flag, a.status)) goto drain;
     {
       const int x = d.h * kD;
@@ -246,17 +280,14 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
   const uint32_t res0 = ptx::smem_u32(sm + BL::kRes), res1 = res0 + kTileBytes;
   const uint32_t str = ptx::smem_u32(sm + BL::kStr);
   constexpr uint32_t kHalfBytes = kStep * 128;  // 64 rows of a tile
-  uint32_t it_n = 0, s_it = 0, step = 0;
-  DescPipe dp;
-  dp.init(a, DKV);
-  while (dp.more()) {
-    const BwdItemDesc it = dp.take();
+  uint32_t it_n = 0, s_it = 0, step = 0, it_cnt = 0;
+  BwdItemDesc it;
+  while (next_item(sm, bars, it_cnt, false, it, abort_flag, a.status)) {
     if (it.n <= 0) continue;
     if (!bw_wait(bars + kResFull, it_n & 1, abort_flag, a.status)) goto out;
-    if (it_n > 0 && !bw_wait(bars + kAccEmpty, (it_n - 1) & 1, abort_flag, a.status)) goto out;
     ptx::tc_fence_after();
-    ++it_n;
     {
+      const uint32_t ii = it_n++;
       const int nsteps = 2 * it.n;
       const uint32_t step0 = step;
       // the streamed stage of local step ls; waits for it on the tile's first step
@@ -269,26 +300,41 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
         }
         return true;
       };
+      // the first accumulating MMA of an item overwrites the accumulators: the compute
+      // warps must have read the previous item's
+      auto acc_free = [&]() -> bool {
+        if (ii == 0) return true;
+        if (!bw_wait(bars + kAccEmpty, (ii - 1) & 1, abort_flag, a.status)) return false;
+        ptx::tc_fence_after();
+        return true;
+      };
       if constexpr (!DKV) {
-        // S(ls) = Q' K'_h^T into S buffer (step0 + ls) % 2
-        auto issue_s = [&](int ls) -> bool {
+        // S(ls) = Q' K'_h^T into S buffer (step0 + ls) % 2, dP(ls) = dO V_h^T.  dP(ls + 1)
+        // goes out as soon as the compute warps have loaded dP(ls), so both scores of
+        // the next step are ready when this step's compute ends.
+        auto issue_scores = [&](int ls) -> bool {
           int st;
           if (!stage_of(ls, true, st)) return false;
-          mma_scores(tmem + ((step0 + ls) & 1) * kStep, res0,
-                     str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes);
+          const uint32_t half = (uint32_t)(ls & 1) * kHalfBytes;
+          mma_scores(tmem + ((step0 + ls) & 1) * kStep, res0, str + (2 * st) * kTileBytes + half);
+          mma_scores(tmem + 128, res1, str + (2 * st + 1) * kTileBytes + half);
+          ptx::umma_commit(bars + kSyFull);
+          if (ls == nsteps - 1) ptx::umma_commit(bars + kResEmpty);  // Q' and dO read for the last time
           return true;
         };
-        if (!issue_s(0)) goto out;
+        if (!issue_scores(0)) goto out;
         for (int ls = 0; ls < nsteps; ++ls) {
           int st;
           stage_of(ls, false, st);
-          const uint32_t kb = str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes;
-          const uint32_t vb = str + (2 * st + 1) * kTileBytes + (ls & 1) * kHalfBytes;
-          mma_scores(tmem + 128, res1, vb);  // dP = dO V_h^T
-          ptx::umma_commit(bars + kSyFull);
-          if (ls + 1 < nsteps && !issue_s(ls + 1)) goto out;
+          if (ls + 1 < nsteps) {
+            if (!bw_wait(bars + kDpFree, (step0 + ls) & 1, abort_flag, a.status)) goto out;
+            ptx::tc_fence_after();
+            if (!issue_scores(ls + 1)) goto out;
+          }
           if (!bw_wait(bars + kXReady, (step0 + ls) & 1, abort_flag, a.status)) goto out;
           ptx::tc_fence_after();
+          if (ls == 0 && !acc_free()) goto out;
+          const uint32_t kb = str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes;
           mma_acc(tmem + 192, tmem + ((step0 + ls) & 1) * kStep, kb, ls > 0);  // dQ += dS K'_h
           if (ls & 1) ptx::umma_commit(bars + kStrEmpty + st);
         }
@@ -300,6 +346,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
           mma_scores(tmem + 0, res0, str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes);
           mma_scores(tmem + 64, res1, str + (2 * st + 1) * kTileBytes + (ls & 1) * kHalfBytes);
           ptx::umma_commit(bars + kSyFull);
+          if (ls == nsteps - 1) ptx::umma_commit(bars + kResEmpty);  // K' and V read for the last time
           return true;
         };
         if (!issue_scores(0)) goto out;
@@ -308,6 +355,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
           stage_of(ls, false, st);
           if (!bw_wait(bars + kXReady, (step0 + ls) & 1, abort_flag, a.status)) goto out;
           ptx::tc_fence_after();
+          if (ls == 0 && !acc_free()) goto out;
           const uint32_t qb = str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes;
           const uint32_t ob = str + (2 * st + 1) * kTileBytes + (ls & 1) * kHalfBytes;
           mma_acc(tmem + 128, tmem + 0, ob, ls > 0);   // dV += P^T dO_h
@@ -319,7 +367,6 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
       step += (uint32_t)nsteps;
       s_it += (uint32_t)it.n;
       ptx::umma_commit(bars + kAccFull);
-      ptx::umma_commit(bars + kResEmpty);
     }
   }
 out:
@@ -363,20 +410,6 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* dst) {
   for (int c = 0; c < 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
 }
 
-// The bf16 operands of one 32-column chunk.  DQ: dS from S (s) and dP (d) with the
-// row's constants; bits = the chunk's visibility bits.
-__device__ __forceinline__ void ds_chunk(const uint32_t (&r)[64], uint32_t bits, float sl2, float lse2, float dlt,
-                                         uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl2, -lse2));
-    float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, -lse2));
-    p0 = ((bits >> (2 * e)) & 1u) ? p0 : 0.f;
-    p1 = ((bits >> (2 * e + 1)) & 1u) ? p1 : 0.f;
-    pk[e] = bf16x2(p0 * (__uint_as_float(r[32 + 2 * e]) - dlt), p1 * (__uint_as_float(r[32 + 2 * e + 1]) - dlt));
-  }
-}
-
 // A row's time and type from a tile record (type -1 past the request end).
 __device__ __forceinline__ void rec_row(const KeyTileRec* rec, int row, long long& t, int& ty) {
   t = rec->t[row];
@@ -396,11 +429,9 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
   const KeyTileRec* rrec = reinterpret_cast<const KeyTileRec*>(sm + BL::kRRec);
   const float2* rrow = reinterpret_cast<const float2*>(sm + BL::kRRow);
   const int H = a.heads;
-  uint32_t it_n = 0, s_it = 0, step = 0;
-  DescPipe dp;
-  dp.init(a, false);
-  while (dp.more()) {
-    const BwdItemDesc it = dp.take();
+  uint32_t it_n = 0, s_it = 0, step = 0, it_cnt = 0;
+  BwdItemDesc it;
+  while (next_item(sm, bars, it_cnt, true, it, abort_flag, a.status)) {
     const int pi = it.tile * kTile + row;
     const bool row_ok = pi < it.len;
     const long long tok = it.tok_start + pi, grow = tok * H + it.h;
@@ -443,13 +474,31 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
         ptx::tc_fence_after();
         const uint32_t sb = tl + (step & 1) * kStep;
         const uint32_t wb[2] = {hh ? vm[2] : vm[0], hh ? vm[3] : vm[1]};  // this step's 64 keys
+        // dP of both chunks and S of the first, then dP's columns go back to the MMA issuer
+        uint32_t d[64], sr[32], pk[16];
+        ptx::tmem_ld32x2_async(tl + 128, tl + 160, d);
+        ptx::tmem_ld32_async(sb, sr);
+        ptx::tmem_wait_ld(d);
+        ptx::tmem_wait_ld32(sr);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bars + kDpFree);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t r[64], pk[16];
-          ptx::tmem_ld32x2_async(sb + 32 * c, tl + 128 + 32 * c, r);
-          ptx::tmem_wait_ld(r);
-          ds_chunk(r, wb[c], sl2, lse2, dlt, pk);
-          ptx::tmem_st16_async(sb + 16 * c, pk);  // over S columns already read
+          if (c == 1) {
+            ptx::tmem_ld32_async(sb + 32, sr);
+            ptx::tmem_wait_ld32(sr);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float p0 = ex2(fmaf(__uint_as_float(sr[2 * e]), sl2, -lse2));
+            float p1 = ex2(fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -lse2));
+            p0 = ((wb[c] >> (2 * e)) & 1u) ? p0 : 0.f;
+            p1 = ((wb[c] >> (2 * e + 1)) & 1u) ? p1 : 0.f;
+            pk[e] = bf16x2(p0 * (__uint_as_float(d[32 * c + 2 * e]) - dlt),
+                           p1 * (__uint_as_float(d[32 * c + 2 * e + 1]) - dlt));
+          }
+          ptx::tmem_st16_async(sb + 16 * c, pk);  // dS over S columns already read
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -489,7 +538,8 @@ __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& n, volatile 
 }
 
 // DKV: thread = key row of the item's tile (and, while the masks are built, a row of
-// the query tile).
+// the query tile).  The column bits of the next query tile are built while the tensor
+// core runs the second half of the current one (two buffers of column bits).
 __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t tmem,
                                 volatile int* abort_flag) {
   const int lane = threadIdx.x & 31, quad = (threadIdx.x >> 5) & 3, row = quad * 32 + lane;
@@ -500,11 +550,9 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
   const float2* srow = reinterpret_cast<const float2*>(sm + BL::kSRow);
   uint32_t* colS = reinterpret_cast<uint32_t*>(sm + BL::kCol);
   const int H = a.heads;
-  uint32_t it_n = 0, s_it = 0, step = 0, grp = 0;
-  DescPipe dp;
-  dp.init(a, true);
-  while (dp.more()) {
-    const BwdItemDesc it = dp.take();
+  uint32_t it_n = 0, s_it = 0, step = 0, grp = 0, cbuf = 0, it_cnt = 0;
+  BwdItemDesc it;
+  while (next_item(sm, bars, it_cnt, true, it, abort_flag, a.status)) {
     const int pj = it.tile * kTile + row;
     const bool key_ok = pj < it.len;
     const long long growk = (it.tok_start + pj) * H + it.h;
@@ -518,20 +566,16 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
     const long long tj = rrec->t[row];
     Cursor cur;
     cur.init(a.qlist, it);
-    for (int j = 0; j < it.n; ++j) {
-      int qt, cls;
-      cur.next(qt, cls);
-      const int st = (int)(s_it % kNS);
-      const uint32_t ph = (s_it / kNS) & 1;
-      ++s_it;
-      if (!bw_wait_warp(bars + kStrFull + st, ph, abort_flag, a.status)) return;
-      // as query row `row` of query tile qt: its visibility bits over the key tile
-      const float2* rows = srow + st * kTile;
+    // Column bits of the item's j-th query tile (stage st) into buffer `buf`: as query
+    // row `row` of the tile, this thread builds the row's bits over the key tile; each
+    // warp then transposes its 32 rows into per-key words.
+    auto prepare = [&](int j, int qt, int cls, int st, uint32_t ph, uint32_t buf) -> bool {
+      if (!bw_wait_warp(bars + kStrFull + st, ph, abort_flag, a.status)) return false;
       const int qi = qt * kTile + row;
       long long tq;
       int tyq;
       rec_row(srec + st, row, tq, tyq);
-      const bool live = qi < it.len && rows[row].x != -INFINITY;
+      const bool live = qi < it.len && srow[st * kTile + row].x != -INFINITY;
       const uint32_t f = live ? ~0u : 0u;
       uint32_t vm[4] = {f, f, f, f};
       if (cls != REC_ATTN_TILE_FULL) {
@@ -543,21 +587,36 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + kResEmpty);
       }
-      // lane b takes the bits of key 32 w + b over this warp's 32 queries
-      uint32_t colw[4];
 #pragma unroll
-      for (int wd = 0; wd < 4; ++wd) colw[wd] = transpose32(vm[wd], lane);
-      if (!group_sync(bars + kGroup, grp, abort_flag, a.status)) return;  // last tile's readers are done
-#pragma unroll
-      for (int wd = 0; wd < 4; ++wd) colS[(32 * wd + lane) * 4 + quad] = colw[wd];
+      for (int wd = 0; wd < 4; ++wd) colS[buf * (kTile * 4) + (32 * wd + lane) * 4 + quad] = transpose32(vm[wd], lane);
+      return true;
+    };
+    int qt, cls;
+    cur.next(qt, cls);
+    int st = (int)(s_it % kNS);
+    if (!prepare(0, qt, cls, st, (s_it / kNS) & 1, cbuf)) return;
+    ++s_it;
+    for (int j = 0; j < it.n; ++j) {
+      // every thread's words of this tile are written, and every thread has read the
+      // other buffer's (a tile ago), which prepare() overwrites next
       if (!group_sync(bars + kGroup, grp, abort_flag, a.status)) return;
-      const uint4 cm = reinterpret_cast<const uint4*>(colS)[row];
-#pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh, ++step) {
-        if (!bw_wait_warp(bars + kSyFull, step & 1, abort_flag, a.status)) return;
+      const uint4 cm = reinterpret_cast<const uint4*>(colS)[cbuf * kTile + row];
+      const float2* rows = srow + st * kTile;
+      int nqt = 0, ncls = 0, nst = 0;
+      uint32_t nph = 0;
+      if (j + 1 < it.n) {
+        cur.next(nqt, ncls);
+        nst = (int)(s_it % kNS);
+        nph = (s_it / kNS) & 1;
+        ++s_it;
+      }
+      // one 64-query step: P^T and dS^T over the scores' TMEM columns
+      auto do_step = [&](int hh) -> bool {
+        if (!bw_wait_warp(bars + kSyFull, step & 1, abort_flag, a.status)) return false;
+        ++step;
         ptx::tc_fence_after();
         const uint32_t wb[2] = {hh ? cm.z : cm.x, hh ? cm.w : cm.y};  // this step's 64 queries
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           uint32_t r[64], pk[16];
           ptx::tmem_ld32x2_async(tl + 32 * c, tl + 64 + 32 * c, r);
@@ -588,21 +647,33 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bars + kXReady);
-      }
+        return true;
+      };
+      if (!do_step(0)) return;
+      if (j + 1 < it.n && !prepare(j + 1, nqt, ncls, nst, nph, cbuf ^ 1u)) return;
+      if (!do_step(1)) return;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + kStrEmpty + st);  // the stage's record and constants were read
+      st = nst;
+      cbuf ^= 1u;
     }
     if (!bw_wait_warp(bars + kAccFull, it_n & 1, abort_flag, a.status)) return;
     ++it_n;
     ptx::tc_fence_after();
-    uint32_t acc[64];
-    ptx::tmem_ld64(tl + 128, acc);
-    if (key_ok) store_row(dvr, acc, 1.f, false, 0.f, a.omega);
+    uint32_t acc[64], wv[32];
+    ptx::tmem_ld64(tl + 128, acc);  // dV, packed before dK is read
+#pragma unroll
+    for (int p = 0; p < 32; ++p) wv[p] = bf16x2(__uint_as_float(acc[2 * p]), __uint_as_float(acc[2 * p + 1]));
     ptx::tmem_ld64(tl + 192, acc);
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
-    if (key_ok) store_row(dkr, acc, a.scale, a.rotate != 0, (float)(tj - it.t_ref), a.omega);
+    if (key_ok) {
+      uint4* d4 = reinterpret_cast<uint4*>(dvr);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) d4[c] = make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
+      store_row(dkr, acc, a.scale, a.rotate != 0, (float)(tj - it.t_ref), a.omega);
+    }
   }
 }
 
@@ -711,9 +782,14 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     }
     ptx::mbar_init(bars + kSyFull, 1);
     ptx::mbar_init(bars + kXReady, 4);
+    ptx::mbar_init(bars + kDpFree, 4);
     ptx::mbar_init(bars + kAccFull, 1);
     ptx::mbar_init(bars + kAccEmpty, 4);
     ptx::mbar_init(bars + kGroup, 128);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bars + kItemFull + i, 1);
+      ptx::mbar_init(bars + kItemEmpty + i, 1 + 4);  // the MMA issuer and the four compute warps
+    }
     ptx::mbar_init(bars + kMmaDone, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -745,6 +821,15 @@ __global__ void __launch_bounds__(kThreadsB, 2)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kCols);
+  }
+  // the last CTA to leave resets the item counter for the next launch
+  if (threadIdx.x == 0) {
+    int* counter = a.counters + (DKV ? 5 : 3);
+    __threadfence();
+    if (atomicAdd(counter + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(counter, 0);
+      atomicExch(counter + 1, 0);
+    }
   }
 }
 

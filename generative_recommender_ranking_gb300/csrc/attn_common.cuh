@@ -67,6 +67,7 @@ struct BwdArgs {
   const KeyTileRec* krec;  // per tile: type bitmaps and times (tensor-core kernels' masks)
   long long n_items;       // tiles x heads
   int* status;             // device status word (first error wins)
+  int* counters;           // [3], [4]: dQ item counter and exit ticket; [5], [6]: dK/dV (reset at kernel end)
   long long n_tiles;
   // tensor-core path (bf16): per-plan schedule and per-call row constants
   const BwdItemDesc* desc;  // [2][n_items]: dQ items, then dK/dV items (mirrored key tiles)
