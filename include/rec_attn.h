@@ -237,9 +237,13 @@ rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const void* q, const v
  *             alias any input or each other.  All tensors 16-byte aligned.
  * The plan must be the forward's (same offsets, times, types, params) and made by
  * rec_attn_plan (not query-pruned).  Supported: bf16 with head_dim 64, fp32 with
- * head_dim 32 or 64 (else UNSUPPORTED).  The first call takes T * H floats of
- * workspace from the library pool on `stream` (released with the plan).  CUDA cores,
- * fp32 arithmetic; gradients are rounded once to params->dtype.
+ * head_dim 32 or 64 (else UNSUPPORTED).  The first call takes workspace from the
+ * library pool on `stream` (released with the plan): for bf16 the per-plan item
+ * schedule (96 B per tile and head, 4 B per tile pair) and the rows' constants
+ * (8 B per tile row and head); for fp32 T * H floats.  bf16: tensor cores (bf16
+ * operands, fp32 accumulation; P and dS rounded to bf16 for their MMAs, as in the
+ * forward's P); fp32: CUDA cores in fp32.  Gradients are rounded once to
+ * params->dtype.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM.
  */
 rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
