@@ -245,7 +245,8 @@ rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queri
   // workspace layout
   const size_t elem = params->dtype == REC_ATTN_BF16 ? 2 : 4;
   const size_t qk_bytes = (size_t)T * params->num_heads * params->head_dim * elem;
-  const WsLayout lay = ws_layout(batch, NT, NC, params->num_heads, params->use_rope ? qk_bytes : 0);
+  const WsLayout lay = ws_layout(batch, NT, NC, params->num_heads, params->use_rope ? qk_bytes : 0,
+                                 mask_capacity(NT, NC));
   plan->ws_bytes = lay.total;
 
   cudaMemPool_t pool;
@@ -287,6 +288,7 @@ rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queri
   if (e == cudaSuccess)
     e = launch_plan(plan->mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t, plan->ty, batch, NT,
                     plan->side);
+  if (e == cudaSuccess) e = launch_build_masks(plan->mask, pd, plan->num_sms, plan->side);
   if (e == cudaSuccess) e = cudaEventRecord(plan->ev_plan, plan->side);
   if (e != cudaSuccess) {
     cudaStreamWaitEvent(plan->stream, plan->ev_plan, 0);
@@ -436,6 +438,7 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
   a.meta = plan->pd.meta; a.qreq = plan->pd.qreq; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
   a.items = plan->pd.items; a.t = plan->t; a.ty = plan->ty;
   a.counters = plan->pd.counters; a.krec = plan->pd.krec; a.qkeep = plan->pd.qkeep;
+  a.kslot = plan->pd.kslot; a.mtab = plan->pd.mtab;
   a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = plan->pd.status;
   a.out_gate = f ? f->out_gate : nullptr;
   a.n_items = plan->NT * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale; a.mask = plan->mask;

@@ -23,6 +23,8 @@ struct AttnArgs {
   int* counters;     // [1]: dynamic item counter, [2]: exit ticket (both reset at kernel end)
   const KeyTileRec* krec;
   const int* qkeep;  // [B] first kept user position of each request (query pruning)
+  const int* kslot;       // per key-tile list entry: mask-table slot (-1: build the bits)
+  const uint32_t* mtab;   // mask table: [slot][128 rows][4 words]
   long long n_items; // query tiles x heads
   int heads;
   float scale;       // softmax scale (natural-log domain)
@@ -136,6 +138,7 @@ struct WorkItem {
   int n;             // non-SKIP key tiles; -1: every row of the tile is pruned
   int keep;          // first kept user position of the request (query pruning)
   const uint32_t* list;
+  const int* slots;  // mask-table slots of the list's entries
 };
 
 __device__ __forceinline__ WorkItem decode_item(const AttnArgs& a, long long w, bool ordered) {
@@ -149,6 +152,7 @@ __device__ __forceinline__ WorkItem decode_item(const AttnArgs& a, long long w, 
   it.n = a.kcount[qg];
   it.keep = a.qkeep[b];
   it.list = a.klist + it.m.cls_start + (long long)it.qt * it.m.ntiles;
+  it.slots = a.kslot + it.m.cls_start + (long long)it.qt * it.m.ntiles;
   return it;
 }
 

@@ -47,6 +47,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;          // keep the reference max until it is exceeded by 2^8
 constexpr int kRecBytes = (int)sizeof(KeyTileRec);
+constexpr int kMaskBytes = kTile * 16;  // a PARTIAL tile's 128 rows of visibility bits (mask table)
+constexpr int kStageRec = kMaskBytes > kRecBytes ? kMaskBytes : kRecBytes;  // per K/V stage: one or the other
 constexpr int kChunk = 64;                   // keys per S chunk (a 128-key tile is two chunks)
 
 template <int D>
@@ -104,6 +106,8 @@ static_assert(sizeof(ItemDesc) == 32, "");
 struct StageInfo {
   int kt;
   int cls;
+  int tab;  // PARTIAL: 1 = the stage holds the tile's rows of the mask table, 0 = the key record
+  int pad;
 };
 
 template <int D>
@@ -114,10 +118,10 @@ struct Layout {
   static constexpr int kQ = 0;                                   // [stream][QB]
   static constexpr int kK = kQ + kStreams * QB * kQBytes;        // [stream][NS]
   static constexpr int kV = kK + kStreams * NS * kKVBytes;       // [stream][NS]
-  static constexpr int kRec = kV + kStreams * NS * kKVBytes;      // [stream][NS] KeyTileRec
-  static constexpr int kQRec = kRec + kStreams * NS * kRecBytes;  // [stream][QB] KeyTileRec of the query tile
+  static constexpr int kRec = kV + kStreams * NS * kKVBytes;      // [stream][NS] KeyTileRec or mask rows
+  static constexpr int kQRec = kRec + kStreams * NS * kStageRec;  // [stream][QB] KeyTileRec of the query tile
   static constexpr int kInfo = kQRec + kStreams * QB * kRecBytes; // [stream][NS] StageInfo
-  static constexpr int kItems = (kInfo + kStreams * NS * 8 + 15) & ~15;  // [stream][2] ItemDesc
+  static constexpr int kItems = (kInfo + kStreams * NS * (int)sizeof(StageInfo) + 15) & ~15;  // [stream][2] ItemDesc
   static constexpr int kBars = (kItems + kStreams * 2 * 32 + 7) & ~7;
   static constexpr int kBarsPerStream = 2 + 2 + 2 * QB + 4 * NS + 9;
   static constexpr int kTotal = kBars + kStreams * kBarsPerStream * 8 + 16;
@@ -199,7 +203,7 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
   uint8_t* qbuf = sm + L::kQ + s * QB * L::kQBytes;
   uint8_t* kbuf = sm + L::kK + s * NS * L::kKVBytes;
   uint8_t* vbuf = sm + L::kV + s * NS * L::kKVBytes;
-  uint8_t* rbuf = sm + L::kRec + s * NS * kRecBytes;
+  uint8_t* rbuf = sm + L::kRec + s * NS * kStageRec;
   uint8_t* qrbuf = sm + L::kQRec + s * QB * kRecBytes;
   uint32_t it_cnt = 0, q_it = 0, kv_it = 0;
   bool q_used[QB], k_used[NS], v_used[NS];
@@ -239,6 +243,7 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
     ++q_it;
     for (int j = 0; j < it.n; ++j) {
       const uint32_t e = it.list[j];
+      const int slot = it.slots[j];
       const int kt = (int)(e & 0xffffffu), cl = (int)(e >> 24);
       const int st = (int)(kv_it % NS);
       const uint32_t ph = (kv_it / NS) & 1;
@@ -247,11 +252,14 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
       info[st].cls = cl;
       const bool partial = cl != REC_ATTN_TILE_FULL;
       const int y = (int)(it.m.tok_start + (long long)kt * kTile);
-      ptx::mbar_arrive_expect_tx(B.k_full + st, L::kKVBytes + (partial ? kRecBytes : 0));
+      const bool tab = partial && slot >= 0;
+      info[st].tab = tab ? 1 : 0;
+      ptx::mbar_arrive_expect_tx(B.k_full + st, L::kKVBytes + (partial ? (tab ? kMaskBytes : kRecBytes) : 0));
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
         ptx::tma_load_2d(kbuf + st * L::kKVBytes + c * kSlab, tk, it.h * D + c * 64, y, B.k_full + st);
-      if (partial) ptx::bulk_load(rbuf + st * kRecBytes, a.krec + it.m.tile_start + kt, kRecBytes, B.k_full + st);
+      if (tab) ptx::bulk_load(rbuf + st * kStageRec, a.mtab + (long long)slot * (kMaskBytes / 4), kMaskBytes, B.k_full + st);
+      else if (partial) ptx::bulk_load(rbuf + st * kStageRec, a.krec + it.m.tile_start + kt, kRecBytes, B.k_full + st);
       k_used[st] = true; k_ph[st] = ph;
       if (!wait_bar(B.v_empty + st, ph ^ 1, abort_flag, a.status)) goto drain;
       ptx::mbar_arrive_expect_tx(B.v_full + st, L::kKVBytes);
@@ -492,7 +500,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
   constexpr bool WIDE = Cfg<D>::WIDE;
   const ItemDesc* items = reinterpret_cast<const ItemDesc*>(sm + L::kItems) + s * 2;
   const StageInfo* info = reinterpret_cast<const StageInfo*>(sm + L::kInfo) + s * NS;
-  const KeyTileRec* recs = reinterpret_cast<const KeyTileRec*>(sm + L::kRec) + s * NS;
+  const uint8_t* recs = sm + L::kRec + s * NS * kStageRec;  // per stage: key record or mask rows
   const KeyTileRec* qrecs = reinterpret_cast<const KeyTileRec*>(sm + L::kQRec) + s * L::QB;
   const int lane = threadIdx.x & 31;
   const int quad = (threadIdx.x >> 5) & 3;  // TMEM lanes this warp may access
@@ -556,7 +564,14 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       const StageInfo inf = info[st];
       const bool partial = inf.cls != REC_ATTN_TILE_FULL;
       uint32_t vm[4] = {~0u, ~0u, ~0u, ~0u};
-      if (partial) build_mask(rm, recs + st, inf.kt * kTile, vm);
+      if (partial) {
+        if (inf.tab) {
+          const uint4 w = reinterpret_cast<const uint4*>(recs + st * kStageRec)[row];
+          vm[0] = w.x; vm[1] = w.y; vm[2] = w.z; vm[3] = w.w;
+        } else {
+          build_mask(rm, reinterpret_cast<const KeyTileRec*>(recs + st * kStageRec), inf.kt * kTile, vm);
+        }
+      }
       if constexpr (WIDE) {
         const uint32_t t = ch++;
         if (!wait_bar_warp(B.s_full, t & 1, abort_flag, a.status)) return;

@@ -10,6 +10,7 @@ namespace recattn {
 cudaError_t launch_plan(const MaskP& mp, int heads, const PlanDev& pd, const long long* offsets_dev,
                         const long long* t, const int8_t* ty, int batch, long long n_tiles,
                         cudaStream_t st);
+cudaError_t launch_build_masks(const MaskP& mp, const PlanDev& pd, int num_sms, cudaStream_t st);
 cudaError_t launch_count_pairs(const MaskP& mp, const PlanDev& pd, const long long* t,
                                const int8_t* ty, long long n_tiles, cudaStream_t st);
 cudaError_t launch_rope(const RopeArgs& a, int dtype, long long n_tiles, cudaStream_t st);

@@ -126,7 +126,8 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   const size_t elem = params->dtype == REC_ATTN_BF16 ? 2 : 4;
   const size_t tensor_bytes = (size_t)T * params->num_heads * params->head_dim * elem;
   // workspace layout inside the static array
-  const WsLayout lay = ws_layout(batch, NT, NC, params->num_heads, params->use_rope ? tensor_bytes : 0);
+  // no mask table here: the kernels build every PARTIAL tile's bits themselves
+  const WsLayout lay = ws_layout(batch, NT, NC, params->num_heads, params->use_rope ? tensor_bytes : 0, 0);
   if (lay.total > kScratchBytes) return REC_ATTN_ERR_UNSUPPORTED;  // batch too large for the static workspace
   if (T > 0) {
     if (!offsets_dev || !timestamps_dev || !types_dev || !q || !k || !v || !out) return REC_ATTN_ERR_INVALID_ARG;
@@ -225,6 +226,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   AttnArgs a;
   a.meta = pd.meta; a.qreq = pd.qreq; a.kcount = pd.kcount; a.klist = pd.klist; a.items = pd.items;
   a.counters = pd.counters; a.krec = pd.krec; a.qkeep = pd.qkeep;
+  a.kslot = pd.kslot; a.mtab = pd.mtab;
   a.t = t; a.ty = types_dev; a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = pd.status;
   a.out_gate = nullptr;
   a.n_items = NT * params->num_heads; a.heads = params->num_heads;

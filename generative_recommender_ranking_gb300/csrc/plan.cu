@@ -8,6 +8,7 @@
 // masked is never loaded, and a tile whose every pair is visible runs without
 // per-element mask evaluation.
 #include "rec_attn_internal.cuh"
+#include "row_mask.cuh"
 
 namespace recattn {
 
@@ -265,14 +266,33 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
       }
       continue;
     }
-    const uint8_t* row = pd.cls + m.cls_start + (long long)qt * m.ntiles;
-    uint32_t* out = pd.klist + m.cls_start + (long long)qt * m.ntiles;
+    const long long rb = m.cls_start + (long long)qt * m.ntiles;  // the query tile's row of pairs
+    const uint8_t* row = pd.cls + rb;
+    uint32_t* out = pd.klist + rb;
     int n = 0, nfull = 0;
     for (int k0 = 0; k0 < m.ntiles; k0 += 32) {
       const int kt = k0 + lane;
       const uint32_t c = kt < m.ntiles ? row[kt] : 0u;
       const unsigned bal = __ballot_sync(0xffffffffu, c != 0);
-      if (c) out[n + __popc(bal & ((1u << lane) - 1u))] = (uint32_t)kt | (c << 24);
+      // PARTIAL pairs take the next mask-table slots (while there are any)
+      const unsigned pb = __ballot_sync(0xffffffffu, c == REC_ATTN_TILE_PARTIAL);
+      int s0 = 0;
+      if (lane == 0 && pb) s0 = atomicAdd(&pd.counters[7], __popc(pb));
+      s0 = __shfl_sync(0xffffffffu, s0, 0);
+      if (c) {
+        const int j = n + __popc(bal & ((1u << lane) - 1u));
+        out[j] = (uint32_t)kt | (c << 24);
+        int slot = -1;
+        if (c == REC_ATTN_TILE_PARTIAL) {
+          const int s = s0 + __popc(pb & ((1u << lane) - 1u));
+          if (s < pd.mcap) {
+            slot = s;
+            pd.minfo[s] = make_int2((int)(m.tile_start + qt), kt);
+          }
+          pd.pslot[rb + kt] = slot;
+        }
+        pd.kslot[rb + j] = slot;
+      }
       n += __popc(bal);
       nfull += __popc(__ballot_sync(0xffffffffu, c == REC_ATTN_TILE_FULL));
     }
@@ -397,6 +417,39 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   }
 }
 
+// The mask table: per slot (a PARTIAL pair), each of the query tile's 128 rows builds its
+// visibility bits over the key tile exactly as the attention kernels would (row time and
+// type from the query tile's record, key times and types from the key tile's record,
+// which is staged in shared memory).  Slots are visited with a grid stride.
+__global__ void __launch_bounds__(kTile) k_build_masks(MaskP mp, PlanDev pd) {
+  __shared__ KeyTileRec s_rec;
+  const int used = min(__ldcg(pd.counters + 7), pd.mcap);
+  const int r = threadIdx.x;
+  for (int s = blockIdx.x; s < used; s += gridDim.x) {
+    const int2 info = pd.minfo[s];
+    const long long g = info.x;
+    const int kt = info.y;
+    const ReqMeta m = pd.meta[pd.qreq[g]];
+    const int qt = (int)(g - m.tile_start);
+    __syncthreads();  // the previous slot's readers of s_rec are done
+    const uint4* src = reinterpret_cast<const uint4*>(pd.krec + m.tile_start + kt);
+    for (int i = r; i < (int)(sizeof(KeyTileRec) / 16); i += blockDim.x) reinterpret_cast<uint4*>(&s_rec)[i] = src[i];
+    __syncthreads();
+    const KeyTileRec* qr = pd.krec + g;
+    const long long ti = qr->t[r];
+    int tyi = -1;
+#pragma unroll
+    for (int c = 0; c < kTypes; ++c)
+      if ((qr->typebits[c][r >> 5] >> (r & 31)) & 1u) tyi = c;
+    const int pi = qt * kTile + r;
+    RowMask rm;
+    row_mask_setup(mp, pi < m.len, pi, ti, tyi, rm);
+    uint32_t vm[4];
+    build_mask(rm, &s_rec, kt * kTile, vm);
+    reinterpret_cast<uint4*>(pd.mtab)[(long long)s * kTile + r] = make_uint4(vm[0], vm[1], vm[2], vm[3]);
+  }
+}
+
 // Visible-pair counter: one block per query tile, one thread per query row.
 __global__ void __launch_bounds__(kTile) k_count_pairs(MaskP mp, PlanDev pd, const long long* t,
                                                        const int8_t* ty) {
@@ -444,6 +497,13 @@ cudaError_t launch_plan(const MaskP& mp, int heads, const PlanDev& pd, const lon
                         cudaStream_t st) {
   if (batch <= 0) return cudaSuccess;
   k_plan<<<batch, kPlanThreads, 0, st>>>(mp, heads, pd, offsets_dev, t, ty, n_tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_masks(const MaskP& mp, const PlanDev& pd, int num_sms, cudaStream_t st) {
+  if (pd.mcap <= 0) return cudaSuccess;
+  const int grid = pd.mcap < 8 * num_sms ? pd.mcap : 8 * num_sms;
+  k_build_masks<<<grid, kTile, 0, st>>>(mp, pd);
   return cudaGetLastError();
 }
 

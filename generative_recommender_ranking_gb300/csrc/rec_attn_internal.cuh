@@ -67,9 +67,18 @@ struct PlanDev {
   int* roff;            // [B+1]: first item of each request in `items` (in rorder order)
   int* qkeep;           // [B]: query pruning: user tokens before this position compute nothing
   int* treq;            // [NT]: request of each tile (uploaded with the request table)
-  int* counters;        // [8]: plan ticket, attention item counter, attention exit ticket
+  int* counters;        // [8]: plan ticket, attention item counter and exit ticket, backward
+                        // item counters and exit tickets, mask-table slot counter
   int* status;          // [1]: first device error (rec_attn_status)
   unsigned long long* pairs;  // [1]: visible-pair counter
+  // Mask table: the 128 rows' visibility bits of PARTIAL tile pairs, built once per plan
+  // (the masks do not depend on the head), for up to mcap pairs; the others build their
+  // bits in the kernels.
+  int* kslot;           // [NC], aligned with klist: table slot of the entry, -1 if none
+  int* pslot;           // [NC], class-matrix order: table slot of the pair, -1 if none
+  int2* minfo;          // [mcap]: (global query tile, key tile) of each slot
+  uint32_t* mtab;       // [mcap][128 rows][4 words]
+  int mcap;
 };
 
 // History compression: one request of the batch, and the kernel arguments.

@@ -57,58 +57,65 @@ struct Chunk<float> {
   }
 };
 
-// One block per global tile.  Thread work unit: one token and one 16-byte chunk of
-// its head row, for every head, so each angle's sin/cos is computed once per token;
-// heads are processed four at a time with the eight 16-byte loads in flight together
-// (kept raw until used, so the registers stay within the four-blocks-per-SM budget).
+// Thread work unit: one token and one 16-byte chunk of its head rows, for every head,
+// so each angle's sin/cos is computed once per token.  A block covers 256 / chunks
+// tokens of one tile (chunks = 16-byte chunks per head row, 8 or 16), so a tile takes
+// chunks / 2 blocks and each thread one unit.  The first four heads' 16-byte loads of Q
+// and K go out before the angle math (they do not depend on the time), later heads four
+// at a time, all kept raw until used.
 template <typename E>
 __global__ void __launch_bounds__(256, 4) k_rope(RopeArgs a) {
   using C = Chunk<E>;
   constexpr int kPairs = C::kPairs;
-  const long long g = blockIdx.x;
+  const int chunks = a.head_dim / (2 * kPairs);
+  const int tpb = (int)blockDim.x / chunks;  // tokens per block
+  const int bpt = kTile / tpb;               // blocks per tile
+  const long long g = blockIdx.x / bpt;
   const ReqMeta m = a.meta[a.tile_req[g]];
   const int tl = (int)(g - m.tile_start);
-  const long long t_ref = a.t[m.tok_start];
-  const int chunks = a.head_dim / (2 * kPairs);
   const int rows = min(kTile, m.len - tl * kTile);
+  const int r = (int)(blockIdx.x % bpt) * tpb + (int)threadIdx.x / chunks;
+  const int c = (int)threadIdx.x % chunks;
+  if (r >= rows) return;
   const char* __restrict__ q = static_cast<const char*>(a.q);
   const char* __restrict__ k = static_cast<const char*>(a.k);
   char* __restrict__ qr = static_cast<char*>(a.qr);
   char* __restrict__ kr = static_cast<char*>(a.kr);
   const long long head_bytes = (long long)a.head_dim * (long long)sizeof(E);
-  for (int idx = threadIdx.x; idx < rows * chunks; idx += blockDim.x) {
-    const int r = idx / chunks, c = idx - r * chunks;
-    const long long tok = m.tok_start + tl * kTile + r;
-    const float dt = (float)(a.t[tok] - t_ref);  // exact int64 difference, then fp32
-    float sn[kPairs], cs[kPairs];
+  const long long tok = m.tok_start + tl * kTile + r;
+  const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
+  uint4 rq[4], rk[4];  // raw 16-byte chunks of four heads
+  auto load4 = [&](int h0) {
 #pragma unroll
-    for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
-    const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
-    for (int h0 = 0; h0 < a.heads; h0 += 4) {
-      uint4 rq[4], rk[4];  // raw 16-byte chunks of four heads, all loads in flight together
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (h0 + u < a.heads) {
-          rq[u] = *reinterpret_cast<const uint4*>(q + row0 + (h0 + u) * head_bytes);
-          rk[u] = *reinterpret_cast<const uint4*>(k + row0 + (h0 + u) * head_bytes);
-        }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (h0 + u >= a.heads) break;
-        float x[8], y[8];
-        C::unpack(rq[u], x);
-        C::unpack(rk[u], y);
-#pragma unroll
-        for (int p = 0; p < kPairs; ++p) {
-          const float x0 = x[2 * p], x1 = x[2 * p + 1], y0 = y[2 * p], y1 = y[2 * p + 1];
-          x[2 * p] = x0 * cs[p] - x1 * sn[p];
-          x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
-          y[2 * p] = y0 * cs[p] - y1 * sn[p];
-          y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
-        }
-        C::store(qr + row0 + (h0 + u) * head_bytes, x);
-        C::store(kr + row0 + (h0 + u) * head_bytes, y);
+    for (int u = 0; u < 4; ++u)
+      if (h0 + u < a.heads) {
+        rq[u] = *reinterpret_cast<const uint4*>(q + row0 + (h0 + u) * head_bytes);
+        rk[u] = *reinterpret_cast<const uint4*>(k + row0 + (h0 + u) * head_bytes);
       }
+  };
+  load4(0);
+  const float dt = (float)(a.t[tok] - a.t[m.tok_start]);  // exact int64 difference, then fp32
+  float sn[kPairs], cs[kPairs];
+#pragma unroll
+  for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
+  for (int h0 = 0; h0 < a.heads; h0 += 4) {
+    if (h0 > 0) load4(h0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (h0 + u >= a.heads) break;
+      float x[8], y[8];
+      C::unpack(rq[u], x);
+      C::unpack(rk[u], y);
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        const float x0 = x[2 * p], x1 = x[2 * p + 1], y0 = y[2 * p], y1 = y[2 * p + 1];
+        x[2 * p] = x0 * cs[p] - x1 * sn[p];
+        x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
+        y[2 * p] = y0 * cs[p] - y1 * sn[p];
+        y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
+      }
+      C::store(qr + row0 + (h0 + u) * head_bytes, x);
+      C::store(kr + row0 + (h0 + u) * head_bytes, y);
     }
   }
 }
@@ -228,8 +235,11 @@ cudaError_t launch_rope_fused(const RopeArgs& a, const FusedArgs& f, int dtype, 
 
 cudaError_t launch_rope(const RopeArgs& a, int dtype, long long n_tiles, cudaStream_t st) {
   if (n_tiles <= 0) return cudaSuccess;
-  if (dtype == REC_ATTN_BF16) k_rope<__nv_bfloat16><<<(unsigned)n_tiles, 256, 0, st>>>(a);
-  else k_rope<float><<<(unsigned)n_tiles, 256, 0, st>>>(a);
+  // 256 threads = 256 / chunks tokens per block, chunks / 2 blocks per tile
+  const int chunks = a.head_dim * (dtype == REC_ATTN_BF16 ? 2 : 4) / 16;
+  const unsigned blocks = (unsigned)(n_tiles * (chunks / 2));
+  if (dtype == REC_ATTN_BF16) k_rope<__nv_bfloat16><<<blocks, 256, 0, st>>>(a);
+  else k_rope<float><<<blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -9,14 +9,25 @@
 namespace recattn {
 
 struct WsLayout {
-  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, it, rc, ro, rf, qk, tr, rq, rk, total;
+  size_t hdr, meta, box, rec, cls, kl, kc, qc, qr, it, rc, ro, rf, qk, tr, ks, ps, mi, mt, rq, rk, total;
+  int mcap;
 };
+
+// Slots of the mask table: enough for a few PARTIAL tile pairs per tile (causal and
+// windowed masks have one to five), never more than there are pairs.
+inline int mask_capacity(long long NT, long long NC) {
+  const long long c = 8 * NT + 1024;
+  return (int)(c < NC ? c : NC);
+}
 
 inline size_t ws_up(size_t x) { return (x + 255) & ~size_t(255); }
 
-// rot_bytes: bytes of one rotated [T][H][d] copy (0 when the RoPE is off).
-inline WsLayout ws_layout(long long batch, long long NT, long long NC, long long heads, size_t rot_bytes) {
+// rot_bytes: bytes of one rotated [T][H][d] copy (0 when the RoPE is off); mcap: slots
+// of the mask table (0: none).
+inline WsLayout ws_layout(long long batch, long long NT, long long NC, long long heads, size_t rot_bytes,
+                          int mcap) {
   WsLayout L;
+  L.mcap = mcap;
   size_t off = 0;
   L.hdr = off; off = ws_up(off + 256);
   L.meta = off; off = ws_up(off + sizeof(ReqMeta) * (size_t)batch);
@@ -33,6 +44,10 @@ inline WsLayout ws_layout(long long batch, long long NT, long long NC, long long
   L.ro = off; off = ws_up(off + 4 * (size_t)batch);
   L.rf = off; off = ws_up(off + 4 * ((size_t)batch + 1));
   L.qk = off; off = ws_up(off + 4 * (size_t)batch);
+  L.ks = off; off = ws_up(off + 4 * (size_t)NC);
+  L.ps = off; off = ws_up(off + 4 * (size_t)NC);
+  L.mi = off; off = ws_up(off + 8 * (size_t)mcap);
+  L.mt = off; off = ws_up(off + 16 * (size_t)kTile * (size_t)mcap);
   L.rq = off; off = ws_up(off + rot_bytes);
   L.rk = off; off = ws_up(off + rot_bytes);
   L.total = off;
@@ -58,6 +73,11 @@ inline PlanDev ws_bind(char* w, const WsLayout& L) {
   pd.roff = reinterpret_cast<int*>(w + L.rf);
   pd.qkeep = reinterpret_cast<int*>(w + L.qk);
   pd.treq = reinterpret_cast<int*>(w + L.tr);
+  pd.kslot = reinterpret_cast<int*>(w + L.ks);
+  pd.pslot = reinterpret_cast<int*>(w + L.ps);
+  pd.minfo = reinterpret_cast<int2*>(w + L.mi);
+  pd.mtab = reinterpret_cast<uint32_t*>(w + L.mt);
+  pd.mcap = L.mcap;
   return pd;
 }
 
