@@ -87,9 +87,25 @@ __device__ __forceinline__ T warp_max(T v) {
   return v;
 }
 
+// hist[bin] += 1 for every active lane with one shared atomic per distinct bin of the
+// warp (many lanes often share a bin); returns the counter's old value plus the lane's
+// rank among the lanes with its bin.  Every lane of the warp calls it.
+__device__ __forceinline__ int agg_inc(int* hist, int bin, bool active) {
+  const unsigned grp = __match_any_sync(0xffffffffu, active ? bin : -1);
+  const int lane = threadIdx.x & 31, leader = __ffs(grp) - 1;
+  int base = 0;
+  if (active && lane == leader) base = atomicAdd(&hist[bin], __popc(grp));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(grp & ((1u << lane) - 1u));
+}
+
 constexpr int kPlanThreads = 512;
 constexpr int kCostBins = 4096;
 constexpr int kStageTiles = 4096;
+// shared scratch of the planner: the request's tile boxes while the pairs are
+// classified, then (last block only) the cost histogram and per-tile costs
+constexpr int kScratchBytes = 4 * (kCostBins + kStageTiles);
+constexpr int kStageBoxTiles = kScratchBytes / (int)(kTypes * sizeof(TileBox));  // 256
 
 // In-place exclusive scan of kCostBins counters by one block of kPlanThreads threads.
 __device__ void block_exclusive_scan_bins(int* hist, int* part) {
@@ -116,6 +132,7 @@ __device__ void block_exclusive_scan_bins(int* hist, int* part) {
 __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, PlanDev pd,
                                                        const long long* offsets, const long long* t,
                                                        const int8_t* ty, long long n_tiles) {
+  __shared__ __align__(16) unsigned char s_scratch[kScratchBytes];
   const int b = blockIdx.x;
   const ReqMeta m = pd.meta[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
@@ -221,12 +238,19 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
     pd.qkeep[b] = pos;
   }
 
-  // Phase 2: class of every (query tile, key tile) pair of the request.
+  // Phase 2: class of every (query tile, key tile) pair of the request, with the
+  // request's boxes staged in shared memory when they fit.
   const long long npairs = (long long)m.ntiles * m.ntiles;
+  const bool staged_boxes = m.ntiles <= kStageBoxTiles;
+  TileBox* s_box = reinterpret_cast<TileBox*>(s_scratch);
+  if (staged_boxes)
+    for (int i = threadIdx.x; i < m.ntiles * kTypes; i += blockDim.x) s_box[i] = pd.boxes[m.tile_start * kTypes + i];
+  __syncthreads();
+  const TileBox* boxes = staged_boxes ? s_box : pd.boxes + m.tile_start * kTypes;
   for (long long idx = threadIdx.x; idx < npairs; idx += blockDim.x) {
     const int qt = (int)(idx / m.ntiles), kt = (int)(idx % m.ntiles);
-    const TileBox* qb = pd.boxes + (m.tile_start + qt) * kTypes;
-    const TileBox* kb = pd.boxes + (m.tile_start + kt) * kTypes;
+    const TileBox* qb = boxes + qt * kTypes;
+    const TileBox* kb = boxes + kt * kTypes;
     int lo = kAll, hi = kNone;
     for (int a = 0; a < kTypes; ++a) {
       const TileBox q = qb[a];
@@ -316,9 +340,9 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   //    head by head, inside a head from the last query tile to the first, so the
   //    items running at the same time share K'/V tiles in L2.
   __shared__ int s_ticket;
-  __shared__ int s_hist[kCostBins];
+  int* s_hist = reinterpret_cast<int*>(s_scratch);  // [kCostBins] (the boxes are no longer read)
+  int* s_qc = s_hist + kCostBins;                    // [kStageTiles] per-tile costs (n_tiles <= kStageTiles)
   __shared__ int s_part[kPlanThreads];
-  __shared__ int s_qc[kStageTiles];  // per-tile costs (when n_tiles <= kStageTiles)
   __shared__ unsigned long long s_sum;
   __shared__ int s_max, s_nheavy;
   __threadfence();
@@ -339,10 +363,16 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
       if (staged) s_qc[q] = c;
       part += (unsigned long long)c;
     }
-    atomicAdd(&s_sum, part);
     int rmax = 1;
     for (int r = threadIdx.x; r < B; r += blockDim.x) rmax = max(rmax, __ldcg(pd.rcost + r));
-    atomicMax(&s_max, rmax);
+    // one shared atomic per warp (512 contending ones took microseconds)
+#pragma unroll
+    for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    rmax = warp_max(rmax);
+    if ((threadIdx.x & 31) == 0) {
+      atomicAdd(&s_sum, part);
+      atomicMax(&s_max, rmax);
+    }
   }
   __syncthreads();
   const long long total = (long long)s_sum;
@@ -370,13 +400,19 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   }
   // requests by cost, descending
   const long long mx = s_max;
-  for (int r = threadIdx.x; r < B; r += blockDim.x)
-    atomicAdd(&s_hist[kCostBins - 1 - (int)((long long)__ldcg(pd.rcost + r) * (kCostBins - 1) / mx)], 1);
+  // (whole warps in both loops: requests of equal cost share a bin)
+  for (int r0 = threadIdx.x & ~31; r0 < B; r0 += blockDim.x) {
+    const int r = r0 + (threadIdx.x & 31);
+    const int key = r < B ? (int)((long long)__ldcg(pd.rcost + r) * (kCostBins - 1) / mx) : 0;
+    agg_inc(s_hist, kCostBins - 1 - key, r < B);
+  }
   __syncthreads();
   block_exclusive_scan_bins(s_hist, s_part);
-  for (int r = threadIdx.x; r < B; r += blockDim.x) {
-    const int key = (int)((long long)__ldcg(pd.rcost + r) * (kCostBins - 1) / mx);
-    pd.rorder[atomicAdd(&s_hist[kCostBins - 1 - key], 1)] = r;
+  for (int r0 = threadIdx.x & ~31; r0 < B; r0 += blockDim.x) {
+    const int r = r0 + (threadIdx.x & 31);
+    const int key = r < B ? (int)((long long)__ldcg(pd.rcost + r) * (kCostBins - 1) / mx) : 0;
+    const int pos = agg_inc(s_hist, kCostBins - 1 - key, r < B);
+    if (r < B) pd.rorder[pos] = r;
   }
   __syncthreads();
   // light items per request (in rorder order) -> first light item of each request
