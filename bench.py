@@ -370,9 +370,13 @@ def run_ours(args):
         fwd(p, q, k, v)
         return p
 
-    # grow the library's workspace pool to K live plans first, so no timed step
-    # waits on a driver allocation
+    # grow the library's workspace pool to K live plans first (with the backward's
+    # workspace, made on a plan's first backward call), so no timed step waits on a
+    # driver allocation
     pre = [mkplan(off_d, t, ty, stream) for _ in range(args.steps)]
+    if args.backward:
+        for p_ in pre:
+            fwd(p_, q, k, v)
     for p_ in pre:
         bd.rec_attn_free(p_)
     for _ in range(max(args.warmup, 3)):

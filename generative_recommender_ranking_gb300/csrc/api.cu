@@ -508,10 +508,13 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   if (T == 0) return REC_ATTN_OK;
   const bool tc = p.dtype == REC_ATTN_BF16;
   const long long n_items = plan->NT * p.num_heads;
-  // bf16 workspace: descriptors [2][n_items] | row constants [H][NT][128] | lists [NC]
+  // bf16 workspace: descriptors [2][n_items] | row constants [H][NT][128] | lists [NC] |
+  // their mask-table slots [NC] | the mask table's columns [mcap][128][4]
   const size_t off_rowc = (size_t)2 * n_items * sizeof(BwdItemDesc);
   const size_t off_ql = off_rowc + (size_t)plan->NT * p.num_heads * kTile * sizeof(float2);
-  const size_t ws_bytes = tc ? off_ql + (size_t)plan->NC * sizeof(uint32_t) : (size_t)T * p.num_heads * sizeof(float);
+  const size_t off_qs = off_ql + (((size_t)plan->NC * sizeof(uint32_t) + 15) & ~(size_t)15);
+  const size_t off_ct = off_qs + (((size_t)plan->NC * sizeof(int) + 15) & ~(size_t)15);
+  const size_t ws_bytes = tc ? off_ct + (size_t)plan->pd.mcap * kTile * 16 : (size_t)T * p.num_heads * sizeof(float);
   if (!plan->bwd_ws) {
     cudaMemPool_t pool;
     e = pool_for(plan->device, &pool);
@@ -548,6 +551,9 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   a.desc = tc ? reinterpret_cast<const BwdItemDesc*>(bws) : nullptr;
   a.rowc = tc ? reinterpret_cast<float2*>(bws + off_rowc) : nullptr;
   a.qlist = tc ? reinterpret_cast<const uint32_t*>(bws + off_ql) : nullptr;
+  a.kslot = plan->pd.kslot; a.mtab = plan->pd.mtab;
+  a.qslot = tc ? reinterpret_cast<const int*>(bws + off_qs) : nullptr;
+  a.ctab = tc ? reinterpret_cast<const uint32_t*>(bws + off_ct) : nullptr;
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.rows = T * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale;
   a.rotate = p.use_rope; a.mask = plan->mask;
@@ -563,7 +569,10 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
     sa.cls = plan->pd.cls; sa.t = plan->t; sa.n_tiles = plan->NT; sa.n_items = n_items; sa.heads = p.num_heads;
     sa.desc = reinterpret_cast<BwdItemDesc*>(bws);
     sa.qlist = reinterpret_cast<uint32_t*>(bws + off_ql);
-    e = launch_bwd_schedule(sa, st);
+    sa.pslot = plan->pd.pslot; sa.qslot = reinterpret_cast<int*>(bws + off_qs);
+    sa.counters = plan->pd.counters; sa.mtab = plan->pd.mtab;
+    sa.ctab = reinterpret_cast<uint32_t*>(bws + off_ct); sa.mcap = plan->pd.mcap;
+    e = launch_bwd_schedule(sa, plan->num_sms, st);
     if (e != cudaSuccess) return from_cuda(e);
     plan->bwd_sched = true;
   }

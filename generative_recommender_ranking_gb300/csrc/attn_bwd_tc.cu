@@ -37,7 +37,9 @@
 // visibility bits (row_mask.cuh), built from the key tile's planner record; in DKV
 // each thread first acts as a row of the query tile, builds that row's bits against
 // the item's key tile, and the warps transpose the bits into per-key columns with
-// shuffles.  FULL tiles skip the mask.  The MMAs of one thread run in issue order, so
+// shuffles.  PARTIAL pairs with a slot in the plan's mask table skip both: DQ reads the
+// table's rows, DKV its columns (transposed once per plan by k_bwd_colmask), bulk-copied
+// with the streamed tile.  FULL tiles skip the mask.  The MMAs of one thread run in issue order, so
 // an MMA that overwrites TMEM columns an earlier MMA reads needs no wait.  Every
 // mbarrier wait is bounded (REC_ATTN_ERR_TIMEOUT in the status word).
 #include <cuda_bf16.h>
@@ -57,6 +59,8 @@ constexpr int kStep = 64;                   // keys (DQ) or queries (DKV) per MM
 constexpr int kTileBytes = kTile * kD * 2;  // one [128][64] bf16 tile, 128-byte swizzled
 constexpr int kNS = 2;                      // stages of the streamed ring
 constexpr int kRecB = (int)sizeof(KeyTileRec);
+constexpr int kMaskB = kTile * 16;  // a PARTIAL pair's 128 rows (or columns) of the mask table
+constexpr int kStageRecB = kMaskB > kRecB ? kMaskB : kRecB;  // per streamed stage: one or the other
 constexpr int kThreadsB = 192;
 constexpr uint32_t kCols = 256;
 constexpr uint64_t kWaitNsB = 2000000000ull;  // 2 s
@@ -86,7 +90,7 @@ struct BL {
   static constexpr int kRes = 0;                             // [2] resident tiles
   static constexpr int kStr = kRes + 2 * kTileBytes;         // [kNS][2] streamed tiles
   static constexpr int kSRec = kStr + 2 * kNS * kTileBytes;  // [kNS] records of the streamed tiles
-  static constexpr int kSRow = kSRec + kNS * kRecB;          // DKV: [kNS] row constants of the query tiles
+  static constexpr int kSRow = kSRec + kNS * kStageRecB;     // DKV: [kNS] row constants of the query tiles
   static constexpr int kRRec = kSRow + kNS * kRowB;          // record of the item's tile
   static constexpr int kRRow = kRRec + kRecB;                // DQ: row constants of the query tile
   static constexpr int kCol = kRRow + kRowB;                 // DKV: [2][128 keys] 128 query bits
@@ -161,16 +165,21 @@ __device__ __forceinline__ bool next_item(uint8_t* sm, uint64_t* bars, uint32_t&
   return true;
 }
 
-// The streamed tiles of an item, in order: request-local tile index and class.
+// The streamed tiles of an item, in order: request-local tile index, class and
+// mask-table slot (-1: none).
 struct Cursor {
   const uint32_t* list;
+  const int* slots;
   int r;
-  __device__ __forceinline__ void init(const uint32_t* base, const BwdItemDesc& d) {
+  __device__ __forceinline__ void init(const uint32_t* base, const int* slot_base, const BwdItemDesc& d) {
     list = base + d.list;
+    slots = slot_base + d.list;
     r = 0;
   }
-  __device__ __forceinline__ void next(int& tile, int& cls) {
-    const uint32_t e = list[r++];
+  __device__ __forceinline__ void next(int& tile, int& cls, int& slot) {
+    const uint32_t e = list[r];
+    slot = slots[r];
+    ++r;
     tile = (int)(e & 0xffffffu);
     cls = (int)(e >> 24);
   }
@@ -228,20 +237,28 @@ __device__ void bwd_producer(const BwdArgs& a, const void* const (&res)[2], cons
       res_ph = it_n & 1;
       ++it_n;
       Cursor cur;
-      cur.init(lists, d);
+      cur.init(lists, DKV ? a.qslot : a.kslot, d);
       for (int j = 0; j < d.n; ++j) {
-        int tile, cls;
-        cur.next(tile, cls);
+        int tile, cls, tslot;
+        cur.next(tile, cls, tslot);
         const int st = (int)(s_it % kNS);
         const uint32_t ph = (s_it / kNS) & 1;
         if (!bw_wait(bars + kStrEmpty + st, ph ^ 1, abort_flag, a.status)) goto drain;
         const long long gs = (long long)d.tile_start + tile;
-        const bool rec = DKV || cls != REC_ATTN_TILE_FULL;  // DQ reads a key record on PARTIAL tiles only
+        // PARTIAL tiles with a mask-table slot: the tile's rows (DQ) or columns (DKV) of the
+        // table; otherwise DQ reads the key record on PARTIAL tiles, DKV the query record
+        const bool tab = cls != REC_ATTN_TILE_FULL && tslot >= 0;
+        const bool rec = !tab && (DKV || cls != REC_ATTN_TILE_FULL);
         const int ys = (int)(d.tok_start + (long long)tile * kTile);
-        ptx::mbar_arrive_expect_tx(bars + kStrFull + st, 2 * kTileBytes + (rec ? kRecB : 0) + (DKV ? kRowB : 0));
+        ptx::mbar_arrive_expect_tx(bars + kStrFull + st,
+                                   2 * kTileBytes + (tab ? kMaskB : rec ? kRecB : 0) + (DKV ? kRowB : 0));
         ptx::tma_load_2d(sm + BL::kStr + (2 * st) * kTileBytes, str[0], x, ys, bars + kStrFull + st);
         ptx::tma_load_2d(sm + BL::kStr + (2 * st + 1) * kTileBytes, str[1], x, ys, bars + kStrFull + st);
-        if (rec) ptx::bulk_load(sm + BL::kSRec + st * kRecB, a.krec + gs, kRecB, bars + kStrFull + st);
+        if (tab)
+          ptx::bulk_load(sm + BL::kSRec + st * kStageRecB, (DKV ? a.ctab : a.mtab) + (long long)tslot * (kMaskB / 4),
+                         kMaskB, bars + kStrFull + st);
+        else if (rec)
+          ptx::bulk_load(sm + BL::kSRec + st * kStageRecB, a.krec + gs, kRecB, bars + kStrFull + st);
         if (DKV) ptx::bulk_load(sm + BL::kSRow + st * kRowB, rows_h + gs * kTile, kRowB, bars + kStrFull + st);
         str_used[st] = true;
         str_ph[st] = ph;
@@ -425,7 +442,7 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
   const int lane = threadIdx.x & 31, quad = (threadIdx.x >> 5) & 3, row = quad * 32 + lane;
   const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
   const float sl2 = a.scale * kLog2e;
-  const KeyTileRec* srec = reinterpret_cast<const KeyTileRec*>(sm + BL::kSRec);
+  const uint8_t* sstage = sm + BL::kSRec;  // per stage: key record or mask-table rows
   const KeyTileRec* rrec = reinterpret_cast<const KeyTileRec*>(sm + BL::kRRec);
   const float2* rrow = reinterpret_cast<const float2*>(sm + BL::kRRow);
   const int H = a.heads;
@@ -453,10 +470,10 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
     RowMask rm;
     row_mask_setup(a.mask, live, pi, ti, tyi, rm);
     Cursor cur;
-    cur.init(a.klist, it);
+    cur.init(a.klist, a.kslot, it);
     for (int j = 0; j < it.n; ++j) {
-      int kt, cls;
-      cur.next(kt, cls);
+      int kt, cls, tslot;
+      cur.next(kt, cls, tslot);
       const int st = (int)(s_it % kNS);
       const uint32_t ph = (s_it / kNS) & 1;
       ++s_it;
@@ -464,7 +481,12 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
       uint32_t vm[4] = {f, f, f, f};
       if (cls != REC_ATTN_TILE_FULL) {
         if (!bw_wait_warp(bars + kStrFull + st, ph, abort_flag, a.status)) return;
-        build_mask(rm, srec + st, kt * kTile, vm);
+        if (tslot >= 0) {  // the row's words of the mask table (zero for rows that see no key)
+          const uint4 w = reinterpret_cast<const uint4*>(sstage + st * kStageRecB)[row];
+          vm[0] = w.x; vm[1] = w.y; vm[2] = w.z; vm[3] = w.w;
+        } else {
+          build_mask(rm, reinterpret_cast<const KeyTileRec*>(sstage + st * kStageRecB), kt * kTile, vm);
+        }
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + kStrEmpty + st);  // the stage's record was read
@@ -546,7 +568,7 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
   const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
   const float sl2 = a.scale * kLog2e;
   const KeyTileRec* rrec = reinterpret_cast<const KeyTileRec*>(sm + BL::kRRec);
-  const KeyTileRec* srec = reinterpret_cast<const KeyTileRec*>(sm + BL::kSRec);
+  const uint8_t* sstage = sm + BL::kSRec;  // per stage: query record or mask-table columns
   const float2* srow = reinterpret_cast<const float2*>(sm + BL::kSRow);
   uint32_t* colS = reinterpret_cast<uint32_t*>(sm + BL::kCol);
   const int H = a.heads;
@@ -565,16 +587,30 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
     if (!bw_wait_warp(bars + kResFull, it_n & 1, abort_flag, a.status)) return;  // the key tile's record
     const long long tj = rrec->t[row];
     Cursor cur;
-    cur.init(a.qlist, it);
-    // Column bits of the item's j-th query tile (stage st) into buffer `buf`: as query
-    // row `row` of the tile, this thread builds the row's bits over the key tile; each
-    // warp then transposes its 32 rows into per-key words.
-    auto prepare = [&](int j, int qt, int cls, int st, uint32_t ph, uint32_t buf) -> bool {
+    cur.init(a.qlist, a.qslot, it);
+    // Column bits of the item's j-th query tile (stage st) into buffer `buf`: the key's
+    // words of the mask table's columns when the pair has a slot; otherwise, as query
+    // row `row` of the tile, this thread builds the row's bits over the key tile and
+    // each warp transposes its 32 rows into per-key words.
+    auto prepare = [&](int j, int qt, int cls, int tslot, int st, uint32_t ph, uint32_t buf) -> bool {
       if (!bw_wait_warp(bars + kStrFull + st, ph, abort_flag, a.status)) return false;
+      // after the item's last read of the key tile's record, its buffer may be refilled
+      auto release_rec = [&]() {
+        if (j == it.n - 1) {
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bars + kResEmpty);
+        }
+      };
+      if (cls != REC_ATTN_TILE_FULL && tslot >= 0) {
+        reinterpret_cast<uint4*>(colS + buf * (kTile * 4))[row] =
+            reinterpret_cast<const uint4*>(sstage + st * kStageRecB)[row];
+        release_rec();
+        return true;
+      }
       const int qi = qt * kTile + row;
       long long tq;
       int tyq;
-      rec_row(srec + st, row, tq, tyq);
+      rec_row(reinterpret_cast<const KeyTileRec*>(sstage + st * kStageRecB), row, tq, tyq);
       const bool live = qi < it.len && srow[st * kTile + row].x != -INFINITY;
       const uint32_t f = live ? ~0u : 0u;
       uint32_t vm[4] = {f, f, f, f};
@@ -583,18 +619,15 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         row_mask_setup(a.mask, live, qi, tq, tyq, rm);
         build_mask(rm, rrec, it.tile * kTile, vm);
       }
-      if (j == it.n - 1) {  // the key tile's record is not read again in this item
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + kResEmpty);
-      }
+      release_rec();
 #pragma unroll
       for (int wd = 0; wd < 4; ++wd) colS[buf * (kTile * 4) + (32 * wd + lane) * 4 + quad] = transpose32(vm[wd], lane);
       return true;
     };
-    int qt, cls;
-    cur.next(qt, cls);
+    int qt, cls, tslot;
+    cur.next(qt, cls, tslot);
     int st = (int)(s_it % kNS);
-    if (!prepare(0, qt, cls, st, (s_it / kNS) & 1, cbuf)) return;
+    if (!prepare(0, qt, cls, tslot, st, (s_it / kNS) & 1, cbuf)) return;
     ++s_it;
     for (int j = 0; j < it.n; ++j) {
       // every thread's words of this tile are written, and every thread has read the
@@ -602,10 +635,10 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
       if (!group_sync(bars + kGroup, grp, abort_flag, a.status)) return;
       const uint4 cm = reinterpret_cast<const uint4*>(colS)[cbuf * kTile + row];
       const float2* rows = srow + st * kTile;
-      int nqt = 0, ncls = 0, nst = 0;
+      int nqt = 0, ncls = 0, nslot = -1, nst = 0;
       uint32_t nph = 0;
       if (j + 1 < it.n) {
-        cur.next(nqt, ncls);
+        cur.next(nqt, ncls, nslot);
         nst = (int)(s_it % kNS);
         nph = (s_it / kNS) & 1;
         ++s_it;
@@ -650,7 +683,7 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         return true;
       };
       if (!do_step(0)) return;
-      if (j + 1 < it.n && !prepare(j + 1, nqt, ncls, nst, nph, cbuf ^ 1u)) return;
+      if (j + 1 < it.n && !prepare(j + 1, nqt, ncls, nslot, nst, nph, cbuf ^ 1u)) return;
       if (!do_step(1)) return;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + kStrEmpty + st);  // the stage's record and constants were read
@@ -726,12 +759,16 @@ __global__ void __launch_bounds__(128) k_bwd_schedule(BwdSchedArgs s) {
   if (i < s.n_tiles) {
     const ReqMeta m = s.meta[s.qreq[i]];
     const int kt = (int)(i - m.tile_start);
-    const uint8_t* col = s.cls + m.cls_start + kt;
     uint32_t* out = s.qlist + m.cls_start + (long long)kt * m.ntiles;
+    int* out_slot = s.qslot + m.cls_start + (long long)kt * m.ntiles;
     int n = 0;
     for (int qt = 0; qt < m.ntiles; ++qt) {
-      const int c = col[(long long)qt * m.ntiles];
-      if (c != REC_ATTN_TILE_SKIP) out[n++] = (uint32_t)qt | ((uint32_t)c << 24);
+      const long long pair = m.cls_start + (long long)qt * m.ntiles + kt;
+      const int c = s.cls[pair];
+      if (c == REC_ATTN_TILE_SKIP) continue;
+      out[n] = (uint32_t)qt | ((uint32_t)c << 24);
+      out_slot[n] = c == REC_ATTN_TILE_PARTIAL ? s.pslot[pair] : -1;
+      ++n;
     }
     return;
   }
@@ -759,6 +796,21 @@ __global__ void __launch_bounds__(128) k_bwd_schedule(BwdSchedArgs s) {
   d.tile = kt;
   d.n = n;
   s.desc[s.n_items + w] = d;
+}
+
+// The mask table's columns (once per plan): per slot, each warp transposes its 32 query
+// rows' words into per-key words, so key j of the tile finds the 128 query bits of its
+// column as four words.
+__global__ void __launch_bounds__(kTile) k_bwd_colmask(BwdSchedArgs s) {
+  const int used = min(__ldcg(s.counters + 7), s.mcap);
+  const int r = threadIdx.x, lane = r & 31, quad = r >> 5;
+  for (int slot = blockIdx.x; slot < used; slot += gridDim.x) {
+    const uint4 w = reinterpret_cast<const uint4*>(s.mtab)[(long long)slot * kTile + r];
+    const uint32_t vm[4] = {w.x, w.y, w.z, w.w};
+    uint32_t* out = s.ctab + (long long)slot * kTile * 4;
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) out[(32 * wd + lane) * 4 + quad] = transpose32(vm[wd], lane);
+  }
 }
 
 // ------------------------------------------------------------------ kernel
@@ -843,10 +895,13 @@ cudaError_t launch_mode(const CUtensorMap (&maps)[4], const BwdArgs& a, int grid
 
 }  // namespace
 
-cudaError_t launch_bwd_schedule(const BwdSchedArgs& s, cudaStream_t st) {
+cudaError_t launch_bwd_schedule(const BwdSchedArgs& s, int num_sms, cudaStream_t st) {
   const long long n = s.n_tiles + s.n_items;
   if (n <= 0) return cudaSuccess;
   k_bwd_schedule<<<(unsigned)((n + 127) / 128), 128, 0, st>>>(s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || s.mcap <= 0) return e;
+  k_bwd_colmask<<<s.mcap < 8 * num_sms ? s.mcap : 8 * num_sms, kTile, 0, st>>>(s);
   return cudaGetLastError();
 }
 

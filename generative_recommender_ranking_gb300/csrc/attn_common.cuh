@@ -75,6 +75,10 @@ struct BwdArgs {
   const BwdItemDesc* desc;  // [2][n_items]: dQ items, then dK/dV items (mirrored key tiles)
   const uint32_t* qlist;    // per key tile: query tiles with a non-SKIP class (qt | class << 24)
   float2* rowc;             // [H][n_tiles][128]: {lse * log2(e) (-inf: the row sees no key), D}
+  const int* kslot;         // per key-tile list entry: mask-table slot (-1: build the bits)
+  const uint32_t* mtab;     // mask table, rows: [slot][128 query rows][4 words over the keys]
+  const int* qslot;         // per query-tile list entry (qlist): mask-table slot, -1 if none
+  const uint32_t* ctab;     // mask table, columns: [slot][128 keys][4 words over the queries]
   const int* kcount;       // per query tile: entries in its key-tile list
   const uint32_t* klist;   // per query tile: non-SKIP key tiles (kt | class << 24)
   const uint8_t* cls;      // per request: ntiles x ntiles class matrix
@@ -110,6 +114,12 @@ struct BwdSchedArgs {
   int heads;
   BwdItemDesc* desc;
   uint32_t* qlist;
+  const int* pslot;         // per (query tile, key tile): mask-table slot, -1 if none
+  int* qslot;               // written: per qlist entry, the pair's slot
+  const int* counters;      // [7]: mask-table slots handed out
+  const uint32_t* mtab;
+  uint32_t* ctab;           // written: the table's columns
+  int mcap;
 };
 
 // Fused steps of the prologue, applied before the rotation: QK-RMSNorm
