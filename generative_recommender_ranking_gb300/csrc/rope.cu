@@ -159,30 +159,27 @@ template <typename E>
 __global__ void __launch_bounds__(256, 3) k_rope_fused(RopeArgs a, FusedArgs f) {
   using C = Chunk<E>;
   constexpr int kPairs = C::kPairs;
-  const long long g = blockIdx.x;
+  // one (token, chunk) unit per thread, 256 / chunks tokens of one tile per block (as in
+  // k_rope); a block's warps hold whole head rows, so every lane runs the row sums
+  const int chunks = a.head_dim / (2 * kPairs);
+  const int tpb = (int)blockDim.x / chunks;  // tokens per block
+  const int bpt = kTile / tpb;               // blocks per tile
+  const long long g = blockIdx.x / bpt;
   const ReqMeta m = a.meta[a.tile_req[g]];
   const int tl = (int)(g - m.tile_start);
-  const long long t_ref = a.t[m.tok_start];
-  const int chunks = a.head_dim / (2 * kPairs);
   const int rows = min(kTile, m.len - tl * kTile);
-  const int total = rows * chunks;
-  const int lane = threadIdx.x & 31;
   const long long head_bytes = (long long)a.head_dim * (long long)sizeof(E);
-  for (int base = threadIdx.x - lane; base < total; base += blockDim.x) {
-    const int idx = base + lane;
-    const bool act = idx < total;
-    const int r = act ? idx / chunks : 0, c = act ? idx - r * chunks : 0;
+  {
+    const int rr = (int)(blockIdx.x % bpt) * tpb + (int)threadIdx.x / chunks;
+    const bool act = rr < rows;  // inactive lanes carry zeros through the row sums
+    const int r = act ? rr : 0, c = (int)threadIdx.x % chunks;
     const long long tok = m.tok_start + tl * kTile + r;
-    const float dt = act ? (float)(a.t[tok] - t_ref) : 0.f;
-    float sn[kPairs], cs[kPairs];
-#pragma unroll
-    for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
     const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
     const bool qg = f.q_gate != nullptr, kg = f.k_gate != nullptr;
     // two heads at a time: their q, k and gate chunks (up to eight 16-byte loads) in flight
-    // together, kept raw until used
-    for (int h0 = 0; h0 < a.heads; h0 += 2) {
-      uint4 rq[2], rk[2], rgq[2], rgk[2];
+    // together, kept raw until used; the first two heads' loads go out before the angles
+    uint4 rq[2], rk[2], rgq[2], rgk[2];
+    auto load2 = [&](int h0) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         rq[u] = rk[u] = rgq[u] = rgk[u] = make_uint4(0u, 0u, 0u, 0u);
@@ -194,6 +191,14 @@ __global__ void __launch_bounds__(256, 3) k_rope_fused(RopeArgs a, FusedArgs f) 
           if (kg) rgk[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(f.k_gate) + off);
         }
       }
+    };
+    load2(0);
+    const float dt = act ? (float)(a.t[tok] - a.t[m.tok_start]) : 0.f;
+    float sn[kPairs], cs[kPairs];
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
+    for (int h0 = 0; h0 < a.heads; h0 += 2) {
+      if (h0 > 0) load2(h0);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         if (h0 + u >= a.heads) break;  // uniform across the block
@@ -228,8 +233,10 @@ __global__ void __launch_bounds__(256, 3) k_rope_fused(RopeArgs a, FusedArgs f) 
 
 cudaError_t launch_rope_fused(const RopeArgs& a, const FusedArgs& f, int dtype, long long n_tiles, cudaStream_t st) {
   if (n_tiles <= 0) return cudaSuccess;
-  if (dtype == REC_ATTN_BF16) k_rope_fused<__nv_bfloat16><<<(unsigned)n_tiles, 256, 0, st>>>(a, f);
-  else k_rope_fused<float><<<(unsigned)n_tiles, 256, 0, st>>>(a, f);
+  const int chunks = a.head_dim * (dtype == REC_ATTN_BF16 ? 2 : 4) / 16;
+  const unsigned blocks = (unsigned)(n_tiles * (chunks / 2));  // 256 / chunks tokens per block
+  if (dtype == REC_ATTN_BF16) k_rope_fused<__nv_bfloat16><<<blocks, 256, 0, st>>>(a, f);
+  else k_rope_fused<float><<<blocks, 256, 0, st>>>(a, f);
   return cudaGetLastError();
 }
 
