@@ -750,12 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // gated d = 64: registers move from the role warpgroup (warps 0-3) to the two softmax
-  // warpgroups; launched with 168 per thread (checked on the host): 128*56 + 256*224
-  // = 384*168
-  constexpr bool kSplitRegs = GATE && D == 64;
   if (warp < kRoleWarps) {
-    if constexpr (kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     const int s = warp & 1;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
@@ -764,7 +759,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       else run_mma<D>(a, sm, s, B, tmem, abort_flag);
     }
   } else {
-    if constexpr (kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
     const int s = (warp - kRoleWarps) >> 2;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
@@ -795,14 +789,6 @@ cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap&
   cudaError_t e =
       cudaFuncSetAttribute(k_attn_tc<D, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
   if (e != cudaSuccess) return e;
-  if (GATE && D == 64) {
-    // the register split inside the kernel needs 384 x 168 registers at launch; with
-    // fewer, setmaxnreg.inc could never be granted, so refuse to launch instead
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, k_attn_tc<D, GATE>);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs * kThreads < 128 * 56 + 256 * 224) return cudaErrorInvalidConfiguration;
-  }
   k_attn_tc<D, GATE><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
   return cudaGetLastError();
 }
