@@ -80,6 +80,26 @@ def _traffic(workload: str):
         return None
 
 
+def _compress_traffic(workload: str, spec: str):
+    """DRAM bytes of one compression launch from the committed ncu capture, or None (no
+    capture for this case, or the kernel sources changed since it was taken)."""
+    path = os.path.join(ROOT, "profiles", "k_compress_dram_traffic.json")
+    try:
+        import hashlib
+        with open(path) as f:
+            d = json.load(f)
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        x = d["cases"].get(f"{workload}/{spec}")
+        if h.hexdigest() != d["sources_sha256"] or x is None:
+            return None
+        return float(x["dram_bytes_read"] + x["dram_bytes_write"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def _workload(name, rank, batch=None):
     kw = {}
     if rank:
@@ -270,7 +290,9 @@ def run_compress(args):
                                         "width": int(x.shape[1]), "segments": segs,
                                         "l2": "flushed between timed steps (256 MiB write)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "k_compress",
+                     "frac": gbs / pk["hbm_gbs"],
+                     "traffic": _compress_traffic(args.workload, args.compress) if args.batch is None else None,
+                     "kernel": "k_compress",
                      "peak_source": pk["source"], "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": ms},
         "gpu_launches": args.steps}), flush=True)
     return 0
@@ -515,7 +537,10 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": all_flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": (7 if args.backward else 3) * args.steps,
+        # per step: k_plan, k_build_masks, k_rope, k_attn_tc; the backward adds k_rope,
+        # k_bwd_schedule, k_bwd_colmask (a new plan each step), k_bwd_rowc and the two
+        # k_bwd_tc modes (the fp32 path: k_rope, k_bwd_delta, k_bwd_dq, k_bwd_dkv)
+        "gpu_launches": (4 + ((6 if bf16 else 4) if args.backward else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
