@@ -104,3 +104,78 @@ def test_backward_rejects_pruned_plans_and_bad_pointers():
                             torch.empty_like(x))
     finally:
         bd.rec_attn_free(plan)
+
+
+def _sub_workload(w, reqs):
+    """The requests `reqs` of w as a workload of their own (attention never crosses a
+    request, so their gradients are those of the full batch) and their global rows."""
+    rows = np.concatenate([np.arange(w.offsets[b], w.offsets[b + 1]) for b in reqs])
+    lens = [int(w.offsets[b + 1] - w.offsets[b]) for b in reqs]
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    sub = W.Workload(**{**w.__dict__, "offsets": off, "t": w.t[rows], "types": w.types[rows],
+                        "q": w.q[rows], "k": w.k[rows], "v": w.v[rows]})
+    return sub, rows
+
+
+def _full_size_backward(w):
+    tens = gu.device_inputs(w)
+    plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    try:
+        out = torch.empty_like(tens["q"])
+        lse = torch.empty((w.total_tokens, w.num_heads), dtype=torch.float32, device=out.device)
+        bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out, lse)
+        g_host = _grad_inputs(w)
+        dout = gu.device_inputs(W.Workload(**{**w.__dict__, "q": g_host}))["q"]
+        dq, dk, dv = (torch.full_like(tens["q"], float("nan")) for _ in range(3))
+        bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], out, lse, dout, dq, dk, dv)
+        torch.cuda.synchronize()
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
+    return g_host, dout, lse, (dq, dk, dv)
+
+
+@pytest.mark.parametrize("name", ["cadet", "sort", "mtgr"])
+def test_backward_full_size_sampled_requests(name):
+    """The full-size workload in the launch configuration the benchmark times; whole
+    requests (first, last, longest and two seeded others) checked against the oracle."""
+    w = W.make(name)
+    g_host, _, _, grads = _full_size_backward(w)
+    lens = np.diff(w.offsets)
+    rng = np.random.default_rng(5)
+    reqs = sorted(set([0, w.batch - 1, int(np.argmax(lens))] + [int(x) for x in rng.choice(w.batch, 2, replace=False)]))
+    sub, rows = _sub_workload(w, reqs)
+    ref = oracle.attention_bwd(gu.oracle_params(sub), sub.offsets, sub.t, sub.types, sub.q, sub.k, sub.v,
+                               g_host[rows])
+    rel_tol, max_tol = _tol(w)
+    idx = torch.from_numpy(rows).to(grads[0].device)
+    for what, got, r in zip(("dq", "dk", "dv"), grads, ref):
+        assert not torch.isnan(got).any(), f"{what}: unwritten rows"
+        x = gu.to_f64(got[idx])
+        rel = np.linalg.norm(x - r) / max(np.linalg.norm(r), 1e-30)
+        mx = np.max(np.abs(x - r))
+        assert rel <= rel_tol and mx <= max_tol * max(np.max(np.abs(r)), 1e-30), (name, what, rel, mx)
+
+
+@pytest.mark.parametrize("name", ["cadet", "sort", "mtgr", "tm20k_window"])
+def test_backward_full_size_dv_column_sums(name):
+    """A property that holds at any size: each visible query row's probabilities sum to
+    one, so per head sum_j dV_j = sum of dO_i over the rows that see at least one key
+    (lse finite).  Checked per request against float64 sums of the bf16 gradients."""
+    w = W.make(name)
+    _, dout, lse, (_, _, dv) = _full_size_backward(w)
+    seen = torch.isfinite(lse)                                       # [T, H]
+    want = (dout.double() * seen[:, :, None]).cpu().numpy()
+    got = dv.double().cpu().numpy()
+    scale = np.abs(want).max()
+    for b in range(w.batch):
+        s, e = int(w.offsets[b]), int(w.offsets[b + 1])
+        if e == s:
+            continue
+        ws, gs = want[s:e].sum(0), got[s:e].sum(0)                   # [H, d]
+        # Unbiased roundings: P to bf16 before the dV contraction (each row's sum moves by
+        # at most 2^-9 relative) and dV itself to bf16 (2^-9 relative per row); their sums
+        # over the request have standard deviations below 2^-9 times the columns' norms.
+        # Eight of them; a lost 128-row tile of dO moves the sum by about sqrt(128).
+        tol = 8 * 2.0 ** -9 * (np.sqrt((want[s:e] ** 2).sum(0)) + np.sqrt((got[s:e] ** 2).sum(0))) + 1e-6 * scale
+        assert np.all(np.abs(gs - ws) <= tol), (name, b, float(np.max(np.abs(gs - ws) - tol)))
