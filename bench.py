@@ -503,7 +503,8 @@ def run_ours(args):
         if bf16:
             roof = {"bound": "tensor", "achieved": bwd_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": bwd_tflops / pk["bf16_tflops"], "traffic": None,
-                    "kernel": "k_bwd_delta + k_bwd_tc<dQ> + k_bwd_tc<dK,dV> (backward, tensor cores)",
+                    "kernel": "rec_attn_bwd: k_rope + k_bwd_rowc + k_bwd_tc<dQ> + k_bwd_tc<dK,dV> "
+                              "(+ the new plan's k_bwd_schedule, k_bwd_colmask; tensor cores)",
                     "peak_source": pk["source"],
                     "algorithmic_flops_per_launch": 2.5 * flops_fwd, "ms_per_launch": bwd_ms,
                     "forward_attention": fwd_part}
@@ -511,7 +512,7 @@ def run_ours(args):
             fp32_peak = FP32_FMA_PEAK_TFLOPS
             roof = {"bound": "alu", "achieved": bwd_tflops, "peak": fp32_peak, "unit": "TFLOP/s",
                     "frac": bwd_tflops / fp32_peak, "traffic": None,
-                    "kernel": "k_bwd_delta + k_bwd_dq + k_bwd_dkv (backward, CUDA cores, fp32)",
+                    "kernel": "rec_attn_bwd: k_rope + k_bwd_delta + k_bwd_dq + k_bwd_dkv (CUDA cores, fp32)",
                     "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2070 MHz",
                     "algorithmic_flops_per_launch": 2.5 * flops_fwd, "ms_per_launch": bwd_ms,
                     "forward_attention": fwd_part}
