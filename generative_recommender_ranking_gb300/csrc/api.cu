@@ -48,8 +48,9 @@ struct rec_attn_plan_s {
   CUtensorMap maps[3];
   // Planning runs on a library side stream (after the caller's stream has produced the
   // offsets, times and types: ev_in), so the RoPE prologue of rec_attn_fwd, on the
-  // caller's stream, overlaps the planning kernel.  The prologue waits only for the
-  // request-table upload (ev_meta); the attention kernel waits for the planner (ev_plan).
+  // caller's stream, overlaps the planning kernels.  The prologue waits for the
+  // request-table upload and, when long requests are split, the planner's first kernel
+  // (ev_meta); the attention kernel waits for the planner (ev_plan).
   cudaStream_t side = nullptr;
   cudaEvent_t ev_in = nullptr, ev_meta = nullptr, ev_plan = nullptr;
   // optional kernel timing: events around the RoPE prologue and the attention kernel
@@ -284,10 +285,9 @@ rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queri
       for (int i = 0; i < meta[b].ntiles; ++i) treq[meta[b].tile_start + i] = b;
     e = cudaMemcpyAsync(pd.meta, up.data(), up.size(), cudaMemcpyHostToDevice, plan->side);
   }
-  if (e == cudaSuccess) e = cudaEventRecord(plan->ev_meta, plan->side);
   if (e == cudaSuccess)
-    e = launch_plan(plan->mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t, plan->ty, batch, NT,
-                    plan->side);
+    e = launch_plan(plan->mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t,
+                    plan->ty, batch, NT, plan->ev_meta, plan->side);
   if (e == cudaSuccess) e = launch_build_masks(plan->mask, pd, plan->num_sms, plan->side);
   if (e == cudaSuccess) e = cudaEventRecord(plan->ev_plan, plan->side);
   if (e != cudaSuccess) {

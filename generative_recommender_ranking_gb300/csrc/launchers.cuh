@@ -7,9 +7,13 @@
 
 namespace recattn {
 
+// prologue_ok (may be null) is recorded on st once the RoPE prologue, on another stream,
+// may start: before the planner when it is one kernel, after its first kernel when a
+// long request's tiles are split over several blocks (so the second kernel's blocks,
+// launched first, are not queued behind the prologue's).
 cudaError_t launch_plan(const MaskP& mp, int heads, const PlanDev& pd, const long long* offsets_dev,
                         const long long* t, const int8_t* ty, int batch, long long n_tiles,
-                        cudaStream_t st);
+                        cudaEvent_t prologue_ok, cudaStream_t st);
 cudaError_t launch_build_masks(const MaskP& mp, const PlanDev& pd, int num_sms, cudaStream_t st);
 cudaError_t launch_count_pairs(const MaskP& mp, const PlanDev& pd, const long long* t,
                                const int8_t* ty, long long n_tiles, cudaStream_t st);

@@ -203,7 +203,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   mask.keep_user = -1;  // every query
   const long long* t = reinterpret_cast<const long long*>(timestamps_dev);
   if (e == cudaSuccess)
-    e = launch_plan(mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), t, types_dev, batch, NT, s);
+    e = launch_plan(mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), t, types_dev, batch, NT, nullptr, s);
   if (e != cudaSuccess) return status_of(e);
 
   const void* qs = q;

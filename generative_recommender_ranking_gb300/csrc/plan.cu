@@ -129,84 +129,124 @@ __device__ void block_exclusive_scan_bins(int* hist, int* part) {
   __syncthreads();
 }
 
+// The request holding tile g: the last b whose tiles start at or before g (an empty
+// request shares its first tile index with the next one and is passed over).
+__device__ __forceinline__ int request_of_tile(const ReqMeta* meta, int batch, long long g) {
+  int lo = 0, hi = batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (meta[mid].tile_start <= g) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+constexpr int kTileWarps = 8;   // k_plan_tiles: tiles per block, one warp each
+constexpr int kSplitTiles = 32;  // mean tiles per request from which a request's tiles are split
+
+// Phase 1 for tile tl of request m, by one warp: per-type bounding boxes, and the
+// key-tile record the attention kernels build visibility bits from.
+__device__ void tile_stats(const PlanDev& pd, const long long* t, const int8_t* ty, const ReqMeta& m, int tl,
+                           int lane) {
+  long long kt_t[4];
+  int kt_y[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int pos = tl * kTile + u * 32 + lane;
+    kt_t[u] = 0;
+    kt_y[u] = -1;
+    if (pos < m.len) {
+      const long long tt = t[m.tok_start + pos];
+      const int c = ty[m.tok_start + pos];
+      if ((unsigned)c > 3u || tt >= kTimeLimit || tt <= -kTimeLimit) set_status(pd.status, REC_ATTN_ERR_DEVICE_INPUT);
+      kt_t[u] = tt;
+      kt_y[u] = (unsigned)c > 3u ? -1 : c;
+    }
+  }
+  // next key's type and time, for the sortedness check of each type's run
+  long long nx_t[4];
+  int nx_y[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    nx_t[u] = __shfl_down_sync(0xffffffffu, kt_t[u], 1);
+    nx_y[u] = __shfl_down_sync(0xffffffffu, kt_y[u], 1);
+    const long long t0 = __shfl_sync(0xffffffffu, kt_t[u < 3 ? u + 1 : u], 0);
+    const int y0 = __shfl_sync(0xffffffffu, kt_y[u < 3 ? u + 1 : u], 0);
+    if (lane == 31) { nx_t[u] = t0; nx_y[u] = u < 3 ? y0 : -1; }
+  }
+  KeyTileRec* rec = pd.krec + (m.tile_start + tl);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) rec->t[u * 32 + lane] = kt_t[u];
+#pragma unroll
+  for (int c = 0; c < kTypes; ++c) {
+    int n = 0, pmn = 0x7fffffff, pmx = -1;
+    long long tmn = 0x7fffffffffffffffLL, tmx = -0x7fffffffffffffffLL - 1;
+    bool bad = false;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool mine = kt_y[u] == c;
+      const unsigned bits = __ballot_sync(0xffffffffu, mine);
+      if (lane == 0) rec->typebits[c][u] = bits;
+      if (mine) {
+        const int pos = tl * kTile + u * 32 + lane;
+        n += 1;
+        pmn = min(pmn, pos); pmx = max(pmx, pos);
+        tmn = min(tmn, kt_t[u]); tmx = max(tmx, kt_t[u]);
+        bad |= (nx_y[u] == c && nx_t[u] < kt_t[u]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    const int a0 = warp_min(pmn), a1 = warp_max(pmx);
+    const long long a2 = warp_min(tmn), a3 = warp_max(tmx);
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      TileBox bx;
+      bx.cnt = n; bx.pmin = a0; bx.pmax = a1; bx.pad = 0; bx.tmin = a2; bx.tmax = a3;
+      pd.boxes[(m.tile_start + tl) * kTypes + c] = bx;
+      rec->run_lo[c] = n ? a0 - tl * kTile : 0;
+      rec->run_n[c] = n;
+      rec->sorted[c] = (n > 0 && a1 - a0 + 1 == n && !any_bad) ? 1 : 0;
+      rec->pad[c] = 0;
+    }
+  }
+}
+
+// Phase 1 over the packed batch, one warp per tile (the planner's first kernel when a
+// request's query tiles are split over several blocks).  Also zeroes the per-request
+// costs those blocks add up.
+__global__ void __launch_bounds__(32 * kTileWarps) k_plan_tiles(PlanDev pd, const long long* t, const int8_t* ty,
+                                                               int batch, long long n_tiles) {
+  for (long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x; r < batch;
+       r += (long long)gridDim.x * blockDim.x)
+    pd.rcost[r] = 0;
+  const long long g = (long long)blockIdx.x * kTileWarps + (threadIdx.x >> 5);
+  if (g >= n_tiles) return;  // whole warps
+  const ReqMeta m = pd.meta[request_of_tile(pd.meta, batch, g)];
+  tile_stats(pd, t, ty, m, (int)(g - m.tile_start), threadIdx.x & 31);
+}
+
+// Phases 1 to 3 for one request (slices == 1), or phases 2 and 3 for one slice of it
+// (phase 1 then ran in k_plan_tiles): block b * slices + sl takes the query tiles
+// qt = sl, sl + slices, ... of request b, so few long requests still fill the GPU.
+// Phase 4 in the last block to finish.
 __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, PlanDev pd,
                                                        const long long* offsets, const long long* t,
-                                                       const int8_t* ty, long long n_tiles) {
+                                                       const int8_t* ty, int batch, int slices,
+                                                       long long n_tiles) {
   __shared__ __align__(16) unsigned char s_scratch[kScratchBytes];
-  const int b = blockIdx.x;
+  const int b = (int)(blockIdx.x / slices), sl = (int)(blockIdx.x % slices);
   const ReqMeta m = pd.meta[b];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   // the device offsets must describe the same requests as the host copy
-  if (threadIdx.x == 0 && (offsets[b] != m.tok_start || offsets[b + 1] != m.tok_start + m.len))
+  if (sl == 0 && threadIdx.x == 0 && (offsets[b] != m.tok_start || offsets[b + 1] != m.tok_start + m.len))
     set_status(pd.status, REC_ATTN_ERR_DEVICE_INPUT);
-
-  // Phase 1 (one warp per tile): per-type bounding boxes, and the key-tile record the
-  // attention kernel builds visibility bits from.
-  for (int tl = warp; tl < m.ntiles; tl += nwarps) {
-    long long kt_t[4];
-    int kt_y[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int pos = tl * kTile + u * 32 + lane;
-      kt_t[u] = 0;
-      kt_y[u] = -1;
-      if (pos < m.len) {
-        const long long tt = t[m.tok_start + pos];
-        const int c = ty[m.tok_start + pos];
-        if ((unsigned)c > 3u || tt >= kTimeLimit || tt <= -kTimeLimit) set_status(pd.status, REC_ATTN_ERR_DEVICE_INPUT);
-        kt_t[u] = tt;
-        kt_y[u] = (unsigned)c > 3u ? -1 : c;
-      }
-    }
-    // next key's type and time, for the sortedness check of each type's run
-    long long nx_t[4];
-    int nx_y[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      nx_t[u] = __shfl_down_sync(0xffffffffu, kt_t[u], 1);
-      nx_y[u] = __shfl_down_sync(0xffffffffu, kt_y[u], 1);
-      const long long t0 = __shfl_sync(0xffffffffu, kt_t[u < 3 ? u + 1 : u], 0);
-      const int y0 = __shfl_sync(0xffffffffu, kt_y[u < 3 ? u + 1 : u], 0);
-      if (lane == 31) { nx_t[u] = t0; nx_y[u] = u < 3 ? y0 : -1; }
-    }
-    KeyTileRec* rec = pd.krec + (m.tile_start + tl);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) rec->t[u * 32 + lane] = kt_t[u];
-#pragma unroll
-    for (int c = 0; c < kTypes; ++c) {
-      int n = 0, pmn = 0x7fffffff, pmx = -1;
-      long long tmn = 0x7fffffffffffffffLL, tmx = -0x7fffffffffffffffLL - 1;
-      bool bad = false;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const bool mine = kt_y[u] == c;
-        const unsigned bits = __ballot_sync(0xffffffffu, mine);
-        if (lane == 0) rec->typebits[c][u] = bits;
-        if (mine) {
-          const int pos = tl * kTile + u * 32 + lane;
-          n += 1;
-          pmn = min(pmn, pos); pmx = max(pmx, pos);
-          tmn = min(tmn, kt_t[u]); tmx = max(tmx, kt_t[u]);
-          bad |= (nx_y[u] == c && nx_t[u] < kt_t[u]);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-      const int a0 = warp_min(pmn), a1 = warp_max(pmx);
-      const long long a2 = warp_min(tmn), a3 = warp_max(tmx);
-      const bool any_bad = __any_sync(0xffffffffu, bad);
-      if (lane == 0) {
-        TileBox bx;
-        bx.cnt = n; bx.pmin = a0; bx.pmax = a1; bx.pad = 0; bx.tmin = a2; bx.tmax = a3;
-        pd.boxes[(m.tile_start + tl) * kTypes + c] = bx;
-        rec->run_lo[c] = n ? a0 - tl * kTile : 0;
-        rec->run_n[c] = n;
-        rec->sorted[c] = (n > 0 && a1 - a0 + 1 == n && !any_bad) ? 1 : 0;
-        rec->pad[c] = 0;
-      }
-    }
+  // this block's query tiles
+  const int nrows = m.ntiles > sl ? (m.ntiles - sl + slices - 1) / slices : 0;
+  if (slices == 1) {
+    for (int tl = warp; tl < m.ntiles; tl += nwarps) tile_stats(pd, t, ty, m, tl, lane);
+    __syncthreads();
   }
-  __syncthreads();
 
   // Query pruning: the position of the first kept user token, i.e. the keep_user-th
   // user token (GLOBAL or HIST) counted from the end of the request (0: every query).
@@ -235,12 +275,12 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
       }
     }
     s_keep = pos;
-    pd.qkeep[b] = pos;
+    if (sl == 0) pd.qkeep[b] = pos;
   }
 
-  // Phase 2: class of every (query tile, key tile) pair of the request, with the
-  // request's boxes staged in shared memory when they fit.
-  const long long npairs = (long long)m.ntiles * m.ntiles;
+  // Phase 2: class of every (query tile, key tile) pair of the block's query tiles, with
+  // the request's boxes staged in shared memory when they fit.
+  const long long npairs = (long long)nrows * m.ntiles;
   const bool staged_boxes = m.ntiles <= kStageBoxTiles;
   TileBox* s_box = reinterpret_cast<TileBox*>(s_scratch);
   if (staged_boxes)
@@ -248,7 +288,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   __syncthreads();
   const TileBox* boxes = staged_boxes ? s_box : pd.boxes + m.tile_start * kTypes;
   for (long long idx = threadIdx.x; idx < npairs; idx += blockDim.x) {
-    const int qt = (int)(idx / m.ntiles), kt = (int)(idx % m.ntiles);
+    const int qt = sl + (int)(idx / m.ntiles) * slices, kt = (int)(idx % m.ntiles);
     const TileBox* qb = boxes + qt * kTypes;
     const TileBox* kb = boxes + kt * kTypes;
     int lo = kAll, hi = kNone;
@@ -267,7 +307,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
     if (hi == kNone) cl = REC_ATTN_TILE_SKIP;
     else if (lo == kAll && k_full) cl = REC_ATTN_TILE_FULL;
     else cl = REC_ATTN_TILE_PARTIAL;
-    pd.cls[m.cls_start + idx] = cl;
+    pd.cls[m.cls_start + (long long)qt * m.ntiles + kt] = cl;
   }
   __syncthreads();
 
@@ -275,7 +315,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   __shared__ int s_rcost;
   if (threadIdx.x == 0) s_rcost = 0;
   __syncthreads();
-  for (int qt = warp; qt < m.ntiles; qt += nwarps) {
+  for (int ri = warp; ri < nrows; ri += nwarps) {
+    const int qt = sl + ri * slices;
     // a query tile whose every token is a user token before the first kept one
     // computes nothing: no key list, no cost, the kernels skip it
     const TileBox* qbx = pd.boxes + (m.tile_start + qt) * kTypes;
@@ -330,7 +371,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) pd.rcost[b] = s_rcost;
+  if (threadIdx.x == 0) {
+    if (slices == 1) pd.rcost[b] = s_rcost;
+    else if (s_rcost) atomicAdd(pd.rcost + b, s_rcost);
+  }
 
   // Phase 4: the last block to finish writes the work-item order.  The order only
   // affects load balance and cache reuse, never results.
@@ -351,7 +395,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   __syncthreads();
   if (s_ticket != (int)gridDim.x - 1) return;
   __threadfence();
-  const int B = gridDim.x;
+  const int B = batch;
   const bool staged = n_tiles <= kStageTiles;
   if (threadIdx.x == 0) { s_sum = 0; s_max = 1; s_nheavy = 0; }
   for (int i = threadIdx.x; i < kCostBins; i += blockDim.x) s_hist[i] = 0;
@@ -442,14 +486,36 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   }
   if (threadIdx.x == 0) pd.roff[B] = (int)carry;
   __syncthreads();
-  // one thread per (request, head): its light query tiles, last to first
-  for (long long kh = threadIdx.x; kh < (long long)B * heads; kh += blockDim.x) {
-    const int k = (int)(kh / heads), h = (int)(kh % heads);
-    const ReqMeta rm = pd.meta[__ldcg(pd.rorder + k)];
-    const int r0 = __ldcg(pd.roff + k), nl = (__ldcg(pd.roff + k + 1) - r0) / heads;
-    long long w = r0 + (long long)h * nl;
-    for (int qt = rm.ntiles - 1; qt >= 0; --qt)
-      if (heavy_items == 0 || !heavy(rm.tile_start + qt)) pd.items[w++] = (int)((rm.tile_start + qt) * heads + h);
+  // each (request, head): its light query tiles, last to first.  A warp takes 32 of
+  // them: each lane looks up one (its loads all in flight together), then the warp
+  // writes them one after the other, lane i taking the i-th tile of each group of 32
+  // counted from the end.
+  const long long n_kh = (long long)B * heads;
+  for (long long base = (long long)warp * 32; base < n_kh; base += (long long)nwarps * 32) {
+    long long my_ts = 0, my_w = 0;
+    int my_nt = 0, my_h = 0;
+    if (base + lane < n_kh) {
+      const int k = (int)((base + lane) / heads);
+      my_h = (int)((base + lane) % heads);
+      const ReqMeta rm = pd.meta[__ldcg(pd.rorder + k)];
+      const int r0 = __ldcg(pd.roff + k), nl = (__ldcg(pd.roff + k + 1) - r0) / heads;
+      my_ts = rm.tile_start;
+      my_nt = rm.ntiles;
+      my_w = r0 + (long long)my_h * nl;
+    }
+    const int cnt = (int)min(32LL, n_kh - base);
+    for (int i = 0; i < cnt; ++i) {
+      const long long ts = __shfl_sync(0xffffffffu, my_ts, i);
+      const int nt = __shfl_sync(0xffffffffu, my_nt, i), h = __shfl_sync(0xffffffffu, my_h, i);
+      long long w = __shfl_sync(0xffffffffu, my_w, i);
+      for (int top = nt - 1; top >= 0; top -= 32) {
+        const int qt = top - lane;
+        const bool light = qt >= 0 && (heavy_items == 0 || !heavy(ts + qt));
+        const unsigned bl = __ballot_sync(0xffffffffu, light);
+        if (light) pd.items[w + __popc(bl & ((1u << lane) - 1u))] = (int)((ts + qt) * heads + h);
+        w += __popc(bl);
+      }
+    }
   }
 }
 
@@ -530,9 +596,33 @@ __global__ void __launch_bounds__(kTile) k_count_pairs(MaskP mp, PlanDev pd, con
 
 cudaError_t launch_plan(const MaskP& mp, int heads, const PlanDev& pd, const long long* offsets_dev,
                         const long long* t, const int8_t* ty, int batch, long long n_tiles,
-                        cudaStream_t st) {
-  if (batch <= 0) return cudaSuccess;
-  k_plan<<<batch, kPlanThreads, 0, st>>>(mp, heads, pd, offsets_dev, t, ty, n_tiles);
+                        cudaEvent_t prologue_ok, cudaStream_t st) {
+  if (batch <= 0) return prologue_ok ? cudaEventRecord(prologue_ok, st) : cudaSuccess;
+  // One block per request while requests are short: the planner then runs beside the
+  // RoPE prologue and ends first.  Long requests (the pair classification grows with
+  // the square of a request's tiles) are split over enough blocks for two per SM, with
+  // phase 1 in a kernel of its own before them.
+  long long slices = 1;
+  const long long mean_tiles = (n_tiles + batch - 1) / batch;
+  if (mean_tiles >= kSplitTiles) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    slices = (2LL * sms + batch - 1) / batch;
+    if (slices > mean_tiles) slices = mean_tiles;
+  }
+  if (slices > 1) {
+    const long long tile_blocks = (n_tiles + kTileWarps - 1) / kTileWarps;
+    k_plan_tiles<<<(unsigned)tile_blocks, 32 * kTileWarps, 0, st>>>(pd, t, ty, batch, n_tiles);
+  } else {
+    slices = 1;
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && prologue_ok) e = cudaEventRecord(prologue_ok, st);
+  if (e != cudaSuccess) return e;
+  k_plan<<<(unsigned)(batch * slices), kPlanThreads, 0, st>>>(mp, heads, pd, offsets_dev, t, ty, batch,
+                                                              (int)slices, n_tiles);
   return cudaGetLastError();
 }
 
