@@ -110,6 +110,12 @@ def _workload(name, rank, batch=None):
     return W.make(name, **kw)
 
 
+def _planner_split(w: W.Workload) -> int:
+    """1 when the planner runs its per-tile kernel apart (mean tiles per request >= 32)."""
+    n_tiles = int(sum((int(n) + 127) // 128 for n in np.diff(w.offsets)))
+    return int(w.batch > 0 and -(-n_tiles // w.batch) >= 32)
+
+
 def _config(w: W.Workload, name: str, parallelism: str):
     lens = np.diff(w.offsets)
     return {"workload": name, "batch": w.batch, "tokens": w.total_tokens,
@@ -538,10 +544,11 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": all_flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-        # per step: k_plan, k_build_masks, k_rope, k_attn_tc; the backward adds k_rope,
-        # k_bwd_schedule, k_bwd_colmask (a new plan each step), k_bwd_rowc and the two
-        # k_bwd_tc modes (the fp32 path: k_rope, k_bwd_delta, k_bwd_dq, k_bwd_dkv)
-        "gpu_launches": (4 + ((6 if bf16 else 4) if args.backward else 0)) * args.steps,
+        # per step: k_plan (plus k_plan_tiles when requests average 32 tiles or more and
+        # the planner splits them), k_build_masks, k_rope, k_attn_tc; the backward adds
+        # k_rope, k_bwd_schedule, k_bwd_colmask (a new plan each step), k_bwd_rowc and the
+        # two k_bwd_tc modes (the fp32 path: k_rope, k_bwd_delta, k_bwd_dq, k_bwd_dkv)
+        "gpu_launches": (4 + _planner_split(w) + ((6 if bf16 else 4) if args.backward else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
