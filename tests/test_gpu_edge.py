@@ -185,3 +185,36 @@ def test_time_clauses_with_and_without_sorted_runs(case):
     w = _custom(lengths, t=t, types=types, mask=dict(use_delay=True, delay_s=3600, window=0,
                                                      hist_bidirectional=False))
     _check_all(w)
+
+
+def test_split_planner_with_empty_and_tiny_requests():
+    """Requests averaging 32 tiles or more: the planner splits each request's query tiles
+    over several blocks.  Empty and one-token requests sit between the long ones."""
+    lengths = [8000, 0, 1, 9000, 0, 7000]
+    rng = np.random.default_rng(23)
+    T = sum(lengths)
+    t = W.EPOCH + np.sort(rng.integers(0, 10**7, size=T)).astype(np.int64)
+    ty = np.full(T, W.HIST, dtype=np.int8)
+    s = 0
+    for n in lengths:  # a few GLOBAL tokens first and candidates last in each request
+        if n > 100:
+            ty[s:s + 16] = W.GLOBAL
+            ty[s + n - 40:s + n] = W.CAND
+            t[s + n - 40:s + n] = t[s + n - 41]
+        s += n
+    w = _custom(lengths, t=t, types=ty, mask=dict(use_delay=True, delay_s=3600, window=700,
+                                                   hist_bidirectional=False))
+    n_tiles = sum((n + 127) // 128 for n in lengths)
+    assert -(-n_tiles // len(lengths)) >= 32  # the split planner
+    out, lse, plan = gu.run_gpu(w, with_lse=True)
+    try:
+        op = gu.oracle_params(w)
+        np.testing.assert_array_equal(bd.rec_attn_tile_classes(plan),
+                                      oracle.tile_classes(op, w.offsets, w.t, w.types))
+        assert bd.rec_attn_visible_pairs(plan) == oracle.visible_pairs(op, w.offsets, w.t, w.types)
+        rows = gu.sample_rows(w, per_request=64, max_requests=len(lengths))
+        ref = oracle.attention(op, w.offsets, w.t, w.types, w.q, w.k, w.v, rows=rows)
+        gu.assert_close(w, gu.to_f64(out[torch.from_numpy(rows).cuda()]), ref, "split planner")
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
