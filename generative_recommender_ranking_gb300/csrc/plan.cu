@@ -486,11 +486,22 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
   }
   if (threadIdx.x == 0) pd.roff[B] = (int)carry;
   __syncthreads();
-  // each (request, head): its light query tiles, last to first.  A warp takes 32 of
-  // them: each lane looks up one (its loads all in flight together), then the warp
-  // writes them one after the other, lane i taking the i-th tile of each group of 32
-  // counted from the end.
+  // each (request, head): its light query tiles, last to first
   const long long n_kh = (long long)B * heads;
+  if (slices == 1) {  // short requests: one thread per (request, head)
+    for (long long kh = threadIdx.x; kh < n_kh; kh += blockDim.x) {
+      const int k = (int)(kh / heads), h = (int)(kh % heads);
+      const ReqMeta rm = pd.meta[__ldcg(pd.rorder + k)];
+      const int r0 = __ldcg(pd.roff + k), nl = (__ldcg(pd.roff + k + 1) - r0) / heads;
+      long long w = r0 + (long long)h * nl;
+      for (int qt = rm.ntiles - 1; qt >= 0; --qt)
+        if (heavy_items == 0 || !heavy(rm.tile_start + qt)) pd.items[w++] = (int)((rm.tile_start + qt) * heads + h);
+    }
+    return;
+  }
+  // long requests: a warp takes 32 of them; each lane looks up one (its loads all in
+  // flight together), then the warp writes them one after the other, lane i taking the
+  // i-th tile of each group of 32 counted from the end
   for (long long base = (long long)warp * 32; base < n_kh; base += (long long)nwarps * 32) {
     long long my_ts = 0, my_w = 0;
     int my_nt = 0, my_h = 0;
