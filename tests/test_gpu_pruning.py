@@ -99,3 +99,15 @@ def test_target_attention_full_size_serving():
     # each candidate sees every history event older than t_req - 1 h, and itself
     assert len(kept) == w.batch * 500
     assert pairs == _pairs_of_rows(w, kept)
+
+
+@pytest.mark.parametrize("keep", [0, 37, 3000, -1])
+def test_pruned_parity_split_planner(keep):
+    # requests of 40 tiles: the planner splits each request's query tiles over several
+    # blocks, every one of which finds the first kept position for itself
+    w = W.tm20k("window", batch=2, n_hist=5000, heads=2)
+    n_tiles = sum((int(n) + 127) // 128 for n in np.diff(w.offsets))
+    assert -(-n_tiles // w.batch) >= 32
+    rows = gu.sample_rows(w, per_request=200)
+    pairs, kept = _run(w, keep, sample=rows)
+    assert len(kept) == (w.total_tokens if keep < 0 else w.batch * (min(keep, 5000) + 1))
