@@ -60,9 +60,9 @@ def _peaks():
 
 
 def _traffic(workload: str):
-    """DRAM bytes (read + write) of one attention launch from the committed ncu capture,
-    or None when the capture is for another workload or the kernel sources have changed
-    since the counters were taken."""
+    """DRAM bytes (read + write) of one attention launch from the committed ncu capture
+    ("<workload>" or "<workload>/fused"), or None when there is no capture of that case or
+    the kernel sources have changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "k_attn_tc_dram_traffic.json")
     try:
         import hashlib
@@ -488,7 +488,8 @@ def run_ours(args):
     attn_tflops = flops_fwd / (attn_ms * 1e-3) / 1e12
     attn_gbs = bytes_attn / (attn_ms * 1e-3) / 1e9
     # full-size default batch only: the capture was taken on that launch
-    traffic = _traffic(args.workload) if (args.batch is None and world == 1 and not args.fused) else None
+    traffic = (_traffic(args.workload + ("/fused" if args.fused else ""))
+               if (args.batch is None and world == 1) else None)
     hbm_bound = (flops_fwd / bytes_attn) < (pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9))
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
