@@ -53,6 +53,8 @@ def _close(w, a, b):
     lambda: W.sort(batch=2, n_special=16, n_hist=500, n_cand=50, window=128),
     lambda: W.cadet(batch=4, n_pairs=200),
     lambda: W.tiny_fp32(),
+    # requests of 36 tiles: the planner splits their query tiles over several blocks
+    lambda: W.tm20k("window", batch=2, n_hist=4500, heads=2),
 ])
 def test_noalloc_matches_plan_api_twice_in_a_row(make):
     w = make()
