@@ -274,16 +274,16 @@ rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queri
     delete plan;
     return from_cuda(e);
   }
-  e = cudaMemsetAsync(w + lay.hdr, 0, 256, plan->side);
-  if (e == cudaSuccess && batch > 0) {
-    // the request table and the request of every tile (so the prologue needs no search),
-    // laid out as in the workspace and uploaded in one copy
-    std::vector<char> up(lay.tr - lay.meta + sizeof(int) * (size_t)NT);
-    std::memcpy(up.data(), meta.data(), sizeof(ReqMeta) * (size_t)batch);
-    int* treq = reinterpret_cast<int*>(up.data() + (lay.tr - lay.meta));
+  {
+    // the zeroed header (counters, status word), the request table and the request of
+    // every tile (so the prologue needs no search), laid out as in the workspace and
+    // uploaded in one copy (a pageable copy: staged before the call returns)
+    std::vector<char> up(lay.tr - lay.hdr + sizeof(int) * (size_t)NT, 0);
+    if (batch > 0) std::memcpy(up.data() + (lay.meta - lay.hdr), meta.data(), sizeof(ReqMeta) * (size_t)batch);
+    int* treq = reinterpret_cast<int*>(up.data() + (lay.tr - lay.hdr));
     for (int32_t b = 0; b < batch; ++b)
       for (int i = 0; i < meta[b].ntiles; ++i) treq[meta[b].tile_start + i] = b;
-    e = cudaMemcpyAsync(pd.meta, up.data(), up.size(), cudaMemcpyHostToDevice, plan->side);
+    e = cudaMemcpyAsync(w + lay.hdr, up.data(), up.size(), cudaMemcpyHostToDevice, plan->side);
   }
   if (e == cudaSuccess)
     e = launch_plan(plan->mask, params->num_heads, pd, reinterpret_cast<const long long*>(offsets_dev), plan->t,
