@@ -2,7 +2,9 @@
 (GLOBAL, HIST, RT, CAND), times sorted, perturbed or repeated, and random mask
 parameters (delay, window, bidirectional history).  Each case checks the tile classes
 and visible-pair count bit for bit, every output row and lse within the bf16
-tolerances, and, for a third of the cases, the gradients."""
+tolerances, and, for a third of the cases, the gradients.  Further variants run the same
+layouts with head_dim 128, through the fp32 path, through query-pruned plans and through
+the fused QK-RMSNorm and gates."""
 import numpy as np
 import pytest
 import torch
@@ -22,7 +24,7 @@ def _built():
     gu.ensure_built()
 
 
-def _case(seed):
+def _case(seed, dtype="bf16", d=64):
     rng = np.random.default_rng(1000 + seed)
     B = int(rng.integers(1, 5))
     lengths = [int(x) for x in rng.integers(1, 700, size=B)]
@@ -54,9 +56,11 @@ def _case(seed):
         s += n
     mask = dict(use_delay=bool(rng.random() < 0.6), delay_s=int(rng.choice([0, 60, 3600, 86400])),
                 window=int(rng.choice([0, 0, 16, 100, 256])), hist_bidirectional=bool(rng.random() < 0.25))
-    x = [W.round_to_bf16_bits(rng.standard_normal((T, 2, 64)).astype(np.float32) * 0.5) for _ in range(3)]
+    x = [rng.standard_normal((T, 2, d)).astype(np.float32) * 0.5 for _ in range(3)]
+    if dtype == "bf16":
+        x = [W.round_to_bf16_bits(a) for a in x]
     off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
-    return W.Workload(f"random{seed}", 2, 64, "bf16", off, t, types, *x, mask,
+    return W.Workload(f"random{seed}", 2, d, dtype, off, t, types, *x, mask,
                       dict(use_rope=True, phi_min=1e-4, dt_max_s=float(W.YEAR), rope_base=6e5))
 
 
@@ -93,3 +97,58 @@ def test_random_mask_layouts(seed):
         assert bd.rec_attn_device_status(plan) == bd.OK
     finally:
         bd.rec_attn_free(plan)
+
+
+VARIANTS = ("d128", "fp32", "pruned", "fused")
+
+
+@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_random_mask_layouts_variants(variant, seed):
+    w = _case(100 + seed, dtype="fp32" if variant == "fp32" else "bf16",
+              d=128 if variant == "d128" else (32 if variant == "fp32" else 64))
+    if w.total_tokens == 0:
+        pytest.skip("empty batch (the edge tests cover it)")
+    op = gu.oracle_params(w)
+    tens = gu.device_inputs(w)
+    p = gu.params_for(w)
+    keep = int(np.random.default_rng(seed).integers(0, 400)) if variant == "pruned" else -1
+    if variant == "pruned":
+        plan = bd.rec_attn_plan_query_pruned(p, keep, tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    else:
+        plan = bd.rec_attn_plan(p, tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    fused = None
+    try:
+        out = torch.full_like(tens["q"], float("nan"))
+        if variant == "fused":
+            fi = W.fused_inputs(w)
+            dev = {n: torch.from_numpy(np.ascontiguousarray(getattr(fi, n).view(np.int16)
+                                                            if getattr(fi, n).dtype == np.uint16
+                                                            else getattr(fi, n))).cuda()
+                   for n in ("q_norm_w", "k_norm_w", "q_gate", "k_gate", "out_gate")}
+            for n in ("q_gate", "k_gate", "out_gate"):
+                dev[n] = dev[n].view(torch.bfloat16)
+            bd.rec_attn_fwd_fused(plan, tens["q"], tens["k"], tens["v"], out, None, None,
+                                  q_norm_weight=dev["q_norm_w"], k_norm_weight=dev["k_norm_w"],
+                                  norm_eps=fi.norm_eps, q_gate=dev["q_gate"], k_gate=dev["k_gate"],
+                                  out_gate=dev["out_gate"])
+            fused = oracle.Fused(norm_eps=fi.norm_eps, q_norm_w=fi.q_norm_w.astype(np.float64),
+                                 k_norm_w=fi.k_norm_w.astype(np.float64), q_gate=fi.q_gate, k_gate=fi.k_gate,
+                                 out_gate=fi.out_gate)
+        else:
+            bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out)
+        torch.cuda.synchronize()
+        assert bd.rec_attn_device_status(plan) == bd.OK
+        np.testing.assert_array_equal(bd.rec_attn_tile_classes(plan),
+                                      oracle.tile_classes(op, w.offsets, w.t, w.types))
+    finally:
+        bd.rec_attn_free(plan)
+    rows = oracle.kept_rows(w.offsets, w.types, keep) if variant == "pruned" else None
+    ref = oracle.attention(op, w.offsets, w.t, w.types, w.q, w.k, w.v, rows=rows, fused=fused)
+    o = gu.to_f64(out)
+    if rows is not None:
+        written = np.zeros(w.total_tokens, dtype=bool)
+        written[rows] = True
+        assert np.isnan(o[~written]).all(), "a pruned row was written"
+        o = o[rows]
+    gu.assert_close(w, o, ref, f"{w.name}/{variant}")
