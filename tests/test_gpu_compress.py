@@ -63,3 +63,63 @@ def test_compress_parity(name):
         assert np.all(err <= 2.0 ** -8 * np.abs(ref_x) + 1e-5), float(err.max())
     else:
         assert np.all(err <= 1e-6 * np.maximum(1.0, np.abs(ref_x))), float(err.max())
+
+
+def _random_case(seed):
+    rng = np.random.default_rng(3000 + seed)
+    B = int(rng.integers(1, 6))
+    lengths = [int(x) for x in rng.integers(0, 600, size=B)]
+    hb = np.zeros(B, dtype=np.int64)
+    hl = np.zeros(B, dtype=np.int64)
+    for b, n in enumerate(lengths):
+        if n and rng.random() < 0.85:
+            lo = int(rng.integers(0, max(1, n // 4)))
+            hi = int(rng.integers(lo, n + 1))
+            hb[b], hl[b] = lo, hi - lo
+    segs = [(int(rng.integers(1, 300)), int(rng.integers(1, 10))) for _ in range(int(rng.integers(1, 5)))]
+    if rng.random() < 0.7:
+        segs[-1] = (-1, segs[-1][1])
+    else:  # bounded segments only: the last one reaches past the longest history
+        covered = sum(n for n, _ in segs[:-1])
+        segs[-1] = (max(segs[-1][0], int(hl.max()) - covered + int(rng.integers(0, 5)), 1), segs[-1][1])
+    dtype = "fp32" if rng.random() < 0.25 else "bf16"
+    width = int(rng.choice([64, 128, 256, 512])) if dtype == "bf16" else int(rng.choice([32, 64, 128]))
+    T = sum(lengths)
+    x = rng.standard_normal((T, width)).astype(np.float32)
+    if dtype == "bf16":
+        x = W.round_to_bf16_bits(x)
+    t = W.EPOCH + np.sort(rng.integers(0, 10**7, size=T)).astype(np.int64)
+    ty = rng.integers(0, 4, size=T).astype(np.int8)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    return off, hb, hl, segs, x, t, ty, dtype
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_compress_random_segments(seed):
+    """Seeded random batches (empty requests and histories included), history ranges and
+    recency segments (1 to 4, bounded or not, groups of 1 to 9), bf16 and fp32 rows."""
+    off, hb, hl, segs, x_host, t_host, ty_host, dtype = _random_case(seed)
+    out_off = bd.rec_attn_compress_lengths(off, hb, hl, segs)
+    ref_off, ref_x, ref_t, ref_ty = oracle.compress(off, hb, hl, segs, x_host, t_host, ty_host)
+    assert np.array_equal(out_off, ref_off)
+    n = int(out_off[-1])
+    if n == 0:
+        return
+    if dtype == "bf16":
+        x = torch.from_numpy(x_host.view(np.int16)).cuda().view(torch.bfloat16)
+    else:
+        x = torch.from_numpy(x_host).cuda()
+    x_out = torch.full((n, x.shape[1]), float("nan"), dtype=x.dtype, device=x.device)
+    t_out = torch.full((n,), -1, dtype=torch.int64, device=x.device)
+    ty_out = torch.full((n,), -1, dtype=torch.int8, device=x.device)
+    bd.rec_attn_compress(off, hb, hl, segs, x, torch.from_numpy(t_host).cuda(), torch.from_numpy(ty_host).cuda(),
+                         x_out, t_out, ty_out)
+    torch.cuda.synchronize()
+    assert np.array_equal(t_out.cpu().numpy(), ref_t)
+    assert np.array_equal(ty_out.cpu().numpy(), ref_ty)
+    got = x_out.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref_x)
+    if dtype == "bf16":
+        assert np.all(err <= 2.0 ** -8 * np.abs(ref_x) + 1e-5), float(err.max())
+    else:
+        assert np.all(err <= 1e-6 * np.maximum(1.0, np.abs(ref_x))), float(err.max())
