@@ -396,6 +396,7 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
     if (e != cudaSuccess) return from_cuda(e);
     RopeArgs ra;
     ra.meta = plan->pd.meta; ra.tile_req = plan->pd.treq; ra.batch = plan->batch; ra.t = plan->t;
+    ra.ty = plan->ty; ra.skip_user_q = 0;
     ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
     ra.heads = p.num_heads; ra.head_dim = p.head_dim;
     std::memcpy(ra.omega, plan->omega, sizeof ra.omega);  // all zero without the RoPE
@@ -415,9 +416,11 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
     if (e != cudaSuccess) return from_cuda(e);
     RopeArgs ra;
     ra.meta = plan->pd.meta; ra.tile_req = plan->pd.treq; ra.batch = plan->batch; ra.t = plan->t;
+    ra.ty = plan->ty; ra.skip_user_q = 0;
     ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
     ra.heads = p.num_heads; ra.head_dim = p.head_dim;
     std::memcpy(ra.omega, plan->omega, sizeof ra.omega);
+    ra.skip_user_q = plan->mask.keep_user == 0 ? 1 : 0;  // target attention: no user token queries
     e = launch_rope(ra, p.dtype, plan->NT, st);
     if (e == cudaSuccess && plan->timing) e = cudaEventRecord(plan->ev[1], st);
     if (e != cudaSuccess) return from_cuda(e);
@@ -529,6 +532,7 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
     if (e != cudaSuccess) return from_cuda(e);
     RopeArgs ra;
     ra.meta = plan->pd.meta; ra.tile_req = plan->pd.treq; ra.batch = plan->batch; ra.t = plan->t;
+    ra.ty = plan->ty; ra.skip_user_q = 0;
     ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
     ra.heads = p.num_heads; ra.head_dim = p.head_dim;
     std::memcpy(ra.omega, plan->omega, sizeof ra.omega);

@@ -37,6 +37,8 @@ struct RopeArgs {
   const int* tile_req;     // [NT] request of each tile (uploaded with the request table)
   int batch;               // requests in meta (the prologue needs nothing the planner writes)
   const long long* t;
+  const int8_t* ty;        // token types (read only when skip_user_q)
+  int skip_user_q;         // 1: no Q' for GLOBAL / HIST tokens (a plan where no user token queries)
   const void* q;
   const void* k;
   void* qr;                // rotated outputs, same layout [T][H][d]

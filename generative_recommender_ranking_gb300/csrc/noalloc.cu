@@ -211,6 +211,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   if (params->use_rope) {
     RopeArgs ra;
     ra.meta = pd.meta; ra.tile_req = pd.treq; ra.batch = batch; ra.t = t;
+    ra.ty = types_dev; ra.skip_user_q = 0;
     ra.q = q; ra.k = k; ra.qr = w + lay.rq; ra.kr = w + lay.rk;
     ra.heads = params->num_heads; ra.head_dim = params->head_dim;
     for (int i = 0; i < kMaxPairs; ++i)

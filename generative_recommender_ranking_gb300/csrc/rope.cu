@@ -57,12 +57,62 @@ struct Chunk<float> {
   }
 };
 
+// One (token, chunk) unit of the prologue: K' and, when WQ, Q' for every head.  The
+// first four heads' 16-byte loads go out before the angle math (they do not depend on
+// the time), later heads four at a time, all kept raw until used.
+template <typename E, bool WQ>
+__device__ __forceinline__ void rope_rows(const RopeArgs& a, const char* __restrict__ q, const char* __restrict__ k,
+                                          char* __restrict__ qr, char* __restrict__ kr, long long head_bytes,
+                                          long long tok, long long row0, int c, long long t_ref) {
+  using C = Chunk<E>;
+  constexpr int kPairs = C::kPairs;
+  uint4 rq[4], rk[4];  // raw 16-byte chunks of four heads
+  auto load4 = [&](int h0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (h0 + u < a.heads) {
+        if constexpr (WQ) rq[u] = *reinterpret_cast<const uint4*>(q + row0 + (h0 + u) * head_bytes);
+        rk[u] = *reinterpret_cast<const uint4*>(k + row0 + (h0 + u) * head_bytes);
+      }
+  };
+  load4(0);
+  const float dt = (float)(a.t[tok] - t_ref);  // exact int64 difference, then fp32
+  float sn[kPairs], cs[kPairs];
+#pragma unroll
+  for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
+  for (int h0 = 0; h0 < a.heads; h0 += 4) {
+    if (h0 > 0) load4(h0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (h0 + u >= a.heads) break;
+      float y[8];
+      C::unpack(rk[u], y);
+      if constexpr (WQ) {
+        float x[8];
+        C::unpack(rq[u], x);
+#pragma unroll
+        for (int p = 0; p < kPairs; ++p) {
+          const float x0 = x[2 * p], x1 = x[2 * p + 1];
+          x[2 * p] = x0 * cs[p] - x1 * sn[p];
+          x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
+        }
+        C::store(qr + row0 + (h0 + u) * head_bytes, x);
+      }
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        const float y0 = y[2 * p], y1 = y[2 * p + 1];
+        y[2 * p] = y0 * cs[p] - y1 * sn[p];
+        y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
+      }
+      C::store(kr + row0 + (h0 + u) * head_bytes, y);
+    }
+  }
+}
+
 // Thread work unit: one token and one 16-byte chunk of its head rows, for every head,
 // so each angle's sin/cos is computed once per token.  A block covers 256 / chunks
 // tokens of one tile (chunks = 16-byte chunks per head row, 8 or 16), so a tile takes
-// chunks / 2 blocks and each thread one unit.  The first four heads' 16-byte loads of Q
-// and K go out before the angle math (they do not depend on the time), later heads four
-// at a time, all kept raw until used.
+// chunks / 2 blocks and each thread one unit (`rope_rows`).
 template <typename E>
 __global__ void __launch_bounds__(256, 4) k_rope(RopeArgs a) {
   using C = Chunk<E>;
@@ -84,40 +134,11 @@ __global__ void __launch_bounds__(256, 4) k_rope(RopeArgs a) {
   const long long head_bytes = (long long)a.head_dim * (long long)sizeof(E);
   const long long tok = m.tok_start + tl * kTile + r;
   const long long row0 = tok * a.heads * head_bytes + (long long)c * 16;
-  uint4 rq[4], rk[4];  // raw 16-byte chunks of four heads
-  auto load4 = [&](int h0) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (h0 + u < a.heads) {
-        rq[u] = *reinterpret_cast<const uint4*>(q + row0 + (h0 + u) * head_bytes);
-        rk[u] = *reinterpret_cast<const uint4*>(k + row0 + (h0 + u) * head_bytes);
-      }
-  };
-  load4(0);
-  const float dt = (float)(a.t[tok] - a.t[m.tok_start]);  // exact int64 difference, then fp32
-  float sn[kPairs], cs[kPairs];
-#pragma unroll
-  for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
-  for (int h0 = 0; h0 < a.heads; h0 += 4) {
-    if (h0 > 0) load4(h0);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (h0 + u >= a.heads) break;
-      float x[8], y[8];
-      C::unpack(rq[u], x);
-      C::unpack(rk[u], y);
-#pragma unroll
-      for (int p = 0; p < kPairs; ++p) {
-        const float x0 = x[2 * p], x1 = x[2 * p + 1], y0 = y[2 * p], y1 = y[2 * p + 1];
-        x[2 * p] = x0 * cs[p] - x1 * sn[p];
-        x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
-        y[2 * p] = y0 * cs[p] - y1 * sn[p];
-        y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
-      }
-      C::store(qr + row0 + (h0 + u) * head_bytes, x);
-      C::store(kr + row0 + (h0 + u) * head_bytes, y);
-    }
-  }
+  const long long t_ref = a.t[m.tok_start];
+  // a plan in which no user token queries never reads their Q' rows (their query tiles
+  // are skipped or their rows are computed and not written), so they are not rotated
+  if (a.skip_user_q && is_user(a.ty[tok])) rope_rows<E, false>(a, q, k, qr, kr, head_bytes, tok, row0, c, t_ref);
+  else rope_rows<E, true>(a, q, k, qr, kr, head_bytes, tok, row0, c, t_ref);
 }
 
 // Sum of v over the `group` consecutive lanes that hold one head row (group is a
