@@ -120,6 +120,9 @@ def lib() -> ctypes.CDLL:
         L.orc_visible.restype = ctypes.c_int
         L.orc_mask.argtypes = [P, ctypes.c_int64, vp, vp, vp]
         L.orc_mask.restype = None
+        L.orc_mask_block.argtypes = [P, ctypes.c_int64, vp, vp, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_int64, vp]
+        L.orc_mask_block.restype = None
         L.orc_visible_pairs.argtypes = [P, ctypes.c_int32, vp, vp, vp]
         L.orc_visible_pairs.restype = ctypes.c_uint64
         L.orc_rope.argtypes = [P, ctypes.c_int64, vp, vp]
@@ -176,6 +179,17 @@ def mask(p: Params, t, ty) -> np.ndarray:
     out = np.zeros((L, L), dtype=np.uint8)
     cp = p.c()
     lib().orc_mask(ctypes.byref(cp), L, _ptr(t), _ptr(ty), _ptr(out))
+    return out
+
+
+def mask_block(p: Params, t, ty, i0: int, ni: int, j0: int, nj: int) -> np.ndarray:
+    """Rows [i0, i0+ni) x keys [j0, j0+nj) of the mask of a single request (uint8,
+    1 = visible; 0 past the request end)."""
+    t, ty = _c64(t), _c8(ty)
+    out = np.zeros((ni, nj), dtype=np.uint8)
+    cp = p.c()
+    lib().orc_mask_block(ctypes.byref(cp), t.shape[0], _ptr(t), _ptr(ty), int(i0), int(ni), int(j0), int(nj),
+                         _ptr(out))
     return out
 
 

@@ -119,6 +119,17 @@ void orc_mask(const orc_params* p, int64_t L, const int64_t* t, const int8_t* ty
       out[i * L + j] = (uint8_t)orc_visible(p, i, t[i], ty[i], j, t[j], ty[j]);
 }
 
+/* The block [i0, i0 + ni) x [j0, j0 + nj) of orc_mask, with 0 for an index past the
+ * request end (no such token). */
+void orc_mask_block(const orc_params* p, int64_t L, const int64_t* t, const int8_t* ty,
+                    int64_t i0, int64_t ni, int64_t j0, int64_t nj, uint8_t* out) {
+  for (int64_t a = 0; a < ni; ++a)
+    for (int64_t c = 0; c < nj; ++c) {
+      const int64_t i = i0 + a, j = j0 + c;
+      out[a * nj + c] = (i < L && j < L) ? (uint8_t)orc_visible(p, i, t[i], ty[i], j, t[j], ty[j]) : 0;
+    }
+}
+
 uint64_t orc_visible_pairs(const orc_params* p, int32_t B, const int64_t* offsets,
                            const int64_t* t, const int8_t* ty) {
   uint64_t n = 0;

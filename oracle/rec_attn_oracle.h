@@ -33,6 +33,9 @@ int orc_visible(const orc_params* p, int64_t pi, int64_t ti, int ty_i,
                 int64_t pj, int64_t tj, int ty_j);
 /* L x L mask of one request, row-major, 1 = visible. */
 void orc_mask(const orc_params* p, int64_t L, const int64_t* t, const int8_t* ty, uint8_t* out);
+/* Block [i0, i0+ni) x [j0, j0+nj) of that mask, row-major; indices >= L give 0. */
+void orc_mask_block(const orc_params* p, int64_t L, const int64_t* t, const int8_t* ty,
+                    int64_t i0, int64_t ni, int64_t j0, int64_t nj, uint8_t* out);
 /* Exact number of visible (query, key) pairs over the batch (per head). */
 uint64_t orc_visible_pairs(const orc_params* p, int32_t B, const int64_t* offsets,
                            const int64_t* t, const int8_t* ty);

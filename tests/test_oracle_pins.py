@@ -110,6 +110,43 @@ def test_mask_matches_hand_enumeration(orc, fname):
     assert np.array_equal(got, expect), f"\n{got}\n!=\n{expect}"
 
 
+@pytest.mark.parametrize("fname", mask_files())
+def test_mask_block_matches_hand_enumeration(orc, fname):
+    """Every block of the hand-enumerated masks, with indices running past the request
+    end (those entries are 0: there is no such token)."""
+    types, times, prm, expect = load_mask(fname)
+    p = _params(orc, window=int(prm["window"]),
+                use_delay=prm["delay"] != "none",
+                delay_s=0 if prm["delay"] == "none" else int(prm["delay"]),
+                hist_bidirectional=bool(int(prm["bidirectional"])))
+    L = len(types)
+    padded = np.zeros((L + 3, L + 3), dtype=np.uint8)
+    padded[:L, :L] = expect
+    for i0 in range(L + 1):
+        for j0 in range(L + 1):
+            for ni, nj in ((1, 1), (2, 3), (L, 1), (3, L + 3 - j0)):
+                ni = min(ni, L + 3 - i0)
+                got = orc.mask_block(p, times, types, i0, ni, j0, nj)
+                assert np.array_equal(got, padded[i0:i0 + ni, j0:j0 + nj]), (fname, i0, j0, ni, nj)
+
+
+def test_mask_block_causal_closed_form(orc):
+    """A causal history of L tokens: the block of rows [i0, i0+n) x keys [j0, j0+n)
+    holds #{(i, j): j <= i} (counted in closed form), here for 128-token tiles."""
+    L = 1000
+    t = np.zeros(L, dtype=np.int64)
+    ty = np.ones(L, dtype=np.int8)
+    p = _params(orc)
+    for qt, kt in ((0, 0), (3, 1), (2, 5), (7, 7), (7, 3)):
+        i0, j0, n = 128 * qt, 128 * kt, 128
+        blk = orc.mask_block(p, t, ty, i0, n, j0, n)
+        expect = 0
+        for i in range(i0, min(i0 + n, L)):
+            lo, hi = j0, min(j0 + n, L, i + 1)
+            expect += max(0, hi - lo)
+        assert int(blk.sum()) == expect, (qt, kt)
+
+
 def test_pair_counts_match_page(orc):
     g = load_json("pair_counts.json")
     L, N = g["L"], g["N"]
