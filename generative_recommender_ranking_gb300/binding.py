@@ -287,6 +287,27 @@ def rec_attn_visible_pairs(plan: Plan) -> int:
     return int(n.value)
 
 
+MASK_APPLIED, MASK_BUILT, MASK_PREDICATE = 0, 1, 2
+
+
+def rec_attn_applied_masks(plan: Plan, pairs, mode: int = MASK_APPLIED):
+    """Visibility bits the attention kernels apply to (request, query tile, key tile)
+    pairs: returns (bits uint32 [n, 128, 4], list class uint8 [n] (0xff: not listed),
+    mask-table slot int32 [n])."""
+    L = lib()
+    vp = ctypes.c_void_p
+    L.rec_attn_applied_masks.argtypes = [vp, ctypes.c_int32, vp, ctypes.c_int32, vp, vp, vp]
+    L.rec_attn_applied_masks.restype = ctypes.c_int
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 3))
+    n = pr.shape[0]
+    bits = np.zeros((n, TILE, 4), dtype=np.uint32)
+    cls = np.zeros(n, dtype=np.uint8)
+    slot = np.zeros(n, dtype=np.int32)
+    _check("rec_attn_applied_masks", L.rec_attn_applied_masks(plan.handle, n, _ptr(pr), int(mode), _ptr(bits),
+                                                              _ptr(cls), _ptr(slot)))
+    return bits, cls, slot
+
+
 def rec_attn_device_status(plan: Plan) -> int:
     s = ctypes.c_int32()
     _check("rec_attn_device_status", lib().rec_attn_device_status(plan.handle, ctypes.byref(s)))

@@ -32,6 +32,7 @@ struct rec_attn_plan_s {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   PlanDev pd{};
+  std::vector<int> req_tiles;  // host copy: tiles of each request (argument checks)
   void* qrot = nullptr;
   void* krot = nullptr;
   void* qk_extra = nullptr;  // Q'/K' buffers of a plan without the RoPE, made on the first fused call
@@ -226,6 +227,13 @@ rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queri
   if (plan->p.softmax_scale == 0.f) plan->p.softmax_scale = 1.f / std::sqrt((float)params->head_dim);
   plan->batch = batch;
   plan->T = T; plan->NT = NT; plan->NC = NC;
+  try {
+    plan->req_tiles.resize((size_t)batch);
+  } catch (...) {
+    delete plan;
+    return REC_ATTN_ERR_OOM;
+  }
+  for (int32_t b = 0; b < batch; ++b) plan->req_tiles[b] = meta[b].ntiles;
   plan->stream = static_cast<cudaStream_t>(stream);
   plan->t = reinterpret_cast<const long long*>(timestamps_dev);
   plan->ty = types_dev;
@@ -773,6 +781,48 @@ REC_ATTN_API rec_attn_status rec_attn_visible_pairs(rec_attn_plan_t* plan, uint6
   if (e == cudaSuccess) e = cudaMemcpyAsync(&n, plan->pd.pairs, sizeof n, cudaMemcpyDeviceToHost, plan->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(plan->stream);
   if (e == cudaSuccess) *host_out = n;
+  return from_cuda(e);
+}
+
+REC_ATTN_API rec_attn_status rec_attn_applied_masks(rec_attn_plan_t* plan, int32_t n_pairs, const int32_t* pairs_host,
+                                                    int32_t mode, uint32_t* bits_host, uint8_t* list_class_host,
+                                                    int32_t* slot_host) {
+  if (!plan || n_pairs < 0 || (n_pairs > 0 && (!pairs_host || !bits_host))) return REC_ATTN_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 2) return REC_ATTN_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_pairs; ++i) {
+    const int32_t b = pairs_host[3 * i], qt = pairs_host[3 * i + 1], kt = pairs_host[3 * i + 2];
+    if (b < 0 || b >= plan->batch) return REC_ATTN_ERR_INVALID_ARG;
+    const int nt = plan->req_tiles[b];
+    if (qt < 0 || qt >= nt || kt < 0 || kt >= nt) return REC_ATTN_ERR_INVALID_ARG;
+  }
+  if (n_pairs == 0) return REC_ATTN_OK;
+  const size_t bits_bytes = (size_t)n_pairs * kTile * 16;
+  const size_t pairs_bytes = ((size_t)n_pairs * 12 + 255) & ~(size_t)255;
+  const size_t cls_bytes = ((size_t)n_pairs + 255) & ~(size_t)255;
+  cudaStream_t st = plan->stream;
+  cudaMemPool_t pool;
+  char* buf = nullptr;
+  cudaError_t e = pool_for(plan->device, &pool);
+  if (e == cudaSuccess)
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), bits_bytes + pairs_bytes + cls_bytes +
+                                (size_t)n_pairs * 4, pool, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  int* d_pairs = reinterpret_cast<int*>(buf + bits_bytes);
+  uint8_t* d_cls = reinterpret_cast<uint8_t*>(buf + bits_bytes + pairs_bytes);
+  int* d_slot = reinterpret_cast<int*>(buf + bits_bytes + pairs_bytes + cls_bytes);
+  e = cudaStreamWaitEvent(st, plan->ev_plan, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_pairs, pairs_host, (size_t)n_pairs * 12, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = launch_export_masks(plan->mask, plan->pd, plan->t, plan->ty, d_pairs, n_pairs, mode,
+                            reinterpret_cast<uint32_t*>(buf), d_cls, d_slot, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(bits_host, buf, bits_bytes, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && list_class_host)
+    e = cudaMemcpyAsync(list_class_host, d_cls, (size_t)n_pairs, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && slot_host)
+    e = cudaMemcpyAsync(slot_host, d_slot, (size_t)n_pairs * 4, cudaMemcpyDeviceToHost, st);
+  const cudaError_t ef = cudaFreeAsync(buf, st);
+  if (e == cudaSuccess) e = ef;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return from_cuda(e);
 }
 

@@ -17,6 +17,12 @@ cudaError_t launch_plan(const MaskP& mp, int heads, const PlanDev& pd, const lon
 cudaError_t launch_build_masks(const MaskP& mp, const PlanDev& pd, int num_sms, cudaStream_t st);
 cudaError_t launch_count_pairs(const MaskP& mp, const PlanDev& pd, const long long* t,
                                const int8_t* ty, long long n_tiles, cudaStream_t st);
+// pairs: device int[n_pairs][3] (request, query tile, key tile), validated by the caller;
+// bits: [n_pairs][128][4]; lcls: the pair's class in its query tile's list (0xff: not
+// listed, never loaded); lslot: its mask-table slot (-1: none).
+cudaError_t launch_export_masks(const MaskP& mp, const PlanDev& pd, const long long* t, const int8_t* ty,
+                                const int* pairs, int n_pairs, int mode, uint32_t* bits, uint8_t* lcls, int* lslot,
+                                cudaStream_t st);
 cudaError_t launch_rope(const RopeArgs& a, int dtype, long long n_tiles, cudaStream_t st);
 cudaError_t launch_rope_fused(const RopeArgs& a, const FusedArgs& f, int dtype, long long n_tiles,
                               cudaStream_t st);

@@ -326,6 +326,40 @@ rec_attn_status rec_attn_tile_classes(rec_attn_plan_t* plan, uint8_t* host_out,
 rec_attn_status rec_attn_visible_pairs(rec_attn_plan_t* plan, uint64_t* host_out);
 
 /*
+ * rec_attn_applied_masks -- diagnostic copy of the visibility bits the attention
+ * kernels apply, for named (query tile, key tile) pairs of a plan, so that a test can
+ * hold them bit for bit against the mask predicate above (the pages' rule that masked
+ * pairs get -inf, not a small constant: LazFormer review page, section 2.3, Eq. 19-21;
+ * CADET delay rule; SORT section 3.1; MTGR hybrid mask).
+ *
+ *   n_pairs       number of pairs (>= 0).
+ *   pairs_host    host int32[n_pairs][3]: (request b, query tile qt, key tile kt),
+ *                 tiles numbered from 0 within request b (qt, kt < ceil(len_b / 128)).
+ *   mode          0: what rec_attn_fwd's tensor-core kernel (bf16) applies: the plan's
+ *                 mask-table rows where the pair has a table slot, the kernel's own row
+ *                 construction otherwise;
+ *                 1: the kernel's row construction for every PARTIAL pair (what a pair
+ *                 beyond the table's capacity, and rec_attn_fwd_noalloc, apply);
+ *                 2: the per-pair predicate of the CUDA-core kernels (fp32 path).
+ *   bits_host     host uint32[n_pairs][128][4]: for query row r of the tile (request-
+ *                 local position 128 qt + r), bit (c % 32) of word c / 32 is 1 when key
+ *                 c of the key tile (position 128 kt + c) enters the row's softmax.  A
+ *                 pair absent from the query tile's key-tile list (SKIP, or a tile of
+ *                 pruned queries) is never loaded: all zero.  A FULL pair takes no mask:
+ *                 all one.  Rows past the request end are zero except in FULL pairs
+ *                 (computed and discarded).
+ *   list_class_host  optional host uint8[n_pairs]: the class in the list entry
+ *                 (REC_ATTN_TILE_*, 0xff when the pair is not listed).
+ *   slot_host     optional host int32[n_pairs]: the pair's mask-table slot (-1: none).
+ * Takes a temporary buffer from the library pool on the plan's stream and
+ * synchronizes it.  Errors: INVALID_ARG (NULL plan or arrays, mode, a pair outside
+ * the plan), OOM, CUDA.
+ */
+rec_attn_status rec_attn_applied_masks(rec_attn_plan_t* plan, int32_t n_pairs, const int32_t* pairs_host,
+                                       int32_t mode, uint32_t* bits_host, uint8_t* list_class_host,
+                                       int32_t* slot_host);
+
+/*
  * rec_attn_device_status -- status word the plan's kernels wrote (REC_ATTN_OK,
  * REC_ATTN_ERR_DEVICE_INPUT or REC_ATTN_ERR_TIMEOUT; the first error wins).
  * Synchronizes the plan's stream.  Errors: INVALID_ARG, CUDA.

@@ -94,3 +94,79 @@ def sample_rows(w: W.Workload, per_request=48, max_requests=6, seed=0):
         cand |= set(int(x) for x in rng.integers(0, L, size=per_request))
         rows += [s + c for c in sorted(cand)]
     return np.array(sorted(set(rows)), dtype=np.int64)
+
+
+def unpack_bits(bits: np.ndarray) -> np.ndarray:
+    """[n, 128, 4] uint32 row words -> [n, 128, 128] uint8 (key c = bit c % 32 of word c / 32)."""
+    b = np.ascontiguousarray(bits, dtype="<u4").view(np.uint8)
+    return np.unpackbits(b, axis=-1, bitorder="little")
+
+
+def all_pairs(w: W.Workload, requests=None):
+    """(request, query tile, key tile) for every tile pair of the given requests."""
+    out = []
+    for b in (range(w.batch) if requests is None else requests):
+        nt = (int(w.offsets[b + 1] - w.offsets[b]) + 127) // 128
+        if nt:
+            qt, kt = np.meshgrid(np.arange(nt), np.arange(nt), indexing="ij")
+            out.append(np.stack([np.full(nt * nt, b), qt.ravel(), kt.ravel()], axis=1))
+    return np.concatenate(out).astype(np.int32) if out else np.zeros((0, 3), dtype=np.int32)
+
+
+def check_applied_masks(w: W.Workload, plan, pairs, op, modes=(0, 1, 2), tile_cls=None):
+    """Hold the visibility bits the kernels apply (rec_attn_applied_masks, every mode)
+    bit for bit against the oracle's mask on the same pairs.  A pair missing from the
+    key-tile lists must have no visible pair (and is applied as all zero); a FULL pair
+    must be all visible over a complete key tile; a PARTIAL pair's bits must equal the
+    mask on the request's rows, with zeros for keys past the request end.  tile_cls
+    (optional): the oracle's classes as a dict, whose non-SKIP pairs must be exactly the
+    listed ones with the same class.  Pairs are checked request by request.  Returns
+    {mode: (pairs checked, pairs with a mask-table slot, PARTIAL pairs)}."""
+    pairs = np.asarray(pairs, dtype=np.int32).reshape(-1, 3)
+    stats = {m: [0, 0, 0] for m in modes}
+    for b in np.unique(pairs[:, 0]).tolist():
+        pb = pairs[pairs[:, 0] == b]
+        s, e = int(w.offsets[b]), int(w.offsets[b + 1])
+        L = e - s
+        nk = 128 * ((L + 127) // 128)
+        ref = {qt: oracle.mask_block(op, w.t[s:e], w.types[s:e], 128 * qt, 128, 0, nk)
+               for qt in np.unique(pb[:, 1]).tolist()}
+        for mode in modes:
+            bits, lcls, slot = bd.rec_attn_applied_masks(plan, pb, mode)
+            got = unpack_bits(bits)
+            for n, (_, qt, kt) in enumerate(pb.tolist()):
+                rows = min(128, L - 128 * qt)
+                blk = ref[qt][:, 128 * kt:128 * kt + 128]
+                g = got[n]
+                where = f"{w.name} mode {mode} pair (b={b}, qt={qt}, kt={kt}) list class {lcls[n]}"
+                if lcls[n] == 0xFF:
+                    assert not blk.any(), f"{where}: a visible pair in a tile the kernels never load"
+                    assert not g.any(), where
+                elif lcls[n] == bd.TILE_FULL:
+                    assert L - 128 * kt >= 128 and blk[:rows].all(), f"{where}: FULL over a masked pair"
+                    assert g.all(), where
+                else:
+                    assert lcls[n] == bd.TILE_PARTIAL, where
+                    bad = np.argwhere(g[:rows] != blk[:rows])
+                    assert bad.size == 0, f"{where}: {len(bad)} bits differ, first (row, key) {bad[:4].tolist()}"
+                    assert not g[rows:].any(), f"{where}: bits set on rows past the request end"
+                    stats[mode][2] += 1
+                if tile_cls is not None:
+                    c = int(tile_cls[(b, qt, kt)])
+                    assert (lcls[n] == 0xFF) == (c == bd.TILE_SKIP) and (c == bd.TILE_SKIP or lcls[n] == c), where
+            stats[mode][0] += len(pb)
+            stats[mode][1] += int((slot >= 0).sum())
+    return {m: tuple(v) for m, v in stats.items()}
+
+
+def tile_class_map(w: W.Workload, cls: np.ndarray):
+    """The flat request-major class array as a dict (b, qt, kt) -> class."""
+    out, i = {}, 0
+    for b in range(w.batch):
+        nt = (int(w.offsets[b + 1] - w.offsets[b]) + 127) // 128
+        blk = cls[i:i + nt * nt].reshape(nt, nt)
+        for qt in range(nt):
+            for kt in range(nt):
+                out[(b, qt, kt)] = blk[qt, kt]
+        i += nt * nt
+    return out
