@@ -1,16 +1,19 @@
 """Benchmark of the masked time-RoPE attention forward on GB300.
 
 One step = the whole hot path over one batch: plan (tile statistics, tile
-classes, key-tile lists, schedule), time-RoPE prologue, fused masked attention,
-plan release.  Default workload: CADET-style impression/action sequences, B=256
-requests x 512 tokens, H=4, d=64, bf16, causal + 1 h delay mask, time-RoPE.
+classes, key-tile lists, mask table, schedule), time-RoPE prologue, fused masked
+attention, plan release.  Default workload: TM20K / LazFormer long histories,
+B=16 requests x (20000 history tokens + 1 target), H=8, d=64, bf16, full causal
+attention, time-RoPE (the largest single-GPU configuration).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 Prints one JSON line.  `value` is TFLOP/s counted over visible (query, key) pairs
-(4 * d * H per pair) for the whole step, inputs resident in HBM; L2 is flushed
-between timed steps.  `--impl reference` times the fp64 CPU oracle on the host
-cores instead (a bounded sample of the same workload per step).
+(4 * d * H per pair) for the whole step (mean over the K timed steps), inputs
+resident in HBM; L2 is flushed between timed steps.  The line also carries the
+medians of 50 iterations (after 10 warm-ups) of the forward alone and of plan +
+forward.  `--impl reference` times the fp64 CPU oracle on the host cores instead
+(a bounded sample of the same workload per step).
 Under torchrun each rank runs its own batch of the same shape (weak scaling); the
 reported value is the total work of all ranks over the slowest rank's time.
 """
@@ -181,14 +184,71 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def _oracle_sample(w: W.Workload, budget_s: float, keep: int = -1):
-    """Time the fp64 oracle on the first requests of the workload (all heads; with
-    query pruning, the computed rows only) until about `budget_s` seconds of work;
-    returns (seconds, visible pairs, requests, threads)."""
+LONG_REQUEST = 4096  # requests longer than this are sampled by rows for the CPU oracle
+
+
+def _sample_rows(w: W.Workload, rows_per_request: int, keep: int = -1, seed: int = 4242) -> np.ndarray:
+    """Seeded query rows (sorted global indices), up to rows_per_request per request:
+    always the first and last rows, the rows at the 128-token tile edges around the
+    window and the global-token boundary, the rest uniform.  Under query pruning only
+    computed rows are drawn."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    kept = None if keep < 0 else set(oracle.kept_rows(w.offsets, w.types, keep).tolist())
+    win = int(w.mask.get("window", 0))
+    out = []
+    for b in range(w.batch):
+        s, e = int(w.offsets[b]), int(w.offsets[b + 1])
+        L = e - s
+        cand = np.arange(L) if kept is None else np.array([i for i in range(L) if s + i in kept], dtype=np.int64)
+        if len(cand) == 0:
+            continue
+        if len(cand) <= rows_per_request:
+            out.extend((s + cand).tolist())
+            continue
+        n_glob = int((w.types[s:e] == W.GLOBAL).sum())
+        must = {int(cand[0]), int(cand[-1])}
+        for x in (127, 128, n_glob - 1, n_glob, win - 1, win, win + 1, n_glob + win - 1, n_glob + win):
+            if 0 <= x < L and (kept is None or s + x in kept):
+                must.add(int(x))
+        rest = np.setdiff1d(cand, np.fromiter(must, dtype=np.int64))
+        pick = rng.choice(rest, size=max(0, rows_per_request - len(must)), replace=False)
+        out.extend(sorted(s + np.concatenate([np.fromiter(must, dtype=np.int64), pick])))
+    return np.array(sorted(out), dtype=np.int64)
+
+
+def _oracle_rows(w: W.Workload, rows: np.ndarray, threads: int):
+    """Time the fp64 oracle on the given query rows (all heads); returns (seconds,
+    visible pairs of those rows per head)."""
+    import oracle
+    p = oracle.Params(w.num_heads, w.head_dim, **w.mask, **w.rope)
+    t0 = time.perf_counter()
+    oracle.attention(p, w.offsets, w.t, w.types, w.q, w.k, w.v, rows=rows, threads=threads)
+    secs = time.perf_counter() - t0
+    pairs = 0
+    req = np.searchsorted(w.offsets, rows, side="right") - 1
+    for b in np.unique(req).tolist():
+        s, e = int(w.offsets[b]), int(w.offsets[b + 1])
+        for i in (rows[req == b] - s).tolist():
+            pairs += int(oracle.mask_block(p, w.t[s:e], w.types[s:e], i, 1, 0, e - s).sum())
+    return secs, pairs
+
+
+def _oracle_sample(w: W.Workload, budget_s: float, keep: int = -1, rows_per_request: int = 2048, seed: int = 4242):
+    """Time the fp64 oracle on a bounded sample of the workload (all heads; with query
+    pruning, the computed rows only).  Requests up to LONG_REQUEST tokens: whole
+    requests from the first, doubling the count until about `budget_s` seconds of work.
+    Longer requests (the 20K-token histories): rows_per_request seeded rows of every
+    request.  Returns (seconds, visible pairs per head, description, threads)."""
     import oracle
     oracle.build()
-    p = oracle.Params(w.num_heads, w.head_dim, **w.mask, **w.rope)
     threads = os.cpu_count() or 1
+    if w.batch and int(np.diff(w.offsets).max()) > LONG_REQUEST:
+        rows = _sample_rows(w, rows_per_request, keep, seed)
+        secs, pairs = _oracle_rows(w, rows, threads)
+        return secs, pairs, f"{rows_per_request} seeded rows of each of the {w.batch} requests (first, last, tile, " \
+                            f"window and global-token boundary rows included), all heads", threads
+    p = oracle.Params(w.num_heads, w.head_dim, **w.mask, **w.rope)
     done, secs, pairs = 0, 0.0, 0
     chunk = 1
     while done < w.batch and secs < budget_s:
@@ -209,26 +269,35 @@ def _oracle_sample(w: W.Workload, budget_s: float, keep: int = -1):
                 pairs += int(oracle.mask(p, w.t[sl][bs:be], w.types[sl][bs:be])[r].sum())
         done += n
         chunk *= 2
-    return secs, pairs, done, threads
+    return secs, pairs, f"first {done} of {w.batch} requests, all heads", threads
 
 
 def run_reference(args):
-    """--impl reference: the fp64 CPU oracle on the host cores, same metric."""
+    """--impl reference: the fp64 CPU oracle on the host cores, same metric.  Each step
+    is a bounded sample of the workload, sized so that warm-up and steps take about a
+    minute together."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
     w = _workload(args.workload, 0, args.batch)
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        _oracle_sample(w, per_step / 4, args.keep_user_queries)
-    tot_s, tot_pairs, reqs = 0.0, 0, []
+    long_req = w.batch and int(np.diff(w.offsets).max()) > LONG_REQUEST
+    rows_per_request = 512
+    if long_req:
+        # calibrate the rows per request on a first small sample (counted as warm-up)
+        s0, _, _, _ = _oracle_sample(w, per_step, args.keep_user_queries, rows_per_request=8, seed=1)
+        rows_per_request = int(max(4, min(512, 8 * per_step / max(s0, 1e-3))))
+    for i in range(args.warmup):
+        _oracle_sample(w, per_step / 4, args.keep_user_queries, rows_per_request=max(4, rows_per_request // 4),
+                       seed=100 + i)
+    tot_s, tot_pairs, desc = 0.0, 0, ""
     threads = 1
-    for _ in range(args.steps):
-        s, pairs, n, threads = _oracle_sample(w, per_step, args.keep_user_queries)
+    for i in range(args.steps):
+        s, pairs, desc, threads = _oracle_sample(w, per_step, args.keep_user_queries,
+                                                 rows_per_request=rows_per_request, seed=1000 + i)
         tot_s += s
         tot_pairs += pairs
-        reqs.append(n)
     flops = 4.0 * w.head_dim * w.num_heads * tot_pairs
     value = flops / tot_s / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
@@ -237,7 +306,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(w, args.workload, "host cores"),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": f"first {min(reqs)}-{max(reqs)} of {w.batch} requests per step, all heads"},
+                             "sample": f"per step: {desc}"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -410,6 +479,18 @@ def run_ours(args):
     for _ in range(max(args.warmup, 3)):
         bd.rec_attn_free(step())
     torch.cuda.synchronize(dev)
+    # the clock sampler starts here: warm-up continues, under the same load, until at
+    # least args.soak_s seconds have passed, so the clocks sampled around the timed
+    # region are those of a GPU that has been busy for a while
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    soak0 = time.perf_counter()
+    n_soak = 0
+    while time.perf_counter() - soak0 < args.soak_s:
+        for _ in range(8):
+            flush.zero_()
+            bd.rec_attn_free(step())
+            n_soak += 1
+        torch.cuda.synchronize(dev)
 
     # ---- timed region: K steps, each bracketed by CUDA events on the launch stream
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -417,7 +498,6 @@ def run_ours(args):
     plans = []
     if args.backward:
         bwd_events = []
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -432,7 +512,6 @@ def run_ours(args):
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kt = [bd.rec_attn_read_timings(p) for p in plans]
     status = max(bd.rec_attn_device_status(p) for p in plans)
@@ -440,6 +519,35 @@ def run_ours(args):
         bd.rec_attn_free(p)
     if status != bd.OK:
         raise RuntimeError(f"device status {status}: {bd.rec_attn_status_string(status)}")
+
+    # ---- medians of args.median_iters iterations after 10 warm-ups: the forward alone
+    # (one plan reused, as every layer of a model reuses it) and plan + forward
+    def median_ms(fn, iters):
+        for _ in range(10):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        torch.cuda.synchronize(dev)
+        for a_, b_ in evs:
+            flush.zero_()
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a_.elapsed_time(b_) for a_, b_ in evs)
+
+    medians = None
+    if args.median_iters > 0 and not args.backward:
+        reused = mkplan(off_d, t, ty, stream)
+        med_fwd = median_ms(lambda: fwd(reused, q, k, v), args.median_iters)
+        bd.rec_attn_free(reused)
+        med_step = median_ms(lambda: bd.rec_attn_free(step()), args.median_iters)
+        medians = {"iterations": args.median_iters, "warmup": 10, "fwd_ms": med_fwd, "plan_fwd_ms": med_step,
+                   "fwd_tflops": flops_fwd / (med_fwd * 1e-3) / 1e12,
+                   "plan_fwd_tflops": flops_fwd / (med_step * 1e-3) / 1e12}
+    clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = (f"sampled every 200 ms over {args.soak_s:.1f} s of warm-up steps ({n_soak}), the "
+                            f"timed region and the median runs, back to back under load")
     total_ms = float(sum(step_ms))
     attn_ms = statistics.mean(x[1] for x in kt)
     bwd_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in bwd_events) if args.backward else 0.0
@@ -553,11 +661,14 @@ def run_ours(args):
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
+    if medians is not None:
+        line["median"] = medians
     if world == 1 and not args.no_cpu_baseline:
-        secs, cpairs, nreq, threads = _oracle_sample(w, args.cpu_budget, args.keep_user_queries)
+        secs, cpairs, desc, threads = _oracle_sample(w, args.cpu_budget, args.keep_user_queries)
         cval = 4.0 * w.head_dim * w.num_heads * cpairs / secs / 1e12
         line["cpu_baseline"] = {"value": cval, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": f"first {nreq} of {w.batch} requests, all heads ({secs:.1f} s)"}
+                                "sample": f"{desc} ({secs:.1f} s measured)",
+                                "full_batch_s_extrapolated": secs * pairs / max(cpairs, 1)}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -569,7 +680,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="cadet", choices=W.NAMES + W.EXTRA_NAMES)
+    ap.add_argument("--workload", default="tm20k_full", choices=W.NAMES + W.EXTRA_NAMES)
     ap.add_argument("--keep-user-queries", type=int, default=-1,
                     help="query pruning: compute every non-user query and the last N user queries of "
                          "each request (-1: all; 0: target attention)")
@@ -578,6 +689,10 @@ def main(argv=None):
                     help="override the workload's number of requests (small profiling cases)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=2.0,
+                    help="seconds of extra warm-up steps, with the clock sampler running, before the timed region")
+    ap.add_argument("--median-iters", type=int, default=50,
+                    help="iterations of the median runs (forward alone, plan + forward); 0 to skip")
     ap.add_argument("--compress", default=None, choices=sorted(COMPRESS_SPECS),
                     help="time history compression of the workload's key rows instead (HBM-bound)")
     ap.add_argument("--backward", action="store_true",
