@@ -5,8 +5,9 @@ allocator, or a serving loop that cannot pay cudaMalloc's latency per request).
 It keeps its workspace in one static device array, so these checks call it through
 the C-ABI twice in a row and compare each result with the plan-based entry points
 (rec_attn_plan + rec_attn_fwd) on the same inputs, within the tolerance the other
-GPU tests use; a second, different batch then checks that nothing from the first
-call leaks into the next.  The file is named to be collected last, and it passes
+GPU tests use and, since both run the same kernels on the same mask bits, bit for
+bit; a second, different batch then checks that nothing from the first call leaks
+into the next.  The device's free memory must not change across the later calls.  The file is named to be collected last, and it passes
 both alone in a fresh process and after the rest of the suite.
 """
 import numpy as np
@@ -40,6 +41,7 @@ def _noalloc(w, tens):
 
 
 def _close(w, a, b):
+    assert torch.equal(a, b), "the no-allocation path differs from the plan API"
     a64, b64 = gu.to_f64(a), gu.to_f64(b)
     assert not np.isnan(a64).any()
     d = np.abs(a64 - b64)
@@ -60,8 +62,19 @@ def test_noalloc_matches_plan_api_twice_in_a_row(make):
     w = make()
     tens = gu.device_inputs(w)
     ref = _reference(w, tens)
-    for _ in range(2):
-        _close(w, _noalloc(w, tens), ref)
+    out = torch.full_like(tens["q"], float("nan"))
+    free = []
+    for _ in range(3):
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
+        bd.rec_attn_fwd_noalloc(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"],
+                                tens["q"], tens["k"], tens["v"], out)
+        torch.cuda.synchronize()
+        _close(w, out, ref)
+    free.append(torch.cuda.mem_get_info()[0])
+    # the first call may load the library's kernels; later calls take no device memory
+    assert free[1] == free[2] == free[3], free
 
 
 def test_noalloc_state_does_not_leak_between_batches():
