@@ -287,6 +287,57 @@ def rec_attn_visible_pairs(plan: Plan) -> int:
     return int(n.value)
 
 
+@dataclass
+class KVCache:
+    handle: int
+    batch: int
+    max_cands: int
+    _keep: tuple = ()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        rec_attn_cache_free(self)
+
+
+def rec_attn_cache_create(params: RecAttnParams, hist_offsets_host, hist_t, hist_types, k_hist, v_hist,
+                          max_cands: int, stream=None) -> KVCache:
+    """Cache the rotated history keys, values, times and types of a batch of requests
+    (serving: candidate micro-batches are then scored against them)."""
+    L = lib()
+    vp = ctypes.c_void_p
+    L.rec_attn_cache_create.argtypes = [ctypes.POINTER(RecAttnParams), ctypes.c_int32, vp, vp, vp, vp, vp,
+                                        ctypes.c_int32, vp, ctypes.POINTER(vp)]
+    L.rec_attn_cache_create.restype = ctypes.c_int
+    off = np.ascontiguousarray(np.asarray(hist_offsets_host, dtype=np.int64))
+    h = ctypes.c_void_p()
+    _check("rec_attn_cache_create", L.rec_attn_cache_create(
+        ctypes.byref(params), len(off) - 1, _ptr(off), _ptr(hist_t), _ptr(hist_types), _ptr(k_hist), _ptr(v_hist),
+        int(max_cands), _stream(stream), ctypes.byref(h)))
+    return KVCache(h.value, len(off) - 1, int(max_cands))
+
+
+def rec_attn_cache_score(cache: KVCache, cand_offsets_host, cand_t, q, k, v, out, lse=None, stream=None) -> None:
+    """Outputs of one micro-batch of candidates per request against the cached history."""
+    L = lib()
+    vp = ctypes.c_void_p
+    L.rec_attn_cache_score.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.rec_attn_cache_score.restype = ctypes.c_int
+    off = np.ascontiguousarray(np.asarray(cand_offsets_host, dtype=np.int64))
+    _check("rec_attn_cache_score", L.rec_attn_cache_score(cache.handle, _ptr(off), _ptr(cand_t), _ptr(q), _ptr(k),
+                                                          _ptr(v), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def rec_attn_cache_free(cache: KVCache) -> None:
+    if cache is not None and cache.handle:
+        L = lib()
+        L.rec_attn_cache_free.argtypes = [ctypes.c_void_p]
+        L.rec_attn_cache_free.restype = None
+        L.rec_attn_cache_free(cache.handle)
+        cache.handle = 0
+
+
 MASK_APPLIED, MASK_BUILT, MASK_PREDICATE = 0, 1, 2
 
 

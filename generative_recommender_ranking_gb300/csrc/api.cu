@@ -835,3 +835,269 @@ REC_ATTN_API rec_attn_status rec_attn_device_status(rec_attn_plan_t* plan, int32
   if (e == cudaSuccess) *status_out = s;
   return from_cuda(e);
 }
+
+// ---------------------------------------------------------------------------------
+// Serving with a cached history (M-FALCON, HSTU notes on the blog index page: the
+// user's history keys and values are computed once and every candidate micro-batch
+// reads them; CADET's serving section scores hundreds of candidates per request).
+//
+// The cache keeps every request's rows in a combined layout: the history rows, then
+// max_cands candidate slots.  Creation rotates the history keys once (K'), copies the
+// values, times and types.  A scoring call writes its candidates into the slots
+// (rotated Q' and K' against the same per-request reference time, V, time, type
+// CAND; unused slots are zero padding that no real token sees), plans a layer in
+// which only non-user tokens query (target attention over [history, slots]), runs
+// the attention kernel on the cached, already rotated rows, and gathers the
+// candidates' outputs back to the caller's packed layout.
+
+struct rec_attn_kv_cache_s {
+  rec_attn_params p{};   // the caller's parameters
+  rec_attn_params pp{};  // those of the per-call plans: the rows are already rotated
+  int device = 0;
+  int32_t batch = 0;
+  int32_t max_cands = 0;
+  long long Tc = 0;                 // rows of the combined layout
+  std::vector<int64_t> comb_off;    // [B+1] host: request b owns rows comb_off[b] ..
+  std::vector<long long> hist_len;  // [B]
+  void* buf = nullptr;              // combined Q', K', V, O, lse, t, types, offsets
+  void *q, *k, *v, *o;
+  float* lse = nullptr;
+  long long* t = nullptr;
+  int8_t* ty = nullptr;
+  int64_t* off_dev = nullptr;
+  float omega[kMaxPairs] = {};
+};
+
+namespace {
+
+// Region table of k_rope_slots / k_slots_gather: SlotReq per request, then the
+// request and first row of every 128-row chunk; staged through one pool buffer.
+struct SlotTable {
+  std::vector<char> host;
+  size_t off_chunk_req = 0, off_chunk_row0 = 0;
+  long long n_chunks = 0;
+};
+
+SlotTable slot_table(const std::vector<SlotReq>& reqs) {
+  SlotTable st;
+  std::vector<int> creq, crow;
+  for (size_t b = 0; b < reqs.size(); ++b)
+    for (int r0 = 0; r0 < reqs[b].cap; r0 += kTile) {
+      creq.push_back((int)b);
+      crow.push_back(r0);
+    }
+  st.n_chunks = (long long)creq.size();
+  st.off_chunk_req = ((reqs.size() * sizeof(SlotReq)) + 15) & ~(size_t)15;
+  st.off_chunk_row0 = st.off_chunk_req + ((creq.size() * 4 + 15) & ~(size_t)15);
+  st.host.assign(st.off_chunk_row0 + crow.size() * 4 + 16, 0);
+  std::memcpy(st.host.data(), reqs.data(), reqs.size() * sizeof(SlotReq));
+  std::memcpy(st.host.data() + st.off_chunk_req, creq.data(), creq.size() * 4);
+  std::memcpy(st.host.data() + st.off_chunk_row0, crow.data(), crow.size() * 4);
+  return st;
+}
+
+// Upload a region table into pool memory on `st` (freed in stream order by the caller).
+cudaError_t upload_table(const SlotTable& tab, int device, cudaStream_t st, void** dev) {
+  cudaMemPool_t pool;
+  cudaError_t e = pool_for(device, &pool);
+  if (e == cudaSuccess) e = cudaMallocFromPoolAsync(dev, tab.host.size(), pool, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(*dev, tab.host.data(), tab.host.size(), cudaMemcpyHostToDevice, st);
+  return e;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+REC_ATTN_API rec_attn_status rec_attn_cache_create(const rec_attn_params* params, int32_t batch,
+                                                   const int64_t* hist_offsets_host, const int64_t* hist_t_dev,
+                                                   const int8_t* hist_types_dev, const void* k_hist,
+                                                   const void* v_hist, int32_t max_cands, void* stream,
+                                                   rec_attn_kv_cache_t** cache_out) {
+  if (!cache_out) return REC_ATTN_ERR_INVALID_ARG;
+  *cache_out = nullptr;
+  rec_attn_status s = check_params(params);
+  if (s != REC_ATTN_OK) return s;
+  if (batch < 1 || !hist_offsets_host || max_cands < 1) return REC_ATTN_ERR_INVALID_ARG;
+  if (hist_offsets_host[0] != 0) return REC_ATTN_ERR_INVALID_ARG;
+  long long Th = 0, Tc = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const long long len = hist_offsets_host[b + 1] - hist_offsets_host[b];
+    if (len < 0) return REC_ATTN_ERR_INVALID_ARG;
+    if (len + max_cands > REC_ATTN_MAX_REQUEST_LEN) return REC_ATTN_ERR_UNSUPPORTED;
+    Tc += len + max_cands;
+  }
+  Th = hist_offsets_host[batch];
+  if (Tc >= (1LL << 31)) return REC_ATTN_ERR_UNSUPPORTED;
+  if (Th > 0 && (!hist_t_dev || !hist_types_dev || !k_hist || !v_hist || !aligned16(k_hist) || !aligned16(v_hist)))
+    return REC_ATTN_ERR_INVALID_ARG;
+
+  rec_attn_kv_cache_s* c = new (std::nothrow) rec_attn_kv_cache_s();
+  if (!c) return REC_ATTN_ERR_OOM;
+  try {
+    c->comb_off.resize((size_t)batch + 1);
+    c->hist_len.resize((size_t)batch);
+  } catch (...) {
+    delete c;
+    return REC_ATTN_ERR_OOM;
+  }
+  c->p = *params;
+  if (c->p.softmax_scale == 0.f) c->p.softmax_scale = 1.f / std::sqrt((float)params->head_dim);
+  c->pp = c->p;
+  c->pp.use_rope = 0;
+  c->batch = batch;
+  c->max_cands = max_cands;
+  c->Tc = Tc;
+  c->comb_off[0] = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    c->hist_len[b] = hist_offsets_host[b + 1] - hist_offsets_host[b];
+    c->comb_off[b + 1] = c->comb_off[b] + c->hist_len[b] + max_cands;
+  }
+  if (params->use_rope)
+    for (int i = 0; i < params->head_dim / 2 && i < kMaxPairs; ++i)
+      c->omega[i] = (float)(params->phi_min / params->dt_max_s *
+                            std::pow(params->rope_base, 2.0 * i / (double)params->head_dim));
+  const size_t elem = params->dtype == REC_ATTN_BF16 ? 2 : 4;
+  const size_t rows_bytes = ws_up((size_t)Tc * params->num_heads * params->head_dim * elem);
+  const size_t lse_bytes = ws_up((size_t)Tc * params->num_heads * 4);
+  const size_t t_bytes = ws_up((size_t)Tc * 8), ty_bytes = ws_up((size_t)Tc), off_bytes = ws_up(8 * ((size_t)batch + 1));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaGetDevice(&c->device);
+  cudaMemPool_t pool;
+  if (e == cudaSuccess) e = pool_for(c->device, &pool);
+  if (e == cudaSuccess)
+    e = cudaMallocFromPoolAsync(&c->buf, 4 * rows_bytes + lse_bytes + t_bytes + ty_bytes + off_bytes, pool, st);
+  if (e != cudaSuccess) { delete c; return from_cuda(e); }
+  char* w = static_cast<char*>(c->buf);
+  c->q = w; c->k = w + rows_bytes; c->v = w + 2 * rows_bytes; c->o = w + 3 * rows_bytes;
+  c->lse = reinterpret_cast<float*>(w + 4 * rows_bytes);
+  c->t = reinterpret_cast<long long*>(w + 4 * rows_bytes + lse_bytes);
+  c->ty = reinterpret_cast<int8_t*>(w + 4 * rows_bytes + lse_bytes + t_bytes);
+  c->off_dev = reinterpret_cast<int64_t*>(w + 4 * rows_bytes + lse_bytes + t_bytes + ty_bytes);
+  // history rows: rotated keys, values, times and types (queries stay zero: no user
+  // token queries in a scoring call); the candidate slots are written by each call
+  std::vector<SlotReq> reqs((size_t)batch);
+  for (int32_t b = 0; b < batch; ++b) {
+    SlotReq& r = reqs[b];
+    r.src_start = hist_offsets_host[b];
+    r.dst_start = c->comb_off[b];
+    r.ref_row = hist_offsets_host[b];
+    r.ref_dst = 0;
+    r.len = r.cap = (int)c->hist_len[b];
+    r.pad = 0;
+  }
+  const SlotTable tab = slot_table(reqs);
+  void* dtab = nullptr;
+  e = cudaMemsetAsync(c->q, 0, rows_bytes, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->off_dev, c->comb_off.data(), 8 * ((size_t)batch + 1),
+                                            cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && tab.n_chunks > 0) {
+    e = upload_table(tab, c->device, st, &dtab);
+    if (e == cudaSuccess) {
+      SlotArgs a{};
+      a.req = static_cast<const SlotReq*>(dtab);
+      a.chunk_req = reinterpret_cast<const int*>(static_cast<char*>(dtab) + tab.off_chunk_req);
+      a.chunk_row0 = reinterpret_cast<const int*>(static_cast<char*>(dtab) + tab.off_chunk_row0);
+      a.t_src = reinterpret_cast<const long long*>(hist_t_dev);
+      a.ty_src = hist_types_dev;
+      a.q_src = nullptr; a.k_src = k_hist; a.v_src = v_hist;
+      a.q_dst = nullptr; a.k_dst = c->k; a.v_dst = c->v; a.t_dst = c->t; a.ty_dst = c->ty;
+      a.heads = params->num_heads; a.head_dim = params->head_dim;
+      std::memcpy(a.omega, c->omega, sizeof a.omega);
+      e = launch_rope_slots(a, params->dtype, tab.n_chunks, st);
+    }
+    if (dtab) {
+      const cudaError_t ef = cudaFreeAsync(dtab, st);
+      if (e == cudaSuccess) e = ef;
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaFreeAsync(c->buf, st);
+    delete c;
+    return from_cuda(e);
+  }
+  *cache_out = c;
+  return REC_ATTN_OK;
+}
+
+REC_ATTN_API rec_attn_status rec_attn_cache_score(rec_attn_kv_cache_t* c, const int64_t* cand_offsets_host,
+                                                  const int64_t* cand_t_dev, const void* q_cand, const void* k_cand,
+                                                  const void* v_cand, void* out, float* lse, void* stream) {
+  if (!c || !cand_offsets_host || cand_offsets_host[0] != 0) return REC_ATTN_ERR_INVALID_ARG;
+  for (int32_t b = 0; b < c->batch; ++b) {
+    const long long n = cand_offsets_host[b + 1] - cand_offsets_host[b];
+    if (n < 0 || n > c->max_cands) return REC_ATTN_ERR_INVALID_ARG;
+  }
+  const long long Nc = cand_offsets_host[c->batch];
+  const rec_attn_params& p = c->p;
+  const size_t elem = p.dtype == REC_ATTN_BF16 ? 2 : 4;
+  if (Nc > 0) {
+    if (!cand_t_dev || !q_cand || !k_cand || !v_cand || !out) return REC_ATTN_ERR_INVALID_ARG;
+    const void* ptrs[4] = {q_cand, k_cand, v_cand, out};
+    for (const void* x : ptrs)
+      if (!aligned16(x)) return REC_ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return REC_ATTN_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)Nc * p.num_heads * p.head_dim * elem;
+    if (overlaps(out, bytes, q_cand, bytes) || overlaps(out, bytes, k_cand, bytes) ||
+        overlaps(out, bytes, v_cand, bytes) || (lse && overlaps(lse, (size_t)Nc * p.num_heads * 4, out, bytes)))
+      return REC_ATTN_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (dev != c->device) return REC_ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the candidate slots: rotated Q' and K' against the request's reference time (its
+  // first history row, else its first candidate), V, time and type CAND; padding after
+  std::vector<SlotReq> reqs((size_t)c->batch);
+  for (int32_t b = 0; b < c->batch; ++b) {
+    SlotReq& r = reqs[b];
+    r.src_start = cand_offsets_host[b];
+    r.dst_start = c->comb_off[b] + c->hist_len[b];
+    r.ref_dst = c->hist_len[b] > 0 ? 1 : 0;
+    r.ref_row = c->hist_len[b] > 0 ? c->comb_off[b] : cand_offsets_host[b];
+    r.len = (int)(cand_offsets_host[b + 1] - cand_offsets_host[b]);
+    r.cap = c->max_cands;
+    r.pad = 0;
+  }
+  const SlotTable tab = slot_table(reqs);
+  void* dtab = nullptr;
+  e = upload_table(tab, c->device, st, &dtab);
+  SlotArgs a{};
+  if (e == cudaSuccess) {
+    a.req = static_cast<const SlotReq*>(dtab);
+    a.chunk_req = reinterpret_cast<const int*>(static_cast<char*>(dtab) + tab.off_chunk_req);
+    a.chunk_row0 = reinterpret_cast<const int*>(static_cast<char*>(dtab) + tab.off_chunk_row0);
+    a.t_src = reinterpret_cast<const long long*>(cand_t_dev);
+    a.ty_src = nullptr;
+    a.ty_const = REC_ATTN_CAND;
+    a.q_src = q_cand; a.k_src = k_cand; a.v_src = v_cand;
+    a.q_dst = c->q; a.k_dst = c->k; a.v_dst = c->v; a.t_dst = c->t; a.ty_dst = c->ty;
+    a.o_comb = c->o; a.lse_comb = c->lse; a.o_out = out; a.lse_out = lse;
+    a.heads = p.num_heads; a.head_dim = p.head_dim;
+    std::memcpy(a.omega, c->omega, sizeof a.omega);
+    e = launch_rope_slots(a, p.dtype, tab.n_chunks, st);
+  }
+  // target attention over [history, slots] on the cached rows (no rotation in the plan)
+  rec_attn_plan_t* plan = nullptr;
+  rec_attn_status s = REC_ATTN_OK;
+  if (e == cudaSuccess) {
+    s = plan_impl(&c->pp, 0, c->batch, c->comb_off.data(), c->off_dev, reinterpret_cast<const int64_t*>(c->t), c->ty,
+                  st, &plan);
+    if (s == REC_ATTN_OK) s = fwd_impl(plan, c->q, c->k, c->v, nullptr, c->o, lse ? c->lse : nullptr, st);
+    if (s == REC_ATTN_OK) e = launch_slots_gather(a, p.dtype, tab.n_chunks, st);
+    if (plan) rec_attn_free(plan);
+  }
+  if (dtab) {
+    const cudaError_t ef = cudaFreeAsync(dtab, st);
+    if (e == cudaSuccess) e = ef;
+  }
+  if (s != REC_ATTN_OK) return s;
+  return from_cuda(e);
+}
+
+REC_ATTN_API void rec_attn_cache_free(rec_attn_kv_cache_t* c) {
+  if (!c) return;
+  if (c->buf) cudaFree(c->buf);  // synchronizes: the cache's rows may still be read
+  delete c;
+}

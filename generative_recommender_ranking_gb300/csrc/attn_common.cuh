@@ -47,6 +47,46 @@ struct RopeArgs {
   float omega[kMaxPairs];  // rad per second, pair i
 };
 
+// Serving with a cached history (M-FALCON): one region of a request's rows in the
+// cache's combined layout, filled by k_rope_slots from packed source rows.  The
+// first `len` destination rows take source rows src_start.. (rotated keys and
+// queries, copied values, times, types); rows len..cap-1 are padding (zeros, the
+// time of the last source row or the reference, the constant type).
+struct SlotReq {
+  long long src_start;  // first source row
+  long long dst_start;  // first destination row
+  long long ref_row;    // row holding the request's rotation reference time
+  int ref_dst;          // 1: ref_row indexes the destination times, 0: the source times
+  int len;              // source rows
+  int cap;              // destination rows (len <= cap)
+  int pad;
+};
+static_assert(sizeof(SlotReq) == 40, "");
+
+struct SlotArgs {
+  const SlotReq* req;
+  const int* chunk_req;    // per 128-row chunk of the regions: its request
+  const int* chunk_row0;   // and its first row within the region
+  const long long* t_src;  // [source rows]
+  const int8_t* ty_src;    // [source rows], or null: every written row takes ty_const
+  int ty_const;
+  const void* q_src;       // [source][H][d] or null (no queries)
+  const void* k_src;
+  const void* v_src;
+  void* q_dst;             // [destination][H][d]
+  void* k_dst;
+  void* v_dst;
+  long long* t_dst;
+  int8_t* ty_dst;
+  // gather direction (k_slots_gather): out rows of the source layout from the destination layout
+  const void* o_comb;      // [destination][H][d]
+  const float* lse_comb;   // [destination][H] or null
+  void* o_out;             // [source][H][d]
+  float* lse_out;          // [source][H] or null
+  int heads, head_dim;
+  float omega[kMaxPairs];  // rad per second, pair i (all zero: no rotation)
+};
+
 // One backward work item as the tensor-core kernels read it (one 48-byte record per
 // item and mode, written once per plan by k_bwd_schedule).
 struct BwdItemDesc {

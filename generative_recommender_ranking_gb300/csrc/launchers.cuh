@@ -26,6 +26,10 @@ cudaError_t launch_export_masks(const MaskP& mp, const PlanDev& pd, const long l
 cudaError_t launch_rope(const RopeArgs& a, int dtype, long long n_tiles, cudaStream_t st);
 cudaError_t launch_rope_fused(const RopeArgs& a, const FusedArgs& f, int dtype, long long n_tiles,
                               cudaStream_t st);
+// Serving with a cached history: regions of rows into / out of the combined layout
+// (n_chunks 128-row chunks listed in a.chunk_req / a.chunk_row0).
+cudaError_t launch_rope_slots(const SlotArgs& a, int dtype, long long n_chunks, cudaStream_t st);
+cudaError_t launch_slots_gather(const SlotArgs& a, int dtype, long long n_chunks, cudaStream_t st);
 cudaError_t launch_attn_simt(const AttnArgs& a, int head_dim, cudaStream_t st);
 cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, int head_dim, cudaStream_t st);
 cudaError_t launch_attn_bwd_simt(const BwdArgs& a, int head_dim, long long n_tiles, cudaStream_t st);

@@ -250,7 +250,119 @@ __global__ void __launch_bounds__(256, 3) k_rope_fused(RopeArgs a, FusedArgs f) 
   }
 }
 
+// Rows of one 128-row chunk of a region into the cache's combined layout (serving
+// with a cached history): rotated K (and Q), copied V, times and types; padding rows
+// past the region's source rows get zeros.  One (row, 16-byte chunk) unit per thread
+// over every head, 256 / chunks rows per block as in k_rope.
+template <typename E>
+__global__ void __launch_bounds__(256, 4) k_rope_slots(SlotArgs a) {
+  using C = Chunk<E>;
+  constexpr int kPairs = C::kPairs;
+  const int chunks = a.head_dim / (2 * kPairs);
+  const int tpb = (int)blockDim.x / chunks;
+  const int bpt = kTile / tpb;
+  const long long g = blockIdx.x / bpt;
+  const SlotReq rq = a.req[a.chunk_req[g]];
+  const int row = a.chunk_row0[g] + (int)(blockIdx.x % bpt) * tpb + (int)threadIdx.x / chunks;
+  const int c = (int)threadIdx.x % chunks;
+  if (row >= rq.cap) return;
+  const long long head_bytes = (long long)a.head_dim * (long long)sizeof(E);
+  const long long dst = rq.dst_start + row;
+  const long long d0 = dst * a.heads * head_bytes + (long long)c * 16;
+  if (row >= rq.len) {  // padding
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int h = 0; h < a.heads; ++h) {
+      *reinterpret_cast<uint4*>(static_cast<char*>(a.k_dst) + d0 + h * head_bytes) = z;
+      *reinterpret_cast<uint4*>(static_cast<char*>(a.v_dst) + d0 + h * head_bytes) = z;
+      if (a.q_dst) *reinterpret_cast<uint4*>(static_cast<char*>(a.q_dst) + d0 + h * head_bytes) = z;
+    }
+    if (c == 0) {
+      const long long t_ref = rq.ref_dst ? a.t_dst[rq.ref_row] : a.t_src[rq.ref_row];
+      a.t_dst[dst] = rq.len > 0 ? a.t_src[rq.src_start + rq.len - 1] : t_ref;
+      a.ty_dst[dst] = (int8_t)a.ty_const;
+    }
+    return;
+  }
+  const long long src = rq.src_start + row;
+  const long long s0 = src * a.heads * head_bytes + (long long)c * 16;
+  const long long t_ref = rq.ref_dst ? a.t_dst[rq.ref_row] : a.t_src[rq.ref_row];
+  const long long ts = a.t_src[src];
+  const float dt = (float)(ts - t_ref);  // exact int64 difference, then fp32
+  float sn[kPairs], cs[kPairs];
+#pragma unroll
+  for (int p = 0; p < kPairs; ++p) sincosf(dt * a.omega[c * kPairs + p], &sn[p], &cs[p]);
+  for (int h = 0; h < a.heads; ++h) {
+    const long long so = s0 + h * head_bytes, dof = d0 + h * head_bytes;
+    const uint4 rk = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.k_src) + so);
+    const uint4 rv = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.v_src) + so);
+    float y[8];
+    C::unpack(rk, y);
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) {
+      const float y0 = y[2 * p], y1 = y[2 * p + 1];
+      y[2 * p] = y0 * cs[p] - y1 * sn[p];
+      y[2 * p + 1] = y0 * sn[p] + y1 * cs[p];
+    }
+    C::store(static_cast<char*>(a.k_dst) + dof, y);
+    *reinterpret_cast<uint4*>(static_cast<char*>(a.v_dst) + dof) = rv;
+    if (a.q_src) {
+      float x[8];
+      C::load(static_cast<const char*>(a.q_src) + so, x);
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        const float x0 = x[2 * p], x1 = x[2 * p + 1];
+        x[2 * p] = x0 * cs[p] - x1 * sn[p];
+        x[2 * p + 1] = x0 * sn[p] + x1 * cs[p];
+      }
+      C::store(static_cast<char*>(a.q_dst) + dof, x);
+    }
+  }
+  if (c == 0) {
+    a.t_dst[dst] = ts;
+    a.ty_dst[dst] = a.ty_src ? a.ty_src[src] : (int8_t)a.ty_const;
+  }
+}
+
+// The outputs of a region's source rows back from the combined layout (16 bytes per
+// thread; the lse of a row by its first chunk's thread).
+__global__ void __launch_bounds__(256) k_slots_gather(SlotArgs a, int elem) {
+  const int chunks = a.head_dim * elem / 16;
+  const int tpb = (int)blockDim.x / chunks;
+  const int bpt = kTile / tpb;
+  const long long g = blockIdx.x / bpt;
+  const SlotReq rq = a.req[a.chunk_req[g]];
+  const int row = a.chunk_row0[g] + (int)(blockIdx.x % bpt) * tpb + (int)threadIdx.x / chunks;
+  const int c = (int)threadIdx.x % chunks;
+  if (row >= rq.len) return;
+  const long long head_bytes = (long long)a.head_dim * elem;
+  const long long src = rq.src_start + row, dst = rq.dst_start + row;
+  for (int h = 0; h < a.heads; ++h)
+    *reinterpret_cast<uint4*>(static_cast<char*>(a.o_out) + (src * a.heads + h) * head_bytes + c * 16) =
+        *reinterpret_cast<const uint4*>(static_cast<const char*>(a.o_comb) + (dst * a.heads + h) * head_bytes +
+                                        c * 16);
+  if (a.lse_out && c == 0)
+    for (int h = 0; h < a.heads; ++h) a.lse_out[src * a.heads + h] = a.lse_comb[dst * a.heads + h];
+}
+
 }  // namespace
+
+cudaError_t launch_rope_slots(const SlotArgs& a, int dtype, long long n_chunks, cudaStream_t st) {
+  if (n_chunks <= 0) return cudaSuccess;
+  const int chunks = a.head_dim * (dtype == REC_ATTN_BF16 ? 2 : 4) / 16;
+  const unsigned blocks = (unsigned)(n_chunks * (chunks / 2));
+  if (dtype == REC_ATTN_BF16) k_rope_slots<__nv_bfloat16><<<blocks, 256, 0, st>>>(a);
+  else k_rope_slots<float><<<blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slots_gather(const SlotArgs& a, int dtype, long long n_chunks, cudaStream_t st) {
+  if (n_chunks <= 0) return cudaSuccess;
+  const int elem = dtype == REC_ATTN_BF16 ? 2 : 4;
+  const int chunks = a.head_dim * elem / 16;
+  const unsigned blocks = (unsigned)(n_chunks * (chunks / 2));
+  k_slots_gather<<<blocks, 256, 0, st>>>(a, elem);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_fused(const RopeArgs& a, const FusedArgs& f, int dtype, long long n_tiles, cudaStream_t st) {
   if (n_tiles <= 0) return cudaSuccess;

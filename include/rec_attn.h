@@ -326,6 +326,64 @@ rec_attn_status rec_attn_tile_classes(rec_attn_plan_t* plan, uint8_t* host_out,
 rec_attn_status rec_attn_visible_pairs(rec_attn_plan_t* plan, uint64_t* host_out);
 
 /*
+ * Serving with a cached history (M-FALCON, HSTU notes on the blog index page: the
+ * history's keys and values are computed once per user and every micro-batch of
+ * candidates is scored against them; CADET review page, scoring hundreds of
+ * candidates per request within its latency budget).
+ *
+ * rec_attn_cache_create -- cache the rotated history keys K', the values V, times and
+ * types of a batch of requests, with room for up to max_cands candidates each.
+ *   params           as for rec_attn_plan (copied).
+ *   batch            requests B >= 1.
+ *   hist_offsets_host host int64[B+1]: history rows [offsets[b], offsets[b+1]) of
+ *                    request b in the packed inputs below (offsets[0] = 0); read
+ *                    during the call.  A history may be empty.
+ *   hist_t_dev       device int64[Th] times; hist_types_dev device int8[Th], user-side
+ *                    types (REC_ATTN_GLOBAL, REC_ATTN_HIST, REC_ATTN_RT).
+ *   k_hist, v_hist   device [Th][H][d] in params->dtype, 16-byte aligned; read during
+ *                    the call's stream work only (the cache keeps its own copies).
+ *   max_cands        candidate slots per request (>= 1).
+ *   stream           cudaStream_t of the work; cache_out receives the cache.
+ * The cache owns one device buffer from the library pool: for each request
+ * hist_len + max_cands rows of Q', K', V and O, their times and types, and lse.
+ * Errors: INVALID_ARG (params, offsets, NULL or misaligned pointers), UNSUPPORTED
+ * (a request longer than REC_ATTN_MAX_REQUEST_LEN with its slots, 2^31 rows), OOM,
+ * CUDA.  On error *cache_out is NULL.
+ *
+ * rec_attn_cache_score -- score one micro-batch of candidates per request against
+ * the cached history.  Candidate c of request b gets the attention output over
+ * [history of b, c] under the mask predicate above (it sees the history rows the
+ * predicate allows and itself; CAND -> CAND is self only, so the other candidates of
+ * the micro-batch do not change it).
+ *   cand_offsets_host host int64[B+1]: candidates [offsets[b], offsets[b+1]) belong to
+ *                    request b, at most max_cands each; read during the call.
+ *   cand_t_dev       device int64[Nc] candidate times (type REC_ATTN_CAND).
+ *   q_cand, k_cand, v_cand device [Nc][H][d] in params->dtype, 16-byte aligned.
+ *   out              device [Nc][H][d], written in full (rows that see no key: 0);
+ *                    may not alias the inputs.  lse: optional device float[Nc][H].
+ * The candidates are rotated against the same per-request reference time as the
+ * cached history (its first row; the first candidate when the history is empty),
+ * written into the cache's slots (unused slots padded), and one target-attention
+ * pass runs over the cached rows.  Calls on one cache must not overlap on the GPU
+ * (they share the slots).  A small table is staged through the library pool on
+ * `stream`, and each call plans on the library's side stream as rec_attn_plan does.
+ * Errors: INVALID_ARG (NULL cache or pointers, misalignment, aliasing, more than
+ * max_cands candidates, another current device), OOM, CUDA.  Asynchronous.
+ *
+ * rec_attn_cache_free -- release a cache (NULL-safe).  Synchronizes the device
+ * (cudaFree), so work still reading the cache completes first.
+ */
+typedef struct rec_attn_kv_cache_s rec_attn_kv_cache_t; /* opaque */
+rec_attn_status rec_attn_cache_create(const rec_attn_params* params, int32_t batch,
+                                      const int64_t* hist_offsets_host, const int64_t* hist_t_dev,
+                                      const int8_t* hist_types_dev, const void* k_hist, const void* v_hist,
+                                      int32_t max_cands, void* stream, rec_attn_kv_cache_t** cache_out);
+rec_attn_status rec_attn_cache_score(rec_attn_kv_cache_t* cache, const int64_t* cand_offsets_host,
+                                     const int64_t* cand_t_dev, const void* q_cand, const void* k_cand,
+                                     const void* v_cand, void* out, float* lse, void* stream);
+void rec_attn_cache_free(rec_attn_kv_cache_t* cache);
+
+/*
  * rec_attn_applied_masks -- diagnostic copy of the visibility bits the attention
  * kernels apply, for named (query tile, key tile) pairs of a plan, so that a test can
  * hold them bit for bit against the mask predicate above (the pages' rule that masked
