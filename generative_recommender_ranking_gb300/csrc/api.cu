@@ -492,7 +492,7 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   const rec_attn_params& p = plan->p;
   const long long T = plan->T;
   const bool dim_ok = p.dtype == REC_ATTN_BF16 ? p.head_dim == 64 : (p.head_dim == 32 || p.head_dim == 64);
-  if (!dim_ok || plan->mask.keep_user >= 0) return REC_ATTN_ERR_UNSUPPORTED;
+  if (!dim_ok) return REC_ATTN_ERR_UNSUPPORTED;
   if (T > 0) {
     const void* ptrs[8] = {q, k, v, out, dout, dq, dk, dv};
     for (const void* x : ptrs)
@@ -552,6 +552,7 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   if (e != cudaSuccess) return from_cuda(e);
   BwdArgs a;
   a.meta = plan->pd.meta; a.batch = plan->batch; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
+  a.qkeep = plan->pd.qkeep;
   a.items = plan->pd.items; a.qreq = plan->pd.qreq; a.krec = plan->pd.krec;
   a.n_items = plan->NT * p.num_heads;
   a.status = plan->pd.status;

@@ -144,8 +144,10 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dq(BwdArgs a) {
     }
     ti = a.t[tok];
     tyi = a.ty[tok];
-    lse = a.lse[row];
-    dlt = a.delta[row];
+    if (query_kept(tyi, pi, a.qkeep[b])) {  // a pruned query has no output: no gradient
+      lse = a.lse[row];
+      dlt = a.delta[row];
+    }
   }
   const bool live = row_ok && lse != -INFINITY;
   bool thr_ok; long long thr;
@@ -244,8 +246,9 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dkv(BwdArgs a) {
       const long long qrow = (m.tok_start + pi) * H + h;
       sm.t[c] = ok ? a.t[m.tok_start + pi] : 0;
       sm.ty[c] = ok ? (int)a.ty[m.tok_start + pi] : -1;
-      sm.lse[c] = ok ? a.lse[qrow] : -INFINITY;
-      sm.dlt[c] = ok ? a.delta[qrow] : 0.f;
+      const bool kept = ok && query_kept(sm.ty[c], pi, a.qkeep[b]);  // pruned queries give no gradient
+      sm.lse[c] = kept ? a.lse[qrow] : -INFINITY;
+      sm.dlt[c] = kept ? a.delta[qrow] : 0.f;
     }
     __syncthreads();
     for (int c = 0; c < kTile; ++c) {

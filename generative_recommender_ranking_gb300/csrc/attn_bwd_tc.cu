@@ -718,14 +718,19 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
 __global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
   const long long g = blockIdx.x;
   const int h = blockIdx.y, H = a.heads;
-  const ReqMeta m = a.meta[a.qreq[g]];
+  const int b = a.qreq[g];
+  const ReqMeta m = a.meta[b];
   const int tile = (int)(g - m.tile_start);
   const int sub = threadIdx.x & 7;
   float2* out = a.rowc + ((long long)h * a.n_tiles + g) * kTile;
+  const int keep = a.qkeep[b];
 #pragma unroll 1
   for (int r = threadIdx.x >> 3; r < kTile; r += 32) {
     const int p = tile * kTile + r;
-    const bool ok = p < m.len;
+    const bool in = p < m.len;
+    // a pruned query (a query-pruned plan) has no output, so no gradient flows from it;
+    // its forward lse and O were never written
+    const bool ok = in && query_kept(a.ty[m.tok_start + p], p, keep);
     const long long row = (m.tok_start + p) * H + h;
     float acc = 0.f;
     if (ok) {
@@ -743,8 +748,10 @@ __global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     if (sub == 0) {
-      const float l = ok ? a.lse[row] : -INFINITY;
-      out[r] = make_float2(l == -INFINITY ? -INFINITY : l * kLog2e, acc);
+      // rows past the request end and rows that see no key: lse = -inf; pruned rows:
+      // +inf, so every P of the row is exp2(s - inf) = 0 whatever mask bits it has
+      const float l = ok ? a.lse[row] : (in ? INFINITY : -INFINITY);
+      out[r] = make_float2(ok && l == -INFINITY ? -INFINITY : l * kLog2e, acc);
     }
   }
 }

@@ -122,6 +122,7 @@ struct BwdArgs {
   const int* qslot;         // per query-tile list entry (qlist): mask-table slot, -1 if none
   const uint32_t* ctab;     // mask table, columns: [slot][128 keys][4 words over the queries]
   const int* kcount;       // per query tile: entries in its key-tile list
+  const int* qkeep;        // [B] query pruning: user tokens before this position compute nothing
   const uint32_t* klist;   // per query tile: non-SKIP key tiles (kt | class << 24)
   const uint8_t* cls;      // per request: ntiles x ntiles class matrix
   const long long* t;

@@ -235,8 +235,13 @@ rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const void* q, const v
  *   dout      device [T][H][d] in params->dtype: dLoss/dout.
  *   dq, dk, dv  device [T][H][d] in params->dtype, written in full; they may not
  *             alias any input or each other.  All tensors 16-byte aligned.
- * The plan must be the forward's (same offsets, times, types, params) and made by
- * rec_attn_plan (not query-pruned).  Supported: bf16 with head_dim 64, fp32 with
+ * The plan must be the forward's (same offsets, times, types, params).  On a
+ * query-pruned plan (rec_attn_plan_query_pruned) the gradients are those of the
+ * computed rows' outputs: pruned queries have no output, so their out and lse rows
+ * are never read, their dout rows are ignored (they must still be finite: they pass
+ * through the tensor cores with zero weights), their dq rows are zero and they add
+ * nothing to dk and dv.
+ * Supported: bf16 with head_dim 64, fp32 with
  * head_dim 32 or 64 (else UNSUPPORTED).  The first call takes workspace from the
  * library pool on `stream` (released with the plan): for bf16 the per-plan item
  * schedule (96 B per tile and head, 4 B per tile pair) and the rows' constants

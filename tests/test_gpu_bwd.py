@@ -84,17 +84,59 @@ def test_backward_parity(name):
                 assert np.all(x[s:e][m.sum(0) == 0] == 0.0)
 
 
-def test_backward_rejects_pruned_plans_and_bad_pointers():
-    w = CASES["cadet"]()
+PRUNED = {
+    "sort": (lambda: W.sort(batch=2, n_hist=400, n_cand=40, window=96), 130),
+    "mtgr": (lambda: W.mtgr(batch=3, hist=(150, 300), rt=(20, 60), cand=(10, 30)), 40),
+    "cadet_serving_ta": (lambda: W.cadet_serving(batch=2, n_hist=300, n_cand=50), 0),
+    "tiny_fp32": (lambda: W.tiny_fp32(batch=3, n_hist=200, n_cand=20), 70),
+}
+
+
+@pytest.mark.parametrize("name", list(PRUNED))
+def test_backward_query_pruned_plans(name):
+    """A pruned layer's loss reads only the computed rows, so its gradients are the full
+    backward's with dO zeroed at the pruned rows.  Here the pruned rows' out and lse
+    (left unwritten by the forward) hold NaN and their dout rows large finite garbage;
+    none of it may reach a gradient.  Pruned rows' dq is exactly zero."""
+    make, keep = PRUNED[name]
+    w = make()
     tens = gu.device_inputs(w)
-    plan = bd.rec_attn_plan_query_pruned(gu.params_for(w), 10, tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
-    x = torch.empty_like(tens["q"])
-    lse = torch.empty((w.total_tokens, w.num_heads), dtype=torch.float32, device=x.device)
+    plan = bd.rec_attn_plan_query_pruned(gu.params_for(w), keep, tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    rows = oracle.kept_rows(w.offsets, w.types, keep)
+    pruned = np.ones(w.total_tokens, dtype=bool)
+    pruned[rows] = False
+    assert pruned.any() and not pruned.all()
     try:
-        with pytest.raises(bd.RecAttnError):
-            bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], x, lse, x, *(torch.empty_like(x) for _ in range(3)))
+        out = torch.full_like(tens["q"], float("nan"))
+        lse = torch.full((w.total_tokens, w.num_heads), float("nan"), dtype=torch.float32, device=out.device)
+        bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out, lse)
+        g_host = _grad_inputs(w)
+        dout = gu.device_inputs(W.Workload(**{**w.__dict__, "q": g_host}))["q"]
+        dout[torch.from_numpy(pruned).cuda()] = 1e4
+        dq, dk, dv = (torch.full_like(tens["q"], float("nan")) for _ in range(3))
+        bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], out, lse, dout, dq, dk, dv)
+        torch.cuda.synchronize()
+        assert bd.rec_attn_device_status(plan) == bd.OK
     finally:
         bd.rec_attn_free(plan)
+    g_ref = g_host.copy()
+    g_ref[pruned] = 0
+    ref = oracle.attention_bwd(gu.oracle_params(w), w.offsets, w.t, w.types, w.q, w.k, w.v, g_ref)
+    rel_tol, max_tol = _tol(w)
+    for what, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        x = gu.to_f64(got)
+        assert np.isfinite(x).all(), f"{what}: unwritten or non-finite values"
+        rel = np.linalg.norm(x - r) / max(np.linalg.norm(r), 1e-30)
+        mx = np.max(np.abs(x - r))
+        assert rel <= rel_tol and mx <= max_tol * max(np.max(np.abs(r)), 1e-30), (name, what, rel, mx)
+    assert np.all(gu.to_f64(dq)[pruned] == 0.0)
+
+
+def test_backward_rejects_bad_pointers():
+    w = CASES["cadet"]()
+    tens = gu.device_inputs(w)
+    x = torch.empty_like(tens["q"])
+    lse = torch.empty((w.total_tokens, w.num_heads), dtype=torch.float32, device=x.device)
     plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
     try:
         dq = torch.empty_like(x)
