@@ -491,7 +491,8 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   if (!plan) return REC_ATTN_ERR_INVALID_ARG;
   const rec_attn_params& p = plan->p;
   const long long T = plan->T;
-  const bool dim_ok = p.dtype == REC_ATTN_BF16 ? p.head_dim == 64 : (p.head_dim == 32 || p.head_dim == 64);
+  const bool dim_ok = p.dtype == REC_ATTN_BF16 ? (p.head_dim == 64 || p.head_dim == 128)
+                                               : (p.head_dim == 32 || p.head_dim == 64);
   if (!dim_ok) return REC_ATTN_ERR_UNSUPPORTED;
   if (T > 0) {
     const void* ptrs[8] = {q, k, v, out, dout, dq, dk, dv};
@@ -594,7 +595,7 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   const long long cols = (long long)p.num_heads * p.head_dim;
   for (int i = 0; i < 4; ++i)
     if (!encode_map(&maps[i], srcs[i], T, cols)) return REC_ATTN_ERR_CUDA;
-  return from_cuda(launch_attn_bwd_tc(a, maps, plan->num_sms, st));
+  return from_cuda(launch_attn_bwd_tc(a, maps, p.head_dim, plan->num_sms, st));
 }
 
 namespace {

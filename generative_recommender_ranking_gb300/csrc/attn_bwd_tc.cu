@@ -1,5 +1,5 @@
 // attn_bwd_tc.cu -- backward pass of the masked time-RoPE attention on the sm_103a
-// tensor cores (bf16 inputs and gradients, fp32 accumulation, head_dim 64).
+// tensor cores (bf16 inputs and gradients, fp32 accumulation, head_dim 64 or 128).
 //
 // Gradients of O = Softmax(QK^T/sqrt(d) + M) V (TM20K review page, section 2.1;
 // LazFormer review page, Eq. 19-21) through the time-RoPE (CADET review page, time
@@ -9,8 +9,9 @@
 //   mode DKV:  dV_j = sum_i P_ij dO_i,  dK'_j = scale sum_i dS_ij Q'_i
 // and dQ = R(t_i)^T dQ', dK = R(t_j)^T dK' (the rotation is orthogonal).
 //
-// Both modes share one persistent kernel shape: two CTAs per SM (256 TMEM columns
-// each) and six warps -- warp 0 loads with TMA, one thread of warp 1 issues every MMA,
+// Both modes share one persistent kernel shape: at head_dim 64 two CTAs per SM (256
+// TMEM columns each), at 128 one (512 columns: the accumulators are twice as wide), and
+// six warps -- warp 0 loads with TMA, one thread of warp 1 issues every MMA,
 // warps 2..5 are the compute warpgroup (one TMEM lane, i.e. one tile row, per
 // thread).  The producer claims the planner's (tile, head) items from a global counter
 // and publishes each item's descriptor in shared memory for the other roles; mode DKV
@@ -25,8 +26,8 @@
 //        double-buffered, so the next step's S runs during this step's compute.
 //   DKV  S^T = K' Q'_h^T and dP^T = V dO_h^T; the compute warps write P^T and dS^T
 //        (bf16) over them; dV += P^T dO_h and dK += dS^T Q'_h.
-// TMEM columns:  DQ   S[0] 0..63 | S[1] 64..127 | dP 128..191 | dQ 192..255
-//                DKV  S^T 0..63 | dP^T 64..127 | dV 128..191 | dK 192..255
+// TMEM columns:  DQ   S[0] 0..63 | S[1] 64..127 | dP 128..191 | dQ 192..192+d
+//                DKV  S^T 0..63 | dP^T 64..127 | dV 128..128+d | dK 128+d..128+2d
 // The accumulators stay in TMEM across an item's tiles; the epilogue scales, undoes
 // the rotation and writes bf16 rows.  Everything a compute thread needs besides TMEM
 // comes through shared memory with the tiles: the planner's records of the item's tile
@@ -54,15 +55,23 @@ namespace recattn {
 
 namespace {
 
-constexpr int kD = 64;
 constexpr int kStep = 64;                   // keys (DQ) or queries (DKV) per MMA step
-constexpr int kTileBytes = kTile * kD * 2;  // one [128][64] bf16 tile, 128-byte swizzled
+constexpr int kSlab = kTile * 128;          // 128 rows x 64 bf16 columns, 128-byte swizzled
 constexpr int kNS = 2;                      // stages of the streamed ring
+// Per head dimension: a [128][D] bf16 tile is D / 64 slabs; TMEM columns of the
+// accumulators (DQ: S[0] 0..63 | S[1] 64..127 | dP 128..191 | dQ 192..; DKV: S^T 0..63 |
+// dP^T 64..127 | dV 128.. | dK 128 + D..); d = 64 runs two CTAs per SM, d = 128 one.
+template <int D>
+struct BCfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr uint32_t kCols = D == 64 ? 256 : 512;
+  static constexpr int kBlocksPerSM = D == 64 ? 2 : 1;
+  static constexpr uint32_t kDQ = 192, kDV = 128, kDK = 128 + D;
+};
 constexpr int kRecB = (int)sizeof(KeyTileRec);
 constexpr int kMaskB = kTile * 16;  // a PARTIAL pair's 128 rows (or columns) of the mask table
 constexpr int kStageRecB = kMaskB > kRecB ? kMaskB : kRecB;  // per streamed stage: one or the other
 constexpr int kThreadsB = 192;
-constexpr uint32_t kCols = 256;
 constexpr uint64_t kWaitNsB = 2000000000ull;  // 2 s
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -86,7 +95,9 @@ enum : int {
 
 // Byte offsets from the 1024-aligned base of dynamic shared memory.
 constexpr int kRowB = kTile * 8;  // {lse2, D} of a tile's rows
+template <int D>
 struct BL {
+  static constexpr int kTileBytes = BCfg<D>::kTileBytes;
   static constexpr int kRes = 0;                             // [2] resident tiles
   static constexpr int kStr = kRes + 2 * kTileBytes;         // [kNS][2] streamed tiles
   static constexpr int kSRec = kStr + 2 * kNS * kTileBytes;  // [kNS] records of the streamed tiles
@@ -99,11 +110,14 @@ struct BL {
   static constexpr int kTotal = kBarsOff + kNumBars * 8 + 16;  // + abort flag and TMEM slot
   static constexpr int kDynamic = kTotal + 1024;               // slack to align the base
 };
-static_assert(BL::kSRec % 16 == 0 && BL::kSRow % 16 == 0 && BL::kRRec % 16 == 0 && BL::kRRow % 16 == 0 &&
-                  BL::kCol % 16 == 0,
+static_assert(BL<64>::kSRec % 16 == 0 && BL<64>::kSRow % 16 == 0 && BL<64>::kRRec % 16 == 0 &&
+                  BL<64>::kRRow % 16 == 0 && BL<64>::kCol % 16 == 0 && BL<128>::kSRec % 16 == 0 &&
+                  BL<128>::kSRow % 16 == 0 && BL<128>::kRRec % 16 == 0 && BL<128>::kRRow % 16 == 0 &&
+                  BL<128>::kCol % 16 == 0,
               "bulk-copy alignment");
-static_assert(BL::kBarsOff % 8 == 0, "mbarrier alignment");
-static_assert(2 * (BL::kDynamic + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(BL<64>::kBarsOff % 8 == 0 && BL<128>::kBarsOff % 8 == 0, "mbarrier alignment");
+static_assert(2 * (BL<64>::kDynamic + 1024) <= 228 * 1024, "two CTAs per SM at d = 64");
+static_assert(BL<128>::kDynamic <= 227 * 1024, "one CTA per SM at d = 128");
 
 __device__ __forceinline__ bool bw_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status) {
   return bounded_wait(bar, parity, abort_flag, status, kWaitNsB);
@@ -143,6 +157,7 @@ __device__ __forceinline__ BwdItemDesc unpack_desc(const uint4 (&nx)[3]) {
 
 // Consumer side of the item slots: the next item's descriptor, or false at the end
 // (or after an abort).  warp_arrive: the compute warps arrive once per warp.
+template <int D>
 __device__ __forceinline__ bool next_item(uint8_t* sm, uint64_t* bars, uint32_t& it_cnt, bool warp_arrive,
                                           BwdItemDesc& d, volatile int* abort_flag, int* status) {
   const int slot = (int)(it_cnt & 1);
@@ -151,7 +166,7 @@ __device__ __forceinline__ bool next_item(uint8_t* sm, uint64_t* bars, uint32_t&
   const bool ok = warp_arrive ? bw_wait_warp(bars + kItemFull + slot, ph, abort_flag, status)
                               : bw_wait(bars + kItemFull + slot, ph, abort_flag, status);
   if (!ok) return false;
-  const ItemSlot* is = reinterpret_cast<const ItemSlot*>(sm + BL::kItems) + slot;
+  const ItemSlot* is = reinterpret_cast<const ItemSlot*>(sm + BL<D>::kItems) + slot;
   const uint4 nx[3] = {is->d[0], is->d[1], is->d[2]};
   const int end = is->end;
   if (warp_arrive) {
@@ -191,7 +206,7 @@ struct Cursor {
 //        (+ the key tile's record when the tile is PARTIAL).
 //   DKV: resident K', V + the key tile's record; streamed Q', dO + the query tile's
 //        record and row constants.
-template <bool DKV>
+template <int D, bool DKV>
 __device__ void bwd_producer(const BwdArgs& a, const void* const (&res)[2], const void* const (&str)[2],
                              uint8_t* sm, uint64_t* bars, volatile int* abort_flag) {
   const uint32_t* lists = DKV ? a.qlist : a.klist;
@@ -200,7 +215,9 @@ __device__ void bwd_producer(const BwdArgs& a, const void* const (&res)[2], cons
   uint32_t res_ph = 0, str_ph[kNS];
   for (int i = 0; i < kNS; ++i) { str_used[i] = false; str_ph[i] = 0; }
   const uint4* descs = reinterpret_cast<const uint4*>(a.desc + (DKV ? a.n_items : 0));
-  ItemSlot* slots = reinterpret_cast<ItemSlot*>(sm + BL::kItems);
+  using L = BL<D>;
+  constexpr int kTileBytes = L::kTileBytes;
+  ItemSlot* slots = reinterpret_cast<ItemSlot*>(sm + L::kItems);
   int* counter = a.counters + (DKV ? 5 : 3);
   for (;;) {
     const long long w = atomicAdd(counter, 1);
@@ -224,15 +241,18 @@ __device__ void bwd_producer(const BwdArgs& a, const void* const (&res)[2], cons
 
     if (!bw_wait(bars + kResEmpty, (it_n & 1) ^ 1, abort_flag, a.status)) goto drain;
     {
-      const int x = d.h * kD;
+      const int x = d.h * D;
       const long long g = (long long)d.tile_start + d.tile;
       const float2* rows_h = a.rowc + (long long)d.h * a.n_tiles * kTile;  // head h's row constants
       ptx::mbar_arrive_expect_tx(bars + kResFull, 2 * kTileBytes + kRecB + (DKV ? 0 : kRowB));
       const int y = (int)(d.tok_start + (long long)d.tile * kTile);
-      ptx::tma_load_2d(sm + BL::kRes, res[0], x, y, bars + kResFull);
-      ptx::tma_load_2d(sm + BL::kRes + kTileBytes, res[1], x, y, bars + kResFull);
-      ptx::bulk_load(sm + BL::kRRec, a.krec + g, kRecB, bars + kResFull);
-      if (!DKV) ptx::bulk_load(sm + BL::kRRow, rows_h + g * kTile, kRowB, bars + kResFull);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        ptx::tma_load_2d(sm + L::kRes + c * kSlab, res[0], x + 64 * c, y, bars + kResFull);
+        ptx::tma_load_2d(sm + L::kRes + kTileBytes + c * kSlab, res[1], x + 64 * c, y, bars + kResFull);
+      }
+      ptx::bulk_load(sm + L::kRRec, a.krec + g, kRecB, bars + kResFull);
+      if (!DKV) ptx::bulk_load(sm + L::kRRow, rows_h + g * kTile, kRowB, bars + kResFull);
       res_used = true;
       res_ph = it_n & 1;
       ++it_n;
@@ -252,14 +272,19 @@ __device__ void bwd_producer(const BwdArgs& a, const void* const (&res)[2], cons
         const int ys = (int)(d.tok_start + (long long)tile * kTile);
         ptx::mbar_arrive_expect_tx(bars + kStrFull + st,
                                    2 * kTileBytes + (tab ? kMaskB : rec ? kRecB : 0) + (DKV ? kRowB : 0));
-        ptx::tma_load_2d(sm + BL::kStr + (2 * st) * kTileBytes, str[0], x, ys, bars + kStrFull + st);
-        ptx::tma_load_2d(sm + BL::kStr + (2 * st + 1) * kTileBytes, str[1], x, ys, bars + kStrFull + st);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          ptx::tma_load_2d(sm + L::kStr + (2 * st) * kTileBytes + c * kSlab, str[0], x + 64 * c, ys,
+                           bars + kStrFull + st);
+          ptx::tma_load_2d(sm + L::kStr + (2 * st + 1) * kTileBytes + c * kSlab, str[1], x + 64 * c, ys,
+                           bars + kStrFull + st);
+        }
         if (tab)
-          ptx::bulk_load(sm + BL::kSRec + st * kStageRecB, (DKV ? a.ctab : a.mtab) + (long long)tslot * (kMaskB / 4),
+          ptx::bulk_load(sm + L::kSRec + st * kStageRecB, (DKV ? a.ctab : a.mtab) + (long long)tslot * (kMaskB / 4),
                          kMaskB, bars + kStrFull + st);
         else if (rec)
-          ptx::bulk_load(sm + BL::kSRec + st * kStageRecB, a.krec + gs, kRecB, bars + kStrFull + st);
-        if (DKV) ptx::bulk_load(sm + BL::kSRow + st * kRowB, rows_h + gs * kTile, kRowB, bars + kStrFull + st);
+          ptx::bulk_load(sm + L::kSRec + st * kStageRecB, a.krec + gs, kRecB, bars + kStrFull + st);
+        if (DKV) ptx::bulk_load(sm + L::kSRow + st * kRowB, rows_h + gs * kTile, kRowB, bars + kStrFull + st);
         str_used[st] = true;
         str_ph[st] = ph;
         ++s_it;
@@ -275,31 +300,41 @@ drain:
 
 // ------------------------------------------------------------------ MMA issuer
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) { return ptx::smem_desc_sw128(addr, 16, 1024); }
-__device__ __forceinline__ uint64_t mndesc(uint32_t addr) { return ptx::smem_desc_sw128(addr, kTileBytes, 1024); }
+// MN-major operand: 64-column blocks of N one slab apart
+__device__ __forceinline__ uint64_t mndesc(uint32_t addr) { return ptx::smem_desc_sw128(addr, kSlab, 1024); }
 
-// D = A B^T over K = 64 (both operands K-major, B = 64 rows of a tile): N = 64.
+// Scores over K = D (both operands K-major, the K steps of 16 columns four per slab;
+// B = 64 rows of a tile): N = 64.
+template <int D>
 __device__ __forceinline__ void mma_scores(uint32_t d, uint32_t a_addr, uint32_t b_addr) {
   constexpr uint32_t id = ptx::idesc_bf16_f32(kTile, kStep, false, false);
 #pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) ptx::umma_f16(d, kdesc(a_addr + kk * 32), kdesc(b_addr + kk * 32), id, kk > 0);
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kSlab + (kk & 3) * 32;
+    ptx::umma_f16(d, kdesc(a_addr + off), kdesc(b_addr + off), id, kk > 0);
+  }
 }
 // D (+)= A B with A (128 x 64, bf16) in TMEM and B = 64 rows of a tile as the K
-// dimension (MN-major: the tile's 64 columns are N).
+// dimension (MN-major: the tile's D columns are N).
+template <int D>
 __device__ __forceinline__ void mma_acc(uint32_t d, uint32_t a_tmem, uint32_t b_rows, bool accumulate) {
-  constexpr uint32_t id = ptx::idesc_bf16_f32(kTile, kD, false, true);
+  constexpr uint32_t id = ptx::idesc_bf16_f32(kTile, D, false, true);
 #pragma unroll
   for (int kk = 0; kk < kStep / 16; ++kk)
     ptx::umma_f16_ts(d, a_tmem + kk * 8, mndesc(b_rows + kk * 16 * 128), id, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-template <bool DKV>
+template <int D, bool DKV>
 __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t tmem, volatile int* abort_flag) {
-  const uint32_t res0 = ptx::smem_u32(sm + BL::kRes), res1 = res0 + kTileBytes;
-  const uint32_t str = ptx::smem_u32(sm + BL::kStr);
+  using L = BL<D>;
+  using C = BCfg<D>;
+  constexpr int kTileBytes = L::kTileBytes;
+  const uint32_t res0 = ptx::smem_u32(sm + L::kRes), res1 = res0 + kTileBytes;
+  const uint32_t str = ptx::smem_u32(sm + L::kStr);
   constexpr uint32_t kHalfBytes = kStep * 128;  // 64 rows of a tile
   uint32_t it_n = 0, s_it = 0, step = 0, it_cnt = 0;
   BwdItemDesc it;
-  while (next_item(sm, bars, it_cnt, false, it, abort_flag, a.status)) {
+  while (next_item<D>(sm, bars, it_cnt, false, it, abort_flag, a.status)) {
     if (it.n <= 0) continue;
     if (!bw_wait(bars + kResFull, it_n & 1, abort_flag, a.status)) goto out;
     ptx::tc_fence_after();
@@ -333,8 +368,8 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
           int st;
           if (!stage_of(ls, true, st)) return false;
           const uint32_t half = (uint32_t)(ls & 1) * kHalfBytes;
-          mma_scores(tmem + ((step0 + ls) & 1) * kStep, res0, str + (2 * st) * kTileBytes + half);
-          mma_scores(tmem + 128, res1, str + (2 * st + 1) * kTileBytes + half);
+          mma_scores<D>(tmem + ((step0 + ls) & 1) * kStep, res0, str + (2 * st) * kTileBytes + half);
+          mma_scores<D>(tmem + 128, res1, str + (2 * st + 1) * kTileBytes + half);
           ptx::umma_commit(bars + kSyFull);
           if (ls == nsteps - 1) ptx::umma_commit(bars + kResEmpty);  // Q' and dO read for the last time
           return true;
@@ -352,7 +387,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
           ptx::tc_fence_after();
           if (ls == 0 && !acc_free()) goto out;
           const uint32_t kb = str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes;
-          mma_acc(tmem + 192, tmem + ((step0 + ls) & 1) * kStep, kb, ls > 0);  // dQ += dS K'_h
+          mma_acc<D>(tmem + C::kDQ, tmem + ((step0 + ls) & 1) * kStep, kb, ls > 0);  // dQ += dS K'_h
           if (ls & 1) ptx::umma_commit(bars + kStrEmpty + st);
         }
       } else {
@@ -360,8 +395,8 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
         auto issue_scores = [&](int ls) -> bool {
           int st;
           if (!stage_of(ls, true, st)) return false;
-          mma_scores(tmem + 0, res0, str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes);
-          mma_scores(tmem + 64, res1, str + (2 * st + 1) * kTileBytes + (ls & 1) * kHalfBytes);
+          mma_scores<D>(tmem + 0, res0, str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes);
+          mma_scores<D>(tmem + 64, res1, str + (2 * st + 1) * kTileBytes + (ls & 1) * kHalfBytes);
           ptx::umma_commit(bars + kSyFull);
           if (ls == nsteps - 1) ptx::umma_commit(bars + kResEmpty);  // K' and V read for the last time
           return true;
@@ -375,8 +410,8 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
           if (ls == 0 && !acc_free()) goto out;
           const uint32_t qb = str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes;
           const uint32_t ob = str + (2 * st + 1) * kTileBytes + (ls & 1) * kHalfBytes;
-          mma_acc(tmem + 128, tmem + 0, ob, ls > 0);   // dV += P^T dO_h
-          mma_acc(tmem + 192, tmem + 64, qb, ls > 0);  // dK += dS^T Q'_h
+          mma_acc<D>(tmem + C::kDV, tmem + 0, ob, ls > 0);   // dV += P^T dO_h
+          mma_acc<D>(tmem + C::kDK, tmem + 64, qb, ls > 0);  // dK += dS^T Q'_h
           if (ls & 1) ptx::umma_commit(bars + kStrEmpty + st);
           if (ls + 1 < nsteps && !issue_scores(ls + 1)) goto out;
         }
@@ -401,6 +436,7 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 // One output row: x * scale, then (rotate) R(dt)^T over adjacent pairs, as bf16.  The
 // angles (at most a few tens of radians) take the hardware sine and cosine: their
 // error, about 1e-5 rad here, is far below the bf16 rounding of the result.
+// (64 columns of a row at dst; omega: their 32 rotation pairs)
 __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t (&acc)[64], float scale, bool rotate,
                                          float dt, const float* omega) {
   uint32_t w[32];
@@ -421,10 +457,11 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t (&a
   for (int c = 0; c < 8; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
+template <int D>
 __device__ __forceinline__ void zero_row(__nv_bfloat16* dst) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int c = 0; c < 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
+  for (int c = 0; c < D / 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
 }
 
 // A row's time and type from a tile record (type -1 past the request end).
@@ -437,8 +474,10 @@ __device__ __forceinline__ void rec_row(const KeyTileRec* rec, int row, long lon
 }
 
 // DQ: thread = query row of the item's tile.
+template <int D>
 __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t tmem,
                                volatile int* abort_flag) {
+  using BL = recattn::BL<D>;
   const int lane = threadIdx.x & 31, quad = (threadIdx.x >> 5) & 3, row = quad * 32 + lane;
   const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
   const float sl2 = a.scale * kLog2e;
@@ -448,13 +487,13 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
   const int H = a.heads;
   uint32_t it_n = 0, s_it = 0, step = 0, it_cnt = 0;
   BwdItemDesc it;
-  while (next_item(sm, bars, it_cnt, true, it, abort_flag, a.status)) {
+  while (next_item<D>(sm, bars, it_cnt, true, it, abort_flag, a.status)) {
     const int pi = it.tile * kTile + row;
     const bool row_ok = pi < it.len;
     const long long tok = it.tok_start + pi, grow = tok * H + it.h;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + grow * kD;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + grow * D;
     if (it.n <= 0) {  // no visible key tile
-      if (row_ok) zero_row(dst);
+      if (row_ok) zero_row<D>(dst);
       continue;
     }
     // the row's time, type and constants, loaded with Q'
@@ -531,12 +570,26 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
     if (!bw_wait_warp(bars + kAccFull, it_n & 1, abort_flag, a.status)) return;
     ++it_n;
     ptx::tc_fence_after();
-    uint32_t acc[64];
-    ptx::tmem_ld64(tl + 192, acc);
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
-    if (row_ok) store_row(dst, acc, a.scale, a.rotate != 0, (float)(ti - it.t_ref), a.omega);
+    if constexpr (D == 64) {
+      uint32_t acc[64];
+      ptx::tmem_ld64(tl + BCfg<D>::kDQ, acc);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
+      if (row_ok) store_row(dst, acc, a.scale, a.rotate != 0, (float)(ti - it.t_ref), a.omega);
+    } else {
+#pragma unroll 1
+      for (int hc = 0; hc < D / 64; ++hc) {
+        uint32_t acc[64];
+        ptx::tmem_ld64(tl + BCfg<D>::kDQ + 64 * hc, acc);
+        if (hc == D / 64 - 1) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
+        }
+        if (row_ok) store_row(dst + 64 * hc, acc, a.scale, a.rotate != 0, (float)(ti - it.t_ref), a.omega + 32 * hc);
+      }
+    }
   }
 }
 
@@ -562,8 +615,10 @@ __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& n, volatile 
 // DKV: thread = key row of the item's tile (and, while the masks are built, a row of
 // the query tile).  The column bits of the next query tile are built while the tensor
 // core runs the second half of the current one (two buffers of column bits).
+template <int D>
 __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t tmem,
                                 volatile int* abort_flag) {
+  using BL = recattn::BL<D>;
   const int lane = threadIdx.x & 31, quad = (threadIdx.x >> 5) & 3, row = quad * 32 + lane;
   const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
   const float sl2 = a.scale * kLog2e;
@@ -574,14 +629,14 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
   const int H = a.heads;
   uint32_t it_n = 0, s_it = 0, step = 0, grp = 0, cbuf = 0, it_cnt = 0;
   BwdItemDesc it;
-  while (next_item(sm, bars, it_cnt, true, it, abort_flag, a.status)) {
+  while (next_item<D>(sm, bars, it_cnt, true, it, abort_flag, a.status)) {
     const int pj = it.tile * kTile + row;
     const bool key_ok = pj < it.len;
     const long long growk = (it.tok_start + pj) * H + it.h;
-    __nv_bfloat16* dkr = static_cast<__nv_bfloat16*>(a.dk) + growk * kD;
-    __nv_bfloat16* dvr = static_cast<__nv_bfloat16*>(a.dv) + growk * kD;
+    __nv_bfloat16* dkr = static_cast<__nv_bfloat16*>(a.dk) + growk * D;
+    __nv_bfloat16* dvr = static_cast<__nv_bfloat16*>(a.dv) + growk * D;
     if (it.n <= 0) {  // no query sees this key tile
-      if (key_ok) { zero_row(dkr); zero_row(dvr); }
+      if (key_ok) { zero_row<D>(dkr); zero_row<D>(dvr); }
       continue;
     }
     if (!bw_wait_warp(bars + kResFull, it_n & 1, abort_flag, a.status)) return;  // the key tile's record
@@ -693,19 +748,25 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
     if (!bw_wait_warp(bars + kAccFull, it_n & 1, abort_flag, a.status)) return;
     ++it_n;
     ptx::tc_fence_after();
-    uint32_t acc[64], wv[32];
-    ptx::tmem_ld64(tl + 128, acc);  // dV, packed before dK is read
+    // 64 columns at a time: dV packed and stored, then dK scaled, rotated back and stored
+#pragma unroll 1
+    for (int hc = 0; hc < D / 64; ++hc) {
+      uint32_t acc[64], wv[32];
+      ptx::tmem_ld64(tl + BCfg<D>::kDV + 64 * hc, acc);  // dV, packed before dK is read
 #pragma unroll
-    for (int p = 0; p < 32; ++p) wv[p] = bf16x2(__uint_as_float(acc[2 * p]), __uint_as_float(acc[2 * p + 1]));
-    ptx::tmem_ld64(tl + 192, acc);
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
-    if (key_ok) {
-      uint4* d4 = reinterpret_cast<uint4*>(dvr);
+      for (int p = 0; p < 32; ++p) wv[p] = bf16x2(__uint_as_float(acc[2 * p]), __uint_as_float(acc[2 * p + 1]));
+      ptx::tmem_ld64(tl + BCfg<D>::kDK + 64 * hc, acc);
+      if (hc == D / 64 - 1) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
+      }
+      if (key_ok) {
+        uint4* d4 = reinterpret_cast<uint4*>(dvr + 64 * hc);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) d4[c] = make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
-      store_row(dkr, acc, a.scale, a.rotate != 0, (float)(tj - it.t_ref), a.omega);
+        for (int c = 0; c < 8; ++c) d4[c] = make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
+        store_row(dkr + 64 * hc, acc, a.scale, a.rotate != 0, (float)(tj - it.t_ref), a.omega + 32 * hc);
+      }
     }
   }
 }
@@ -715,17 +776,19 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
 // row (16 bytes of dO and O each, coalesced), written with lse * log2(e) as one float2
 // per row into the tile-padded table; rows past the request end and rows that see no
 // key get -inf.
+template <int D>
 __global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
+  constexpr int kLanes = D / 8;  // 16-byte chunks of a row, one per thread
   const long long g = blockIdx.x;
   const int h = blockIdx.y, H = a.heads;
   const int b = a.qreq[g];
   const ReqMeta m = a.meta[b];
   const int tile = (int)(g - m.tile_start);
-  const int sub = threadIdx.x & 7;
+  const int sub = threadIdx.x & (kLanes - 1);
   float2* out = a.rowc + ((long long)h * a.n_tiles + g) * kTile;
   const int keep = a.qkeep[b];
 #pragma unroll 1
-  for (int r = threadIdx.x >> 3; r < kTile; r += 32) {
+  for (int r = threadIdx.x / kLanes; r < kTile; r += 256 / kLanes) {
     const int p = tile * kTile + r;
     const bool in = p < m.len;
     // a pruned query (a query-pruned plan) has no output, so no gradient flows from it;
@@ -734,8 +797,8 @@ __global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
     const long long row = (m.tok_start + p) * H + h;
     float acc = 0.f;
     if (ok) {
-      const uint4 x = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + row * kD)[sub];
-      const uint4 y = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out) + row * kD)[sub];
+      const uint4 x = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + row * D)[sub];
+      const uint4 y = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out) + row * D)[sub];
       const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -744,9 +807,8 @@ __global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
         acc = fmaf(fx.x, fy.x, fmaf(fx.y, fy.y, acc));
       }
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (sub == 0) {
       // rows past the request end and rows that see no key: lse = -inf; pruned rows:
       // +inf, so every P of the row is exp2(s - inf) = 0 whatever mask bits it has
@@ -774,7 +836,8 @@ __global__ void __launch_bounds__(128) k_bwd_schedule(BwdSchedArgs s) {
       const int c = s.cls[pair];
       if (c == REC_ATTN_TILE_SKIP) continue;
       out[n] = (uint32_t)qt | ((uint32_t)c << 24);
-      out_slot[n] = c == REC_ATTN_TILE_PARTIAL ? s.pslot[pair] : -1;
+      const int p = c == REC_ATTN_TILE_PARTIAL ? s.pslot[pair] : -1;
+      out_slot[n] = (p >= 0 && p < s.mcap) ? p : -1;  // a slot always indexes the table
       ++n;
     }
     return;
@@ -822,12 +885,14 @@ __global__ void __launch_bounds__(kTile) k_bwd_colmask(BwdSchedArgs s) {
 
 // ------------------------------------------------------------------ kernel
 // maps: Q', K', V, dO, each a [T][H*64] bf16 view with 64 x 128 boxes.
-template <bool DKV>
-__global__ void __launch_bounds__(kThreadsB, 2)
+template <int D, bool DKV>
+__global__ void __launch_bounds__(kThreadsB, BCfg<D>::kBlocksPerSM)
     k_bwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using BL = recattn::BL<D>;
+  constexpr uint32_t kCols = BCfg<D>::kCols;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + BL::kBarsOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars) + 1;
@@ -867,13 +932,13 @@ __global__ void __launch_bounds__(kThreadsB, 2)
                                   DKV ? (const void*)&tm_v : (const void*)&tm_do};
       const void* const str[2] = {DKV ? (const void*)&tm_q : (const void*)&tm_k,
                                   DKV ? (const void*)&tm_do : (const void*)&tm_v};
-      bwd_producer<DKV>(a, res, str, sm, bars, abort_flag);
+      bwd_producer<D, DKV>(a, res, str, sm, bars, abort_flag);
     }
   } else if (warp == 1) {
-    if ((threadIdx.x & 31) == 0) bwd_mma<DKV>(a, sm, bars, tmem, abort_flag);
+    if ((threadIdx.x & 31) == 0) bwd_mma<D, DKV>(a, sm, bars, tmem, abort_flag);
   } else {
-    if constexpr (DKV) bwd_compute_dkv(a, sm, bars, tmem, abort_flag);
-    else bwd_compute_dq(a, sm, bars, tmem, abort_flag);
+    if constexpr (DKV) bwd_compute_dkv<D>(a, sm, bars, tmem, abort_flag);
+    else bwd_compute_dq<D>(a, sm, bars, tmem, abort_flag);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -892,12 +957,25 @@ __global__ void __launch_bounds__(kThreadsB, 2)
   }
 }
 
-template <bool DKV>
+template <int D, bool DKV>
 cudaError_t launch_mode(const CUtensorMap (&maps)[4], const BwdArgs& a, int grid, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(k_bwd_tc<DKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, BL::kDynamic);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_bwd_tc<D, DKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, BL<D>::kDynamic);
   if (e != cudaSuccess) return e;
-  k_bwd_tc<DKV><<<grid, kThreadsB, BL::kDynamic, st>>>(maps[0], maps[1], maps[2], maps[3], a);
+  k_bwd_tc<D, DKV><<<grid, kThreadsB, BL<D>::kDynamic, st>>>(maps[0], maps[1], maps[2], maps[3], a);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap (&maps)[4], int num_sms, cudaStream_t st) {
+  k_bwd_rowc<D><<<dim3((unsigned)a.n_tiles, (unsigned)a.heads), 256, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long cap = (long long)BCfg<D>::kBlocksPerSM * num_sms;
+  const int grid = (int)(a.n_items < cap ? a.n_items : cap);
+  e = launch_mode<D, false>(maps, a, grid, st);
+  if (e != cudaSuccess) return e;
+  return launch_mode<D, true>(maps, a, grid, st);
 }
 
 }  // namespace
@@ -912,16 +990,14 @@ cudaError_t launch_bwd_schedule(const BwdSchedArgs& s, int num_sms, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap (&maps)[4], int num_sms, cudaStream_t st) {
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap (&maps)[4], int head_dim, int num_sms,
+                               cudaStream_t st) {
   if (a.n_items <= 0) return cudaSuccess;
-  k_bwd_rowc<<<dim3((unsigned)a.n_tiles, (unsigned)a.heads), 256, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const long long cap = 2LL * num_sms;  // two CTAs per SM
-  const int grid = (int)(a.n_items < cap ? a.n_items : cap);
-  e = launch_mode<false>(maps, a, grid, st);
-  if (e != cudaSuccess) return e;
-  return launch_mode<true>(maps, a, grid, st);
+  switch (head_dim) {
+    case 64: return launch_bwd_d<64>(a, maps, num_sms, st);
+    case 128: return launch_bwd_d<128>(a, maps, num_sms, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace recattn

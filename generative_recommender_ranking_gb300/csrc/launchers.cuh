@@ -34,7 +34,8 @@ cudaError_t launch_attn_simt(const AttnArgs& a, int head_dim, cudaStream_t st);
 cudaError_t launch_bwd_delta(const BwdArgs& a, int dtype, int head_dim, cudaStream_t st);
 cudaError_t launch_attn_bwd_simt(const BwdArgs& a, int head_dim, long long n_tiles, cudaStream_t st);
 cudaError_t launch_bwd_schedule(const BwdSchedArgs& s, int num_sms, cudaStream_t st);
-cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap (&maps)[4], int num_sms, cudaStream_t st);
+cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap (&maps)[4], int head_dim, int num_sms,
+                               cudaStream_t st);
 cudaError_t launch_compress(const CompressArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_wait_timeout(int* status, unsigned long long limit_ns, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k,

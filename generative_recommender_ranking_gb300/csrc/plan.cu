@@ -329,6 +329,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(MaskP mp, int heads, Plan
         pd.qcost[g] = 0;
         pd.qreq[g] = b;
       }
+      // its PARTIAL pairs still appear in the backward's per-key-tile lists: no table slot
+      const long long rb = m.cls_start + (long long)qt * m.ntiles;
+      for (int kt = lane; kt < m.ntiles; kt += 32)
+        if (pd.cls[rb + kt] == REC_ATTN_TILE_PARTIAL) pd.pslot[rb + kt] = -1;
       continue;
     }
     const long long rb = m.cls_start + (long long)qt * m.ntiles;  // the query tile's row of pairs

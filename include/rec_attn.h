@@ -241,7 +241,7 @@ rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const void* q, const v
  * are never read, their dout rows are ignored (they must still be finite: they pass
  * through the tensor cores with zero weights), their dq rows are zero and they add
  * nothing to dk and dv.
- * Supported: bf16 with head_dim 64, fp32 with
+ * Supported: bf16 with head_dim 64 or 128, fp32 with
  * head_dim 32 or 64 (else UNSUPPORTED).  The first call takes workspace from the
  * library pool on `stream` (released with the plan): for bf16 the per-plan item
  * schedule (96 B per tile and head, 4 B per tile pair) and the rows' constants

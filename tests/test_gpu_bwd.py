@@ -35,6 +35,11 @@ CASES = {
     "sort_full_len": lambda: W.sort(batch=4),
     "mtgr_many": lambda: W.mtgr(batch=16),
     "tm20k_window_6k": lambda: W.tm20k("window", batch=1, n_hist=6000),
+    # head_dim 128 (one CTA per SM, accumulators twice as wide)
+    "cadet_d128": lambda: W.cadet(batch=3, n_pairs=150, heads=2, head_dim=128),
+    "sort_d128": lambda: W.sort(batch=2, n_hist=300, n_cand=40, window=100, heads=2, head_dim=128),
+    "mtgr_d128": lambda: W.mtgr(batch=3, hist=(150, 300), rt=(20, 60), cand=(10, 30), heads=2, head_dim=128),
+    "cadet_d128_many": lambda: W.cadet(batch=96, n_pairs=150, heads=2, head_dim=128),
 }
 
 
@@ -89,6 +94,7 @@ PRUNED = {
     "mtgr": (lambda: W.mtgr(batch=3, hist=(150, 300), rt=(20, 60), cand=(10, 30)), 40),
     "cadet_serving_ta": (lambda: W.cadet_serving(batch=2, n_hist=300, n_cand=50), 0),
     "tiny_fp32": (lambda: W.tiny_fp32(batch=3, n_hist=200, n_cand=20), 70),
+    "sort_d128": (lambda: W.sort(batch=2, n_hist=300, n_cand=40, window=100, heads=2, head_dim=128), 90),
 }
 
 
