@@ -257,6 +257,22 @@ def rec_attn_compress(offsets_host, hist_begin, hist_len, segments, x, timestamp
     _check("rec_attn_compress", code)
 
 
+def rec_attn_fwd_compress(plan: Plan, q, k, v, hist_begin, hist_len, segments, x_out, t_out, ty_out,
+                          stream=None) -> None:
+    """Attention forward whose output is written already history-compressed
+    (segments = [(length or -1, group), ...] from the most recent; groups <= 32)."""
+    L = lib()
+    vp = ctypes.c_void_p
+    L.rec_attn_fwd_compress.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp]
+    L.rec_attn_fwd_compress.restype = ctypes.c_int
+    hb = np.ascontiguousarray(np.asarray(hist_begin, dtype=np.int64))
+    hl = np.ascontiguousarray(np.asarray(hist_len, dtype=np.int64))
+    sl, sg = _segments(segments)
+    _check("rec_attn_fwd_compress", L.rec_attn_fwd_compress(
+        plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(hb), _ptr(hl), len(sl), _ptr(sl), _ptr(sg), _ptr(x_out),
+        _ptr(t_out), _ptr(ty_out), _stream(stream)))
+
+
 def rec_attn_check_wait_timeout(limit_ms: int = 50, stream=None) -> int:
     """Run the kernels' bounded wait on a barrier nothing arrives at; returns the
     status word it wrote (ERR_TIMEOUT when the failure detection works)."""

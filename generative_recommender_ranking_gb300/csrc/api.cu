@@ -33,6 +33,7 @@ struct rec_attn_plan_s {
   size_t ws_bytes = 0;
   PlanDev pd{};
   std::vector<int> req_tiles;  // host copy: tiles of each request (argument checks)
+  std::vector<int64_t> offsets_host;  // host copy of the request offsets [B+1]
   void* qrot = nullptr;
   void* krot = nullptr;
   void* qk_extra = nullptr;  // Q'/K' buffers of a plan without the RoPE, made on the first fused call
@@ -229,6 +230,7 @@ rec_attn_status plan_impl(const rec_attn_params* params, int32_t keep_user_queri
   plan->T = T; plan->NT = NT; plan->NC = NC;
   try {
     plan->req_tiles.resize((size_t)batch);
+    plan->offsets_host.assign(offsets_host ? offsets_host : nullptr, offsets_host ? offsets_host + batch + 1 : nullptr);
   } catch (...) {
     delete plan;
     return REC_ATTN_ERR_OOM;
@@ -343,12 +345,20 @@ REC_ATTN_API int64_t rec_attn_query_keep(int64_t hist_len, int64_t n_min, int32_
 namespace {
 
 // The forward of rec_attn_fwd and rec_attn_fwd_fused (f == nullptr: no fused step).
+// cmp: the history compression epilogue (the output goes to cmp->x_out, checked by the
+// caller; out and lse are then unused).
 rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
-                         const rec_attn_fused* f, void* out, float* lse, void* stream) {
+                         const rec_attn_fused* f, void* out, float* lse, void* stream,
+                         const CmpArgs* cmp = nullptr) {
   if (!plan) return REC_ATTN_ERR_INVALID_ARG;
   const rec_attn_params& p = plan->p;
   const long long T = plan->T;
-  if (T > 0) {
+  if (T > 0 && cmp) {
+    if (!q || !k || !v) return REC_ATTN_ERR_INVALID_ARG;
+    const void* ptrs[3] = {q, k, v};
+    for (const void* x : ptrs)
+      if (reinterpret_cast<uintptr_t>(x) & 15u) return REC_ATTN_ERR_INVALID_ARG;
+  } else if (T > 0) {
     if (!q || !k || !v || !out) return REC_ATTN_ERR_INVALID_ARG;
     const void* ptrs[4] = {q, k, v, out};
     for (const void* x : ptrs)
@@ -445,7 +455,7 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
     e = cudaEventRecord(plan->ev[2], st);
     if (e != cudaSuccess) return from_cuda(e);
   }
-  AttnArgs a;
+  AttnArgs a{};
   a.meta = plan->pd.meta; a.qreq = plan->pd.qreq; a.kcount = plan->pd.kcount; a.klist = plan->pd.klist;
   a.items = plan->pd.items; a.t = plan->t; a.ty = plan->ty;
   a.counters = plan->pd.counters; a.krec = plan->pd.krec; a.qkeep = plan->pd.qkeep;
@@ -453,6 +463,7 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
   a.q = qs; a.k = ks; a.v = v; a.out = out; a.lse = lse; a.status = plan->pd.status;
   a.out_gate = f ? f->out_gate : nullptr;
   a.n_items = plan->NT * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale; a.mask = plan->mask;
+  if (cmp) a.cmp = *cmp;
   if (p.dtype == REC_ATTN_FP32) {
     e = launch_attn_simt(a, p.head_dim, st);
     return finish_timing(plan, st, e);
@@ -697,6 +708,96 @@ REC_ATTN_API rec_attn_status rec_attn_compress(int32_t batch, const int64_t* off
   if (e == cudaSuccess) e = launch_compress(a, dtype, st);
   cudaError_t e2 = cudaFreeAsync(dreq, st);
   return from_cuda(e != cudaSuccess ? e : e2);
+}
+
+REC_ATTN_API rec_attn_status rec_attn_fwd_compress(rec_attn_plan_t* plan, const void* q, const void* k,
+                                                   const void* v, const int64_t* hist_begin_host,
+                                                   const int64_t* hist_len_host, int32_t n_segments,
+                                                   const int64_t* seg_len, const int32_t* seg_group, void* x_out,
+                                                   int64_t* timestamps_out, int8_t* types_out, void* stream) {
+  if (!plan) return REC_ATTN_ERR_INVALID_ARG;
+  const rec_attn_params& p = plan->p;
+  if (p.dtype != REC_ATTN_BF16 || plan->mask.keep_user >= 0) return REC_ATTN_ERR_UNSUPPORTED;
+  const int32_t B = plan->batch;
+  std::vector<CompressReq> reqs;
+  reqs.reserve((size_t)B);
+  rec_attn_status s = compress_layout(B, plan->offsets_host.data(), hist_begin_host, hist_len_host, n_segments,
+                                      seg_len, seg_group, &reqs, nullptr);
+  if (s != REC_ATTN_OK) return s;
+  for (int i = 0; i < n_segments; ++i)
+    if (seg_group[i] > 32) return REC_ATTN_ERR_UNSUPPORTED;  // a group spans at most two 32-row blocks
+  const long long T = plan->T;
+  const long long rows_out = reqs.empty() ? 0 : reqs.back().out_start + reqs.back().out_len;
+  if (rows_out == 0) return REC_ATTN_OK;
+  if (!x_out || !timestamps_out || !types_out || (reinterpret_cast<uintptr_t>(x_out) & 15u) ||
+      (reinterpret_cast<uintptr_t>(timestamps_out) & 7u))
+    return REC_ATTN_ERR_INVALID_ARG;
+  const size_t row_bytes = (size_t)p.num_heads * p.head_dim * 2;
+  if (overlaps(x_out, rows_out * row_bytes, q, T * row_bytes) || overlaps(x_out, rows_out * row_bytes, k, T * row_bytes) ||
+      overlaps(x_out, rows_out * row_bytes, v, T * row_bytes))
+    return REC_ATTN_ERR_INVALID_ARG;
+  // per request: where its rows go and its first 32-row block boundary in the fix-up buffer
+  std::vector<CmpReq> creq((size_t)B);
+  std::vector<int> lens((size_t)B);
+  long long n_fix = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const CompressReq& r = reqs[b];
+    CmpReq& c = creq[b];
+    c.out_start = r.out_start;
+    c.fix_start = n_fix;
+    c.hist_begin = (int)r.hist_begin;
+    c.hist_len = (int)r.hist_len;
+    c.n_groups = (int)(r.out_len - (r.len - r.hist_len));
+    c.pad = 0;
+    lens[b] = (int)r.len;
+    n_fix += (r.len + 31) / 32;
+  }
+  const size_t off_len = ws_up(sizeof(CmpReq) * (size_t)B);
+  const size_t off_creq = off_len + ws_up(4 * (size_t)B);
+  const size_t off_fix = off_creq + ws_up(sizeof(CompressReq) * (size_t)B);
+  const size_t fix_bytes = (size_t)n_fix * 2 * p.num_heads * p.head_dim * sizeof(float);
+  std::vector<char> up(off_fix, 0);
+  std::memcpy(up.data(), creq.data(), sizeof(CmpReq) * (size_t)B);
+  std::memcpy(up.data() + off_len, lens.data(), 4 * (size_t)B);
+  std::memcpy(up.data() + off_creq, reqs.data(), sizeof(CompressReq) * (size_t)B);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (dev != plan->device) return REC_ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaMemPool_t pool;
+  char* buf = nullptr;
+  e = pool_for(plan->device, &pool);
+  if (e == cudaSuccess) e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), off_fix + fix_bytes, pool, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = cudaMemcpyAsync(buf, up.data(), up.size(), cudaMemcpyHostToDevice, st);  // staged before the call returns
+  CmpArgs c{};
+  c.req = reinterpret_cast<const CmpReq*>(buf);
+  c.x_out = x_out;
+  c.fix = reinterpret_cast<float*>(buf + off_fix);
+  c.n_seg = n_segments;
+  c.span = 1;
+  for (int i = 0; i < kMaxSegments; ++i) {
+    c.seg_len[i] = i < n_segments ? seg_len[i] : 0;
+    c.seg_group[i] = i < n_segments ? seg_group[i] : 1;
+    if (i < n_segments) c.span = std::max(c.span, (int)seg_group[i]);
+  }
+  if (e == cudaSuccess) s = fwd_impl(plan, q, k, v, nullptr, x_out, nullptr, stream, &c);
+  if (e == cudaSuccess && s == REC_ATTN_OK)
+    e = launch_cmp_fixup(c, B, reinterpret_cast<const int*>(buf + off_len), n_fix, p.num_heads, p.head_dim, st);
+  if (e == cudaSuccess && s == REC_ATTN_OK) {
+    // times and types of the output rows (the latest member time, type HIST for merged rows)
+    CompressArgs ca;
+    ca.req = reinterpret_cast<const CompressReq*>(buf + off_creq);
+    ca.batch = B; ca.n_seg = n_segments; ca.rows_out = rows_out;
+    for (int i = 0; i < kMaxSegments; ++i) { ca.seg_len[i] = c.seg_len[i]; ca.seg_group[i] = c.seg_group[i]; }
+    ca.width = 0; ca.x = nullptr; ca.t = plan->t; ca.ty = plan->ty;
+    ca.x_out = nullptr; ca.t_out = reinterpret_cast<long long*>(timestamps_out); ca.ty_out = types_out;
+    e = launch_compress(ca, p.dtype, st);
+  }
+  const cudaError_t ef = cudaFreeAsync(buf, st);
+  if (s != REC_ATTN_OK) return s;
+  return from_cuda(e != cudaSuccess ? e : ef);
 }
 
 REC_ATTN_API rec_attn_status rec_attn_check_wait_timeout(uint32_t limit_ms, int32_t* status_out, void* stream) {

@@ -5,6 +5,57 @@
 
 namespace recattn {
 
+// History compression fused into the attention epilogue: per request, where its rows
+// go (rows before the history copied, history rows summed in groups, rows after it
+// copied) and where its 32-row blocks keep the partial sums of groups that straddle
+// two blocks.
+struct CmpReq {
+  long long out_start;  // first output row of the request
+  long long fix_start;  // first 32-row block boundary of the request in the fix-up buffer
+  int hist_begin, hist_len, n_groups, pad;
+};
+struct CmpArgs {
+  const CmpReq* req;    // [B]
+  void* x_out;          // [rows_out][H][d]
+  float* fix;           // [boundaries][2 parts][H][d] fp32
+  int n_seg;
+  int span;             // largest group (<= 32)
+  long long seg_len[kMaxSegments];  // recency segments from the newest (< 0: the rest)
+  int seg_group[kMaxSegments];
+};
+
+// Output row (global) of request-local row pi and the request-local rows [glo, ghi) of
+// its group: the inverse of the compression's grouping (recency segments counted from
+// the newest row, the oldest group of a segment partial, groups in time order).
+__host__ __device__ __forceinline__ long long cmp_group_of(const CmpArgs& c, const CmpReq& r, int pi, int& glo, int& ghi) {
+  if (pi < r.hist_begin) { glo = pi; ghi = pi + 1; return r.out_start + pi; }
+  if (pi >= r.hist_begin + r.hist_len) {
+    glo = pi; ghi = pi + 1;
+    return r.out_start + pi - r.hist_len + r.n_groups;
+  }
+  const long long Lh = r.hist_len;
+  const long long rank_i = Lh - 1 - (pi - r.hist_begin);  // 0: the newest history row
+  long long rank = 0, newer_groups = 0;
+  for (int u = 0; u < c.n_seg && rank < Lh; ++u) {
+    const long long room = Lh - rank;
+    const long long m = (c.seg_len[u] < 0 || c.seg_len[u] > room) ? room : c.seg_len[u];
+    const long long g = c.seg_group[u];
+    if (rank_i < rank + m) {
+      const long long q = (rank_i - rank) / g;  // 0: the segment's newest group
+      const long long r0 = rank + q * g;
+      const long long r1 = rank + ((q + 1) * g < m ? (q + 1) * g : m);
+      glo = (int)(r.hist_begin + Lh - r1);
+      ghi = (int)(r.hist_begin + Lh - r0);
+      const long long from_newest = newer_groups + q;  // groups between it and the newest row
+      return r.out_start + r.hist_begin + (r.n_groups - 1 - from_newest);
+    }
+    newer_groups += (m + g - 1) / g;
+    rank += m;
+  }
+  glo = pi; ghi = pi + 1;  // unreachable: the segments cover the history
+  return r.out_start + pi;
+}
+
 struct AttnArgs {
   const ReqMeta* meta;
   const int* qreq;
@@ -29,6 +80,7 @@ struct AttnArgs {
   int heads;
   float scale;       // softmax scale (natural-log domain)
   MaskP mask;
+  CmpArgs cmp;       // compression epilogue (kernels instantiated with it only)
 };
 
 // Arguments of the time-RoPE prologue.
@@ -190,6 +242,7 @@ struct WorkItem {
   int h;
   int n;             // non-SKIP key tiles; -1: every row of the tile is pruned
   int keep;          // first kept user position of the request (query pruning)
+  int b;             // request
   const uint32_t* list;
   const int* slots;  // mask-table slots of the list's entries
 };
@@ -204,6 +257,7 @@ __device__ __forceinline__ WorkItem decode_item(const AttnArgs& a, long long w, 
   it.qt = (int)(qg - it.m.tile_start);
   it.n = a.kcount[qg];
   it.keep = a.qkeep[b];
+  it.b = b;
   it.list = a.klist + it.m.cls_start + (long long)it.qt * it.m.ntiles;
   it.slots = a.kslot + it.m.cls_start + (long long)it.qt * it.m.ntiles;
   return it;

@@ -98,7 +98,7 @@ struct ItemDesc {
   int rows;        // valid rows in the tile
   int h;
   int n;           // non-SKIP key tiles; -1: every query of the tile is pruned
-  int end;         // 1: the stream is done
+  int req;         // the item's request; -1: the stream is done
   int keep;        // first kept user position of the request (query pruning)
 };
 static_assert(sizeof(ItemDesc) == 32, "");
@@ -217,7 +217,7 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
     ++it_cnt;
     ItemDesc* d = items + slot;
     if (w >= a.n_items) {
-      d->end = 1;
+      d->req = -1;
       ptx::mbar_arrive(B.item_full + slot);
       break;
     }
@@ -228,7 +228,7 @@ __device__ void run_producer(const AttnArgs& a, const void* tq, const void* tk, 
     d->h = it.h;
     d->n = it.n;
     d->keep = it.keep;
-    d->end = 0;
+    d->req = it.b;
     ptx::mbar_arrive(B.item_full + slot);
     if (it.n <= 0) continue;
     const int qb = (int)(q_it % QB);
@@ -312,7 +312,8 @@ __device__ void run_mma(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, u
     const int slot = (int)(it_cnt & 1);
     if (!wait_bar(B.item_full + slot, (it_cnt >> 1) & 1, abort_flag, a.status)) break;
     ++it_cnt;
-    const int end = items[slot].end, n = items[slot].n;
+    const bool end = items[slot].req < 0;
+    const int n = items[slot].n;
     ptx::mbar_arrive(B.item_empty + slot);
     if (end) break;
     if (n <= 0) continue;
@@ -490,9 +491,58 @@ __device__ __forceinline__ void rescale_o(uint32_t tm_o, float corr) {
   }
 }
 
+// Compression epilogue: 64 output columns (block cb) of this row's O go to its group's
+// output row.  The rows of a 32-row warp block that share a group are summed across
+// lanes (segmented by the group's last lane); a group inside the block is written
+// once, in bf16, by its first lane; a group that straddles a block boundary (groups
+// are at most 32 rows) leaves the block's fp32 partial in the fix-up buffer, part 0
+// from the lower block and part 1 from the upper, summed by k_cmp_fixup.
+template <int D>
+__device__ __forceinline__ void cmp_store(const AttnArgs& a, const CmpReq& cr, int h, int pi, bool row_ok,
+                                          int lane, float (&v)[64], int cb) {
+  const CmpArgs& c = a.cmp;
+  int glo = pi, ghi = pi + 1;
+  long long orow = -1;
+  if (row_ok) orow = cmp_group_of(c, cr, pi, glo, ghi);
+  const unsigned long long key = row_ok ? (unsigned long long)orow : ~0ull - (unsigned long long)lane;
+  const unsigned same = __match_any_sync(0xffffffffu, key);
+  const int last = 31 - __clz(same), first = __ffs(same) - 1;
+  for (int off = 1; off < c.span; off <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+      const float u = __shfl_down_sync(0xffffffffu, v[e], off);
+      if (lane + off <= last) v[e] += u;
+    }
+  }
+  if (!row_ok || lane != first) return;
+  const int H = a.heads;
+  const int r0 = pi - lane;  // the warp block's first request-local row (a multiple of 32)
+  if (glo >= r0 && ghi <= r0 + 32) {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(c.x_out) + (orow * H + h) * D + cb * 64;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t wv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 pb = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+        wv[e] = *reinterpret_cast<const uint32_t*>(&pb);
+      }
+      reinterpret_cast<uint4*>(dst)[q] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+  } else {
+    const bool upper = glo < r0;  // this block holds the group's later rows
+    const long long k = cr.fix_start + (upper ? r0 : r0 + 32) / 32;
+    float* dst = c.fix + ((k * 2 + (upper ? 1 : 0)) * H + h) * D + cb * 64;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
+
 // GATE: the attention output gate is applied in the epilogue (a separate
-// instantiation, so the plain epilogue carries none of its code).
-template <int D, bool GATE>
+// instantiation, so the plain epilogue carries none of its code).  CMP: the output is
+// the history compression of O (cmp_store) instead of O.
+template <int D, bool GATE, bool CMP>
 __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, uint32_t tmem,
                             volatile int* abort_flag) {
   using L = Layout<D>;
@@ -516,13 +566,22 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
     ++it_cnt;
     const ItemDesc d = items[slot];
     ptx::mbar_arrive(B.item_empty + slot);
-    if (d.end) return;
+    if (d.req < 0) return;
     const bool row_ok = row < d.rows;
     const int pi = d.pos0 + row;
     const long long tok = d.tok0 + row;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (tok * H + d.h) * D;
     if (d.n <= 0) {  // no visible key tile: zero rows; -1: a tile of pruned queries
-      if (d.n == 0 && row_ok && query_kept(a.ty[tok], pi, d.keep)) {
+      if constexpr (CMP) {  // every row is computed (no pruning): zeros into the groups
+        const CmpReq cr = a.cmp.req[d.req];
+#pragma unroll 1
+        for (int cb = 0; cb < D / 64; ++cb) {
+          float v[64];
+#pragma unroll
+          for (int e = 0; e < 64; ++e) v[e] = 0.f;
+          cmp_store<D>(a, cr, d.h, pi, row_ok, lane, v, cb);
+        }
+      } else if (d.n == 0 && row_ok && query_kept(a.ty[tok], pi, d.keep)) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
@@ -661,7 +720,12 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
     for (int half = 0; half < D / 64; ++half) {
       uint32_t o[64];
       ptx::tmem_ld64(tm.o + half * 64, o);
-      if (out_ok) {
+      if constexpr (CMP) {
+        float v[64];
+#pragma unroll
+        for (int e = 0; e < 64; ++e) v[e] = __uint_as_float(o[e]) * inv;
+        cmp_store<D>(a, a.cmp.req[d.req], d.h, pi, row_ok, lane, v, half);
+      } else if (out_ok) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           float sc[8];
@@ -690,7 +754,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
         }
       }
     }
-    if (out_ok && a.lse) {
+    if (!CMP && out_ok && a.lse) {
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       a.lse[tok * H + d.h] = l > 0.f ? (m_use + __log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
@@ -698,7 +762,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
   }
 }
 
-template <int D, bool GATE>
+template <int D, bool GATE, bool CMP>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -762,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = (warp - kRoleWarps) >> 2;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
-    run_softmax<D, GATE>(a, sm, s, B, tmem, abort_flag);
+    run_softmax<D, GATE, CMP>(a, sm, s, B, tmem, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -781,22 +845,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool GATE>
+template <int D, bool GATE, bool CMP>
 cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                      int grid, cudaStream_t st) {
   using L = Layout<D>;
   static_assert(L::kDynamic <= 227 * 1024, "shared memory budget");
   cudaError_t e =
-      cudaFuncSetAttribute(k_attn_tc<D, GATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
+      cudaFuncSetAttribute(k_attn_tc<D, GATE, CMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
   if (e != cudaSuccess) return e;
-  k_attn_tc<D, GATE><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
+  k_attn_tc<D, GATE, CMP><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, int grid,
                    cudaStream_t st) {
-  return a.out_gate ? launch_t<D, true>(a, q, k, v, grid, st) : launch_t<D, false>(a, q, k, v, grid, st);
+  if (a.cmp.req) return launch_t<D, false, true>(a, q, k, v, grid, st);
+  return a.out_gate ? launch_t<D, true, false>(a, q, k, v, grid, st) : launch_t<D, false, false>(a, q, k, v, grid, st);
 }
 
 }  // namespace

@@ -15,6 +15,7 @@
 // written once.
 #include <cuda_bf16.h>
 
+#include "attn_common.cuh"
 #include "launchers.cuh"
 #include "rec_attn_internal.cuh"
 
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a) {
   const int vecs = (int)(row_bytes / 16);
   const char* x = static_cast<const char*>(a.x);
   char* y = static_cast<char*>(a.x_out);
-  for (int c = lane; c < vecs; c += 32) {
+  for (int c = lane; a.x && c < vecs; c += 32) {  // (no rows: times and types only)
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (long long s = src_lo; s < src_hi; ++s) V::add(x + s * row_bytes + c * 16, acc);
     V::store(y + row * row_bytes + c * 16, acc);
@@ -135,7 +136,41 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a) {
   }
 }
 
+// The history groups of the fused compression epilogue that straddle a 32-row block
+// boundary: one block per boundary (request-local rows 32k - 1 and 32k); when one group
+// holds both rows, its two fp32 partials are summed and rounded once.
+__global__ void __launch_bounds__(256) k_cmp_fixup(CmpArgs c, int batch, const int* req_len, long long n_fix,
+                                                   int heads, int head_dim) {
+  const long long f = blockIdx.x;
+  if (f >= n_fix) return;
+  int lo_b = 0, hi_b = batch;
+  while (hi_b - lo_b > 1) {
+    const int mid = (lo_b + hi_b) >> 1;
+    if (c.req[mid].fix_start <= f) lo_b = mid;
+    else hi_b = mid;
+  }
+  const CmpReq r = c.req[lo_b];
+  const long long k = f - r.fix_start;
+  const long long R = 32 * k;
+  if (k < 1 || R >= req_len[lo_b]) return;
+  int glo, ghi;
+  const long long orow = cmp_group_of(c, r, (int)(R - 1), glo, ghi);
+  if (ghi <= R) return;  // no group crosses this boundary
+  const int n = heads * head_dim;
+  const float* p0 = c.fix + (f * 2) * n;
+  const float* p1 = p0 + n;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(c.x_out) + orow * n;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = __float2bfloat16_rn(p0[i] + p1[i]);
+}
+
 }  // namespace
+
+cudaError_t launch_cmp_fixup(const CmpArgs& c, int batch, const int* req_len, long long n_fix, int heads,
+                             int head_dim, cudaStream_t st) {
+  if (n_fix <= 0) return cudaSuccess;
+  k_cmp_fixup<<<(unsigned)n_fix, 256, 0, st>>>(c, batch, req_len, n_fix, heads, head_dim);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_compress(const CompressArgs& a, int dtype, cudaStream_t st) {
   if (a.rows_out <= 0) return cudaSuccess;

@@ -224,7 +224,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
     qs = w + lay.rq;
     ks = w + lay.rk;
   }
-  AttnArgs a;
+  AttnArgs a{};
   a.meta = pd.meta; a.qreq = pd.qreq; a.kcount = pd.kcount; a.klist = pd.klist; a.items = pd.items;
   a.counters = pd.counters; a.krec = pd.krec; a.qkeep = pd.qkeep;
   a.kslot = pd.kslot; a.mtab = pd.mtab;

@@ -290,6 +290,33 @@ rec_attn_status rec_attn_compress(int32_t batch, const int64_t* offsets_host,
                                   int8_t* types_out, void* stream);
 
 /*
+ * rec_attn_fwd_compress -- rec_attn_fwd whose output is written already compressed:
+ * the history compression above (same segments, hist_begin / hist_len per request, same
+ * output layout, times and types) applied to the attention output O, fused into the
+ * attention epilogue, so O itself never reaches memory (TM20K review page, LPTM and PATM
+ * compress the history between layers; LazFormer review page, Eq. 16-18, the
+ * compressed history feeds the next layer).  Each output row is the fp32 sum of its
+ * group's O rows (each already normalised), rounded once to bf16.
+ *   plan         a bf16 plan made by rec_attn_plan (not query-pruned: every row is
+ *                needed); its offsets are the compression's request offsets.
+ *   q, k, v      as for rec_attn_fwd.
+ *   hist_begin_host, hist_len_host, n_segments, seg_len, seg_group: as for
+ *                rec_attn_compress; every group size at most 32.
+ *   x_out        device [rows_out][H][d] bf16 (rows_out from rec_attn_compress_lengths),
+ *                16-byte aligned, not overlapping q, k, v; timestamps_out int64
+ *                [rows_out], types_out int8 [rows_out].
+ * Groups that straddle a 32-row block boundary pass their two partial sums through an
+ * fp32 fix-up buffer (from the library pool on `stream`, 2 * H * d * 4 bytes per 32
+ * tokens) and a second kernel; the result is deterministic.
+ * Errors: INVALID_ARG (those of rec_attn_compress and rec_attn_fwd), UNSUPPORTED (fp32
+ * or query-pruned plan, a group larger than 32), OOM, CUDA.  Asynchronous.
+ */
+rec_attn_status rec_attn_fwd_compress(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                                      const int64_t* hist_begin_host, const int64_t* hist_len_host,
+                                      int32_t n_segments, const int64_t* seg_len, const int32_t* seg_group,
+                                      void* x_out, int64_t* timestamps_out, int8_t* types_out, void* stream);
+
+/*
  * rec_attn_check_wait_timeout -- self-check of the failure detection inside the
  * pipelined kernels (the pages have no counterpart: it guards this implementation).
  * Every wait of a kernel on an mbarrier is bounded; on expiry it records
