@@ -141,6 +141,9 @@ def lib() -> ctypes.CDLL:
         L.orc_attention_bwd.argtypes = [P, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp,
                                         vp, vp, vp, ctypes.c_int32]
         L.orc_attention_bwd.restype = ctypes.c_int
+        L.orc_attention_bwd_fused.argtypes = [P, ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, vp,
+                                              ctypes.POINTER(OrcFused), vp] + [vp] * 8 + [ctypes.c_int32]
+        L.orc_attention_bwd_fused.restype = ctypes.c_int
         L.orc_compress.argtypes = [ctypes.c_int32, vp, vp, vp, ctypes.c_int32, vp, vp, ctypes.c_int32,
                                    ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp]
         L.orc_compress.restype = ctypes.c_int64
@@ -327,6 +330,44 @@ def attention_bwd(p: Params, offsets, t, ty, q, k, v, dout, threads: int | None 
     if rc != 0:
         raise ValueError(f"orc_attention_bwd rejected its arguments (rc={rc})")
     return dq, dk, dv
+
+
+def attention_bwd_fused(p: Params, offsets, t, ty, q, k, v, fused: Fused, dout, threads: int | None = None):
+    """fp64 gradients of attention(..., fused=fused) for the upstream gradient dout:
+    a dict with dq, dk, dv, dq_gate, dk_gate, dout_gate ([T, H, d]; zero for a gate that
+    is off) and dq_norm_w, dk_norm_w ([H, d]; zero without that norm)."""
+    offsets, t, ty = _c64(offsets), _c64(t), _c8(ty)
+    q, k, v, dout = (np.ascontiguousarray(a) for a in (q, k, v, dout))
+    dtype = 0 if q.dtype == np.uint16 else 1
+    assert int(offsets[0]) == 0
+    H, d = p.num_heads, p.head_dim
+    T = int(offsets[-1])
+    keep = []
+
+    def arr(a, dt, shape):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a, dtype=dt)
+        assert a.shape == shape, (a.shape, shape)
+        keep.append(a)
+        return _ptr(a)
+
+    gate_dt = np.uint16 if dtype == 0 else np.float32
+    fc = OrcFused(arr(fused.q_norm_w, np.float64, (H, d)), arr(fused.k_norm_w, np.float64, (H, d)),
+                  float(fused.norm_eps), arr(fused.q_gate, gate_dt, (T, H, d)),
+                  arr(fused.k_gate, gate_dt, (T, H, d)), arr(fused.out_gate, gate_dt, (T, H, d)))
+    out = {n: np.zeros((T, H, d)) for n in ("dq", "dk", "dv", "dq_gate", "dk_gate", "dout_gate")}
+    out["dq_norm_w"] = np.zeros((H, d))
+    out["dk_norm_w"] = np.zeros((H, d))
+    cp = p.c()
+    rc = lib().orc_attention_bwd_fused(
+        ctypes.byref(cp), len(offsets) - 1, _ptr(offsets), _ptr(t), _ptr(ty), dtype, _ptr(q), _ptr(k), _ptr(v),
+        ctypes.byref(fc), _ptr(dout), *(_ptr(out[n]) for n in ("dq", "dk", "dv", "dq_gate", "dk_gate", "dout_gate",
+                                                               "dq_norm_w", "dk_norm_w")),
+        int(threads or os.cpu_count() or 1))
+    if rc != 0:
+        raise ValueError(f"orc_attention_bwd_fused rejected its arguments (rc={rc})")
+    return out
 
 
 def compress(offsets, hist_begin, hist_len, segments, x=None, t=None, ty=None):

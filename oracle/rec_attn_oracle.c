@@ -496,6 +496,228 @@ int orc_attention_bwd(const orc_params* p, int32_t B, const int64_t* offsets, co
 }
 
 /* ------------------------------------------------------------------------- */
+/* Backward pass through the fused steps                                      */
+/* ------------------------------------------------------------------------- */
+
+/* The chain rule through the steps orc_attention_fused applies, in reverse order:
+ *   forward, per query / key head vector a:  n = a / r * w  (r = sqrt(mean(a^2) + eps),
+ *   when a norm gain is given), g = n * sigmoid(c) (when a gate is given), x = R(t) g;
+ *   the attention on the x's gives A; the output is O = A * sigmoid(c_o).
+ *   backward:  dA = dO * sigmoid(c_o),  dc_o = dO * A * sigmoid'(c_o);
+ *   the attention backward (bwd_unit's formulas) with dA gives dx_q, dx_k and dV;
+ *   dg = R(t)^T dx;  dc = dg * n * sigmoid'(c),  dn = dg * sigmoid(c);
+ *   da = (w * dn) / r - a * sum_e(dn_e w_e a_e) / (d r^3),  dw += dn * a / r.
+ * sigmoid'(c) = sigmoid(c) (1 - sigmoid(c)).  Every quantity is fp64. */
+typedef struct {
+  const orc_params* p;
+  int32_t B;
+  const int64_t *offsets, *t;
+  const int8_t* ty;
+  int dtype;
+  const void *q, *k, *v, *dout;
+  const orc_fused* f;
+  double *dq, *dk, *dv, *dqg, *dkg, *dog; /* [T][H][d] */
+  double *dqw, *dkw;                      /* [B][H][d]: per-request parts of the gain gradients */
+  int64_t n_units, next_unit;
+} fbwd_job;
+
+/* The forward steps of one head vector: a (input), n (normalised), sg (the gate's
+ * sigmoid, 1 without a gate), r (the norm's root mean square, 1 without a norm) and
+ * the rotated x. */
+static void fbwd_prep(const fbwd_job* J, int is_q, int64_t g, int32_t h, double* a, double* n, double* sg,
+                      double* r, double* x) {
+  const orc_params* p = J->p;
+  const int H = p->num_heads, d = p->head_dim;
+  const int64_t base = (g * H + h) * (int64_t)d;
+  const double* w = is_q ? J->f->q_norm_w : J->f->k_norm_w;
+  const void* gate = is_q ? J->f->q_gate : J->f->k_gate;
+  for (int e = 0; e < d; ++e) a[e] = load_elem(J->dtype, is_q ? J->q : J->k, base + e);
+  *r = 1.0;
+  if (w) {
+    double ss = 0.0;
+    for (int e = 0; e < d; ++e) ss += a[e] * a[e];
+    *r = sqrt(ss / d + J->f->norm_eps);
+    for (int e = 0; e < d; ++e) n[e] = a[e] / *r * w[(int64_t)h * d + e];
+  } else {
+    memcpy(n, a, sizeof(double) * d);
+  }
+  double* gv = x; /* the gated vector, rotated in place below */
+  for (int e = 0; e < d; ++e) {
+    sg[e] = gate ? orc_sigmoid(load_elem(J->dtype, gate, base + e)) : 1.0;
+    gv[e] = n[e] * sg[e];
+  }
+  if (p->use_rope) {
+    double* tmp = (double*)malloc(sizeof(double) * d);
+    orc_rope(p, J->t[g], gv, tmp);
+    memcpy(x, tmp, sizeof(double) * d);
+    free(tmp);
+  }
+}
+
+/* dg -> da (and the gate and gain gradients) for one head vector. */
+static void fbwd_back(const fbwd_job* J, int is_q, int32_t b, int64_t g, int32_t h, const double* dg,
+                      const double* a, const double* n, const double* sg, double r) {
+  const orc_params* p = J->p;
+  const int H = p->num_heads, d = p->head_dim;
+  const int64_t base = (g * H + h) * (int64_t)d;
+  const double* w = is_q ? J->f->q_norm_w : J->f->k_norm_w;
+  const void* gate = is_q ? J->f->q_gate : J->f->k_gate;
+  double* da = (is_q ? J->dq : J->dk) + base;
+  double* dc = (is_q ? J->dqg : J->dkg) + base;
+  double* dw = (is_q ? J->dqw : J->dkw) + ((int64_t)b * H + h) * d;
+  double dot = 0.0;
+  for (int e = 0; e < d; ++e) {
+    const double dn = dg[e] * sg[e];
+    dc[e] = gate ? dg[e] * n[e] * sg[e] * (1.0 - sg[e]) : 0.0;
+    if (w) {
+      dot += dn * w[(int64_t)h * d + e] * a[e];
+      dw[e] += dn * a[e] / r;
+    }
+  }
+  for (int e = 0; e < d; ++e) {
+    const double dn = dg[e] * sg[e];
+    da[e] = w ? w[(int64_t)h * d + e] * dn / r - a[e] * dot / (d * r * r * r) : dn;
+  }
+}
+
+static void fbwd_unit(fbwd_job* J, int32_t b, int32_t h) {
+  const orc_params* p = J->p;
+  const int H = p->num_heads, d = p->head_dim;
+  const int64_t base = J->offsets[b], L = J->offsets[b + 1] - base;
+  if (L <= 0) return;
+  const double scale = p->softmax_scale > 0 ? p->softmax_scale : 1.0 / sqrt((double)d);
+  const size_t Ld = (size_t)L * d;
+  double *qa = malloc(sizeof(double) * Ld), *qn = malloc(sizeof(double) * Ld), *qs = malloc(sizeof(double) * Ld);
+  double *ka = malloc(sizeof(double) * Ld), *kn = malloc(sizeof(double) * Ld), *ks = malloc(sizeof(double) * Ld);
+  double *qx = malloc(sizeof(double) * Ld), *kx = malloc(sizeof(double) * Ld);
+  double *qr = malloc(sizeof(double) * L), *kr = malloc(sizeof(double) * L);
+  double *vv = malloc(sizeof(double) * Ld), *dA = malloc(sizeof(double) * Ld);
+  double* P = calloc((size_t)L * L, sizeof(double));
+  double *gq = calloc(Ld, sizeof(double)), *gk = calloc(Ld, sizeof(double));
+  double* tmp = malloc(sizeof(double) * d);
+  for (int64_t i = 0; i < L; ++i) {
+    fbwd_prep(J, 1, base + i, h, qa + i * d, qn + i * d, qs + i * d, qr + i, qx + i * d);
+    fbwd_prep(J, 0, base + i, h, ka + i * d, kn + i * d, ks + i * d, kr + i, kx + i * d);
+    for (int e = 0; e < d; ++e) vv[i * d + e] = load_elem(J->dtype, J->v, ((base + i) * H + h) * (int64_t)d + e);
+  }
+  /* probabilities (0 where masked or for a row that sees nothing) */
+  for (int64_t i = 0; i < L; ++i) {
+    double m = -INFINITY;
+    double* Pi = P + i * L;
+    for (int64_t j = 0; j < L; ++j) {
+      if (!orc_visible(p, i, J->t[base + i], J->ty[base + i], j, J->t[base + j], J->ty[base + j])) {
+        Pi[j] = -INFINITY;
+        continue;
+      }
+      double acc = 0.0;
+      for (int e = 0; e < d; ++e) acc += qx[i * d + e] * kx[j * d + e];
+      Pi[j] = scale * acc;
+      if (Pi[j] > m) m = Pi[j];
+    }
+    if (m == -INFINITY) {
+      for (int64_t j = 0; j < L; ++j) Pi[j] = 0.0;
+      continue;
+    }
+    double den = 0.0;
+    for (int64_t j = 0; j < L; ++j) den += (Pi[j] == -INFINITY) ? 0.0 : exp(Pi[j] - m);
+    for (int64_t j = 0; j < L; ++j) Pi[j] = (Pi[j] == -INFINITY) ? 0.0 : exp(Pi[j] - m) / den;
+  }
+  /* the output gate: dA = dO * sigmoid(c_o), dc_o = dO * A * sigmoid'(c_o) */
+  for (int64_t i = 0; i < L; ++i) {
+    const int64_t off = ((base + i) * H + h) * (int64_t)d;
+    for (int e = 0; e < d; ++e) {
+      double A = 0.0;
+      for (int64_t j = 0; j < L; ++j) A += P[i * L + j] * vv[j * d + e];
+      const double go = load_elem(J->dtype, J->dout, off + e);
+      const double so = J->f->out_gate ? orc_sigmoid(load_elem(J->dtype, J->f->out_gate, off + e)) : 1.0;
+      dA[i * d + e] = go * so;
+      J->dog[off + e] = J->f->out_gate ? go * A * so * (1.0 - so) : 0.0;
+    }
+  }
+  /* the attention backward with dA */
+  for (int64_t i = 0; i < L; ++i) {
+    const double* Pi = P + i * L;
+    double Di = 0.0;
+    for (int64_t j = 0; j < L; ++j) {
+      if (Pi[j] == 0.0) continue;
+      double dp = 0.0;
+      for (int e = 0; e < d; ++e) dp += dA[i * d + e] * vv[j * d + e];
+      Di += Pi[j] * dp;
+    }
+    for (int64_t j = 0; j < L; ++j) {
+      if (Pi[j] == 0.0) continue;
+      double dp = 0.0;
+      for (int e = 0; e < d; ++e) dp += dA[i * d + e] * vv[j * d + e];
+      const double ds = Pi[j] * (dp - Di);
+      for (int e = 0; e < d; ++e) {
+        J->dv[((base + j) * H + h) * (int64_t)d + e] += Pi[j] * dA[i * d + e];
+        gq[i * d + e] += scale * ds * kx[j * d + e];
+        gk[j * d + e] += scale * ds * qx[i * d + e];
+      }
+    }
+  }
+  /* back through the rotation, the gates and the norms */
+  for (int64_t i = 0; i < L; ++i) {
+    if (p->use_rope) rope_inverse(p, J->t[base + i], gq + i * d, tmp);
+    else memcpy(tmp, gq + i * d, sizeof(double) * d);
+    fbwd_back(J, 1, b, base + i, h, tmp, qa + i * d, qn + i * d, qs + i * d, qr[i]);
+    if (p->use_rope) rope_inverse(p, J->t[base + i], gk + i * d, tmp);
+    else memcpy(tmp, gk + i * d, sizeof(double) * d);
+    fbwd_back(J, 0, b, base + i, h, tmp, ka + i * d, kn + i * d, ks + i * d, kr[i]);
+  }
+  free(qa); free(qn); free(qs); free(ka); free(kn); free(ks); free(qx); free(kx); free(qr); free(kr);
+  free(vv); free(dA); free(P); free(gq); free(gk); free(tmp);
+}
+
+static void* fbwd_worker(void* arg) {
+  fbwd_job* J = (fbwd_job*)arg;
+  for (;;) {
+    int64_t u = __atomic_fetch_add(&J->next_unit, 1, __ATOMIC_RELAXED);
+    if (u >= J->n_units) break;
+    fbwd_unit(J, (int32_t)(u / J->p->num_heads), (int32_t)(u % J->p->num_heads));
+  }
+  return NULL;
+}
+
+int orc_attention_bwd_fused(const orc_params* p, int32_t B, const int64_t* offsets, const int64_t* t,
+                            const int8_t* ty, int32_t dtype, const void* q, const void* k, const void* v,
+                            const orc_fused* f, const void* dout, double* dq, double* dk, double* dv,
+                            double* dq_gate, double* dk_gate, double* dout_gate, double* dq_norm_w,
+                            double* dk_norm_w, int32_t n_threads) {
+  if (!p || !f || B < 0 || !offsets || p->num_heads <= 0 || p->head_dim <= 0 || (p->head_dim & 1)) return -1;
+  if (dtype != ORC_BF16 && dtype != ORC_FP32) return -1;
+  if (!(f->norm_eps >= 0.0) || offsets[0] != 0) return -1;
+  for (int32_t b = 0; b < B; ++b)
+    if (offsets[b + 1] < offsets[b]) return -1;
+  const int H = p->num_heads, d = p->head_dim;
+  const int64_t n = offsets[B] * H * (int64_t)d;
+  double* outs[6] = {dq, dk, dv, dq_gate, dk_gate, dout_gate};
+  for (int i = 0; i < 6; ++i) memset(outs[i], 0, sizeof(double) * (size_t)n);
+  const size_t nw = (size_t)(B > 0 ? B : 1) * H * d;
+  double* pq = calloc(nw, sizeof(double));
+  double* pk = calloc(nw, sizeof(double));
+  fbwd_job J = {p, B, offsets, t, ty, dtype, q, k, v, dout, f, dq, dk, dv, dq_gate, dk_gate, dout_gate,
+                pq, pk, (int64_t)B * H, 0};
+  if (n_threads < 1) n_threads = 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)n_threads);
+  for (int i = 0; i < n_threads; ++i) pthread_create(&th[i], NULL, fbwd_worker, &J);
+  for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+  free(th);
+  /* the gains' gradients: the requests' parts summed in request order */
+  for (int64_t e = 0; e < (int64_t)H * d; ++e) {
+    double sq = 0.0, sk = 0.0;
+    for (int32_t b = 0; b < B; ++b) {
+      sq += pq[(int64_t)b * H * d + e];
+      sk += pk[(int64_t)b * H * d + e];
+    }
+    if (dq_norm_w) dq_norm_w[e] = sq;
+    if (dk_norm_w) dk_norm_w[e] = sk;
+  }
+  free(pq); free(pk);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* History compression                                                        */
 /* ------------------------------------------------------------------------- */
 

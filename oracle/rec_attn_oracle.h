@@ -78,6 +78,15 @@ int orc_attention_fused(const orc_params* p, int32_t B, const int64_t* offsets,
 int orc_attention_bwd(const orc_params* p, int32_t B, const int64_t* offsets, const int64_t* t,
                       const int8_t* ty, int32_t dtype, const void* q, const void* k, const void* v,
                       const void* dout, double* dq, double* dk, double* dv, int32_t n_threads);
+/* Gradients of orc_attention_fused for the upstream gradient dout: dq, dk, dv, the
+ * gate pre-activations' dq_gate, dk_gate, dout_gate ([T][H][d] fp64; zero for a gate
+ * that is off) and the norm gains' dq_norm_w, dk_norm_w ([H][d], NULL to skip).
+ * offsets[0] must be 0.  Returns 0 or -1. */
+int orc_attention_bwd_fused(const orc_params* p, int32_t B, const int64_t* offsets, const int64_t* t,
+                            const int8_t* ty, int32_t dtype, const void* q, const void* k, const void* v,
+                            const orc_fused* f, const void* dout, double* dq, double* dk, double* dv,
+                            double* dq_gate, double* dk_gate, double* dout_gate, double* dq_norm_w,
+                            double* dk_norm_w, int32_t n_threads);
 /* History compression: in request b the tokens [hist_begin[b], hist_begin[b] +
  * hist_len[b]) (time-ordered history) are replaced by sums of groups of consecutive
  * tokens; recency segment i (0 = newest) covers seg_len[i] tokens (< 0: the rest)
