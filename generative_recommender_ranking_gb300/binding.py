@@ -221,6 +221,29 @@ def rec_attn_bwd(plan: Plan, q, k, v, out, lse, dout, dq, dk, dv, stream=None) -
     _check("rec_attn_bwd", code)
 
 
+class RecAttnFusedGrads(ctypes.Structure):
+    _fields_ = [("dq_gate", ctypes.c_void_p), ("dk_gate", ctypes.c_void_p), ("dout_gate", ctypes.c_void_p),
+                ("dq_norm_weight", ctypes.c_void_p), ("dk_norm_weight", ctypes.c_void_p)]
+
+
+def rec_attn_bwd_fused(plan: Plan, q, k, v, out, lse, dout, dq, dk, dv, stream=None, q_norm_weight=None,
+                       k_norm_weight=None, norm_eps: float = 1e-6, q_gate=None, k_gate=None, out_gate=None,
+                       dq_gate=None, dk_gate=None, dout_gate=None, dq_norm_weight=None, dk_norm_weight=None) -> None:
+    """Gradients of rec_attn_fwd_fused (the fused steps' arguments as there) into dq, dk,
+    dv and the gate / gain gradients of the steps that are on."""
+    L = lib()
+    vp = ctypes.c_void_p
+    L.rec_attn_bwd_fused.argtypes = [vp, vp, vp, vp, ctypes.POINTER(RecAttnFused), vp, vp, vp, vp, vp, vp,
+                                     ctypes.POINTER(RecAttnFusedGrads), vp]
+    L.rec_attn_bwd_fused.restype = ctypes.c_int
+    f = RecAttnFused(_ptr(q_norm_weight), _ptr(k_norm_weight), float(norm_eps), _ptr(q_gate), _ptr(k_gate),
+                     _ptr(out_gate))
+    g = RecAttnFusedGrads(_ptr(dq_gate), _ptr(dk_gate), _ptr(dout_gate), _ptr(dq_norm_weight), _ptr(dk_norm_weight))
+    _check("rec_attn_bwd_fused", L.rec_attn_bwd_fused(plan.handle, _ptr(q), _ptr(k), _ptr(v), ctypes.byref(f),
+                                                      _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                                      ctypes.byref(g), _stream(stream)))
+
+
 def _segments(segments):
     sl = np.ascontiguousarray([int(a) for a, _ in segments], dtype=np.int64)
     sg = np.ascontiguousarray([int(g) for _, g in segments], dtype=np.int32)

@@ -496,9 +496,15 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const voi
   return fwd_impl(plan, q, k, v, fused, out, lse, stream);
 }
 
-REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
-                                          const void* out, const float* lse, const void* dout, void* dq,
-                                          void* dk, void* dv, void* stream) {
+namespace {
+
+// The backward of rec_attn_bwd and rec_attn_bwd_fused.  fa: the fused Q/K steps to
+// recompute Q' and K' with (nullptr: the time-RoPE alone); dout_attn: the gradient that
+// reaches the attention itself (dout, or dout * sigmoid(output gate)), while the row
+// constants D = <dout, out> use dout and out as given.
+rec_attn_status bwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, const void* v, const void* out,
+                         const float* lse, const void* dout, const void* dout_attn, void* dq, void* dk, void* dv,
+                         void* stream, const FusedArgs* fa) {
   if (!plan) return REC_ATTN_ERR_INVALID_ARG;
   const rec_attn_params& p = plan->p;
   const long long T = plan->T;
@@ -547,7 +553,31 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   char* bws = static_cast<char*>(plan->bwd_ws);
   const void* qs = q;
   const void* ks = k;
-  if (p.use_rope) {  // Q' and K' again, into the plan's workspace
+  if (fa) {  // the fused steps and the rotation again, into the plan's Q'/K' buffers
+    if (!plan->qrot) {
+      if (!plan->qk_extra) {
+        const size_t elem = p.dtype == REC_ATTN_BF16 ? 2 : 4;
+        const size_t qk_bytes = ((size_t)T * p.num_heads * p.head_dim * elem + 255) & ~(size_t)255;
+        cudaMemPool_t pool;
+        e = pool_for(plan->device, &pool);
+        if (e == cudaSuccess) e = cudaMallocFromPoolAsync(&plan->qk_extra, 2 * qk_bytes, pool, st);
+        if (e != cudaSuccess) { plan->qk_extra = nullptr; return from_cuda(e); }
+        plan->krot = static_cast<char*>(plan->qk_extra) + qk_bytes;
+      }
+      plan->qrot = plan->qk_extra;
+    }
+    e = cudaStreamWaitEvent(st, plan->ev_meta, 0);
+    if (e != cudaSuccess) return from_cuda(e);
+    RopeArgs ra;
+    ra.meta = plan->pd.meta; ra.tile_req = plan->pd.treq; ra.batch = plan->batch; ra.t = plan->t;
+    ra.ty = plan->ty; ra.skip_user_q = 0;
+    ra.q = q; ra.k = k; ra.qr = plan->qrot; ra.kr = plan->krot;
+    ra.heads = p.num_heads; ra.head_dim = p.head_dim;
+    std::memcpy(ra.omega, plan->omega, sizeof ra.omega);  // all zero without the RoPE
+    e = launch_rope_fused(ra, *fa, p.dtype, plan->NT, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    qs = plan->qrot; ks = plan->krot;
+  } else if (p.use_rope) {  // Q' and K' again, into the plan's workspace
     e = cudaStreamWaitEvent(st, plan->ev_meta, 0);
     if (e != cudaSuccess) return from_cuda(e);
     RopeArgs ra;
@@ -570,7 +600,7 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
   a.status = plan->pd.status;
   a.counters = plan->pd.counters;
   a.cls = plan->pd.cls; a.t = plan->t; a.ty = plan->ty;
-  a.q = qs; a.k = ks; a.v = v; a.out = out; a.dout = dout; a.lse = lse;
+  a.q = qs; a.k = ks; a.v = v; a.out = out; a.dout = dout; a.dout_attn = dout_attn; a.lse = lse;
   a.delta = tc ? nullptr : reinterpret_cast<float*>(bws);
   a.n_tiles = plan->NT;
   a.desc = tc ? reinterpret_cast<const BwdItemDesc*>(bws) : nullptr;
@@ -601,12 +631,104 @@ REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, 
     if (e != cudaSuccess) return from_cuda(e);
     plan->bwd_sched = true;
   }
-  CUtensorMap maps[4];  // Q', K', V, dO
-  const void* srcs[4] = {qs, ks, v, dout};
+  CUtensorMap maps[4];  // Q', K', V, the attention's dO
+  const void* srcs[4] = {qs, ks, v, dout_attn};
   const long long cols = (long long)p.num_heads * p.head_dim;
   for (int i = 0; i < 4; ++i)
     if (!encode_map(&maps[i], srcs[i], T, cols)) return REC_ATTN_ERR_CUDA;
   return from_cuda(launch_attn_bwd_tc(a, maps, p.head_dim, plan->num_sms, st));
+}
+
+}  // namespace
+
+REC_ATTN_API rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                                          const void* out, const float* lse, const void* dout, void* dq,
+                                          void* dk, void* dv, void* stream) {
+  return bwd_impl(plan, q, k, v, out, lse, dout, dout, dq, dk, dv, stream, nullptr);
+}
+
+REC_ATTN_API rec_attn_status rec_attn_bwd_fused(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                                                const rec_attn_fused* fused, const void* out, const float* lse,
+                                                const void* dout, void* dq, void* dk, void* dv,
+                                                const rec_attn_fused_grads* grads, void* stream) {
+  if (!plan || !fused || !grads) return REC_ATTN_ERR_INVALID_ARG;
+  const rec_attn_params& p = plan->p;
+  const long long T = plan->T;
+  if (!(fused->norm_eps >= 0.f) || !std::isfinite(fused->norm_eps)) return REC_ATTN_ERR_INVALID_ARG;
+  const bool qside = fused->q_norm_weight || fused->q_gate, kside = fused->k_norm_weight || fused->k_gate;
+  // a gradient for every step that is on
+  if ((fused->q_gate && !grads->dq_gate) || (fused->k_gate && !grads->dk_gate) ||
+      (fused->out_gate && !grads->dout_gate) || (fused->q_norm_weight && !grads->dq_norm_weight) ||
+      (fused->k_norm_weight && !grads->dk_norm_weight))
+    return REC_ATTN_ERR_INVALID_ARG;
+  const size_t elem = p.dtype == REC_ATTN_BF16 ? 2 : 4;
+  const size_t bytes = (size_t)T * p.num_heads * p.head_dim * elem;
+  if (T > 0) {
+    const void* al16[6] = {fused->q_gate, fused->k_gate, fused->out_gate, grads->dq_gate, grads->dk_gate,
+                           grads->dout_gate};
+    for (const void* x : al16)
+      if (reinterpret_cast<uintptr_t>(x) & 15u) return REC_ATTN_ERR_INVALID_ARG;
+    const void* al4[4] = {fused->q_norm_weight, fused->k_norm_weight, grads->dq_norm_weight, grads->dk_norm_weight};
+    for (const void* x : al4)
+      if (reinterpret_cast<uintptr_t>(x) & 3u) return REC_ATTN_ERR_INVALID_ARG;
+    void* gouts[3] = {grads->dq_gate, grads->dk_gate, grads->dout_gate};
+    const void* gins[8] = {q, k, v, out, dout, fused->q_gate, fused->k_gate, fused->out_gate};
+    for (void* g : gouts)
+      for (const void* x : gins)
+        if (g && x && overlaps(g, bytes, x, bytes)) return REC_ATTN_ERR_INVALID_ARG;
+  }
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (dev != plan->device) return REC_ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) return bwd_impl(plan, q, k, v, out, lse, dout, dout, dq, dk, dv, stream, nullptr);
+  // scratch: the attention's dO (with an output gate) and the gradients of the gated,
+  // normalised Q and K (with a Q- or K-side step)
+  const size_t rows = ws_up(bytes);
+  char* scratch = nullptr;
+  const size_t n_scr = (fused->out_gate ? 1 : 0) + (qside ? 1 : 0) + (kside ? 1 : 0);
+  if (n_scr) {
+    cudaMemPool_t pool;
+    e = pool_for(plan->device, &pool);
+    if (e == cudaSuccess) e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), n_scr * rows, pool, st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  char* next = scratch;
+  void* dout_attn = fused->out_gate ? next : const_cast<void*>(dout);
+  if (fused->out_gate) next += rows;
+  void* dgq = qside ? next : dq;
+  if (qside) next += rows;
+  void* dgk = kside ? next : dk;
+  GateArgs ga{};
+  ga.n = (long long)T * p.num_heads * p.head_dim;
+  ga.dout = dout; ga.out = out; ga.gate = fused->out_gate; ga.dout_attn = dout_attn; ga.dgate = grads->dout_gate;
+  if (fused->out_gate) e = launch_bwd_gate(ga, p.dtype, st);
+  FusedArgs fa;
+  fa.q_norm_w = fused->q_norm_weight; fa.k_norm_w = fused->k_norm_weight; fa.eps = fused->norm_eps;
+  fa.q_gate = fused->q_gate; fa.k_gate = fused->k_gate;
+  rec_attn_status s = REC_ATTN_OK;
+  if (e == cudaSuccess) s = bwd_impl(plan, q, k, v, out, lse, dout, dout_attn, dgq, dgk, dv, stream, &fa);
+  for (int side = 0; side < 2 && e == cudaSuccess && s == REC_ATTN_OK; ++side) {
+    if (!(side == 0 ? qside : kside)) continue;
+    NormGateArgs na{};
+    na.rows = T; na.heads = p.num_heads; na.head_dim = p.head_dim; na.eps = fused->norm_eps;
+    na.a = side == 0 ? q : k;
+    na.w = side == 0 ? fused->q_norm_weight : fused->k_norm_weight;
+    na.gate = side == 0 ? fused->q_gate : fused->k_gate;
+    na.dg = side == 0 ? dgq : dgk;
+    na.da = side == 0 ? dq : dk;
+    na.dgate = side == 0 ? grads->dq_gate : grads->dk_gate;
+    na.dw = side == 0 ? grads->dq_norm_weight : grads->dk_norm_weight;
+    if (na.dw) e = cudaMemsetAsync(na.dw, 0, sizeof(float) * (size_t)p.num_heads * p.head_dim, st);
+    if (e == cudaSuccess) e = launch_bwd_norm_gate(na, p.dtype, st);
+  }
+  if (scratch) {
+    const cudaError_t ef = cudaFreeAsync(scratch, st);
+    if (e == cudaSuccess) e = ef;
+  }
+  if (s != REC_ATTN_OK) return s;
+  return from_cuda(e);
 }
 
 namespace {

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dq(BwdArgs a) {
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       q[e] = ld_elem<E>(a.q, row * D + 32 * part + e) * a.scale;
-      go[e] = ld_elem<E>(a.dout, row * D + 32 * part + e);
+      go[e] = ld_elem<E>(a.dout_attn, row * D + 32 * part + e);
     }
     ti = a.t[tok];
     tyi = a.ty[tok];
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(Split<D>::kThreads) k_bwd_dkv(BwdArgs a) {
       const bool ok = pi < m.len;
       const long long src = ((m.tok_start + pi) * H + h) * D + e;
       sm.a[c][e] = ok ? ld_elem<E>(a.q, src) * a.scale : 0.f;
-      sm.b[c][e] = ok ? ld_elem<E>(a.dout, src) : 0.f;
+      sm.b[c][e] = ok ? ld_elem<E>(a.dout_attn, src) : 0.f;
     }
     for (int c = threadIdx.x; c < kTile; c += blockDim.x) {
       const int pi = qt * kTile + c;

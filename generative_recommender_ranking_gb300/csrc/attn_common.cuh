@@ -183,7 +183,8 @@ struct BwdArgs {
   const void* k;           // rotated keys K'
   const void* v;
   const void* out;         // forward output O
-  const void* dout;        // upstream gradient dO
+  const void* dout;        // upstream gradient dO (with out: the row constants <dO, O>)
+  const void* dout_attn;   // the gradient that reaches the attention (dO, or dO * sigmoid(output gate))
   const float* lse;        // forward log-sum-exp [T][H]
   float* delta;            // workspace [T][H]: <dO, O> per row
   void* dq;                // outputs [T][H][d] (w.r.t. the unrotated Q, K)
@@ -227,12 +228,48 @@ struct FusedArgs {
   const void* k_gate;
 };
 
+// Backward through the output gate O = A * sigmoid(c): dA = dO * sigmoid(c) and
+// dc = dO * O * (1 - sigmoid(c)), elementwise over n values.
+struct GateArgs {
+  long long n;
+  const void* dout;
+  const void* out;
+  const void* gate;
+  void* dout_attn;
+  void* dgate;
+};
+
+// Backward through the QK-RMSNorm and the sigmoid gate of one side (Q or K): per
+// (token, head) row a (the input), the gain w[h] and the gate c (either may be null) and
+// dg, the gradient of the gated, normalised row: da, dc and the gain gradient dw
+// (fp32 [H][d], zeroed by the caller, accumulated).
+struct NormGateArgs {
+  long long rows;  // tokens
+  int heads, head_dim;
+  float eps;
+  const void* a;
+  const float* w;
+  const void* gate;
+  const void* dg;
+  void* da;
+  void* dgate;
+  float* dw;
+};
+
 // sigmoid(x) = (1 + tanh(x / 2)) / 2, one hardware tanh (relative error about 2^-11,
 // below the bf16 rounding that follows) and one FMA.
 __device__ __forceinline__ float sigmoidf_fast(float x) {
   float th;
   asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * x));
   return fmaf(0.5f, th, 0.5f);
+}
+
+// The gates' sigmoid per I/O type: bf16 paths take the hardware tanh (its error is
+// below the bf16 rounding that follows), fp32 paths one exponential.
+template <typename E>
+__device__ __forceinline__ float sigmoid_io(float x) {
+  if constexpr (sizeof(E) == 2) return sigmoidf_fast(x);
+  else return 1.f / (1.f + __expf(-x));
 }
 
 // One work item: (query tile, head).

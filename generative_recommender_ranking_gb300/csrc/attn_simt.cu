@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kTile) k_attn_simt(AttnArgs a) {
   if (a.out_gate) {  // the attention output gate, O * sigmoid(g)
     const float* g = static_cast<const float*>(a.out_gate) + (tok * H + it.h) * D;
 #pragma unroll
-    for (int e = 0; e < D; ++e) dst[e] = o[e] * inv * sigmoidf_fast(g[e]);
+    for (int e = 0; e < D; ++e) dst[e] = o[e] * inv * sigmoid_io<float>(g[e]);
   } else {
 #pragma unroll
     for (int e = 0; e < D; ++e) dst[e] = o[e] * inv;

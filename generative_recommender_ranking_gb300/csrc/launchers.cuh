@@ -37,6 +37,8 @@ cudaError_t launch_bwd_schedule(const BwdSchedArgs& s, int num_sms, cudaStream_t
 cudaError_t launch_attn_bwd_tc(const BwdArgs& a, const CUtensorMap (&maps)[4], int head_dim, int num_sms,
                                cudaStream_t st);
 cudaError_t launch_compress(const CompressArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_bwd_gate(const GateArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_bwd_norm_gate(const NormGateArgs& a, int dtype, cudaStream_t st);
 // n_fix 32-row block boundaries (per request ceil(len / 32), from CmpReq::fix_start);
 // req_len: device int [B] request lengths.
 cudaError_t launch_cmp_fixup(const CmpArgs& c, int batch, const int* req_len, long long n_fix, int heads,

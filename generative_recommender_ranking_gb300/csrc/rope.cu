@@ -168,7 +168,7 @@ __device__ __forceinline__ void norm_gate(float (&x)[8], bool act, const float* 
   }
   if (gated) {
 #pragma unroll
-    for (int e = 0; e < kElems; ++e) x[e] *= sigmoidf_fast(g[e]);
+    for (int e = 0; e < kElems; ++e) x[e] *= sigmoid_io<E>(g[e]);
   }
 }
 

@@ -256,6 +256,37 @@ rec_attn_status rec_attn_bwd(rec_attn_plan_t* plan, const void* q, const void* k
                              void* dv, void* stream);
 
 /*
+ * rec_attn_bwd_fused -- gradients of rec_attn_fwd_fused: dq, dk, dv and those of the
+ * fused steps' inputs, for the upstream gradient dout (SORT review page, section
+ * 3.3.2; TM20K review page, QK Norm; CADET review page, self-gating).  The chain rule
+ * runs through the output gate (dA = dout * sigmoid(c_o), dc_o = dout * out *
+ * (1 - sigmoid(c_o))), the attention backward of rec_attn_bwd, the rotation, the Q/K
+ * gates (dc = dg * n * sigmoid'(c)) and the QK-RMSNorm (the gains' gradients summed
+ * over every token).
+ *   fused    the forward's rec_attn_fused (same pointers or the same values).
+ *   out, lse the forward's output (gated) and log-sum-exp; dout, dq, dk, dv as for
+ *            rec_attn_bwd.
+ *   grads    dq_gate, dk_gate, dout_gate: device [T][H][d] in params->dtype, required
+ *            for each gate that is on; dq_norm_weight, dk_norm_weight: device float
+ *            [H][d], required for each norm that is on (overwritten, not accumulated).
+ * Scratch from the library pool on `stream`: one [T][H][d] array per output gate and
+ * per side (Q, K) with a step on.  Supported as for rec_attn_bwd.
+ * Errors: those of rec_attn_bwd; INVALID_ARG also for a missing gradient of a step that
+ * is on, misaligned gates or gradients, a gradient aliasing an input.
+ */
+typedef struct {
+  void* dq_gate;          /* [T][H][d] or NULL (q gate off) */
+  void* dk_gate;          /* [T][H][d] or NULL */
+  void* dout_gate;        /* [T][H][d] or NULL */
+  float* dq_norm_weight;  /* [H][d] or NULL (q norm off) */
+  float* dk_norm_weight;  /* [H][d] or NULL */
+} rec_attn_fused_grads;
+rec_attn_status rec_attn_bwd_fused(rec_attn_plan_t* plan, const void* q, const void* k, const void* v,
+                                   const rec_attn_fused* fused, const void* out, const float* lse,
+                                   const void* dout, void* dq, void* dk, void* dv,
+                                   const rec_attn_fused_grads* grads, void* stream);
+
+/*
  * History compression (LazFormer review page, Eq. 16-18 and Table 6; TM20K review page,
  * PATM and LPTM): in request b the history rows [hist_begin[b], hist_begin[b] +
  * hist_len[b]) (request-local, time-ordered) are replaced by sums of groups of
