@@ -490,6 +490,92 @@ def run_serving(args):
     return 0
 
 
+def run_compress_fused(args):
+    """--compress SPEC --fused-epilogue: one layer whose output feeds the next layer
+    compressed.  Fused: plan + rec_attn_fwd_compress (the compression in the attention
+    epilogue; O never reaches memory).  Unfused: plan + rec_attn_fwd + rec_attn_compress.
+    Medians of CUDA-event times over --steps iterations (L2 flushed between them)."""
+    import torch
+    from generative_recommender_ranking_gb300 import binding as bd
+    from generative_recommender_ranking_gb300 import build as bld
+    bld.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = _workload(args.workload, 0, args.batch)
+    segs = COMPRESS_SPECS[args.compress]
+    hb, hl = [], []
+    for b in range(w.batch):
+        s0, e0 = int(w.offsets[b]), int(w.offsets[b + 1])
+        idx = np.nonzero(w.types[s0:e0] == W.HIST)[0]
+        hb.append(int(idx[0]) if len(idx) else 0)
+        hl.append(len(idx))
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        return (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) if a.dtype == np.uint16
+                else torch.from_numpy(a).to(dev))
+
+    q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    t, ty, off_d = to_dev(w.t), to_dev(w.types), to_dev(w.offsets)
+    params = bd.make_params(w.num_heads, w.head_dim, dtype=w.dtype, **w.mask, **w.rope)
+    out_off = bd.rec_attn_compress_lengths(w.offsets, hb, hl, segs)
+    n = int(out_off[-1])
+    T, H, d = w.total_tokens, w.num_heads, w.head_dim
+    x_out = torch.empty((n, H, d), dtype=q.dtype, device=dev)
+    t_out = torch.empty(n, dtype=torch.int64, device=dev)
+    ty_out = torch.empty(n, dtype=torch.int8, device=dev)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def fused():
+        p = bd.rec_attn_plan(params, w.offsets, off_d, t, ty, stream)
+        bd.rec_attn_fwd_compress(p, q, k, v, hb, hl, segs, x_out, t_out, ty_out, stream)
+        bd.rec_attn_free(p)
+
+    def unfused():
+        p = bd.rec_attn_plan(params, w.offsets, off_d, t, ty, stream)
+        bd.rec_attn_fwd(p, q, k, v, o, None, stream)
+        bd.rec_attn_compress(w.offsets, hb, hl, segs, o.view(T, H * d), t, ty, x_out.view(n, H * d), t_out, ty_out,
+                             stream)
+        bd.rec_attn_free(p)
+
+    def med(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        for a_, b_ in evs:
+            flush.zero_()
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.median(a_.elapsed_time(b_) for a_, b_ in evs)
+
+    tf, tu = med(fused), med(unfused)
+    p = bd.rec_attn_plan(params, w.offsets, off_d, t, ty, stream)
+    pairs = bd.rec_attn_visible_pairs(p)
+    # the attention kernels alone (CUDA events the library records around them)
+    bd.rec_attn_enable_timing(p)
+    bd.rec_attn_fwd_compress(p, q, k, v, hb, hl, segs, x_out, t_out, ty_out, stream)
+    attn_fused = bd.rec_attn_read_timings(p)[1]
+    bd.rec_attn_fwd(p, q, k, v, o, None, stream)
+    attn_plain = bd.rec_attn_read_timings(p)[1]
+    bd.rec_attn_free(p)
+    flops = 4.0 * d * H * pairs
+    print(json.dumps({
+        "metric": "attention layer with compressed output, ms per step (plan + forward + compression)",
+        "value": tf, "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "higher_is_better": False, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "segments": segs, "rows_in": T, "rows_out": n, "heads": H,
+                   "head_dim": d, "l2": "flushed between timed steps (256 MiB write)"},
+        "fused_ms": tf, "unfused_ms": tu, "speedup": tu / tf,
+        "attention_kernel_ms": {"with_compression_epilogue": attn_fused, "plain": attn_plain},
+        "fused_tflops": flops / (tf * 1e-3) / 1e12,
+        "bytes_saved_per_step": 2.0 * T * H * d * 2}), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -817,6 +903,9 @@ def main(argv=None):
                          "(backward) per visible pair and head")
     ap.add_argument("--fused", action="store_true",
                     help="time rec_attn_fwd_fused with QK-RMSNorm, Q/K gates and the output gate on")
+    ap.add_argument("--fused-epilogue", action="store_true",
+                    help="with --compress: the compression fused into the attention epilogue against the "
+                         "forward followed by the compression kernel")
     ap.add_argument("--serving", action="store_true",
                     help="per-request latency of candidate scoring against a cached history (use with "
                          "--workload cadet_serving)")
@@ -825,6 +914,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.serving:
         return run_serving(args)
+    if args.compress and args.fused_epilogue:
+        return run_compress_fused(args)
     if args.compress:
         return run_compress(args)
     if args.impl == "reference":

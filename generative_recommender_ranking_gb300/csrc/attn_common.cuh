@@ -33,20 +33,21 @@ __host__ __device__ __forceinline__ long long cmp_group_of(const CmpArgs& c, con
     glo = pi; ghi = pi + 1;
     return r.out_start + pi - r.hist_len + r.n_groups;
   }
-  const long long Lh = r.hist_len;
-  const long long rank_i = Lh - 1 - (pi - r.hist_begin);  // 0: the newest history row
-  long long rank = 0, newer_groups = 0;
+  // 32-bit arithmetic: requests are shorter than 2^31 rows
+  const int Lh = r.hist_len;
+  const int rank_i = Lh - 1 - (pi - r.hist_begin);  // 0: the newest history row
+  int rank = 0, newer_groups = 0;
   for (int u = 0; u < c.n_seg && rank < Lh; ++u) {
-    const long long room = Lh - rank;
-    const long long m = (c.seg_len[u] < 0 || c.seg_len[u] > room) ? room : c.seg_len[u];
-    const long long g = c.seg_group[u];
+    const int room = Lh - rank;
+    const int m = (c.seg_len[u] < 0 || c.seg_len[u] > room) ? room : (int)c.seg_len[u];
+    const int g = c.seg_group[u];
     if (rank_i < rank + m) {
-      const long long q = (rank_i - rank) / g;  // 0: the segment's newest group
-      const long long r0 = rank + q * g;
-      const long long r1 = rank + ((q + 1) * g < m ? (q + 1) * g : m);
-      glo = (int)(r.hist_begin + Lh - r1);
-      ghi = (int)(r.hist_begin + Lh - r0);
-      const long long from_newest = newer_groups + q;  // groups between it and the newest row
+      const int q = (rank_i - rank) / g;  // 0: the segment's newest group
+      const int r0 = rank + q * g;
+      const int r1 = rank + ((q + 1) * g < m ? (q + 1) * g : m);
+      glo = r.hist_begin + Lh - r1;
+      ghi = r.hist_begin + Lh - r0;
+      const int from_newest = newer_groups + q;  // groups between it and the newest row
       return r.out_start + r.hist_begin + (r.n_groups - 1 - from_newest);
     }
     newer_groups += (m + g - 1) / g;

@@ -504,9 +504,9 @@ __device__ __forceinline__ void cmp_store(const AttnArgs& a, const CmpReq& cr, i
   int glo = pi, ghi = pi + 1;
   long long orow = -1;
   if (row_ok) orow = cmp_group_of(c, cr, pi, glo, ghi);
-  const unsigned long long key = row_ok ? (unsigned long long)orow : ~0ull - (unsigned long long)lane;
-  const unsigned same = __match_any_sync(0xffffffffu, key);
-  const int last = 31 - __clz(same), first = __ffs(same) - 1;
+  const int r0 = pi - lane;  // the warp block's first request-local row (a multiple of 32)
+  // the lanes of this row's group inside the block (groups are runs of consecutive rows)
+  const int first = max(glo, r0) - r0, last = min(ghi, r0 + 32) - 1 - r0;
   for (int off = 1; off < c.span; off <<= 1) {
 #pragma unroll
     for (int e = 0; e < 64; ++e) {
@@ -516,7 +516,6 @@ __device__ __forceinline__ void cmp_store(const AttnArgs& a, const CmpReq& cr, i
   }
   if (!row_ok || lane != first) return;
   const int H = a.heads;
-  const int r0 = pi - lane;  // the warp block's first request-local row (a multiple of 32)
   if (glo >= r0 && ghi <= r0 + 32) {
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(c.x_out) + (orow * H + h) * D + cb * 64;
 #pragma unroll
