@@ -111,3 +111,34 @@ def test_pruned_parity_split_planner(keep):
     rows = gu.sample_rows(w, per_request=200)
     pairs, kept = _run(w, keep, sample=rows)
     assert len(kept) == (w.total_tokens if keep < 0 else w.batch * (min(keep, 5000) + 1))
+
+
+def test_target_attention_ignores_stale_rotated_queries():
+    """In a plan where no user token queries, the prologue leaves the rotated-Q rows of
+    user tokens unwritten, and query tiles that mix user tokens and candidates still pass
+    those rows through the tensor cores.  A previous forward with NaN queries leaves NaN
+    in the pool memory the next plan's rotated-Q buffer takes; the candidates' outputs
+    must still match the oracle and be finite (rows of the score and output tiles are
+    independent)."""
+    w = W.cadet_serving(batch=3, n_hist=700, n_cand=90)
+    tens = gu.device_inputs(w)
+    p = gu.params_for(w)
+    poison = bd.rec_attn_plan(p, tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    out = torch.empty_like(tens["q"])
+    bd.rec_attn_fwd(poison, torch.full_like(tens["q"], float("nan")), tens["k"], tens["v"], out)
+    torch.cuda.synchronize()
+    bd.rec_attn_free(poison)
+    torch.cuda.synchronize()
+    plan = bd.rec_attn_plan_query_pruned(p, 0, tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    try:
+        out = torch.full_like(tens["q"], float("nan"))
+        bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out)
+        torch.cuda.synchronize()
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
+    rows = oracle.kept_rows(w.offsets, w.types, 0)
+    ref = oracle.attention(gu.oracle_params(w), w.offsets, w.t, w.types, w.q, w.k, w.v, rows=rows)
+    got = gu.to_f64(out)[rows]
+    assert np.isfinite(got).all()
+    gu.assert_close(w, got, ref, "target attention after a NaN forward")
