@@ -809,6 +809,28 @@ def run_ours(args):
     h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in names)
     d2h = out.numel() * out.element_size()
 
+    # the host link alone (median of 5 copies each way, nothing else running): with the
+    # copies overlapped, the e2e step cannot be shorter than the slower direction's copy
+    def copy_ms(up: bool) -> float:
+        S = sets[0]
+        ts = []
+        for _ in range(6):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_ = up_s if up else down_s
+            a_.record(s_)
+            with torch.cuda.stream(s_):
+                if up:
+                    for n in names:
+                        S["in"][n].copy_(host_in[n], non_blocking=True)
+                else:
+                    S["hout"].copy_(S["out"], non_blocking=True)
+            b_.record(s_)
+            torch.cuda.synchronize(dev)
+            ts.append(a_.elapsed_time(b_))
+        return statistics.median(ts[1:])
+
+    up_ms, down_ms = copy_ms(True), copy_ms(False)
+
     # slowest rank's times, total work of all ranks
     (total_ms, e2e_ms, attn_max), (all_flops, all_tokens) = sharding.aggregate(
         [total_ms, e2e_ms, attn_ms], [flops, float(tokens)], device=dev)
@@ -882,7 +904,12 @@ def run_ours(args):
         "e2e": {"value": all_flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
                 "schedule": "every step uploads its inputs and downloads its output; uploads and downloads "
-                            "on two copy streams overlap the neighbouring steps' compute (two buffer sets)"},
+                            "on two copy streams overlap the neighbouring steps' compute (two buffer sets)",
+                "link": {"h2d_gbs": h2d / (up_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (down_ms * 1e-3) / 1e9,
+                         "h2d_ms_per_step": up_ms, "d2h_ms_per_step": down_ms,
+                         "bound_ms_per_step": max(ms_step, up_ms, down_ms),
+                         "note": "pinned copies timed alone on this box; the overlapped step is bounded "
+                                 "below by the slowest of compute, upload and download"}},
         # per step: k_plan (plus k_plan_tiles when requests average 32 tiles or more and
         # the planner splits them), k_build_masks, k_rope, k_attn_tc; the backward adds
         # k_rope, k_bwd_schedule, k_bwd_colmask (a new plan each step), k_bwd_rowc and the
