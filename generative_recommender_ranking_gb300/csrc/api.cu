@@ -61,53 +61,9 @@ struct rec_attn_plan_s {
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
 };
 
-namespace {
+namespace recattn {
 
-std::mutex g_pool_mu;
-std::map<int, cudaMemPool_t> g_pools;
-std::map<int, cudaStream_t> g_side;
-
-// Library-owned non-blocking stream per device for the RoPE prologue.
-cudaError_t side_stream_for(int device, cudaStream_t* out) {
-  std::lock_guard<std::mutex> lk(g_pool_mu);
-  auto it = g_side.find(device);
-  if (it != g_side.end()) { *out = it->second; return cudaSuccess; }
-  cudaStream_t st;
-  cudaError_t e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
-  if (e != cudaSuccess) return e;
-  g_side[device] = st;
-  *out = st;
-  return cudaSuccess;
-}
-
-rec_attn_status from_cuda(cudaError_t e) {
-  if (e == cudaSuccess) return REC_ATTN_OK;
-  if (e == cudaErrorMemoryAllocation) return REC_ATTN_ERR_OOM;
-  return REC_ATTN_ERR_CUDA;
-}
-
-// Library-owned pool per device; it keeps freed blocks so repeated plan/free cycles
-// do not return to the driver.
-cudaError_t pool_for(int device, cudaMemPool_t* out) {
-  std::lock_guard<std::mutex> lk(g_pool_mu);
-  auto it = g_pools.find(device);
-  if (it != g_pools.end()) { *out = it->second; return cudaSuccess; }
-  cudaMemPoolProps props;
-  std::memset(&props, 0, sizeof props);
-  props.allocType = cudaMemAllocationTypePinned;
-  props.location.type = cudaMemLocationTypeDevice;
-  props.location.id = device;
-  cudaMemPool_t pool;
-  cudaError_t e = cudaMemPoolCreate(&pool, &props);
-  if (e != cudaSuccess) return e;
-  uint64_t keep = ~0ull;
-  e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-  if (e != cudaSuccess) return e;
-  g_pools[device] = pool;
-  *out = pool;
-  return cudaSuccess;
-}
-
+// Parameter checks and tensor maps shared with the no-allocation entry point.
 rec_attn_status check_params(const rec_attn_params* p) {
   if (!p) return REC_ATTN_ERR_INVALID_ARG;
   if (p->abi_version != REC_ATTN_ABI_VERSION) return REC_ATTN_ERR_INVALID_ARG;
@@ -156,6 +112,55 @@ bool encode_map(CUtensorMap* m, const void* base, long long T, long long cols) {
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+}  // namespace recattn
+
+namespace {
+
+std::mutex g_pool_mu;
+std::map<int, cudaMemPool_t> g_pools;
+std::map<int, cudaStream_t> g_side;
+
+// Library-owned non-blocking stream per device for the RoPE prologue.
+cudaError_t side_stream_for(int device, cudaStream_t* out) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  auto it = g_side.find(device);
+  if (it != g_side.end()) { *out = it->second; return cudaSuccess; }
+  cudaStream_t st;
+  cudaError_t e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return e;
+  g_side[device] = st;
+  *out = st;
+  return cudaSuccess;
+}
+
+rec_attn_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return REC_ATTN_OK;
+  if (e == cudaErrorMemoryAllocation) return REC_ATTN_ERR_OOM;
+  return REC_ATTN_ERR_CUDA;
+}
+
+// Library-owned pool per device; it keeps freed blocks so repeated plan/free cycles
+// do not return to the driver.
+cudaError_t pool_for(int device, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  auto it = g_pools.find(device);
+  if (it != g_pools.end()) { *out = it->second; return cudaSuccess; }
+  cudaMemPoolProps props;
+  std::memset(&props, 0, sizeof props);
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = device;
+  cudaMemPool_t pool;
+  cudaError_t e = cudaMemPoolCreate(&pool, &props);
+  if (e != cudaSuccess) return e;
+  uint64_t keep = ~0ull;
+  e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  if (e != cudaSuccess) return e;
+  g_pools[device] = pool;
+  *out = pool;
+  return cudaSuccess;
 }
 
 // Closes the attention kernel's timing window: events 0..1 bracket the RoPE

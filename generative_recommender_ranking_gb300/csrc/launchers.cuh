@@ -47,4 +47,10 @@ cudaError_t launch_wait_timeout(int* status, unsigned long long limit_ns, cudaSt
 cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k,
                            const CUtensorMap& v, int head_dim, int grid, cudaStream_t st);
 
+// Host helpers shared by the entry points (api.cu): the parameter checks of
+// rec_attn_params, and a 2-D TMA map over a [T][cols] bf16 tensor (box 64 columns x
+// 128 rows, 128-byte swizzle).
+rec_attn_status check_params(const rec_attn_params* p);
+bool encode_map(CUtensorMap* m, const void* base, long long T, long long cols);
+
 }  // namespace recattn

@@ -61,43 +61,6 @@ rec_attn_status scratch_address(int* device, void** out) {
   return REC_ATTN_OK;
 }
 
-rec_attn_status validate(const rec_attn_params* p) {
-  if (!p || p->abi_version != REC_ATTN_ABI_VERSION) return REC_ATTN_ERR_INVALID_ARG;
-  if (p->num_heads < 1 || p->head_dim < 2 || (p->head_dim & 1)) return REC_ATTN_ERR_INVALID_ARG;
-  if (p->dtype != REC_ATTN_BF16 && p->dtype != REC_ATTN_FP32) return REC_ATTN_ERR_INVALID_ARG;
-  if ((p->use_delay | p->use_rope | p->hist_bidirectional) & ~1) return REC_ATTN_ERR_INVALID_ARG;
-  if (p->delay_s < 0 || p->delay_s > (1LL << 62) || p->window < 0) return REC_ATTN_ERR_INVALID_ARG;
-  if (!(std::isfinite(p->softmax_scale) && p->softmax_scale >= 0.f)) return REC_ATTN_ERR_INVALID_ARG;
-  if (p->use_rope && !(std::isfinite(p->phi_min) && std::isfinite(p->dt_max_s) && std::isfinite(p->rope_base) &&
-                       p->dt_max_s > 0.0 && p->rope_base > 0.0))
-    return REC_ATTN_ERR_INVALID_ARG;
-  if (p->dtype == REC_ATTN_BF16 && p->head_dim != 64 && p->head_dim != 128) return REC_ATTN_ERR_UNSUPPORTED;
-  if (p->dtype == REC_ATTN_FP32 && p->head_dim != 32 && p->head_dim != 64) return REC_ATTN_ERR_UNSUPPORTED;
-  if ((long long)p->num_heads * p->head_dim > (1LL << 20)) return REC_ATTN_ERR_UNSUPPORTED;
-  return REC_ATTN_OK;
-}
-
-bool encode_bf16_map(CUtensorMap* m, const void* base, long long rows, long long cols) {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kTile};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params, int32_t batch,
@@ -105,7 +68,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
                                                   const int64_t* timestamps_dev, const int8_t* types_dev,
                                                   const void* q, const void* k, const void* v, void* out,
                                                   float* lse, void* stream) {
-  rec_attn_status st = validate(params);
+  rec_attn_status st = check_params(params);
   if (st != REC_ATTN_OK) return st;
   if (batch < 0 || (batch > 0 && !offsets_host)) return REC_ATTN_ERR_INVALID_ARG;
   // sizes of the workspace pieces (host-only pass over the offsets)
@@ -236,8 +199,8 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   if (params->dtype == REC_ATTN_FP32) return status_of(launch_attn_simt(a, params->head_dim, s));
   CUtensorMap maps[3];
   const long long cols = (long long)params->num_heads * params->head_dim;
-  if (!encode_bf16_map(&maps[0], qs, T, cols) || !encode_bf16_map(&maps[1], ks, T, cols) ||
-      !encode_bf16_map(&maps[2], v, T, cols))
+  if (!encode_map(&maps[0], qs, T, cols) || !encode_map(&maps[1], ks, T, cols) ||
+      !encode_map(&maps[2], v, T, cols))
     return REC_ATTN_ERR_CUDA;
   const int grid = (int)(a.n_items < num_sms ? a.n_items : num_sms);
   return status_of(launch_attn_tc(a, maps[0], maps[1], maps[2], params->head_dim, grid, s));
