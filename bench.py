@@ -38,6 +38,7 @@ from generative_recommender_ranking_gb300 import workloads as W  # noqa: E402
 
 METRIC = "masked-attn fwd TFLOP/s over visible pairs, % of GB300 bf16 peak; tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+E2E_RUNS = 3  # runs of the end-to-end leg; the median is reported
 # history-compression settings: recency segments (length or -1, group size), newest first
 COMPRESS_SPECS = {
     "lazformer_keep1024_g8": [(1024, 1), (-1, 8)],
@@ -802,10 +803,16 @@ def run_ours(args):
 
     e2e_steps(2)  # untimed: the copy streams and the buffer sets warmed up
     torch.cuda.synchronize(dev)
-    e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    e2e_steps(args.steps, e2e_ev)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e2e_ev[0].elapsed_time(e2e_ev[1])
+    # three runs of K steps, the median reported: on these hosts a host-device copy
+    # now and then runs at a fraction of the link's rate (a 4.7 ms upload seen taking
+    # 80 ms), which no schedule can hide; every run is listed with the line
+    e2e_runs = []
+    for _ in range(E2E_RUNS):
+        e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        e2e_steps(args.steps, e2e_ev)
+        torch.cuda.synchronize(dev)
+        e2e_runs.append(e2e_ev[0].elapsed_time(e2e_ev[1]))
+    e2e_ms = statistics.median(e2e_runs)
     h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in names)
     d2h = out.numel() * out.element_size()
 
@@ -905,6 +912,8 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
                 "schedule": "every step uploads its inputs and downloads its output; uploads and downloads "
                             "on two copy streams overlap the neighbouring steps' compute (two buffer sets)",
+                "runs_ms_per_step": [x / args.steps for x in e2e_runs],
+                "statistic": f"median of {E2E_RUNS} runs of {args.steps} steps (this rank)",
                 "link": {"h2d_gbs": h2d / (up_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (down_ms * 1e-3) / 1e9,
                          "h2d_ms_per_step": up_ms, "d2h_ms_per_step": down_ms,
                          "bound_ms_per_step": max(ms_step, up_ms, down_ms),
