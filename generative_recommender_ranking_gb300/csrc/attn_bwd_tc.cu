@@ -82,8 +82,12 @@ enum : int {
   kStrFull,
   kStrEmpty = kStrFull + kNS,
   kSyFull = kStrEmpty + kNS,  // the step's two score MMAs completed
-  kXReady,                    // the compute warps wrote the step's bf16 operands
-  kDpFree,                    // DQ: the compute warps loaded the step's dP
+  kXReady,                    // [2, by step parity] the compute warps wrote the step's bf16 operands
+                              // (in mode DQ the next step's scores go out before this step's
+                              // operands are consumed, so the compute warps may finish a whole step
+                              // ahead of the issuer's wait; with one barrier per parity a barrier
+                              // cannot complete twice before its wait)
+  kDpFree = kXReady + 2,      // DQ: the compute warps loaded the step's dP
   kAccFull,                   // the item's last accumulating MMA completed
   kAccEmpty,                  // the compute warps read the accumulators
   kGroup,                     // DKV: barrier of the 128 compute threads
@@ -92,6 +96,10 @@ enum : int {
   kMmaDone = kItemEmpty + 2,
   kNumBars
 };
+
+// The ready barrier of step `step` (a stream-wide step count) and its wait parity.
+__host__ __device__ constexpr int xready(uint32_t step) { return kXReady + (int)(step & 1u); }
+__host__ __device__ constexpr uint32_t xready_parity(uint32_t step) { return (step >> 1) & 1u; }
 
 // Byte offsets from the 1024-aligned base of dynamic shared memory.
 constexpr int kRowB = kTile * 8;  // {lse2, D} of a tile's rows
@@ -383,7 +391,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
             ptx::tc_fence_after();
             if (!issue_scores(ls + 1)) goto out;
           }
-          if (!bw_wait(bars + kXReady, (step0 + ls) & 1, abort_flag, a.status)) goto out;
+          if (!bw_wait(bars + xready(step0 + ls), xready_parity(step0 + ls), abort_flag, a.status)) goto out;
           ptx::tc_fence_after();
           if (ls == 0 && !acc_free()) goto out;
           const uint32_t kb = str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes;
@@ -405,7 +413,7 @@ __device__ void bwd_mma(const BwdArgs& a, uint8_t* sm, uint64_t* bars, uint32_t 
         for (int ls = 0; ls < nsteps; ++ls) {
           int st;
           stage_of(ls, false, st);
-          if (!bw_wait(bars + kXReady, (step0 + ls) & 1, abort_flag, a.status)) goto out;
+          if (!bw_wait(bars + xready(step0 + ls), xready_parity(step0 + ls), abort_flag, a.status)) goto out;
           ptx::tc_fence_after();
           if (ls == 0 && !acc_free()) goto out;
           const uint32_t qb = str + (2 * st) * kTileBytes + (ls & 1) * kHalfBytes;
@@ -564,7 +572,7 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + kXReady);
+        if (lane == 0) ptx::mbar_arrive(bars + xready(step));
       }
     }
     if (!bw_wait_warp(bars + kAccFull, it_n & 1, abort_flag, a.status)) return;
@@ -734,7 +742,7 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars + kXReady);
+        if (lane == 0) ptx::mbar_arrive(bars + xready(step - 1));  // step was counted on at the wait
         return true;
       };
       if (!do_step(0)) return;
@@ -905,7 +913,7 @@ __global__ void __launch_bounds__(kThreadsB, BCfg<D>::kBlocksPerSM)
       ptx::mbar_init(bars + kStrEmpty + i, 1 + 4);  // MMAs done + the compute warps read the record
     }
     ptx::mbar_init(bars + kSyFull, 1);
-    ptx::mbar_init(bars + kXReady, 4);
+    for (int i = 0; i < 2; ++i) ptx::mbar_init(bars + kXReady + i, 4);
     ptx::mbar_init(bars + kDpFree, 4);
     ptx::mbar_init(bars + kAccFull, 1);
     ptx::mbar_init(bars + kAccEmpty, 4);
