@@ -114,6 +114,14 @@ bool encode_map(CUtensorMap* m, const void* base, long long T, long long cols) {
   return r == CUDA_SUCCESS;
 }
 
+// Long items: rows without a window over requests of at least 64 tiles on average
+// (8192 tokens), where a row's running maximum rarely moves from one key tile to the
+// next, so the softmax takes its lazy maximum; shorter items keep the plain one (the
+// lazy one holds more registers).
+int long_items(const rec_attn_params& p, int batch, long long n_tiles) {
+  return (p.window == 0 && batch > 0 && n_tiles >= 64LL * batch) ? 1 : 0;
+}
+
 }  // namespace recattn
 
 namespace {
@@ -469,6 +477,7 @@ rec_attn_status fwd_impl(rec_attn_plan_t* plan, const void* q, const void* k, co
   a.out_gate = f ? f->out_gate : nullptr;
   a.n_items = plan->NT * p.num_heads; a.heads = p.num_heads; a.scale = p.softmax_scale; a.mask = plan->mask;
   if (cmp) a.cmp = *cmp;
+  a.long_items = long_items(p, plan->batch, plan->NT);
   if (p.dtype == REC_ATTN_FP32) {
     e = launch_attn_simt(a, p.head_dim, st);
     return finish_timing(plan, st, e);

@@ -82,6 +82,7 @@ struct AttnArgs {
   float scale;       // softmax scale (natural-log domain)
   MaskP mask;
   CmpArgs cmp;       // compression epilogue (kernels instantiated with it only)
+  int long_items;    // 1: the items run over many key tiles (the softmax's lazy maximum pays)
 };
 
 // Arguments of the time-RoPE prologue.

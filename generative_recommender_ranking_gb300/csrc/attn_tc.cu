@@ -46,6 +46,7 @@ constexpr int kSlab = kTile * 128;           // 128 rows x 128 B: one 64-column 
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;          // keep the reference max until it is exceeded by 2^8
+constexpr float kLazySum = 256.f;            // LAZY: a chunk whose exponentials sum below this keeps the reference
 constexpr int kRecBytes = (int)sizeof(KeyTileRec);
 constexpr int kMaskBytes = kTile * 16;  // a PARTIAL tile's 128 rows of visibility bits (mask table)
 constexpr int kStageRec = kMaskBytes > kRecBytes ? kMaskBytes : kRecBytes;  // per K/V stage: one or the other
@@ -429,38 +430,11 @@ out:
 }
 
 // ------------------------------------------------------------------ softmax
-// One 64-key chunk of a row: masked scores, lazy reference-max update, P = 2^(x*sl2 - m)
-// rounded to bf16 (packed pairs), the fp32 sum of the exponentials, and the factor
-// (corr, needed when resc) by which O and l must be scaled before P is added.
-__device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[kChunk], bool partial, uint32_t w0, uint32_t w1,
-                                              float sl2, float& m_ref, uint32_t (&pk)[kChunk / 2], float& corr,
-                                              bool& resc, float& rs) {
-  float x[kChunk];
-#pragma unroll
-  for (int e = 0; e < kChunk; ++e) x[e] = __uint_as_float(sr[e]);
-  if (partial) {
-#pragma unroll
-    for (int e = 0; e < kChunk; ++e)
-      if (!(((e < 32 ? w0 : w1) >> (e & 31)) & 1u)) x[e] = -INFINITY;
-  }
-  // row maximum as a depth-4 tree of three-input maxima (21 + 7 + 3 + 1)
-  static_assert(kChunk == 64, "the max tree covers 64 scores");
-  float m1[22], m2[8];
-#pragma unroll
-  for (int i = 0; i < 21; ++i) m1[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
-  m1[21] = x[63];
-#pragma unroll
-  for (int i = 0; i < 7; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
-  m2[7] = m1[21];
-  const float mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
-  const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
-  const float m_new = (m_tile > m_ref + kRescaleLog2) ? m_tile : m_ref;
-  const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-  // O (and l) need scaling only when a finite running max moved; while it is -inf
-  // every P so far was exactly 0, so O and l are 0
-  resc = m_new != m_ref && m_ref != -INFINITY;
-  corr = resc ? ex2(m_ref - m_use) : 1.f;
-  const unsigned long long sl2x2 = pack2(sl2, sl2), negm2 = pack2(-m_use, -m_use);
+// The exponentials of one 64-key chunk against the reference m (log2 domain): P packed
+// to bf16 pairs and the sum rs of the unrounded exponentials.
+__device__ __forceinline__ void exp_chunk(const float (&x)[kChunk], float sl2, float m, uint32_t (&pk)[kChunk / 2],
+                                          float& rs) {
+  const unsigned long long sl2x2 = pack2(sl2, sl2), negm2 = pack2(-m, -m);
   unsigned long long acc0 = 0ull, acc1 = 0ull;  // packed partial sums (+0.0f pairs)
 #pragma unroll
   for (int e = 0; e < kChunk / 2; ++e) {
@@ -476,6 +450,58 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[kChunk], bool
   unpack2(acc0, r0, r1);
   unpack2(acc1, r2, r3);
   rs = (r0 + r1) + (r2 + r3);
+}
+
+// One 64-key chunk of a row: masked scores, lazy reference-max update, P = 2^(x*sl2 - m)
+// in bf16 pairs, the sum rs of the exponentials, and the factor corr (needed when resc)
+// by which O and l must be scaled before P is added.  The reference m_ref moves only when
+// the chunk's maximum exceeds it by 2^kRescaleLog2, so P stays below 2^8.
+//
+// LAZY (rows of many key tiles, where the maximum rarely moves): with a finite reference
+// the exponentials are formed against it at once, and the chunk's maximum is only taken
+// when one of them could be large, which their sum bounds (every term is at most the
+// sum): below kLazySum the chunk is done with no rescale; otherwise (and for a row's
+// first visible chunk) the maximum becomes the reference and the chunk is formed again.
+// This trades the maximum's instructions on most chunks for more live registers.
+template <bool LAZY>
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[kChunk], bool partial, uint32_t w0, uint32_t w1,
+                                              float sl2, float& m_ref, uint32_t (&pk)[kChunk / 2], float& corr,
+                                              bool& resc, float& rs) {
+  float x[kChunk];
+#pragma unroll
+  for (int e = 0; e < kChunk; ++e) x[e] = __uint_as_float(sr[e]);
+  if (partial) {
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e)
+      if (!(((e < 32 ? w0 : w1) >> (e & 31)) & 1u)) x[e] = -INFINITY;
+  }
+  if constexpr (LAZY) {
+    corr = 1.f;
+    resc = false;
+    if (m_ref != -INFINITY) {
+      exp_chunk(x, sl2, m_ref, pk, rs);
+      if (rs < kLazySum) return;
+    }
+  }
+  // row maximum as a depth-4 tree of three-input maxima (21 + 7 + 3 + 1)
+  static_assert(kChunk == 64, "the max tree covers 64 scores");
+  float m1[22], m2[8];
+#pragma unroll
+  for (int i = 0; i < 21; ++i) m1[i] = fmax3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  m1[21] = x[63];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
+  m2[7] = m1[21];
+  const float mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+  const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
+  // LAZY: a sum at or above kLazySum means some term exceeded 2^2, so the maximum moves
+  const float m_new = LAZY ? (m_tile > m_ref ? m_tile : m_ref) : ((m_tile > m_ref + kRescaleLog2) ? m_tile : m_ref);
+  const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+  // O (and l) need scaling only when a finite running max moved; while it is -inf
+  // every P so far was exactly 0, so O and l are 0
+  resc = m_new != m_ref && m_ref != -INFINITY;
+  corr = resc ? ex2(m_ref - m_use) : 1.f;
+  exp_chunk(x, sl2, m_use, pk, rs);
   m_ref = m_new;
 }
 
@@ -540,8 +566,9 @@ __device__ __forceinline__ void cmp_store(const AttnArgs& a, const CmpReq& cr, i
 
 // GATE: the attention output gate is applied in the epilogue (a separate
 // instantiation, so the plain epilogue carries none of its code).  CMP: the output is
-// the history compression of O (cmp_store) instead of O.
-template <int D, bool GATE, bool CMP>
+// the history compression of O (cmp_store) instead of O.  LAZY: softmax_chunk's lazy
+// maximum, for plans whose items run over many key tiles.
+template <int D, bool GATE, bool CMP, bool LAZY>
 __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& B, uint32_t tmem,
                             volatile int* abort_flag) {
   using L = Layout<D>;
@@ -646,7 +673,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
           ptx::mbar_arrive(B.p_full + 1);
           p1_pending = false;
         }
-        softmax_chunk(sr, partial, vm[0], vm[1], sl2, m_ref, pk, corr, resc, rs);
+        softmax_chunk<LAZY>(sr, partial, vm[0], vm[1], sl2, m_ref, pk, corr, resc, rs);
         l = l * corr + rs;
         // P half c may be overwritten once PV_c(t-1) has read it; O may be rescaled
         // once every earlier PV has landed.  Each pv_done[c] completes once per tile
@@ -665,7 +692,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
         ptx::tc_fence_before();
         ptx::mbar_arrive(B.p_full + 0);
         ptx::mbar_arrive(B.s_free);  // S(t) is in registers: S(t+1) may overwrite it
-        softmax_chunk(sr, partial, vm[2], vm[3], sl2, m_ref, pk, corr, resc, rs);
+        softmax_chunk<LAZY>(sr, partial, vm[2], vm[3], sl2, m_ref, pk, corr, resc, rs);
         l = l * corr + rs;
         if (t > 0 && !wait_bar_warp(B.pv_done + 1, (t - 1) & 1, abort_flag, a.status)) return;
         if (__any_sync(0xffffffffu, resc)) {
@@ -687,7 +714,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
           float corr, rs;
           bool resc;
           ptx::tmem_ld64(tm.s + buf * kChunk, sr);
-          softmax_chunk(sr, partial, c ? vm[2] : vm[0], c ? vm[3] : vm[1], sl2, m_ref, pk, corr, resc, rs);
+          softmax_chunk<LAZY>(sr, partial, c ? vm[2] : vm[0], c ? vm[3] : vm[1], sl2, m_ref, pk, corr, resc, rs);
           l = l * corr + rs;
           // O may only be rescaled once PV(ch-1) has landed.  The two pv_done barriers
           // alternate by chunk, and PV(ch+1) cannot start before P(ch+1) exists, so the
@@ -761,7 +788,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
   }
 }
 
-template <int D, bool GATE, bool CMP>
+template <int D, bool GATE, bool CMP, bool LAZY>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
@@ -825,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = (warp - kRoleWarps) >> 2;
     SBars B;
     B.bind<D>(bars + s * L::kBarsPerStream);
-    run_softmax<D, GATE, CMP>(a, sm, s, B, tmem, abort_flag);
+    run_softmax<D, GATE, CMP, LAZY>(a, sm, s, B, tmem, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -844,23 +871,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool GATE, bool CMP>
+template <int D, bool GATE, bool CMP, bool LAZY>
 cudaError_t launch_t(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                      int grid, cudaStream_t st) {
   using L = Layout<D>;
   static_assert(L::kDynamic <= 227 * 1024, "shared memory budget");
   cudaError_t e =
-      cudaFuncSetAttribute(k_attn_tc<D, GATE, CMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
+      cudaFuncSetAttribute(k_attn_tc<D, GATE, CMP, LAZY>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynamic);
   if (e != cudaSuccess) return e;
-  k_attn_tc<D, GATE, CMP><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
+  k_attn_tc<D, GATE, CMP, LAZY><<<grid, kThreads, L::kDynamic, st>>>(q, k, v, a);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch(const AttnArgs& a, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, int grid,
                    cudaStream_t st) {
-  if (a.cmp.req) return launch_t<D, false, true>(a, q, k, v, grid, st);
-  return a.out_gate ? launch_t<D, true, false>(a, q, k, v, grid, st) : launch_t<D, false, false>(a, q, k, v, grid, st);
+  if (a.cmp.req) return launch_t<D, false, true, false>(a, q, k, v, grid, st);
+  if (a.out_gate) return launch_t<D, true, false, false>(a, q, k, v, grid, st);
+  if constexpr (Cfg<D>::WIDE) {
+    if (a.long_items) return launch_t<D, false, false, true>(a, q, k, v, grid, st);
+  }
+  return launch_t<D, false, false, false>(a, q, k, v, grid, st);
 }
 
 }  // namespace

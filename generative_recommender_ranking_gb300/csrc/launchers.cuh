@@ -52,5 +52,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, const CUtensorMap& q, const CUtens
 // 128 rows, 128-byte swizzle).
 rec_attn_status check_params(const rec_attn_params* p);
 bool encode_map(CUtensorMap* m, const void* base, long long T, long long cols);
+// 1 when the plan's items run over many key tiles (AttnArgs::long_items).
+int long_items(const rec_attn_params& p, int batch, long long n_tiles);
 
 }  // namespace recattn

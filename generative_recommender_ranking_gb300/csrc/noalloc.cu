@@ -196,6 +196,7 @@ REC_ATTN_API rec_attn_status rec_attn_fwd_noalloc(const rec_attn_params* params,
   a.n_items = NT * params->num_heads; a.heads = params->num_heads;
   a.scale = params->softmax_scale > 0.f ? params->softmax_scale : 1.f / std::sqrt((float)params->head_dim);
   a.mask = mask;
+  a.long_items = long_items(*params, batch, NT);
   if (params->dtype == REC_ATTN_FP32) return status_of(launch_attn_simt(a, params->head_dim, s));
   CUtensorMap maps[3];
   const long long cols = (long long)params->num_heads * params->head_dim;
