@@ -30,9 +30,9 @@ SMALL = {
     "mtgr": lambda: W.mtgr(batch=4, hist=(150, 400), rt=(20, 80), cand=(10, 40)),
     "tm20k_full": lambda: W.tm20k("full", batch=2, n_hist=1500),
     "tm20k_window": lambda: W.tm20k("window", batch=2, n_hist=1500),
-    # 65 tiles with no window: long enough for the softmax's lazy maximum (requests of
-    # at least 64 tiles on average), every row checked
-    "tm20k_full_long": lambda: W.tm20k("full", batch=1, n_hist=8300, heads=2),
+    # 33 tiles with no window: long enough for the softmax's lazy maximum (requests of
+    # at least 32 tiles on average), every row checked
+    "tm20k_full_long": lambda: W.tm20k("full", batch=2, n_hist=4150, heads=2),
     "cadet_d128": lambda: W.cadet(batch=3, n_pairs=170, heads=2, head_dim=128),
     "sort_d128": lambda: W.sort(batch=2, n_hist=300, n_cand=40, window=100, heads=2, head_dim=128),
 }
