@@ -104,8 +104,12 @@ def _compress_traffic(workload: str, spec: str):
         return None
 
 
-def _workload(name, rank, batch=None, history=None):
+def _workload(name, rank, batch=None, history=None, heads=None, head_dim=None):
     kw = {}
+    if heads:
+        kw["heads"] = heads
+    if head_dim:
+        kw["head_dim"] = head_dim
     if rank:
         base = {"tiny_fp32": 1001, "cadet": 1002, "sort": 1003, "mtgr": 1004}.get(name, 1005)
         kw["seed"] = base + 7919 * rank
@@ -285,7 +289,7 @@ def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
-    w = _workload(args.workload, 0, args.batch, args.history)
+    w = _workload(args.workload, 0, args.batch, args.history, args.heads, args.head_dim)
     per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
     long_req = w.batch and int(np.diff(w.offsets).max()) > LONG_REQUEST
     rows_per_request = 512
@@ -326,7 +330,7 @@ def run_compress(args):
     from generative_recommender_ranking_gb300 import build as bld
     bld.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = _workload(args.workload, 0, args.batch, args.history)
+    w = _workload(args.workload, 0, args.batch, args.history, args.heads, args.head_dim)
     segs = COMPRESS_SPECS[args.compress]
     hb, hl = [], []
     for b in range(w.batch):
@@ -372,7 +376,8 @@ def run_compress(args):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / pk["hbm_gbs"],
                      "traffic": (_compress_traffic(args.workload, args.compress)
-                                 if args.batch is None and args.history is None else None),
+                                 if args.batch is None and args.history is None and args.heads is None
+                                 and args.head_dim is None else None),
                      "kernel": "k_compress",
                      "peak_source": pk["source"], "algorithmic_bytes_per_launch": nbytes, "ms_per_launch": ms},
         "gpu_launches": args.steps}), flush=True)
@@ -390,7 +395,7 @@ def run_serving(args):
     from generative_recommender_ranking_gb300 import build as bld
     bld.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = _workload(args.workload, 0, args.batch, args.history)
+    w = _workload(args.workload, 0, args.batch, args.history, args.heads, args.head_dim)
     params = bd.make_params(w.num_heads, w.head_dim, dtype=w.dtype, **w.mask, **w.rope)
     stream = torch.cuda.current_stream(dev)
 
@@ -506,7 +511,7 @@ def run_compress_fused(args):
     from generative_recommender_ranking_gb300 import build as bld
     bld.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = _workload(args.workload, 0, args.batch, args.history)
+    w = _workload(args.workload, 0, args.batch, args.history, args.heads, args.head_dim)
     segs = COMPRESS_SPECS[args.compress]
     hb, hl = [], []
     for b in range(w.batch):
@@ -602,7 +607,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
 
-    w = _workload(args.workload, rank, args.batch, args.history)
+    w = _workload(args.workload, rank, args.batch, args.history, args.heads, args.head_dim)
     bf16 = w.dtype == "bf16"
     elem = 2 if bf16 else 4
 
@@ -859,7 +864,8 @@ def run_ours(args):
     attn_gbs = bytes_attn / (attn_ms * 1e-3) / 1e9
     # full-size default batch only: the capture was taken on that launch
     traffic = (_traffic(args.workload + ("/fused" if args.fused else ""))
-               if (args.batch is None and args.history is None and world == 1) else None)
+               if (args.batch is None and args.history is None and args.heads is None and args.head_dim is None
+                   and world == 1) else None)
     hbm_bound = (flops_fwd / bytes_attn) < (pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9))
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -965,6 +971,9 @@ def main(argv=None):
                     help="override the workload's number of requests (small profiling cases)")
     ap.add_argument("--history", type=int, default=None,
                     help="tm20k workloads: history tokens per request (default 20000; context runs at 5000)")
+    ap.add_argument("--heads", type=int, default=None, help="override the workload's number of heads")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="override the workload's head dimension (64 or 128 in bf16; 32 or 64 in fp32)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=2.0,
