@@ -38,7 +38,7 @@ from generative_recommender_ranking_gb300 import workloads as W  # noqa: E402
 
 METRIC = "masked-attn fwd TFLOP/s over visible pairs, % of GB300 bf16 peak; tokens/s"
 L2_FLUSH_BYTES = 256 << 20
-E2E_RUNS = 3  # runs of the end-to-end leg; the median is reported
+E2E_RUNS = 5  # runs of the end-to-end leg; the median is reported
 # history-compression settings: recency segments (length or -1, group size), newest first
 COMPRESS_SPECS = {
     "lazformer_keep1024_g8": [(1024, 1), (-1, 8)],
@@ -813,7 +813,7 @@ def run_ours(args):
 
     e2e_steps(2)  # untimed: the copy streams and the buffer sets warmed up
     torch.cuda.synchronize(dev)
-    # three runs of K steps, the median reported: on these hosts a host-device copy
+    # E2E_RUNS runs of K steps, the median reported: on these hosts a host-device copy
     # now and then runs at a fraction of the link's rate (a 4.7 ms upload seen taking
     # 80 ms), which no schedule can hide; every run is listed with the line
     e2e_runs = []

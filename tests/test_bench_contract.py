@@ -53,5 +53,5 @@ def test_gpu_arm_line():
     e = d["e2e"]
     assert e["value"] > 0 and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    assert len(e["runs_ms_per_step"]) == 3 and e["link"]["h2d_gbs"] > 0
+    assert len(e["runs_ms_per_step"]) == 5 and e["link"]["h2d_gbs"] > 0
     assert d["gpu_launches"] > 0
