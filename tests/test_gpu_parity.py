@@ -101,3 +101,39 @@ def test_parity_full_size_sampled(name):
         assert bd.rec_attn_device_status(plan) == bd.OK
     finally:
         bd.rec_attn_free(plan)
+
+
+def test_parity_long_rows_rising_scores():
+    """Rows whose running maximum keeps moving: keys gain a component along a fixed
+    direction that the queries share, growing with the key's position (head 0 steeply,
+    so most 64-key chunks exceed the reference and are formed again against their own
+    maximum; head 1 gently, with bumps, so some do and some do not).  33 tiles a request
+    with no window, so the long-item softmax runs; every row against the oracle."""
+    base = W.tm20k("full", batch=2, n_hist=4150, heads=2)
+    rng = np.random.default_rng(23)
+    T, H, d = base.q.shape
+    u = rng.standard_normal((H, d)).astype(np.float32)
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    q = rng.standard_normal((T, H, d)).astype(np.float32) + 2.0 * u[None]
+    k = rng.standard_normal((T, H, d)).astype(np.float32)
+    for b in range(base.batch):
+        s, e = int(base.offsets[b]), int(base.offsets[b + 1])
+        j = np.arange(e - s, dtype=np.float32)
+        steep = 0.2 * j
+        gentle = 0.03 * j + 6.0 * np.sin(j / 97.0)
+        k[s:e, 0] += steep[:, None] * u[0][None]
+        k[s:e, 1] += gentle[:, None] * u[1][None]
+    w = W.Workload(**{**base.__dict__, "q": W.round_to_bf16_bits(q), "k": W.round_to_bf16_bits(k),
+                      "rope": dict(base.rope, use_rope=False)})
+    out, lse, plan = gu.run_gpu(w, with_lse=True)
+    try:
+        ref, ref_lse = oracle.attention(gu.oracle_params(w), w.offsets, w.t, w.types, w.q, w.k, w.v,
+                                        with_lse=True)
+        gu.assert_close(w, gu.to_f64(out), ref, "rising scores")
+        lg = lse.cpu().numpy().astype(np.float64)
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isfinite(lg), fin)
+        assert np.max(np.abs(lg[fin] - ref_lse[fin]) / np.maximum(1.0, np.abs(ref_lse[fin])), initial=0.0) <= 2e-2
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
