@@ -103,13 +103,26 @@ def test_parity_full_size_sampled(name):
         bd.rec_attn_free(plan)
 
 
-def test_parity_long_rows_rising_scores():
+RISING = {
+    # 33 tiles a request with no window: the long-item softmax (lazy maximum)
+    "tm20k_long": lambda: W.tm20k("full", batch=2, n_hist=4150, heads=2),
+    # short requests: the plain softmax, whose reference moves past 2^8 jumps (O rescaled)
+    "cadet": lambda: W.cadet(batch=4, n_pairs=300, heads=2),
+    # head_dim 128: the chunked layout's rescale
+    "cadet_d128": lambda: W.cadet(batch=3, n_pairs=300, heads=2, head_dim=128),
+    # bidirectional history and real-time events
+    "mtgr": lambda: W.mtgr(batch=3, hist=(300, 600), rt=(40, 80), cand=(10, 30), heads=2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RISING))
+def test_parity_rising_scores(name):
     """Rows whose running maximum keeps moving: keys gain a component along a fixed
-    direction that the queries share, growing with the key's position (head 0 steeply,
-    so most 64-key chunks exceed the reference and are formed again against their own
-    maximum; head 1 gently, with bumps, so some do and some do not).  33 tiles a request
-    with no window, so the long-item softmax runs; every row against the oracle."""
-    base = W.tm20k("full", batch=2, n_hist=4150, heads=2)
+    direction that the queries share, growing with the key's position within its
+    request (head 0 steeply, so most key tiles exceed the reference and O is rescaled
+    or the chunk formed again; head 1 gently, with bumps, so some do and some do not).
+    The time-RoPE is off so the alignment survives; every row against the oracle."""
+    base = RISING[name]()
     rng = np.random.default_rng(23)
     T, H, d = base.q.shape
     u = rng.standard_normal((H, d)).astype(np.float32)
@@ -119,17 +132,15 @@ def test_parity_long_rows_rising_scores():
     for b in range(base.batch):
         s, e = int(base.offsets[b]), int(base.offsets[b + 1])
         j = np.arange(e - s, dtype=np.float32)
-        steep = 0.2 * j
-        gentle = 0.03 * j + 6.0 * np.sin(j / 97.0)
-        k[s:e, 0] += steep[:, None] * u[0][None]
-        k[s:e, 1] += gentle[:, None] * u[1][None]
+        k[s:e, 0] += (0.2 * j)[:, None] * u[0][None]
+        k[s:e, 1] += (0.03 * j + 6.0 * np.sin(j / 97.0))[:, None] * u[1][None]
     w = W.Workload(**{**base.__dict__, "q": W.round_to_bf16_bits(q), "k": W.round_to_bf16_bits(k),
                       "rope": dict(base.rope, use_rope=False)})
     out, lse, plan = gu.run_gpu(w, with_lse=True)
     try:
         ref, ref_lse = oracle.attention(gu.oracle_params(w), w.offsets, w.t, w.types, w.q, w.k, w.v,
                                         with_lse=True)
-        gu.assert_close(w, gu.to_f64(out), ref, "rising scores")
+        gu.assert_close(w, gu.to_f64(out), ref, f"rising scores, {name}")
         lg = lse.cpu().numpy().astype(np.float64)
         fin = np.isfinite(ref_lse)
         assert np.array_equal(np.isfinite(lg), fin)
