@@ -170,3 +170,26 @@ def tile_class_map(w: W.Workload, cls: np.ndarray):
                 out[(b, qt, kt)] = blk[qt, kt]
         i += nt * nt
     return out
+
+
+def rising_scores(base: W.Workload, seed=23, steep=0.2) -> W.Workload:
+    """The same requests with scores that rise along each row: keys gain a component
+    along a fixed per-head direction that the queries share, growing with the key's
+    position within its request (head 0 by `steep` per position, head 1 gently with
+    bumps, further heads untouched), and the time-RoPE off so the alignment survives."""
+    rng = np.random.default_rng(seed)
+    T, H, d = base.q.shape
+    u = rng.standard_normal((H, d)).astype(np.float32)
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    q = rng.standard_normal((T, H, d)).astype(np.float32) + 2.0 * u[None]
+    k = rng.standard_normal((T, H, d)).astype(np.float32)
+    for b in range(base.batch):
+        s, e = int(base.offsets[b]), int(base.offsets[b + 1])
+        j = np.arange(e - s, dtype=np.float32)
+        k[s:e, 0] += (steep * j)[:, None] * u[0][None]
+        if H > 1:
+            k[s:e, 1] += (0.03 * j + 6.0 * np.sin(j / 97.0))[:, None] * u[1][None]
+    if base.dtype == "bf16":
+        q, k = W.round_to_bf16_bits(q), W.round_to_bf16_bits(k)
+    return W.Workload(**{**base.__dict__, "q": q, "k": k, "rope": dict(base.rope, use_rope=False)})
+

@@ -40,6 +40,13 @@ CASES = {
     "sort_d128": lambda: W.sort(batch=2, n_hist=300, n_cand=40, window=100, heads=2, head_dim=128),
     "mtgr_d128": lambda: W.mtgr(batch=3, hist=(150, 300), rt=(20, 60), cand=(10, 30), heads=2, head_dim=128),
     "cadet_d128_many": lambda: W.cadet(batch=96, n_pairs=150, heads=2, head_dim=128),
+    # scores rising along each row (to ~60): P = exp2(s log2 e - lse) with both large.
+    # The key slope stays moderate: D = <dO, O> is formed from the forward's bf16 O, and
+    # in a peaked row dS of the dominant key is mostly that rounding, which dQ then
+    # carries scaled by |K|; with keys of a few hundred that alone exceeds the tolerance
+    "cadet_rising": lambda: gu.rising_scores(W.cadet(batch=3, n_pairs=150, heads=2)),
+    "mtgr_rising_d128": lambda: gu.rising_scores(W.mtgr(batch=3, hist=(150, 300), rt=(20, 60), cand=(10, 30),
+                                                        heads=2, head_dim=128), steep=0.05),
 }
 
 

@@ -122,20 +122,7 @@ def test_parity_rising_scores(name):
     request (head 0 steeply, so most key tiles exceed the reference and O is rescaled
     or the chunk formed again; head 1 gently, with bumps, so some do and some do not).
     The time-RoPE is off so the alignment survives; every row against the oracle."""
-    base = RISING[name]()
-    rng = np.random.default_rng(23)
-    T, H, d = base.q.shape
-    u = rng.standard_normal((H, d)).astype(np.float32)
-    u /= np.linalg.norm(u, axis=1, keepdims=True)
-    q = rng.standard_normal((T, H, d)).astype(np.float32) + 2.0 * u[None]
-    k = rng.standard_normal((T, H, d)).astype(np.float32)
-    for b in range(base.batch):
-        s, e = int(base.offsets[b]), int(base.offsets[b + 1])
-        j = np.arange(e - s, dtype=np.float32)
-        k[s:e, 0] += (0.2 * j)[:, None] * u[0][None]
-        k[s:e, 1] += (0.03 * j + 6.0 * np.sin(j / 97.0))[:, None] * u[1][None]
-    w = W.Workload(**{**base.__dict__, "q": W.round_to_bf16_bits(q), "k": W.round_to_bf16_bits(k),
-                      "rope": dict(base.rope, use_rope=False)})
+    w = gu.rising_scores(RISING[name]())
     out, lse, plan = gu.run_gpu(w, with_lse=True)
     try:
         ref, ref_lse = oracle.attention(gu.oracle_params(w), w.offsets, w.t, w.types, w.q, w.k, w.v,
