@@ -627,13 +627,14 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
       if ((qr->typebits[c][row >> 5] >> (row & 31)) & 1u) tyi = c;
     ptx::mbar_arrive(B.q_empty + qb);  // the Q buffer and its record may be refilled
     const bool out_ok = row_ok && query_kept(tyi, pi, d.keep);  // pruned rows are computed, not written
-    uint4 gpre[8];  // GATE: the gate of the row's first 64 columns, loaded while the item runs
+    // GATE: the row's gate (D bf16, whole 128-byte lines) is prefetched into L2 while the
+    // item runs and read in the epilogue, so no registers hold it through the tiles
     if constexpr (GATE) {
       if (out_ok) {
-        const uint4* g0 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out_gate) +
-                                                         (tok * H + d.h) * D);
+        const char* g0 = reinterpret_cast<const char*>(static_cast<const __nv_bfloat16*>(a.out_gate) +
+                                                       (tok * H + d.h) * D);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) gpre[c] = g0[c];
+        for (int c = 0; c < D * 2 / 128; ++c) asm volatile("prefetch.global.L2 [%0];" ::"l"(g0 + 128 * c));
       }
     }
     RowMask rm;
@@ -758,9 +759,8 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
 #pragma unroll
           for (int e = 0; e < 8; ++e) sc[e] = inv;
           if constexpr (GATE) {
-            const uint4 gv = half == 0 ? gpre[c]
-                                       : reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out_gate) +
-                                                                        (tok * H + d.h) * D + half * 64)[c];
+            const uint4 gv = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out_gate) +
+                                                            (tok * H + d.h) * D + half * 64)[c];
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
