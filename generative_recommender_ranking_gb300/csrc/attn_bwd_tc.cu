@@ -31,10 +31,11 @@
 // The accumulators stay in TMEM across an item's tiles; the epilogue scales, undoes
 // the rotation and writes bf16 rows.  Everything a compute thread needs besides TMEM
 // comes through shared memory with the tiles: the planner's records of the item's tile
-// and the streamed tiles (times, type bitmaps) and the rows' constants
-// {lse * log2(e), D} (k_bwd_rowc, tile-padded so that a bulk copy moves a tile's
-// 128 rows), and the item descriptors (k_bwd_schedule, once per plan) come from the
-// producer.  PARTIAL tiles take the forward's per-row
+// and the streamed tiles (times, type bitmaps) and the rows' constants -lse * log2(e)
+// and -D, stored for row pairs as {-lse2(2k), -lse2(2k+1), -D(2k), -D(2k+1)} so that a
+// pair of query columns takes one f32x2 operation (k_bwd_rowc, tile-padded so that a
+// bulk copy moves a tile's 128 rows), and the item descriptors (k_bwd_schedule, once
+// per plan) come from the producer.  PARTIAL tiles take the forward's per-row
 // visibility bits (row_mask.cuh), built from the key tile's planner record; in DKV
 // each thread first acts as a row of the query tile, builds that row's bits against
 // the item's key tile, and the warps transpose the bits into per-key columns with
@@ -102,7 +103,7 @@ __host__ __device__ constexpr int xready(uint32_t step) { return kXReady + (int)
 __host__ __device__ constexpr uint32_t xready_parity(uint32_t step) { return (step >> 1) & 1u; }
 
 // Byte offsets from the 1024-aligned base of dynamic shared memory.
-constexpr int kRowB = kTile * 8;  // {lse2, D} of a tile's rows
+constexpr int kRowB = kTile * 8;  // {-lse2, -D} of a tile's rows, paired (row_neg_lse2 / row_neg_d)
 template <int D>
 struct BL {
   static constexpr int kTileBytes = BCfg<D>::kTileBytes;
@@ -441,6 +442,37 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// fp32 pairs for the f32x2 instructions (one instruction for two columns)
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// The row-constant table of one tile (128 rows): rows 2k and 2k+1 share 16 bytes,
+// {-lse2(2k), -lse2(2k+1), -D(2k), -D(2k+1)}, with lse2 = lse * log2(e).
+__device__ __forceinline__ float row_neg_lse2(const float* tab, int r) { return tab[(r >> 1) * 4 + (r & 1)]; }
+__device__ __forceinline__ float row_neg_d(const float* tab, int r) { return tab[(r >> 1) * 4 + 2 + (r & 1)]; }
+
 // One output row: x * scale, then (rotate) R(dt)^T over adjacent pairs, as bf16.  The
 // angles (at most a few tens of radians) take the hardware sine and cosine: their
 // error, about 1e-5 rad here, is far below the bf16 rounding of the result.
@@ -491,8 +523,9 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
   const float sl2 = a.scale * kLog2e;
   const uint8_t* sstage = sm + BL::kSRec;  // per stage: key record or mask-table rows
   const KeyTileRec* rrec = reinterpret_cast<const KeyTileRec*>(sm + BL::kRRec);
-  const float2* rrow = reinterpret_cast<const float2*>(sm + BL::kRRow);
+  const float* rrow = reinterpret_cast<const float*>(sm + BL::kRRow);
   const int H = a.heads;
+  const unsigned long long sl2x2 = f2pack(sl2, sl2);
   uint32_t it_n = 0, s_it = 0, step = 0, it_cnt = 0;
   BwdItemDesc it;
   while (next_item<D>(sm, bars, it_cnt, true, it, abort_flag, a.status)) {
@@ -509,11 +542,13 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
     long long ti;
     int tyi;
     rec_row(rrec, row, ti, tyi);
-    const float2 rc = rrow[row];
+    const float nl = row_neg_lse2(rrow, row), nd = row_neg_d(rrow, row);
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(bars + kResEmpty);
-    const bool live = row_ok && rc.x != -INFINITY;  // a row that sees no key contributes nothing
-    const float lse2 = live ? rc.x : 0.f, dlt = rc.y;
+    // a row that sees no key contributes nothing: its P is exp2(s - inf) = 0, so FULL
+    // tiles need no mask for it
+    const bool live = row_ok && nl != INFINITY;
+    const unsigned long long nl2 = f2pack(live ? nl : -INFINITY, live ? nl : -INFINITY), nd2 = f2pack(nd, nd);
     RowMask rm;
     row_mask_setup(a.mask, live, pi, ti, tyi, rm);
     Cursor cur;
@@ -560,12 +595,17 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            float p0 = ex2(fmaf(__uint_as_float(sr[2 * e]), sl2, -lse2));
-            float p1 = ex2(fmaf(__uint_as_float(sr[2 * e + 1]), sl2, -lse2));
-            p0 = ((wb[c] >> (2 * e)) & 1u) ? p0 : 0.f;
-            p1 = ((wb[c] >> (2 * e + 1)) & 1u) ? p1 : 0.f;
-            pk[e] = bf16x2(p0 * (__uint_as_float(d[32 * c + 2 * e]) - dlt),
-                           p1 * (__uint_as_float(d[32 * c + 2 * e + 1]) - dlt));
+            float y0, y1;
+            f2unpack(f2fma(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sl2x2, nl2), y0, y1);
+            float p0 = ex2(y0), p1 = ex2(y1);
+            if (cls != REC_ATTN_TILE_FULL) {
+              p0 = ((wb[c] >> (2 * e)) & 1u) ? p0 : 0.f;
+              p1 = ((wb[c] >> (2 * e + 1)) & 1u) ? p1 : 0.f;
+            }
+            float g0, g1;
+            f2unpack(f2mul(f2pack(p0, p1), f2add(f2pack(__uint_as_float(d[32 * c + 2 * e]),
+                                                        __uint_as_float(d[32 * c + 2 * e + 1])), nd2)), g0, g1);
+            pk[e] = bf16x2(g0, g1);
           }
           ptx::tmem_st16_async(sb + 16 * c, pk);  // dS over S columns already read
         }
@@ -632,7 +672,8 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
   const float sl2 = a.scale * kLog2e;
   const KeyTileRec* rrec = reinterpret_cast<const KeyTileRec*>(sm + BL::kRRec);
   const uint8_t* sstage = sm + BL::kSRec;  // per stage: query record or mask-table columns
-  const float2* srow = reinterpret_cast<const float2*>(sm + BL::kSRow);
+  const float* srow = reinterpret_cast<const float*>(sm + BL::kSRow);
+  const unsigned long long sl2x2 = f2pack(sl2, sl2);
   uint32_t* colS = reinterpret_cast<uint32_t*>(sm + BL::kCol);
   const int H = a.heads;
   uint32_t it_n = 0, s_it = 0, step = 0, grp = 0, cbuf = 0, it_cnt = 0;
@@ -664,7 +705,11 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
           if (lane == 0) ptx::mbar_arrive(bars + kResEmpty);
         }
       };
-      if (cls != REC_ATTN_TILE_FULL && tslot >= 0) {
+      if (cls == REC_ATTN_TILE_FULL) {  // the steps of a FULL tile apply no mask
+        release_rec();
+        return true;
+      }
+      if (tslot >= 0) {
         reinterpret_cast<uint4*>(colS + buf * (kTile * 4))[row] =
             reinterpret_cast<const uint4*>(sstage + st * kStageRecB)[row];
         release_rec();
@@ -674,14 +719,12 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
       long long tq;
       int tyq;
       rec_row(reinterpret_cast<const KeyTileRec*>(sstage + st * kStageRecB), row, tq, tyq);
-      const bool live = qi < it.len && srow[st * kTile + row].x != -INFINITY;
+      const bool live = qi < it.len && row_neg_lse2(srow + st * 2 * kTile, row) != INFINITY;
       const uint32_t f = live ? ~0u : 0u;
       uint32_t vm[4] = {f, f, f, f};
-      if (cls != REC_ATTN_TILE_FULL) {
-        RowMask rm;
-        row_mask_setup(a.mask, live, qi, tq, tyq, rm);
-        build_mask(rm, rrec, it.tile * kTile, vm);
-      }
+      RowMask rm;
+      row_mask_setup(a.mask, live, qi, tq, tyq, rm);
+      build_mask(rm, rrec, it.tile * kTile, vm);
       release_rec();
 #pragma unroll
       for (int wd = 0; wd < 4; ++wd) colS[buf * (kTile * 4) + (32 * wd + lane) * 4 + quad] = transpose32(vm[wd], lane);
@@ -689,6 +732,7 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
     };
     int qt, cls, tslot;
     cur.next(qt, cls, tslot);
+    int scls = cls;  // the class of the query tile the steps run on
     int st = (int)(s_it % kNS);
     if (!prepare(0, qt, cls, tslot, st, (s_it / kNS) & 1, cbuf)) return;
     ++s_it;
@@ -697,7 +741,7 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
       // other buffer's (a tile ago), which prepare() overwrites next
       if (!group_sync(bars + kGroup, grp, abort_flag, a.status)) return;
       const uint4 cm = reinterpret_cast<const uint4*>(colS)[cbuf * kTile + row];
-      const float2* rows = srow + st * kTile;
+      const float* rows = srow + st * 2 * kTile;
       int nqt = 0, ncls = 0, nslot = -1, nst = 0;
       uint32_t nph = 0;
       if (j + 1 < it.n) {
@@ -716,26 +760,36 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         for (int c = 0; c < 2; ++c) {
           uint32_t r[64], pk[16];
           ptx::tmem_ld32x2_async(tl + 32 * c, tl + 64 + 32 * c, r);
-          // {lse2, D} of the chunk's 32 queries, two per 16-byte load (broadcast)
-          const float4* q4 = reinterpret_cast<const float4*>(rows + hh * kStep + c * 32);
+          // {-lse2, -D} of the chunk's 32 queries, a pair per 16-byte load (broadcast)
+          const float4* q4 = reinterpret_cast<const float4*>(rows + (hh * kStep + c * 32) * 2);
           const uint32_t bits = wb[c];
           ptx::tmem_wait_ld(r);
           float p[32];
 #pragma unroll
           for (int g = 0; g < 16; ++g) {
             const float4 k2 = q4[g];
-            const float x0 = ex2(fmaf(__uint_as_float(r[2 * g]), sl2, -k2.x));
-            const float x1 = ex2(fmaf(__uint_as_float(r[2 * g + 1]), sl2, -k2.z));
-            p[2 * g] = ((bits >> (2 * g)) & 1u) ? x0 : 0.f;
-            p[2 * g + 1] = ((bits >> (2 * g + 1)) & 1u) ? x1 : 0.f;
-            pk[g] = bf16x2(p[2 * g], p[2 * g + 1]);
+            float x0, x1;
+            f2unpack(f2fma(f2pack(__uint_as_float(r[2 * g]), __uint_as_float(r[2 * g + 1])), sl2x2,
+                           f2pack(k2.x, k2.y)), x0, x1);
+            x0 = ex2(x0);
+            x1 = ex2(x1);
+            if (scls != REC_ATTN_TILE_FULL) {  // FULL: queries past the request end have -lse2 = -inf
+              x0 = ((bits >> (2 * g)) & 1u) ? x0 : 0.f;
+              x1 = ((bits >> (2 * g + 1)) & 1u) ? x1 : 0.f;
+            }
+            p[2 * g] = x0;
+            p[2 * g + 1] = x1;
+            pk[g] = bf16x2(x0, x1);
           }
           ptx::tmem_st16_async(tl + 16 * c, pk);  // P^T over S^T columns already read
 #pragma unroll
           for (int g = 0; g < 16; ++g) {
             const float4 k2 = q4[g];
-            pk[g] = bf16x2(p[2 * g] * (__uint_as_float(r[32 + 2 * g]) - k2.y),
-                           p[2 * g + 1] * (__uint_as_float(r[32 + 2 * g + 1]) - k2.w));
+            float g0, g1;
+            f2unpack(f2mul(f2pack(p[2 * g], p[2 * g + 1]),
+                           f2add(f2pack(__uint_as_float(r[32 + 2 * g]), __uint_as_float(r[32 + 2 * g + 1])),
+                                 f2pack(k2.z, k2.w))), g0, g1);
+            pk[g] = bf16x2(g0, g1);
           }
           ptx::tmem_st16_async(tl + 64 + 16 * c, pk);  // dS^T over dP^T columns already read
         }
@@ -751,6 +805,7 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + kStrEmpty + st);  // the stage's record and constants were read
       st = nst;
+      scls = ncls;
       cbuf ^= 1u;
     }
     if (!bw_wait_warp(bars + kAccFull, it_n & 1, abort_flag, a.status)) return;
@@ -781,9 +836,10 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
 
 // ------------------------------------------------------------------ row constants
 // Block = (tile g, head h): D_i = <dO_i, O_i> for the tile's 128 rows, eight threads per
-// row (16 bytes of dO and O each, coalesced), written with lse * log2(e) as one float2
-// per row into the tile-padded table; rows past the request end and rows that see no
-// key get -inf.
+// row (16 bytes of dO and O each, coalesced), written negated with -lse * log2(e) into
+// the tile-padded table, rows paired (row_neg_lse2 / row_neg_d).  lse2 is -inf for rows
+// that see no key and +inf for rows past the request end and pruned rows, so that
+// every P of the latter is exp2(s - inf) = 0 whatever mask bits they have.
 template <int D>
 __global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
   constexpr int kLanes = D / 8;  // 16-byte chunks of a row, one per thread
@@ -793,7 +849,7 @@ __global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
   const ReqMeta m = a.meta[b];
   const int tile = (int)(g - m.tile_start);
   const int sub = threadIdx.x & (kLanes - 1);
-  float2* out = a.rowc + ((long long)h * a.n_tiles + g) * kTile;
+  float* out = reinterpret_cast<float*>(a.rowc + ((long long)h * a.n_tiles + g) * kTile);
   const int keep = a.qkeep[b];
 #pragma unroll 1
   for (int r = threadIdx.x / kLanes; r < kTile; r += 256 / kLanes) {
@@ -818,10 +874,9 @@ __global__ void __launch_bounds__(256) k_bwd_rowc(BwdArgs a) {
 #pragma unroll
     for (int o = kLanes / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (sub == 0) {
-      // rows past the request end and rows that see no key: lse = -inf; pruned rows:
-      // +inf, so every P of the row is exp2(s - inf) = 0 whatever mask bits it has
-      const float l = ok ? a.lse[row] : (in ? INFINITY : -INFINITY);
-      out[r] = make_float2(ok && l == -INFINITY ? -INFINITY : l * kLog2e, acc);
+      const float l = ok ? a.lse[row] : INFINITY;
+      out[(r >> 1) * 4 + (r & 1)] = -(l == -INFINITY ? -INFINITY : l * kLog2e);
+      out[(r >> 1) * 4 + 2 + (r & 1)] = -acc;
     }
   }
 }
