@@ -473,12 +473,30 @@ __device__ __forceinline__ unsigned long long f2mul(unsigned long long a, unsign
 __device__ __forceinline__ float row_neg_lse2(const float* tab, int r) { return tab[(r >> 1) * 4 + (r & 1)]; }
 __device__ __forceinline__ float row_neg_d(const float* tab, int r) { return tab[(r >> 1) * 4 + 2 + (r & 1)]; }
 
+// 32 words (64 bf16, one 128-byte row piece) to global memory: 32-byte stores when the
+// gradient buffers are 32-byte aligned (each store then fills whole sectors; the rows of
+// a warp lie H * d * 2 bytes apart), else 16-byte stores.
+__device__ __forceinline__ void st_words(void* dst, const uint32_t (&w)[32], bool wide) {
+  if (wide) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(static_cast<char*>(dst) + 32 * c),
+                   "r"(w[8 * c]), "r"(w[8 * c + 1]), "r"(w[8 * c + 2]), "r"(w[8 * c + 3]), "r"(w[8 * c + 4]),
+                   "r"(w[8 * c + 5]), "r"(w[8 * c + 6]), "r"(w[8 * c + 7])
+                   : "memory");
+  } else {
+    uint4* d4 = static_cast<uint4*>(dst);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  }
+}
+
 // One output row: x * scale, then (rotate) R(dt)^T over adjacent pairs, as bf16.  The
 // angles (at most a few tens of radians) take the hardware sine and cosine: their
 // error, about 1e-5 rad here, is far below the bf16 rounding of the result.
 // (64 columns of a row at dst; omega: their 32 rotation pairs)
 __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t (&acc)[64], float scale, bool rotate,
-                                         float dt, const float* omega) {
+                                         float dt, const float* omega, bool wide) {
   uint32_t w[32];
 #pragma unroll
   for (int p = 0; p < 32; ++p) {
@@ -492,9 +510,7 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t (&a
     }
     w[p] = bf16x2(u, v);
   }
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  st_words(dst, w, wide);
 }
 
 template <int D>
@@ -526,6 +542,7 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
   const float* rrow = reinterpret_cast<const float*>(sm + BL::kRRow);
   const int H = a.heads;
   const unsigned long long sl2x2 = f2pack(sl2, sl2);
+  const bool wide = (reinterpret_cast<uintptr_t>(a.dq) & 31) == 0;  // row pieces 32-byte aligned
   uint32_t it_n = 0, s_it = 0, step = 0, it_cnt = 0;
   BwdItemDesc it;
   while (next_item<D>(sm, bars, it_cnt, true, it, abort_flag, a.status)) {
@@ -624,7 +641,7 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
-      if (row_ok) store_row(dst, acc, a.scale, a.rotate != 0, (float)(ti - it.t_ref), a.omega);
+      if (row_ok) store_row(dst, acc, a.scale, a.rotate != 0, (float)(ti - it.t_ref), a.omega, wide);
     } else {
 #pragma unroll 1
       for (int hc = 0; hc < D / 64; ++hc) {
@@ -635,7 +652,8 @@ __device__ void bwd_compute_dq(const BwdArgs& a, uint8_t* sm, uint64_t* bars, ui
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
         }
-        if (row_ok) store_row(dst + 64 * hc, acc, a.scale, a.rotate != 0, (float)(ti - it.t_ref), a.omega + 32 * hc);
+        if (row_ok)
+          store_row(dst + 64 * hc, acc, a.scale, a.rotate != 0, (float)(ti - it.t_ref), a.omega + 32 * hc, wide);
       }
     }
   }
@@ -674,6 +692,7 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
   const uint8_t* sstage = sm + BL::kSRec;  // per stage: query record or mask-table columns
   const float* srow = reinterpret_cast<const float*>(sm + BL::kSRow);
   const unsigned long long sl2x2 = f2pack(sl2, sl2);
+  const bool wide = ((reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) & 31) == 0;
   uint32_t* colS = reinterpret_cast<uint32_t*>(sm + BL::kCol);
   const int H = a.heads;
   uint32_t it_n = 0, s_it = 0, step = 0, grp = 0, cbuf = 0, it_cnt = 0;
@@ -825,10 +844,8 @@ __device__ void bwd_compute_dkv(const BwdArgs& a, uint8_t* sm, uint64_t* bars, u
         if (lane == 0) ptx::mbar_arrive(bars + kAccEmpty);
       }
       if (key_ok) {
-        uint4* d4 = reinterpret_cast<uint4*>(dvr + 64 * hc);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) d4[c] = make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
-        store_row(dkr + 64 * hc, acc, a.scale, a.rotate != 0, (float)(tj - it.t_ref), a.omega + 32 * hc);
+        st_words(dvr + 64 * hc, wv, wide);
+        store_row(dkr + 64 * hc, acc, a.scale, a.rotate != 0, (float)(tj - it.t_ref), a.omega + 32 * hc, wide);
       }
     }
   }

@@ -235,3 +235,36 @@ def test_backward_full_size_dv_column_sums(name):
         # Eight of them; a lost 128-row tile of dO moves the sum by about sqrt(128).
         tol = 8 * 2.0 ** -9 * (np.sqrt((want[s:e] ** 2).sum(0)) + np.sqrt((got[s:e] ** 2).sum(0))) + 1e-6 * scale
         assert np.all(np.abs(gs - ws) <= tol), (name, b, float(np.max(np.abs(gs - ws) - tol)))
+
+
+@pytest.mark.parametrize("name", ["cadet", "mtgr_d128"])
+def test_backward_gradients_at_16_byte_offsets(name):
+    """The gradient rows go out as 32-byte stores when dq, dk and dv are 32-byte aligned
+    and as 16-byte stores otherwise (the interface promises 16).  Buffers 16 bytes past a
+    32-byte boundary must receive exactly what aligned buffers receive."""
+    w = CASES[name]()
+    tens = gu.device_inputs(w)
+    plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    try:
+        out = torch.empty_like(tens["q"])
+        lse = torch.empty((w.total_tokens, w.num_heads), dtype=torch.float32, device=out.device)
+        bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], out, lse)
+        dout = gu.device_inputs(W.Workload(**{**w.__dict__, "q": _grad_inputs(w)}))["q"]
+        shape, n = tens["q"].shape, tens["q"].numel()
+        aligned = [torch.full_like(tens["q"], float("nan")) for _ in range(3)]
+        shift = 16 // tens["q"].element_size()
+        bufs = [torch.full((n + 64,), float("nan"), dtype=tens["q"].dtype, device=out.device) for _ in range(3)]
+        offset = []
+        for b in bufs:
+            lead = (-b.data_ptr() % 32) // b.element_size() + shift  # 16 bytes past a 32-byte boundary
+            offset.append(b[lead:lead + n].view(shape))
+        assert all(x.data_ptr() % 32 == 16 for x in offset) and all(x.data_ptr() % 32 == 0 for x in aligned)
+        bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], out, lse, dout, *aligned)
+        bd.rec_attn_bwd(plan, tens["q"], tens["k"], tens["v"], out, lse, dout, *offset)
+        torch.cuda.synchronize()
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
+    for what, x, y in zip(("dq", "dk", "dv"), aligned, offset):
+        assert not torch.isnan(x).any(), what
+        assert torch.equal(x, y), what
