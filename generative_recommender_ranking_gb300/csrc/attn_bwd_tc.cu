@@ -480,10 +480,8 @@ __device__ __forceinline__ void st_words(void* dst, const uint32_t (&w)[32], boo
   if (wide) {
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(static_cast<char*>(dst) + 32 * c),
-                   "r"(w[8 * c]), "r"(w[8 * c + 1]), "r"(w[8 * c + 2]), "r"(w[8 * c + 3]), "r"(w[8 * c + 4]),
-                   "r"(w[8 * c + 5]), "r"(w[8 * c + 6]), "r"(w[8 * c + 7])
-                   : "memory");
+      ptx::st_global_v8(static_cast<char*>(dst) + 32 * c, w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3],
+                        w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]);
   } else {
     uint4* d4 = static_cast<uint4*>(dst);
 #pragma unroll

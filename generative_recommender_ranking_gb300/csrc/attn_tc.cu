@@ -584,6 +584,7 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
   const TmemMap tm = tmem_map<D>(tmem + ((uint32_t)(quad * 32) << 16), s);
   const float sl2 = a.scale * 1.4426950408889634f;  // scale * log2(e)
   const int H = a.heads;
+  const bool wide = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;  // O's 64-column pieces 32-byte aligned
   // ch: the stream's S chunk count (chunked) or S tile count (WIDE)
   uint32_t it_cnt = 0, kv_it = 0, ch = 0, o_it = 0, q_it = 0;
   for (;;) {
@@ -753,30 +754,42 @@ __device__ void run_softmax(const AttnArgs& a, uint8_t* sm, int s, const SBars& 
         for (int e = 0; e < 64; ++e) v[e] = __uint_as_float(o[e]) * inv;
         cmp_store<D>(a, a.cmp.req[d.req], d.h, pi, row_ok, lane, v, half);
       } else if (out_ok) {
+        // two 16-byte chunks (16 columns) at a time: one 32-byte store when O is 32-byte
+        // aligned (whole sectors; a warp's rows lie H * d * 2 bytes apart), else two
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float sc[8];
+        for (int c2 = 0; c2 < 4; ++c2) {
+          uint32_t wv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sc[e] = inv;
-          if constexpr (GATE) {
-            const uint4 gv = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out_gate) +
-                                                            (tok * H + d.h) * D + half * 64)[c];
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = 2 * c2 + h2;
+            float sc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sc[e] = inv;
+            if constexpr (GATE) {
+              const uint4 gv = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.out_gate) +
+                                                              (tok * H + d.h) * D + half * 64)[c];
+              const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+                sc[2 * e] *= sigmoidf_fast(gf.x);
+                sc[2 * e + 1] *= sigmoidf_fast(gf.y);
+              }
+            }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
-              sc[2 * e] *= sigmoidf_fast(gf.x);
-              sc[2 * e + 1] *= sigmoidf_fast(gf.y);
+              const __nv_bfloat162 pb = __floats2bfloat162_rn(__uint_as_float(o[c * 8 + 2 * e]) * sc[2 * e],
+                                                              __uint_as_float(o[c * 8 + 2 * e + 1]) * sc[2 * e + 1]);
+              wv[4 * h2 + e] = *reinterpret_cast<const uint32_t*>(&pb);
             }
           }
-          uint32_t wv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(__uint_as_float(o[c * 8 + 2 * e]) * sc[2 * e],
-                                                            __uint_as_float(o[c * 8 + 2 * e + 1]) * sc[2 * e + 1]);
-            wv[e] = *reinterpret_cast<const uint32_t*>(&pb);
+          uint4* dst = reinterpret_cast<uint4*>(orow + half * 64) + 2 * c2;
+          if (wide) {
+            ptx::st_global_v8(dst, wv[0], wv[1], wv[2], wv[3], wv[4], wv[5], wv[6], wv[7]);
+          } else {
+            dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
           }
-          reinterpret_cast<uint4*>(orow + half * 64)[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
     }

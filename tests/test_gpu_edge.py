@@ -218,3 +218,37 @@ def test_split_planner_with_empty_and_tiny_requests():
         assert bd.rec_attn_device_status(plan) == bd.OK
     finally:
         bd.rec_attn_free(plan)
+
+
+@pytest.mark.parametrize("case", ["cadet", "tm20k_long", "cadet_gated", "sort_d128"])
+def test_output_at_16_byte_offset_is_identical(case):
+    """O goes out as 32-byte stores when out is 32-byte aligned and as 16-byte stores
+    otherwise (the interface promises 16); a buffer 16 bytes past a 32-byte boundary gets
+    exactly the aligned result (plain, long-item, gated and head_dim 128 kernels)."""
+    make = {"cadet": lambda: W.cadet(batch=3, n_pairs=150), "cadet_gated": lambda: W.cadet(batch=3, n_pairs=150),
+            "tm20k_long": lambda: W.tm20k("full", batch=1, n_hist=4150, heads=2),
+            "sort_d128": lambda: W.sort(batch=2, n_hist=300, n_cand=40, window=100, heads=2, head_dim=128)}[case]
+    w = make()
+    tens = gu.device_inputs(w)
+    plan = bd.rec_attn_plan(gu.params_for(w), tens["off_h"], tens["off_d"], tens["t"], tens["ty"])
+    try:
+        n = tens["q"].numel()
+        aligned = torch.full_like(tens["q"], float("nan"))
+        buf = torch.full((n + 64,), float("nan"), dtype=tens["q"].dtype, device=aligned.device)
+        lead = (-buf.data_ptr() % 32) // buf.element_size() + 16 // buf.element_size()
+        offset = buf[lead:lead + n].view(tens["q"].shape)
+        assert offset.data_ptr() % 32 == 16 and aligned.data_ptr() % 32 == 0
+        outs = (aligned, offset)
+        if case == "cadet_gated":
+            g = gu.device_inputs(W.Workload(**{**w.__dict__, "q": W.fused_inputs(w).out_gate}))["q"]
+            for o in outs:
+                bd.rec_attn_fwd_fused(plan, tens["q"], tens["k"], tens["v"], o, None, None, out_gate=g)
+        else:
+            for o in outs:
+                bd.rec_attn_fwd(plan, tens["q"], tens["k"], tens["v"], o)
+        torch.cuda.synchronize()
+        assert bd.rec_attn_device_status(plan) == bd.OK
+    finally:
+        bd.rec_attn_free(plan)
+    assert not torch.isnan(aligned).any()
+    assert torch.equal(aligned, offset)
