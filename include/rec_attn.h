@@ -170,7 +170,9 @@ int64_t rec_attn_query_keep(int64_t hist_len, int64_t n_min, int32_t layer, int3
  *   q, k, v   device [T][H][d] row-major, contiguous, in params->dtype (bf16 bit
  *             patterns or fp32), 16-byte aligned, finite.
  *   out       device [T][H][d] in params->dtype; every row is written (rows that see
- *             no key get zeros).  May not alias q, k or v.
+ *             no key get zeros).  May not alias q, k or v.  A 32-byte aligned out is
+ *             written with 32-byte stores (whole sectors), a 16-byte aligned one with
+ *             16-byte stores; the values are the same.
  *   lse       optional device float[T][H]: natural-log sum of exp(scaled scores) over
  *             visible keys, -inf for rows that see no key; NULL to skip.
  *   stream    cudaStream_t for the launches.
@@ -234,7 +236,8 @@ rec_attn_status rec_attn_fwd_fused(rec_attn_plan_t* plan, const void* q, const v
  *   out, lse  the forward's output and log-sum-exp (lse is required here).
  *   dout      device [T][H][d] in params->dtype: dLoss/dout.
  *   dq, dk, dv  device [T][H][d] in params->dtype, written in full; they may not
- *             alias any input or each other.  All tensors 16-byte aligned.
+ *             alias any input or each other.  All tensors 16-byte aligned; dq, dk
+ *             and dv 32-byte aligned are written with 32-byte stores (same values).
  * The plan must be the forward's (same offsets, times, types, params).  On a
  * query-pruned plan (rec_attn_plan_query_pruned) the gradients are those of the
  * computed rows' outputs: pruned queries have no output, so their out and lse rows
