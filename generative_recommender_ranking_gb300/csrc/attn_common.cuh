@@ -170,7 +170,9 @@ struct BwdArgs {
   // tensor-core path (bf16): per-plan schedule and per-call row constants
   const BwdItemDesc* desc;  // [2][n_items]: dQ items, then dK/dV items (mirrored key tiles)
   const uint32_t* qlist;    // per key tile: query tiles with a non-SKIP class (qt | class << 24)
-  float2* rowc;             // [H][n_tiles][128]: {lse * log2(e) (-inf: the row sees no key), D}
+  float2* rowc;             // [H][n_tiles][128 rows]: -lse * log2(e) and -D, rows paired as
+                            // {-lse2(2k), -lse2(2k+1), -D(2k), -D(2k+1)} (lse2 -inf: the row sees
+                            // no key; +inf: past the request end or pruned)
   const int* kslot;         // per key-tile list entry: mask-table slot (-1: build the bits)
   const uint32_t* mtab;     // mask table, rows: [slot][128 query rows][4 words over the keys]
   const int* qslot;         // per query-tile list entry (qlist): mask-table slot, -1 if none
